@@ -1,0 +1,429 @@
+#!/usr/bin/env python3
+"""Throughput of the FP32 GEMM library on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One "step" is one C = alpha*op(A)*op(B) + beta*C call of the headline
+workload: M = N = K = 4096, op = NN, A and B i.i.d. standard normal drawn from
+seed 2, alpha = 1, beta = 0 (the largest case of the 512..4096 square sweep;
+FLOPs per step = 2*M*N*K).  Inputs are resident in HBM when the timed region
+starts; A + B + C = 192 MiB, more than the 129 MB L2, so no extra L2 flush is
+done between steps.  Rank 0 prints ONE JSON line.
+
+Keys beyond the throughput: ``e2e`` (the same metric through the C ABI with the
+operands copied from pinned host memory and the result copied back inside the
+timed region), ``roofline`` (the dominant kernel's FLOP rate against the FP32
+CUDA-core peak 2 * 128 * SMs * f_SM, at the 2070 MHz maximum SM clock),
+``cpu_baseline`` (the CPU oracle timed on a bounded sample of the same product
+on this host's cores), ``clocks`` (nvidia-smi samples taken during the timed
+region), ``vs_size`` (TFLOP/s of the 512..4096 square sweep) and ``configs``
+(TFLOP/s of the other workload families).
+
+``--impl reference`` times the CPU oracle instead (the only other use of the
+oracle here), on a bounded sample per step, and prints the same JSON line with
+"impl": "reference".  Under torchrun with N > 1 only rank 0 runs it.
+"""
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FP32_LANES_PER_SM = 128          # FP32 FMA units per Blackwell SM
+RECIPE_SM_MAX_MHZ = 2070.0       # maximum SM clock of this GB300 pool
+L2_BYTES = 129e6
+
+
+# ----------------------------------------------------------------- helpers
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources; a stored ncu traffic figure is only used
+    while it matches (otherwise the kernel changed since the capture)."""
+    h = hashlib.sha256()
+    for path in sorted(glob.glob(os.path.join(ROOT, "dense_fp32_matrix_10_gb300", "csrc", "*"))):
+        if path.endswith((".cu", ".cuh", ".h")):
+            h.update(os.path.basename(path).encode())
+            h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel_tag: str):
+    """(bytes per launch, note) from profiles/*.md lines
+    'traffic <kernel_tag> <bytes> <source hash>' if the hash matches."""
+    want = kernel_source_hash()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        for ln in open(path, encoding="utf-8"):
+            m = re.match(r"^traffic\s+(\S+)\s+(\d+)\s+(\w+)\s*$", ln.strip())
+            if m and m.group(1) == kernel_tag:
+                if m.group(3) == want:
+                    return int(m.group(2)), os.path.basename(path)
+                return None, f"stale ({os.path.basename(path)} taken on {m.group(3)}, now {want})"
+    return None, "no capture"
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return json.load(open(path))
+    except (OSError, ValueError):
+        return {}
+
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms in a background process; timestamps let
+    us keep only the samples inside the timed region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.gpu = gpu_id
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", *(["-i", str(self.gpu)] if self.gpu is not None else [])],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) >= 10:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not inside:  # region shorter than one sample: take the nearest ones
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            inside = [p for (_, p) in near]
+            window = "nearest samples (timed region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[2]) for p in inside if num(p[2]) is not None]
+        mx = [num(p[3]) for p in inside if num(p[3]) is not None]
+        pw = [num(p[4]) for p in inside if num(p[4]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_median": statistics.median(pw) if pw else None,
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------- distributed
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, value: float, device=None) -> float:
+        """Maximum of `value` over ranks (the slowest rank sets the time)."""
+        if self.pg is None:
+            return value
+        import torch
+        t = torch.tensor([value], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------- GPU timing
+def time_gemm(sg, torch, case, A, B, C, steps, warmup, algo, stream, record_launches=False):
+    """Warm up, then time `steps` back-to-back calls with CUDA events on
+    `stream`.  Returns (ms per step from the region, mean per-launch ms from
+    per-call events, launches counted)."""
+    for _ in range(warmup):
+        sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=algo, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=algo, stream=stream)
+        ev[i][1].record(stream)
+        if record_launches:
+            launches += sg.sgemm_last_launch_count()
+    end.record(stream)
+    torch.cuda.synchronize()
+    region = start.elapsed_time(end) / steps
+    per_launch = sum(a.elapsed_time(b) for a, b in ev) / steps
+    return region, per_launch, launches
+
+
+def tflops(flops, ms):
+    return flops / (ms * 1e-3) / 1e12
+
+
+def run_ours(args, dist):
+    import torch
+    import dense_fp32_matrix_10_gb300 as sg
+    from dense_fp32_matrix_10_gb300 import workloads as W
+
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    dist.init("nccl")
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    stream = torch.cuda.current_stream(dev)
+
+    case = W.HEADLINE
+    A, B, C = (t.to(dev) for t in W.make_inputs(case))
+    flops = case.flops
+
+    # ---- device-resident timed region
+    uuid = str(getattr(props, "uuid", "") or "")
+    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or None))
+    sampler.start()
+    for _ in range(args.warmup):
+        sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=args.algo, stream=stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ms_region, ms_launch, launches = time_gemm(sg, torch, case, A, B, C, args.steps, 0, args.algo,
+                                               stream, record_launches=True)
+    t_wall1 = time.time()
+    dist.barrier()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    ms_step = dist.max(ms_region, dev)
+    value = flops * dist.world / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI: pinned host operands in, result out
+    hA = torch.empty(A.shape, dtype=torch.float32, pin_memory=True)
+    hB = torch.empty(B.shape, dtype=torch.float32, pin_memory=True)
+    hC = torch.empty(C.shape, dtype=torch.float32, pin_memory=True)
+    hA.copy_(A)
+    hB.copy_(B)
+    e2e_steps = max(3, min(args.steps, 30))
+    for i in range(2 + e2e_steps):
+        if i == 2:
+            torch.cuda.synchronize()
+            dist.barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        A.copy_(hA, non_blocking=True)
+        B.copy_(hB, non_blocking=True)
+        sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=args.algo, stream=stream)
+        hC.copy_(C, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = dist.max(e0.elapsed_time(e1) / e2e_steps, dev)
+    e2e = {"value": round(flops * dist.world / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+           "ms_per_step": round(ms_e2e, 4),
+           "h2d_bytes_per_step": int(A.numel() * 4 + B.numel() * 4),
+           "d2h_bytes_per_step": int(C.numel() * 4)}
+
+    # ---- roofline of the dominant (only) kernel of a step
+    peaks = measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz") or RECIPE_SM_MAX_MHZ)
+    peak = 2 * FP32_LANES_PER_SM * sms * sm_max * 1e6 / 1e12
+    achieved = tflops(flops, ms_launch)
+    algo_used = sg.sgemm_algo_name(sg.sgemm_select_algo(
+        0, 0, case.M, case.N, case.K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
+        case.alpha, case.beta, C.data_ptr(), C.stride(0))) if args.algo == "auto" else args.algo
+    tag = f"{algo_used}_nn_4096"
+    traffic, traffic_src = stored_traffic(tag)
+    roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_basis": f"FP32 FFMA: 2 x {FP32_LANES_PER_SM} lanes x {sms} SMs x {sm_max:.0f} MHz "
+                              "(derived from unit counts and the maximum SM clock)",
+                "kernel": tag, "traffic_source": traffic_src,
+                "algorithmic_flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": int(4 * (case.M * case.K + case.K * case.N + case.M * case.N))}
+    if clocks.get("sm_mhz"):
+        roofline["frac_at_observed_clock"] = round(
+            achieved / (2 * FP32_LANES_PER_SM * sms * clocks["sm_mhz"] * 1e6 / 1e12), 4)
+
+    # ---- TFLOP/s vs size and the other workload families (rank 0 context)
+    vs_size, configs = {}, {}
+    if not args.no_sweep:
+        for sc in W.SWEEP:
+            sA, sB, sC = (t.to(dev) for t in W.make_inputs(sc))
+            n = max(5, min(200, int(2e11 / sc.flops)))
+            r, _, _ = time_gemm(sg, torch, sc, sA, sB, sC, n, 3, args.algo, stream)
+            vs_size[str(sc.M)] = round(tflops(sc.flops, r), 3)
+            del sA, sB, sC
+        for sc in [W.SMALL_256, W.SQUARE_1024, W.NT_4096, *W.RAGGED]:
+            sA, sB, sC0 = (t.to(dev) for t in W.make_inputs(sc))
+            sC = sC0.clone()
+            n = max(5, min(200, int(2e11 / sc.flops)))
+            # beta != 0 updates C in place each call; the values drift but the
+            # work per call is identical.
+            r, _, _ = time_gemm(sg, torch, sc, sA, sB, sC, n, 3, args.algo, stream)
+            configs[sc.name] = round(tflops(sc.flops, r), 3)
+            del sA, sB, sC, sC0
+
+    result = {
+        "metric": "SGEMM FP32 TFLOP/s at 4096^3 (NN) and % of GB300 FP32 peak; TFLOP/s vs size",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded i.i.d. standard normal A, B (torch CPU generator, seed 2)",
+        "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K, "op": "NN",
+                   "alpha": case.alpha, "beta": case.beta, "algo": algo_used,
+                   "l2": "inputs (192 MiB) larger than L2 (129 MB); no flush between steps",
+                   "parallelism": "replicas" if dist.world > 1 else "single GPU"},
+        "pct_of_fp32_peak": round(100 * achieved / peak, 2),
+        "e2e": e2e, "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
+        "vs_size": vs_size, "configs": configs,
+        "device": {"name": props.name, "sms": sms, "cc": f"{props.major}.{props.minor}"},
+    }
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(case, A, B, seconds=args.cpu_seconds)
+    dist.close()
+    return result
+
+
+# ----------------------------------------------------------------- CPU oracle
+def cpu_baseline(case, A=None, B=None, seconds=12.0, rows=None):
+    """The CPU oracle (as it stands) on the first `rows` output rows of the
+    product, all columns, on every core this process may use."""
+    import numpy as np
+    import oracle
+    from dense_fp32_matrix_10_gb300 import workloads as W
+    if A is None:
+        A, B, _ = W.make_inputs(case)
+    An = A.cpu().numpy() if hasattr(A, "cpu") else A
+    Bn = B.cpu().numpy() if hasattr(B, "cpu") else B
+    threads = oracle.default_threads()
+    orc = oracle.default()
+    if rows is None:  # calibrate on a small block, then size the sample to ~`seconds`
+        probe = max(threads, 16)
+        t0 = time.perf_counter()
+        orc.sgemm_f64(case.transA, case.transB, case.alpha, np.ascontiguousarray(An[:probe]), Bn,
+                      threads=threads)
+        dt = max(time.perf_counter() - t0, 1e-3)
+        rows = int(min(case.M, max(threads, probe * seconds / dt)))
+    sub = np.ascontiguousarray(An[:rows])
+    t0 = time.perf_counter()
+    orc.sgemm_f64(case.transA, case.transB, case.alpha, sub, Bn, threads=threads)
+    dt = time.perf_counter() - t0
+    f = 2.0 * rows * case.N * case.K
+    return {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {case.M}x{case.N}x{case.K} NN product, all "
+                      f"{case.N} columns ({f / 1e9:.1f} GFLOP in {dt:.1f} s, FP64 accumulation)",
+            "seconds": round(dt, 2), "rows": rows}
+
+
+def run_reference(args, dist):
+    """The oracle on the host cores as the comparison arm (rank 0 only)."""
+    from dense_fp32_matrix_10_gb300 import workloads as W
+    case = W.HEADLINE
+    A, B, _ = W.make_inputs(case)
+    # each step: a bounded sample of rows, sized so that warmup + steps fit in a few minutes
+    total_budget_s = 150.0
+    per_step = max(0.5, total_budget_s / max(1, args.steps + args.warmup))
+    probe = cpu_baseline(case, A, B, seconds=per_step)
+    rows = probe["rows"]
+    for _ in range(args.warmup):
+        cpu_baseline(case, A, B, rows=rows)
+    times = []
+    for _ in range(args.steps):
+        r = cpu_baseline(case, A, B, rows=rows)
+        times.append(r["seconds"])
+    ms = 1e3 * sum(times) / len(times)
+    f = 2.0 * rows * case.N * case.K
+    value = round(f / (ms * 1e-3) / 1e12, 6)
+    return {
+        "impl": "reference",
+        "metric": "SGEMM FP32 TFLOP/s at 4096^3 (NN) and % of GB300 FP32 peak; TFLOP/s vs size",
+        "value": value, "unit": "TFLOP/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded i.i.d. standard normal A, B (torch CPU generator, seed 2)",
+        "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K, "op": "NN",
+                   "alpha": case.alpha, "beta": case.beta,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": probe["cores"],
+                         "kind": "oracle",
+                         "sample": f"rows 0..{rows - 1} of the {case.M}x{case.N}x{case.K} NN product, "
+                                   f"all {case.N} columns, per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--algo", default="auto")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    dist = Dist()
+    if args.impl == "reference":
+        if dist.rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, dist)), flush=True)
+        return 0
+    result = run_ours(args, dist)
+    if dist.rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

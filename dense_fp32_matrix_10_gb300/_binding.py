@@ -1,0 +1,177 @@
+"""ctypes marshalling for the C ABI of libsgemm_gb300.so (see include/sgemm.h).
+
+Nothing here computes: every function forwards its arguments to the library.
+The library is loaded on first use; if it is absent the call raises.
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(HERE, "libsgemm_gb300.so")
+
+OP_N, OP_T = 0, 1
+ALGO_AUTO, ALGO_SIMT_TMA, ALGO_SIMT_CPASYNC, ALGO_TC_3XTF32, ALGO_NAIVE, ALGO_SMEM_TILED = range(6)
+ALGOS = {"auto": ALGO_AUTO, "simt_tma": ALGO_SIMT_TMA, "simt_cpasync": ALGO_SIMT_CPASYNC,
+         "tc_3xtf32": ALGO_TC_3XTF32, "naive": ALGO_NAIVE, "smem_tiled": ALGO_SMEM_TILED}
+STATUS = {0: "SGEMM_SUCCESS", 1: "SGEMM_ERR_INVALID_VALUE", 2: "SGEMM_ERR_ALIASING",
+          3: "SGEMM_ERR_UNSUPPORTED", 4: "SGEMM_ERR_LAUNCH", 5: "SGEMM_ERR_DEVICE_TIMEOUT"}
+
+_lib = None
+_I64 = ctypes.c_int64
+_VP = ctypes.c_void_p
+
+
+class SgemmError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS.get(self.status, self.status)} "
+                         f"({sgemm_status_string(self.status)})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libsgemm_gb300.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is missing: build it with `python -m dense_fp32_matrix_10_gb300.build` "
+            "(or __graft_entry__.build()); there is no fallback implementation")
+    lib = ctypes.CDLL(_LIB_PATH)
+    gemm_args = [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64, ctypes.c_float, _VP, _I64,
+                 _VP, _I64, ctypes.c_float, _VP, _I64, _VP]
+    lib.sgemm.argtypes = gemm_args
+    lib.sgemm.restype = ctypes.c_int
+    lib.sgemm_ex.argtypes = gemm_args + [ctypes.c_int]
+    lib.sgemm_ex.restype = ctypes.c_int
+    lib.sgemm_select_algo.argtypes = [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64, _VP, _I64,
+                                      _VP, _I64, ctypes.c_float, ctypes.c_float, _VP, _I64]
+    lib.sgemm_select_algo.restype = ctypes.c_int
+    lib.sgemm_last_launch_count.argtypes = []
+    lib.sgemm_last_launch_count.restype = ctypes.c_int
+    lib.sgemm_last_device_status.argtypes = [_VP]
+    lib.sgemm_last_device_status.restype = ctypes.c_int
+    lib.sgemm_set_wait_budget_ns.argtypes = [ctypes.c_uint64]
+    lib.sgemm_set_wait_budget_ns.restype = None
+    lib.sgemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _VP]
+    lib.sgemm_selftest_wait_timeout.restype = ctypes.c_int
+    lib.sgemm_status_string.argtypes = [ctypes.c_int]
+    lib.sgemm_status_string.restype = ctypes.c_char_p
+    lib.sgemm_algo_name.argtypes = [ctypes.c_int]
+    lib.sgemm_algo_name.restype = ctypes.c_char_p
+    lib.sgemm_version.argtypes = []
+    lib.sgemm_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _op(t):
+    if isinstance(t, bool):
+        return int(t)
+    if isinstance(t, str) and len(t) == 1:
+        return ord(t)
+    return int(t)
+
+
+def _check(st, where):
+    if st != 0:
+        raise SgemmError(st, where)
+
+
+def sgemm(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    """C = alpha*op(A)*op(B) + beta*C on `stream`; A, B, C are device pointers (int)."""
+    _check(load_library().sgemm(_op(transA), _op(transB), M, N, K, alpha, A, lda, B, ldb, beta,
+                                C, ldc, stream), "sgemm")
+
+
+def sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None,
+             algo=ALGO_AUTO):
+    """As sgemm with the kernel family forced (``algo`` int or name)."""
+    algo = ALGOS[algo] if isinstance(algo, str) else int(algo)
+    _check(load_library().sgemm_ex(_op(transA), _op(transB), M, N, K, alpha, A, lda, B, ldb,
+                                   beta, C, ldc, stream, algo), "sgemm_ex")
+
+
+def sgemm_select_algo(transA, transB, M, N, K, A, lda, B, ldb, alpha, beta, C, ldc) -> int:
+    return load_library().sgemm_select_algo(_op(transA), _op(transB), M, N, K, A, lda, B, ldb,
+                                            alpha, beta, C, ldc)
+
+
+def sgemm_last_launch_count() -> int:
+    return load_library().sgemm_last_launch_count()
+
+
+def sgemm_last_device_status(stream=None) -> int:
+    """Synchronise `stream`; return (and clear) the device status code."""
+    return load_library().sgemm_last_device_status(stream)
+
+
+def sgemm_set_wait_budget_ns(budget_ns: int):
+    load_library().sgemm_set_wait_budget_ns(int(budget_ns))
+
+
+def sgemm_selftest_wait_timeout(budget_ns: int, stream=None):
+    _check(load_library().sgemm_selftest_wait_timeout(int(budget_ns), stream),
+           "sgemm_selftest_wait_timeout")
+
+
+def sgemm_status_string(status: int) -> str:
+    return load_library().sgemm_status_string(int(status)).decode()
+
+
+def sgemm_algo_name(algo: int) -> str:
+    return load_library().sgemm_algo_name(int(algo)).decode()
+
+
+def sgemm_version() -> str:
+    return load_library().sgemm_version().decode()
+
+
+# ------------------------------------------------------------------ torch
+def _matrix(t, name):
+    """(pointer, rows, cols, ld) of a 2-D float32 CUDA tensor with unit column stride."""
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.dim() != 2:
+        raise TypeError(f"{name} must be a 2-D torch.float32 tensor")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    rows, cols = t.shape
+    if cols > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit column stride (row-major)")
+    ld = t.stride(0) if (rows > 1 or t.stride(0) >= cols) else cols
+    if ld < cols:
+        raise ValueError(f"{name} has overlapping rows")
+    return t.data_ptr(), rows, cols, max(ld, 1)
+
+
+def gemm(A, B, C=None, alpha=1.0, beta=0.0, transA=False, transB=False, algo=ALGO_AUTO,
+         stream=None):
+    """C = alpha * op(A) @ op(B) + beta * C with torch CUDA tensors (row-major views).
+
+    A, B are in stored layout (A is K x M when transA, B is N x K when transB).
+    If C is None a new M x N tensor is allocated (beta must then be 0).
+    Runs on ``stream`` (a torch.cuda.Stream) or the current torch stream.
+    """
+    import torch
+    pa, ra, ca, lda = _matrix(A, "A")
+    pb, rb, cb, ldb = _matrix(B, "B")
+    M, Ka = (ca, ra) if transA else (ra, ca)
+    Kb, N = (cb, rb) if transB else (rb, cb)
+    if Ka != Kb:
+        raise ValueError(f"inner dimensions differ: {Ka} vs {Kb}")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        C = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    pc, rc, cc, ldc = _matrix(C, "C")
+    if (rc, cc) != (M, N):
+        raise ValueError(f"C must be {M} x {N}")
+    s = stream if stream is not None else torch.cuda.current_stream(A.device)
+    with torch.cuda.device(A.device):
+        sgemm_ex(int(bool(transA)), int(bool(transB)), M, N, Ka, float(alpha), pa, lda, pb, ldb,
+                 float(beta), pc, ldc, s.cuda_stream, algo)
+    return C

@@ -1,0 +1,375 @@
+// api.cu -- the C ABI declared in include/sgemm.h: argument checks, the
+// degenerate cases, dispatch by shape / layout / alignment, TMA descriptor
+// encoding and the launches.  Everything here is host code except the device
+// status word.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "sgemm.h"
+
+namespace {
+
+using namespace sg;
+
+// Device status word: a kernel that gives up a bounded wait records
+// SGEMM_ERR_DEVICE_TIMEOUT here (one copy per device that loads the library).
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitBudgetNs = 2000000000ull;  // 2 s
+std::atomic<uint64_t> g_wait_budget_ns{kDefaultWaitBudgetNs};
+thread_local int t_last_launches = 0;
+
+struct DeviceState {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  int sm_count = 0, cc_major = 0, cc_minor = 0;
+  int *status = nullptr;
+  std::once_flag kinfo_once[2][2][2][kNumSimtTiles];
+  cudaError_t kinfo_err[2][2][2][kNumSimtTiles] = {};
+  SimtKernelInfo kinfo[2][2][2][kNumSimtTiles] = {};
+};
+DeviceState g_dev[kMaxDevices];
+
+// Returns the current device's state (initialised once per device) or null.
+DeviceState *device_state(sgemm_status_t *why) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    *why = SGEMM_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  DeviceState &d = g_dev[dev];
+  std::call_once(d.once, [&d, dev]() {
+    cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_device_status);
+    d.err = e;
+    if (e != cudaSuccess) cudaGetLastError();
+  });
+  if (d.err != cudaSuccess) {
+    *why = SGEMM_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  if (d.cc_major != 10 || d.cc_minor != 3) {
+    *why = SGEMM_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  return &d;
+}
+
+const SimtKernelInfo *kernel_info(DeviceState &d, int producer, int ta, int tb, int tile) {
+  std::call_once(d.kinfo_once[producer][ta][tb][tile], [&]() {
+    d.kinfo_err[producer][ta][tb][tile] =
+        simt_entry(producer, ta, tb, tile).info(&d.kinfo[producer][ta][tb][tile]);
+    if (d.kinfo_err[producer][ta][tb][tile] != cudaSuccess) cudaGetLastError();
+  });
+  if (d.kinfo_err[producer][ta][tb][tile] != cudaSuccess) return nullptr;
+  return &d.kinfo[producer][ta][tb][tile];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D FP32 tensor map over a row-major matrix of `rows` x `cols` (row stride
+// ld elements), box box_cols x box_rows, zero fill outside.
+bool encode_tmap(CUtensorMap *m, const float *base, int64_t rows, int64_t cols, int64_t ld,
+                 int box_cols, int box_rows, bool swizzle128) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4u};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int norm_op(int t) {
+  switch (t) {
+    case 0: case 'N': case 'n': return 0;
+    case 1: case 'T': case 't': return 1;
+    default: return -1;
+  }
+}
+
+// [lo, hi) byte range of a stored rows x cols matrix with leading dim ld.
+void byte_range(const void *p, int64_t rows, int64_t cols, int64_t ld, uintptr_t *lo, uintptr_t *hi) {
+  *lo = reinterpret_cast<uintptr_t>(p);
+  *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 4);
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+// Indices are 32-bit inside the kernels; tile origins may run up to one tile
+// past the end of a dimension.
+constexpr int64_t kMaxDim = 0x7fffffff - 1024;
+constexpr int64_t kMaxLd = int64_t(1) << 40;  // keeps every byte offset in int64
+
+struct Args {
+  int ta, tb;
+  int64_t M, N, K;
+  float alpha, beta;
+  const float *A;
+  int64_t lda;
+  const float *B;
+  int64_t ldb;
+  float *C;
+  int64_t ldc;
+};
+
+// Host-side validation shared by sgemm_ex and sgemm_select_algo.
+sgemm_status_t validate(const Args &a, bool c_writable) {
+  if (a.ta < 0 || a.tb < 0) return SGEMM_ERR_INVALID_VALUE;
+  if (a.M < 0 || a.N < 0 || a.K < 0) return SGEMM_ERR_INVALID_VALUE;
+  if (a.M > kMaxDim || a.N > kMaxDim || a.K > kMaxDim) return SGEMM_ERR_INVALID_VALUE;
+  const int64_t a_cols = a.ta ? a.M : a.K, b_cols = a.tb ? a.K : a.N;
+  if (a.lda < (a_cols > 1 ? a_cols : 1) || a.lda > kMaxLd) return SGEMM_ERR_INVALID_VALUE;
+  if (a.ldb < (b_cols > 1 ? b_cols : 1) || a.ldb > kMaxLd) return SGEMM_ERR_INVALID_VALUE;
+  if (a.ldc < (a.N > 1 ? a.N : 1) || a.ldc > kMaxLd) return SGEMM_ERR_INVALID_VALUE;
+  if (a.M == 0 || a.N == 0) return SGEMM_SUCCESS;
+  if (c_writable && a.C == nullptr) return SGEMM_ERR_INVALID_VALUE;
+  const bool need_ab = a.K > 0 && a.alpha != 0.0f;
+  if (need_ab && (a.A == nullptr || a.B == nullptr)) return SGEMM_ERR_INVALID_VALUE;
+  if (need_ab && a.C != nullptr) {
+    uintptr_t c0, c1, x0, x1;
+    byte_range(a.C, a.M, a.N, a.ldc, &c0, &c1);
+    byte_range(a.A, a.ta ? a.K : a.M, a_cols, a.lda, &x0, &x1);
+    if (overlaps(c0, c1, x0, x1)) return SGEMM_ERR_ALIASING;
+    byte_range(a.B, a.tb ? a.N : a.K, b_cols, a.ldb, &x0, &x1);
+    if (overlaps(c0, c1, x0, x1)) return SGEMM_ERR_ALIASING;
+  }
+  return SGEMM_SUCCESS;
+}
+
+bool tma_eligible(const Args &a) {
+  return (reinterpret_cast<uintptr_t>(a.A) % 16 == 0) && (reinterpret_cast<uintptr_t>(a.B) % 16 == 0) &&
+         (a.lda % 4 == 0) && (a.ldb % 4 == 0);
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Tile choice for the CUDA-core kernels: the 128 x 128 tile when it fills the
+// SMs, else the 128 x 64 tile (two CTAs per SM) to raise the CTA count.
+int pick_simt_tile(const Args &a, int sm_count) {
+  const int64_t t128 = cdiv(a.M, 128) * cdiv(a.N, 128);
+  if (a.N <= 64) return kTile128x64;
+  return (t128 >= sm_count) ? kTile128x128 : kTile128x64;
+}
+
+sgemm_algo_t auto_algo(const Args &a) {
+  return tma_eligible(a) ? SGEMM_ALGO_SIMT_TMA : SGEMM_ALGO_SIMT_CPASYNC;
+}
+
+sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_t stream) {
+  const int tile = pick_simt_tile(a, d.sm_count);
+  const SimtKernelInfo *ki = kernel_info(d, producer, a.ta, a.tb, tile);
+  if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_LAUNCH;
+
+  SimtParams p;
+  p.A = a.A;
+  p.B = a.B;
+  p.C = a.C;
+  p.lda = a.lda;
+  p.ldb = a.ldb;
+  p.ldc = a.ldc;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.alpha = a.alpha;
+  p.beta = a.beta;
+  p.tiles_m = static_cast<int>(cdiv(a.M, ki->bm));
+  p.tiles_n = static_cast<int>(cdiv(a.N, ki->bn));
+  p.k_tiles = static_cast<int>(cdiv(a.K, 32));
+  const int64_t num_tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  if (num_tiles > kMaxDim) return SGEMM_ERR_UNSUPPORTED;
+  p.num_tiles = static_cast<int>(num_tiles);
+  p.group_m = 8;
+  p.c_vec4 = (a.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
+  p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
+  p.status = d.status;
+
+  CUtensorMap tmA, tmB;
+  std::memset(&tmA, 0, sizeof(tmA));
+  std::memset(&tmB, 0, sizeof(tmB));
+  if (producer == kTma) {
+    // op(A): K-major when stored M x K, MN-major when stored K x M.
+    const bool okA = a.ta == 0 ? encode_tmap(&tmA, a.A, a.M, a.K, a.lda, 32, ki->bm, true)
+                               : encode_tmap(&tmA, a.A, a.K, a.M, a.lda, ki->bm, 32, false);
+    const bool okB = a.tb == 0 ? encode_tmap(&tmB, a.B, a.K, a.N, a.ldb, ki->bn, 32, false)
+                               : encode_tmap(&tmB, a.B, a.N, a.K, a.ldb, 32, ki->bn, true);
+    if (!okA || !okB) return SGEMM_ERR_LAUNCH;
+  }
+  const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
+  const int grid = static_cast<int>(num_tiles < slots ? num_tiles : slots);
+  cudaError_t e = simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, grid, stream);
+  if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  t_last_launches = 1;
+  return SGEMM_SUCCESS;
+}
+
+}  // namespace
+
+namespace sg {
+SimtEntry simt_entry_kTma_0(int transB, int tile);
+SimtEntry simt_entry_kTma_1(int transB, int tile);
+SimtEntry simt_entry_kCpAsync_0(int transB, int tile);
+SimtEntry simt_entry_kCpAsync_1(int transB, int tile);
+
+SimtEntry simt_entry(int producer, int transA, int transB, int tile) {
+  if (producer == kTma) return transA ? simt_entry_kTma_1(transB, tile) : simt_entry_kTma_0(transB, tile);
+  return transA ? simt_entry_kCpAsync_1(transB, tile) : simt_entry_kCpAsync_0(transB, tile);
+}
+}  // namespace sg
+
+extern "C" {
+
+sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                        const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
+                        float *C, int64_t ldc, void *stream, sgemm_algo_t algo) {
+  Args a{norm_op(transA), norm_op(transB), M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
+  if (static_cast<int>(algo) < SGEMM_ALGO_AUTO || static_cast<int>(algo) > SGEMM_ALGO_SMEM_TILED)
+    return SGEMM_ERR_INVALID_VALUE;
+  sgemm_status_t st = validate(a, true);
+  if (st != SGEMM_SUCCESS) return st;
+  t_last_launches = 0;
+  if (M == 0 || N == 0) return SGEMM_SUCCESS;
+
+  sgemm_status_t why = SGEMM_SUCCESS;
+  DeviceState *d = device_state(&why);
+  if (!d) return why;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  if (K == 0 || alpha == 0.0f) {
+    if (launch_scale_c(C, ldc, static_cast<int>(M), static_cast<int>(N), beta, s) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+    t_last_launches = 1;
+    return SGEMM_SUCCESS;
+  }
+
+  if (algo == SGEMM_ALGO_AUTO) algo = auto_algo(a);
+  switch (algo) {
+    case SGEMM_ALGO_SIMT_TMA:
+      if (!tma_eligible(a)) return SGEMM_ERR_UNSUPPORTED;
+      return run_simt(a, *d, kTma, s);
+    case SGEMM_ALGO_SIMT_CPASYNC:
+      return run_simt(a, *d, kCpAsync, s);
+    case SGEMM_ALGO_NAIVE:
+    case SGEMM_ALGO_SMEM_TILED: {
+      PlainParams p{A, B, C, lda, ldb, ldc, static_cast<int>(M), static_cast<int>(N),
+                    static_cast<int>(K), a.ta, a.tb, alpha, beta};
+      cudaError_t e = algo == SGEMM_ALGO_NAIVE ? launch_naive(p, s) : launch_smem_tiled(p, s);
+      if (e == cudaErrorInvalidValue) return SGEMM_ERR_UNSUPPORTED;
+      if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
+      t_last_launches = 1;
+      return SGEMM_SUCCESS;
+    }
+    case SGEMM_ALGO_TC_3XTF32:
+    default:
+      return SGEMM_ERR_UNSUPPORTED;
+  }
+}
+
+sgemm_status_t sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                     const float *A, int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                     int64_t ldc, void *stream) {
+  return sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream,
+                  SGEMM_ALGO_AUTO);
+}
+
+int sgemm_select_algo(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A,
+                      int64_t lda, const float *B, int64_t ldb, float alpha, float beta,
+                      const float *C, int64_t ldc) {
+  Args a{norm_op(transA), norm_op(transB), M, N, K, alpha, beta, A, lda, B, ldb,
+         const_cast<float *>(C), ldc};
+  if (validate(a, false) != SGEMM_SUCCESS) return -1;
+  return static_cast<int>(auto_algo(a));
+}
+
+int sgemm_last_launch_count(void) { return t_last_launches; }
+
+sgemm_status_t sgemm_last_device_status(void *stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  sgemm_status_t why = SGEMM_SUCCESS;
+  DeviceState *d = device_state(&why);
+  if (!d) return why;
+  int v = 0;
+  if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return SGEMM_ERR_LAUNCH;
+  }
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      return SGEMM_ERR_LAUNCH;
+    }
+  }
+  return v == 0 ? SGEMM_SUCCESS : SGEMM_ERR_DEVICE_TIMEOUT;
+}
+
+void sgemm_set_wait_budget_ns(uint64_t budget_ns) {
+  g_wait_budget_ns.store(budget_ns ? budget_ns : kDefaultWaitBudgetNs, std::memory_order_relaxed);
+}
+
+sgemm_status_t sgemm_selftest_wait_timeout(uint64_t budget_ns, void *stream) {
+  sgemm_status_t why = SGEMM_SUCCESS;
+  DeviceState *d = device_state(&why);
+  if (!d) return why;
+  if (launch_wait_selftest(budget_ns, d->status, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
+  return SGEMM_SUCCESS;
+}
+
+const char *sgemm_status_string(sgemm_status_t status) {
+  switch (status) {
+    case SGEMM_SUCCESS: return "success";
+    case SGEMM_ERR_INVALID_VALUE: return "invalid value";
+    case SGEMM_ERR_ALIASING: return "C overlaps A or B";
+    case SGEMM_ERR_UNSUPPORTED: return "unsupported device or arguments";
+    case SGEMM_ERR_LAUNCH: return "CUDA launch failure";
+    case SGEMM_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+const char *sgemm_algo_name(sgemm_algo_t algo) {
+  switch (algo) {
+    case SGEMM_ALGO_AUTO: return "auto";
+    case SGEMM_ALGO_SIMT_TMA: return "simt_tma";
+    case SGEMM_ALGO_SIMT_CPASYNC: return "simt_cpasync";
+    case SGEMM_ALGO_TC_3XTF32: return "tc_3xtf32";
+    case SGEMM_ALGO_NAIVE: return "naive";
+    case SGEMM_ALGO_SMEM_TILED: return "smem_tiled";
+    default: return "unknown";
+  }
+}
+
+const char *sgemm_version(void) { return "0.1.0"; }
+
+}  // extern "C"

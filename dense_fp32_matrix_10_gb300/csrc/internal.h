@@ -1,0 +1,55 @@
+// internal.h -- declarations shared by the library's translation units
+// (host side).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "simt_gemm.cuh"
+
+namespace sg {
+
+// Tile configurations of the CUDA-core kernels (8 x 8 outputs per thread,
+// 32 x 64 per warp).
+enum SimtTile : int {
+  kTile128x128 = 0,  // 4 x 2 math warps
+  kTile128x64 = 1,   // 4 x 1 math warps
+  kNumSimtTiles = 2
+};
+
+struct SimtKernelInfo {
+  int bm, bn, threads, smem_bytes, ctas_per_sm;
+};
+
+// Launches one instantiation; grid = number of persistent CTAs.
+using SimtLaunchFn = cudaError_t (*)(const SimtParams &, const CUtensorMap *, const CUtensorMap *,
+                                     int grid, cudaStream_t);
+// Sets the kernel's shared-memory attribute on the current device (once) and
+// reports its shape and occupancy.
+using SimtInfoFn = cudaError_t (*)(SimtKernelInfo *);
+
+struct SimtEntry {
+  SimtLaunchFn launch;
+  SimtInfoFn info;
+};
+
+// [producer][transA][transB][tile]
+SimtEntry simt_entry(int producer, int transA, int transB, int tile);
+
+// Context kernels and helpers (context.cu).
+struct PlainParams {
+  const float *A;
+  const float *B;
+  float *C;
+  int64_t lda, ldb, ldc;
+  int M, N, K;
+  int transA, transB;
+  float alpha, beta;
+};
+cudaError_t launch_naive(const PlainParams &p, cudaStream_t s);
+cudaError_t launch_smem_tiled(const PlainParams &p, cudaStream_t s);
+cudaError_t launch_scale_c(float *C, int64_t ldc, int M, int N, float beta, cudaStream_t s);
+cudaError_t launch_wait_selftest(uint64_t budget_ns, int *status, cudaStream_t s);
+
+}  // namespace sg

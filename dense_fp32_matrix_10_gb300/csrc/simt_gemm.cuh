@@ -1,0 +1,444 @@
+// simt_gemm.cuh -- CUDA-core (FFMA) single-precision GEMM for sm_103a.
+//
+// C = alpha * op(A) * op(B) + beta * C, row-major FP32.
+//
+// Structure (one persistent CTA per SM slot, warp-specialised):
+//
+//   * a PRODUCER role fills a ring of STAGES shared-memory stages, each holding
+//     one BK = 32 slice of the op(A) block tile (BM x 32) and of the op(B) block
+//     tile (32 x BN).  Two producers exist:
+//       - kTma: one elected thread issues 2-D bulk tensor copies (TMA); the
+//         hardware zero-fills everything outside the matrix, and the copy
+//         completion is counted in bytes on the stage's "full" mbarrier;
+//       - kCpAsync: four warps issue 4-byte cp.async copies (zero-filled
+//         outside the matrix) and arrive on the "full" mbarrier when their
+//         copies land.  This one takes any alignment and leading dimension.
+//   * WARPS_M x WARPS_N MATH warps, each owning a 32 x 64 warp tile, each
+//     thread an 8 x 8 register tile of FP32 accumulators.  Per k they read 8
+//     op(A) and 8 op(B) values from shared memory as float4s and issue 64 FFMA.
+//     A warp releases a stage by arriving on its "empty" mbarrier.
+//   * The epilogue writes alpha * acc + beta * C straight from registers,
+//     float4-wide where the row is aligned, with row/column predicates on the
+//     ragged edges; C is not read when beta == 0.
+//
+// This is the three-level tiling (grid -> block -> warp -> thread registers)
+// and shared-memory reuse of "GPU矩阵乘法优化：共享内存Tiling技术实战" (sections 3.1,
+// 7.3) and of the 2D block tiling (b_m, b_n, b_k) of the cloud.baidu.com
+// article 9456745, with the register tiling and float4 loads of
+// "CUDA矩阵乘法性能优化实战：从朴素内核到寄存器分块与Nsight剖析" (sections 5.2, 5.3)
+// taken to 8 x 8.  Its "prefetch the next tile while computing this one" idea
+// (the double buffering of the Tiling article, section 3.2) becomes a
+// STAGES-deep mbarrier ring filled by a dedicated producer; the +1 padding that
+// those pages use against bank conflicts (Tiling article 4.1; optimisation
+// article 3.3) becomes the TMA 128-byte swizzle on the k-contiguous tiles.
+//
+// Shared-memory layouts of one stage (all FP32):
+//   op(A) tile, A stored M x K (k contiguous, "K-major"):  [BM rows][32 k],
+//       128 B per row, 16-byte chunk j of row m stored at chunk j ^ (m & 7).
+//   op(A) tile, A stored K x M (m contiguous, "MN-major"): [32 k][BM m], dense.
+//   op(B) tile, B stored K x N (n contiguous, "MN-major"): [32 k][BN n], dense.
+//   op(B) tile, B stored N x K (k contiguous, "K-major"):  [BN rows][32 k],
+//       same swizzle as above.
+//
+// Thread -> output mapping inside a 32 x 64 warp tile (lane = 8 * tm + tn,
+// tm in 0..3, tn in 0..7), chosen so that every shared-memory read of a warp
+// touches each bank at most once:
+//   rows: MN-major A: {4tm .. 4tm+3, 16+4tm .. 16+4tm+3};  K-major A: tm + 4r.
+//   cols: MN-major B: {4tn .. 4tn+3, 32+4tn .. 32+4tn+3};  K-major B: tn + 8c.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace sg {
+
+enum Producer : int { kTma = 0, kCpAsync = 1 };
+
+struct SimtParams {
+  const float *A;
+  const float *B;
+  float *C;
+  int64_t lda, ldb, ldc;
+  int M, N, K;
+  float alpha, beta;
+  int tiles_m, tiles_n, k_tiles, num_tiles;
+  int group_m;           // tile-rows per raster group (L2 reuse)
+  int c_vec4;            // ldc % 4 == 0 and C 16-byte aligned
+  uint64_t wait_budget_ns;
+  int *status;
+};
+
+template <int WARPS_M_, int WARPS_N_, bool A_KMAJOR_, bool B_KMAJOR_, int STAGES_, int PRODUCER_>
+struct SimtConfig {
+  static constexpr int WARPS_M = WARPS_M_;
+  static constexpr int WARPS_N = WARPS_N_;
+  static constexpr bool A_KMAJOR = A_KMAJOR_;
+  static constexpr bool B_KMAJOR = B_KMAJOR_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int PRODUCER = PRODUCER_;
+  static constexpr int BM = 32 * WARPS_M;
+  static constexpr int BN = 64 * WARPS_N;
+  static constexpr int BK = 32;
+  static constexpr int MATH_WARPS = WARPS_M * WARPS_N;
+  static constexpr int MATH_THREADS = 32 * MATH_WARPS;
+  // The producer role is a whole warpgroup so that setmaxnreg can hand its
+  // registers to the math warpgroups (register files are per SM
+  // sub-partition: a 9-warp CTA would cap every thread at 168 registers).
+  static constexpr int PRODUCER_WARPS = 4;
+  static constexpr int PRODUCER_THREADS = 32 * PRODUCER_WARPS;
+  static constexpr int THREADS = MATH_THREADS + PRODUCER_THREADS;
+  static constexpr int MIN_CTAS = (MATH_WARPS == 8) ? 1 : 2;  // CTAs per SM
+  // Per-thread registers after the split; launch budget is
+  // THREADS * (65536 / (THREADS * MIN_CTAS)) rounded down to 8.
+  static constexpr int PRODUCER_REGS = 40;
+  static constexpr int MATH_REGS = (MATH_WARPS == 8) ? 232 : 216;
+  static_assert(MATH_WARPS % 4 == 0, "math role must be whole warpgroups");
+  static_assert(PRODUCER_THREADS * PRODUCER_REGS + MATH_THREADS * MATH_REGS <=
+                    THREADS * ((65536 / (THREADS * MIN_CTAS)) & ~7),
+                "register split exceeds the launch budget");
+  static constexpr int A_STAGE_BYTES = BM * BK * 4;
+  static constexpr int B_STAGE_BYTES = BN * BK * 4;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  // stages first (1024-byte aligned for the 128 B swizzle), barriers after
+  static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFFSET + 2 * STAGES * 8 + 1024;  // + alignment slack
+  static_assert(BM <= 256 && BN <= 256, "TMA box extent is at most 256");
+  static_assert(A_STAGE_BYTES % 1024 == 0 && B_STAGE_BYTES % 1024 == 0, "swizzle atom alignment");
+};
+
+// Linear tile index -> (tile_m, tile_n), grouped so that consecutive tiles
+// share op(A) row-blocks in L2.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m,
+                                            int &tm, int &tn) {
+  const int per_group = group_m * tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * group_m;
+  const int rows_here = min(tiles_m - first_m, group_m);
+  const int r = t - g * per_group;
+  tm = first_m + r % rows_here;
+  tn = r / rows_here;
+}
+
+// Byte offset of element (row, k) in a [rows][32] swizzled tile.
+__device__ __forceinline__ uint32_t kmajor_offset(int row, int k) {
+  return static_cast<uint32_t>(row) * 128u +
+         ((static_cast<uint32_t>((k >> 2) ^ (row & 7))) << 4) + (static_cast<uint32_t>(k & 3) << 2);
+}
+
+// ------------------------------------------------------------------ producer
+template <class Cfg>
+__device__ __forceinline__ void produce_tma(const SimtParams &p, const CUtensorMap *tmA,
+                                            const CUtensorMap *tmB, uint32_t smem_base,
+                                            uint32_t full0, uint32_t empty0, bool &ok) {
+  uint32_t it = 0;
+  for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+    int tm, tn;
+    tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    const int m0 = tm * Cfg::BM, n0 = tn * Cfg::BN;
+    for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+      const uint32_t s = it % Cfg::STAGES;
+      const uint32_t round = it / Cfg::STAGES;
+      if (round > 0 &&
+          !wait_parity_bounded(empty0 + 8 * s, (round - 1) & 1, p.wait_budget_ns, p.status)) {
+        ok = false;
+        break;
+      }
+      const uint32_t full = full0 + 8 * s;
+      const uint32_t a_dst = smem_base + s * Cfg::STAGE_BYTES;
+      const uint32_t b_dst = a_dst + Cfg::A_STAGE_BYTES;
+      mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
+      const int k0 = kt * Cfg::BK;
+      if (Cfg::A_KMAJOR)
+        tma_load_2d(a_dst, tmA, full, k0, m0);
+      else
+        tma_load_2d(a_dst, tmA, full, m0, k0);
+      if (Cfg::B_KMAJOR)
+        tma_load_2d(b_dst, tmB, full, k0, n0);
+      else
+        tma_load_2d(b_dst, tmB, full, n0, k0);
+    }
+  }
+  if (!ok) {
+    // Let the copies already issued land before the CTA can end.
+    const uint32_t issued = it;
+    const uint32_t first = issued > Cfg::STAGES ? issued - Cfg::STAGES : 0;
+    for (uint32_t j = first; j < issued; ++j)
+      wait_parity_bounded(full0 + 8 * (j % Cfg::STAGES), (j / Cfg::STAGES) & 1,
+                          p.wait_budget_ns, nullptr);
+  }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t smem_base,
+                                                uint32_t full0, uint32_t empty0, int ptid,
+                                                bool &ok) {
+  constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
+  constexpr int PT = Cfg::PRODUCER_THREADS;
+  uint32_t it = 0;
+  for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+    int tm, tn;
+    tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    const int m0 = tm * BM, n0 = tn * BN;
+    for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+      const uint32_t s = it % Cfg::STAGES;
+      const uint32_t round = it / Cfg::STAGES;
+      if (round > 0 &&
+          !wait_parity_bounded(empty0 + 8 * s, (round - 1) & 1, p.wait_budget_ns, p.status)) {
+        ok = false;
+        break;
+      }
+      const uint32_t a_dst = smem_base + s * Cfg::STAGE_BYTES;
+      const uint32_t b_dst = a_dst + Cfg::A_STAGE_BYTES;
+      const int k0 = kt * BK;
+      // op(A) tile: BM x 32 elements
+#pragma unroll 4
+      for (int e = ptid; e < BM * BK; e += PT) {
+        int m, k;
+        uint32_t off;
+        if (Cfg::A_KMAJOR) {  // consecutive threads walk k inside one row
+          m = e / BK;
+          k = e % BK;
+          off = kmajor_offset(m, k);
+        } else {  // consecutive threads walk m inside one k-row
+          k = e / BM;
+          m = e % BM;
+          off = static_cast<uint32_t>(k * BM + m) * 4u;
+        }
+        const int gm = m0 + m, gk = k0 + k;
+        const bool in = gm < p.M && gk < p.K;
+        const float *src = p.A;
+        if (in) src = Cfg::A_KMAJOR ? p.A + static_cast<int64_t>(gm) * p.lda + gk
+                                    : p.A + static_cast<int64_t>(gk) * p.lda + gm;
+        cp_async_4(a_dst + off, src, in ? 4u : 0u);
+      }
+      // op(B) tile: 32 x BN elements
+#pragma unroll 4
+      for (int e = ptid; e < BN * BK; e += PT) {
+        int n, k;
+        uint32_t off;
+        if (Cfg::B_KMAJOR) {
+          n = e / BK;
+          k = e % BK;
+          off = kmajor_offset(n, k);
+        } else {
+          k = e / BN;
+          n = e % BN;
+          off = static_cast<uint32_t>(k * BN + n) * 4u;
+        }
+        const int gn = n0 + n, gk = k0 + k;
+        const bool in = gn < p.N && gk < p.K;
+        const float *src = p.B;
+        if (in) src = Cfg::B_KMAJOR ? p.B + static_cast<int64_t>(gn) * p.ldb + gk
+                                    : p.B + static_cast<int64_t>(gk) * p.ldb + gn;
+        cp_async_4(b_dst + off, src, in ? 4u : 0u);
+      }
+      cp_async_mbar_arrive_noinc(full0 + 8 * s);
+    }
+  }
+  // Do not leave while this thread's copies are still in flight.
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ consumer
+template <class Cfg>
+__device__ __forceinline__ int thread_row(int tm, int r) {
+  return Cfg::A_KMAJOR ? (tm + 4 * r) : ((r < 4) ? (4 * tm + r) : (16 + 4 * tm + (r - 4)));
+}
+template <class Cfg>
+__device__ __forceinline__ int thread_col(int tn, int c) {
+  return Cfg::B_KMAJOR ? (tn + 8 * c) : ((c < 4) ? (4 * tn + c) : (32 + 4 * tn + (c - 4)));
+}
+
+template <class Cfg>
+__device__ __forceinline__ void mma_stage(float (&acc)[8][8], const char *a_stage,
+                                          const char *b_stage, int wm, int wn, int tm, int tn) {
+  constexpr int BM = Cfg::BM, BN = Cfg::BN;
+  // Per-thread base pointers inside the stage.
+  const char *a_base;
+  const char *b_base;
+  if (Cfg::A_KMAJOR)
+    a_base = a_stage + (wm * 32 + tm) * 128;  // row tm + 4r -> + r * 512
+  else
+    a_base = a_stage + (wm * 32 + 4 * tm) * 4;  // + k * BM * 4, + 64 for rows 16..
+  if (Cfg::B_KMAJOR)
+    b_base = b_stage + (wn * 64 + tn) * 128;  // row tn + 8c -> + c * 1024
+  else
+    b_base = b_stage + (wn * 64 + 4 * tn) * 4;  // + k * BN * 4, + 128 for cols 32..
+
+#pragma unroll
+  for (int kc = 0; kc < 8; ++kc) {  // 4 k per chunk
+    float a[8][4];  // a[r][kk]
+    float b[4][8];  // b[kk][c]
+    if (Cfg::A_KMAJOR) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        // row = wm*32 + tm + 4r: (row & 7) = tm | 4*(r&1)
+        const int sw = (kc ^ (tm | ((r & 1) << 2))) << 4;
+        const float4 v = *reinterpret_cast<const float4 *>(a_base + r * 512 + sw);
+        a[r][0] = v.x; a[r][1] = v.y; a[r][2] = v.z; a[r][3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const char *row = a_base + (kc * 4 + kk) * BM * 4;
+        const float4 v0 = *reinterpret_cast<const float4 *>(row);
+        const float4 v1 = *reinterpret_cast<const float4 *>(row + 64);
+        a[0][kk] = v0.x; a[1][kk] = v0.y; a[2][kk] = v0.z; a[3][kk] = v0.w;
+        a[4][kk] = v1.x; a[5][kk] = v1.y; a[6][kk] = v1.z; a[7][kk] = v1.w;
+      }
+    }
+    if (Cfg::B_KMAJOR) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        // row = wn*64 + tn + 8c: (row & 7) = tn
+        const int sw = (kc ^ tn) << 4;
+        const float4 v = *reinterpret_cast<const float4 *>(b_base + c * 1024 + sw);
+        b[0][c] = v.x; b[1][c] = v.y; b[2][c] = v.z; b[3][c] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const char *row = b_base + (kc * 4 + kk) * BN * 4;
+        const float4 v0 = *reinterpret_cast<const float4 *>(row);
+        const float4 v1 = *reinterpret_cast<const float4 *>(row + 128);
+        b[kk][0] = v0.x; b[kk][1] = v0.y; b[kk][2] = v0.z; b[kk][3] = v0.w;
+        b[kk][4] = v1.x; b[kk][5] = v1.y; b[kk][6] = v1.z; b[kk][7] = v1.w;
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(a[r][kk], b[kk][c], acc[r][c]);
+  }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void epilogue(const SimtParams &p, const float (&acc)[8][8], int m0,
+                                         int n0, int wm, int wn, int tm, int tn) {
+  const bool read_c = p.beta != 0.0f;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int m = m0 + wm * 32 + thread_row<Cfg>(tm, r);
+    if (m >= p.M) continue;
+    float *crow = p.C + static_cast<int64_t>(m) * p.ldc;
+    if (!Cfg::B_KMAJOR) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int n = n0 + wn * 64 + h * 32 + 4 * tn;
+        if (p.c_vec4 && n + 3 < p.N) {
+          float4 v;
+          v.x = acc[r][4 * h + 0] * p.alpha;
+          v.y = acc[r][4 * h + 1] * p.alpha;
+          v.z = acc[r][4 * h + 2] * p.alpha;
+          v.w = acc[r][4 * h + 3] * p.alpha;
+          if (read_c) {
+            const float4 c = *reinterpret_cast<const float4 *>(crow + n);
+            v.x = fmaf(p.alpha, acc[r][4 * h + 0], p.beta * c.x);
+            v.y = fmaf(p.alpha, acc[r][4 * h + 1], p.beta * c.y);
+            v.z = fmaf(p.alpha, acc[r][4 * h + 2], p.beta * c.z);
+            v.w = fmaf(p.alpha, acc[r][4 * h + 3], p.beta * c.w);
+          }
+          *reinterpret_cast<float4 *>(crow + n) = v;
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (n + q < p.N) {
+              const float a = acc[r][4 * h + q];
+              crow[n + q] = read_c ? fmaf(p.alpha, a, p.beta * crow[n + q]) : p.alpha * a;
+            }
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int n = n0 + wn * 64 + thread_col<Cfg>(tn, c);
+        if (n < p.N) {
+          const float a = acc[r][c];
+          crow[n] = read_c ? fmaf(p.alpha, a, p.beta * crow[n]) : p.alpha * a;
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
+    simt_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const SimtParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte alignment of the stage ring (required by the 128 B swizzle).
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t full0 = smem_base + Cfg::BAR_OFFSET;
+  const uint32_t empty0 = full0 + 8 * Cfg::STAGES;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(full0 + 8 * s, Cfg::PRODUCER == kTma ? 1 : Cfg::PRODUCER_THREADS);
+      mbar_init(empty0 + 8 * s, Cfg::MATH_WARPS);
+    }
+    fence_mbar_init();
+  }
+  if (Cfg::PRODUCER == kTma && threadIdx.x == Cfg::MATH_THREADS) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  __syncthreads();
+
+  bool ok = true;
+  if (warp >= Cfg::MATH_WARPS) {
+    // ---------------- producer role
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::PRODUCER_REGS));
+    if (Cfg::PRODUCER == kTma) {
+      if (threadIdx.x == Cfg::MATH_THREADS)
+        produce_tma<Cfg>(p, &tmA, &tmB, smem_base, full0, empty0, ok);
+    } else {
+      produce_cpasync<Cfg>(p, smem_base, full0, empty0, threadIdx.x - Cfg::MATH_THREADS, ok);
+    }
+    return;
+  }
+
+  // ---------------- math role
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::MATH_REGS));
+  const int wm = warp / Cfg::WARPS_N;
+  const int wn = warp % Cfg::WARPS_N;
+  const int tm = lane >> 3;
+  const int tn = lane & 7;
+  uint32_t it = 0;
+  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    int tile_m, tile_n;
+    tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tile_m, tile_n);
+    float acc[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[r][c] = 0.0f;
+
+    for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+      const uint32_t s = it % Cfg::STAGES;
+      const uint32_t round = it / Cfg::STAGES;
+      if (!wait_parity_bounded(full0 + 8 * s, round & 1, p.wait_budget_ns, p.status)) {
+        ok = false;
+        break;
+      }
+      const char *a_stage = reinterpret_cast<const char *>(smem) + s * Cfg::STAGE_BYTES;
+      mma_stage<Cfg>(acc, a_stage, a_stage + Cfg::A_STAGE_BYTES, wm, wn, tm, tn);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
+    if (!ok) break;
+    epilogue<Cfg>(p, acc, tile_m * Cfg::BM, tile_n * Cfg::BN, wm, wn, tm, tn);
+  }
+}
+
+}  // namespace sg

@@ -1,0 +1,74 @@
+// simt_instances.cuh -- defines launch/info wrappers for one family of
+// instantiations of the CUDA-core kernel.  Included by the simt_*.cu units,
+// each of which fixes PRODUCER and TRANS_A to keep translation units small
+// (they compile in parallel).
+#pragma once
+
+#include "internal.h"
+
+namespace sg {
+
+template <class Cfg>
+cudaError_t simt_launch(const SimtParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
+                        int grid, cudaStream_t stream) {
+  simt_gemm_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(*tmA, *tmB, p);
+  return cudaGetLastError();
+}
+
+template <class Cfg>
+cudaError_t simt_info(SimtKernelInfo *info) {
+  cudaError_t e = cudaFuncSetAttribute(simt_gemm_kernel<Cfg>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  // setmaxnreg.inc waits until the CTA's launch registers can cover the new
+  // split; refuse to launch a build whose launch register count is too small.
+  cudaFuncAttributes attr;
+  e = cudaFuncGetAttributes(&attr, simt_gemm_kernel<Cfg>);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs * Cfg::THREADS <
+      Cfg::PRODUCER_THREADS * Cfg::PRODUCER_REGS + Cfg::MATH_THREADS * Cfg::MATH_REGS)
+    return cudaErrorInvalidConfiguration;
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, simt_gemm_kernel<Cfg>, Cfg::THREADS,
+                                                    Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  info->bm = Cfg::BM;
+  info->bn = Cfg::BN;
+  info->threads = Cfg::THREADS;
+  info->smem_bytes = Cfg::SMEM_BYTES;
+  info->ctas_per_sm = occ;
+  return cudaSuccess;
+}
+
+template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR, int TILE>
+struct SimtPick;
+template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR>
+struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x128> {
+  using Cfg = SimtConfig<4, 2, A_KMAJOR, B_KMAJOR, 4, PRODUCER>;
+};
+template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR>
+struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x64> {
+  using Cfg = SimtConfig<4, 1, A_KMAJOR, B_KMAJOR, 4, PRODUCER>;
+};
+
+template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR, int TILE>
+SimtEntry simt_make_entry() {
+  using Cfg = typename SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, TILE>::Cfg;
+  return SimtEntry{&simt_launch<Cfg>, &simt_info<Cfg>};
+}
+
+// A stored M x K (transA = N) is the k-contiguous ("K-major") layout; B stored
+// N x K (transB = T) likewise.
+#define SG_DEFINE_SIMT_FAMILY(PROD, TA)                                                  \
+  SimtEntry simt_entry_##PROD##_##TA(int transB, int tile) {                             \
+    constexpr bool AK = (TA == 0);                                                       \
+    if (transB == 0) {                                                                   \
+      return tile == kTile128x128 ? simt_make_entry<PROD, AK, false, kTile128x128>()     \
+                                  : simt_make_entry<PROD, AK, false, kTile128x64>();      \
+    }                                                                                    \
+    return tile == kTile128x128 ? simt_make_entry<PROD, AK, true, kTile128x128>()        \
+                                : simt_make_entry<PROD, AK, true, kTile128x64>();         \
+  }
+
+}  // namespace sg

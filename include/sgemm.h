@@ -1,0 +1,177 @@
+/*
+ * sgemm.h -- C ABI of a single-precision GEMM library for one NVIDIA GB300
+ * (compute capability 10.3, sm_103a).
+ *
+ * One call computes, on the caller's CUDA stream,
+ *
+ *     C = alpha * op(A) * op(B) + beta * C          op(X) = X or X^T
+ *
+ * for FP32 row-major matrices.  This is the product C(MxN) = A(MxK) x B(KxN) of
+ * "CUDA矩阵乘法性能优化实战：从朴素内核到寄存器分块与Nsight剖析" (section 1.1, and
+ * the matmul_naive/matmul_tiled kernels of sections 2.1 and 3.2, whose
+ * signature matmul(A, B, C, M, N, K) this generalises), in the
+ * D = alpha * A * B^T + beta * C form of the cloud.baidu.com article 9456745
+ * (naive vs 2D block-tiled shared-memory matmul, naive-implementation
+ * paragraph), with both operands optionally transposed.
+ *
+ * Layout (row-major throughout; every leading dimension counts elements):
+ *   op(A) is M x K.  transA = N: A is stored M x K, lda >= max(1, K).
+ *                    transA = T: A is stored K x M, lda >= max(1, M).
+ *   op(B) is K x N.  transB = N: B is stored K x N, ldb >= max(1, N).
+ *                    transB = T: B is stored N x K, ldb >= max(1, K).
+ *   C is M x N, ldc >= max(1, N).
+ * transA / transB accept 0 / 1 (SGEMM_OP_N / SGEMM_OP_T) or the characters
+ * 'N', 'n', 'T', 't'.
+ *
+ * Pointers: A, B and C are DEVICE pointers (cudaMalloc'd, or any allocation the
+ * device can address) on the current device.  The caller owns all of them; the
+ * library never frees, keeps or reallocates them.  C must not overlap A or B.
+ * The library allocates no device memory for any call declared here.
+ *
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ * default stream).  Every call returns as soon as its work is queued; results
+ * are ready once the stream reaches that point.  Argument errors are detected
+ * on the host before anything is queued, and then nothing is launched.
+ *
+ * Numerics: FP32 inputs and outputs; each output's K products are accumulated
+ * in FP32 (FFMA) by the CUDA-core kernels, or from TF32 splits in FP32 by the
+ * 3xTF32 tensor-core kernel.  The result matches the FP64-accumulated product
+ * within a relative Frobenius error of 1e-5 and an absolute elementwise error of
+ * 1e-4 * sqrt(K) for inputs of unit scale, and bit for bit when every input and
+ * every partial sum is an integer below 2^24 in magnitude.  Denormals are kept
+ * (no flush to zero).  Degenerate cases follow BLAS: M == 0 or N == 0 does
+ * nothing; K == 0 or alpha == 0 sets C = beta * C without reading A or B;
+ * beta == 0 never reads C (NaN or garbage there is overwritten).
+ */
+#ifndef DENSE_FP32_MATRIX_10_GB300_SGEMM_H_
+#define DENSE_FP32_MATRIX_10_GB300_SGEMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SGEMM_API __attribute__((visibility("default")))
+#else
+#define SGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sgemm_op {
+  SGEMM_OP_N = 0, /* op(X) = X   */
+  SGEMM_OP_T = 1  /* op(X) = X^T */
+} sgemm_op_t;
+
+typedef enum sgemm_status {
+  SGEMM_SUCCESS = 0,
+  SGEMM_ERR_INVALID_VALUE = 1,  /* bad op, negative or too large M/N/K, leading
+                                   dimension too small, NULL pointer with a
+                                   nonzero extent, unknown algorithm */
+  SGEMM_ERR_ALIASING = 2,       /* C's byte range overlaps A's or B's */
+  SGEMM_ERR_UNSUPPORTED = 3,    /* no CUDA device, or not compute capability 10.3;
+                                   or the requested algorithm cannot take these
+                                   arguments (e.g. TMA with an unaligned ld) */
+  SGEMM_ERR_LAUNCH = 4,         /* a CUDA call failed while queuing the work */
+  SGEMM_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up a bounded wait (reported
+                                   by sgemm_last_device_status) */
+} sgemm_status_t;
+
+/*
+ * Which kernel family runs.  SGEMM_ALGO_AUTO picks by shape, layout and
+ * alignment; the others force one family (for tests and measurement).
+ */
+typedef enum sgemm_algo {
+  SGEMM_ALGO_AUTO = 0,
+  SGEMM_ALGO_SIMT_TMA = 1,     /* CUDA cores, FFMA, 8x8 outputs per thread; a TMA
+                                  producer warp fills a multi-stage ring of
+                                  swizzled shared-memory tiles.  Needs A and B
+                                  16-byte aligned and lda, ldb multiples of 4. */
+  SGEMM_ALGO_SIMT_CPASYNC = 2, /* same consumer warps; producer warps fill the
+                                  ring with 4-byte cp.async.  Any alignment/ld. */
+  SGEMM_ALGO_TC_3XTF32 = 3,    /* tcgen05 tensor cores, TMEM accumulator, each
+                                  FP32 operand split into two TF32 parts and
+                                  three products accumulated. */
+  SGEMM_ALGO_NAIVE = 4,        /* one thread per output, operands read straight
+                                  from global memory (the pages' first kernel;
+                                  for comparison only) */
+  SGEMM_ALGO_SMEM_TILED = 5    /* 16x16 shared-memory tiles, one output per
+                                  thread (the pages' second kernel; comparison) */
+} sgemm_algo_t;
+
+/*
+ * C = alpha * op(A) * op(B) + beta * C, kernel chosen automatically.
+ * Returns SGEMM_SUCCESS once the work is queued on `stream`, or an error code
+ * (see sgemm_status_t) with nothing queued.  Thread-safe.
+ */
+SGEMM_API sgemm_status_t sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                     float alpha, const float *A, int64_t lda,
+                     const float *B, int64_t ldb,
+                     float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * As sgemm(), with the kernel family forced by `algo` (SGEMM_ALGO_AUTO gives
+ * exactly sgemm()).  Returns SGEMM_ERR_UNSUPPORTED, with nothing queued, when
+ * that family cannot take these arguments.
+ */
+SGEMM_API sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                        float alpha, const float *A, int64_t lda,
+                        const float *B, int64_t ldb,
+                        float beta, float *C, int64_t ldc, void *stream,
+                        sgemm_algo_t algo);
+
+/*
+ * The family SGEMM_ALGO_AUTO would run for these arguments, or -1 if the
+ * arguments are invalid.  Host only: queues nothing and touches no device
+ * memory (it reads the device's SM count once).
+ */
+SGEMM_API int sgemm_select_algo(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                      const float *A, int64_t lda, const float *B, int64_t ldb,
+                      float alpha, float beta, const float *C, int64_t ldc);
+
+/*
+ * Number of kernel launches the last successful sgemm()/sgemm_ex() call on the
+ * calling host thread queued (0 for M == 0 or N == 0).
+ */
+SGEMM_API int sgemm_last_launch_count(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word, in which a kernel records that it gave up a bounded wait.  Returns
+ * SGEMM_SUCCESS, SGEMM_ERR_DEVICE_TIMEOUT, or SGEMM_ERR_LAUNCH if the
+ * synchronisation itself failed.
+ */
+SGEMM_API sgemm_status_t sgemm_last_device_status(void *stream);
+
+/*
+ * Sets the limit, in nanoseconds of %globaltimer, that every wait inside the
+ * library's kernels observes before it gives up and records
+ * SGEMM_ERR_DEVICE_TIMEOUT (default 2e9 = 2 s; 0 restores the default).
+ * Affects launches queued after the call, from any thread.
+ */
+SGEMM_API void sgemm_set_wait_budget_ns(uint64_t budget_ns);
+
+/*
+ * Queues one tiny kernel whose single thread waits on a shared-memory mbarrier
+ * that nothing will ever complete, with the same bounded wait the GEMM kernels
+ * use and a budget of `budget_ns`.  It lets a test watch the give-up path end
+ * in SGEMM_ERR_DEVICE_TIMEOUT (read with sgemm_last_device_status) without
+ * faulting or hanging anything.  Returns SGEMM_ERR_LAUNCH if queuing failed.
+ */
+SGEMM_API sgemm_status_t sgemm_selftest_wait_timeout(uint64_t budget_ns, void *stream);
+
+/* Static English text for a status code (never NULL). */
+SGEMM_API const char *sgemm_status_string(sgemm_status_t status);
+
+/* Static name of an algorithm ("auto", "simt_tma", ...), or "unknown". */
+SGEMM_API const char *sgemm_algo_name(sgemm_algo_t algo);
+
+/* Library version as "major.minor.patch". */
+SGEMM_API const char *sgemm_version(void);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* DENSE_FP32_MATRIX_10_GB300_SGEMM_H_ */

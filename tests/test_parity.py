@@ -1,0 +1,287 @@
+"""GPU results of the C ABI against the CPU oracle, element by element.
+
+Covers every workload family (full comparison where the oracle finishes in
+seconds, sampled outputs plus bit-exact integer checks at the full sizes), the
+four op combinations through every kernel family, ragged tails spanning
+several tiles, padded and misaligned leading dimensions, and the degenerate
+cases.  All calls go through the C ABI (ctypes binding).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import dense_fp32_matrix_10_gb300 as sg
+from dense_fp32_matrix_10_gb300 import workloads as W
+from tests.parity import (assert_bit_exact, assert_close, offset_view, padded, sample_indices)
+
+pytestmark = pytest.mark.gpu
+
+OPS = [(0, 0), (0, 1), (1, 0), (1, 1)]
+GEMM_ALGOS = ["simt_tma", "simt_cpasync"]
+ALL_ALGOS = ["auto", "simt_tma", "simt_cpasync", "naive", "smem_tiled"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_fp32_matrix_10_gb300 import build
+    build.build()
+    torch.cuda.init()
+    yield
+    assert sg.sgemm_last_device_status() == 0
+
+
+def run_case(case, algo="auto", A=None, B=None, C=None):
+    """Run `case` on the GPU; returns (GPU result, host inputs).  Forced TMA
+    runs get leading dimensions padded up to a multiple of 4 (16-byte rows)."""
+    if A is None:
+        A, B, C = W.make_inputs(case)
+    dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+    if algo == "simt_tma":
+        dA = padded(dA, (-A.shape[1]) % 4)
+        dB = padded(dB, (-B.shape[1]) % 4)
+    sg.gemm(dA, dB, dC, case.alpha, case.beta, case.transA, case.transB, algo=algo)
+    torch.cuda.synchronize()
+    return dC.cpu().numpy(), (A.numpy(), B.numpy(), C.numpy())
+
+
+def oracle_full(orc, case, A, B, C):
+    return orc.sgemm_f64(case.transA, case.transB, case.alpha, A, B, case.beta,
+                         C if case.beta != 0 else None)
+
+
+# --------------------------------------------------------------- workloads
+SMALL_CASES = [W.SMALL_256, W.SQUARE_1024, W.SWEEP[0], W.SWEEP[1], W.RAGGED[0], W.RAGGED[2]]
+LARGE_CASES = [W.SWEEP[2], W.SWEEP[3], W.NT_4096, W.RAGGED[1]]
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=[c.name for c in SMALL_CASES])
+def test_workload_full(orc, case):
+    G, (A, B, C) = run_case(case)
+    R = oracle_full(orc, case, A, B, C)
+    assert_close(G, R, case.K, case.name)
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=[c.name for c in SMALL_CASES])
+def test_workload_integer_bit_exact(orc, case):
+    ic = case.as_int()
+    G, (A, B, C) = run_case(ic)
+    assert_bit_exact(G, oracle_full(orc, ic, A, B, C), ic.name)
+
+
+@pytest.mark.parametrize("case", LARGE_CASES, ids=[c.name for c in LARGE_CASES])
+def test_workload_sampled(orc, case):
+    G, (A, B, C) = run_case(case)
+    I, J = sample_indices(case.M, case.N, 1500, seed=case.seed)
+    R = orc.sgemm_entries_f64(case.transA, case.transB, case.alpha, A, B, case.beta,
+                              C if case.beta != 0 else None, I, J)
+    assert_close(G[I, J], R, case.K, case.name)
+
+
+@pytest.mark.parametrize("case", LARGE_CASES, ids=[c.name for c in LARGE_CASES])
+def test_workload_integer_sampled_bit_exact(orc, case):
+    ic = case.as_int()
+    G, (A, B, C) = run_case(ic)
+    I, J = sample_indices(ic.M, ic.N, 1500, seed=ic.seed)
+    R = orc.sgemm_entries_f64(ic.transA, ic.transB, ic.alpha, A, B, ic.beta,
+                              C if ic.beta != 0 else None, I, J)
+    assert_bit_exact(G[I, J], R, ic.name)
+
+
+def test_full_size_integer_row_sums():
+    """A property that holds at any size: with all-ones op(B), every output of
+    row i is alpha * sum_k op(A)[i, k] (exact for small integers), checked over
+    the whole 4096^3 output."""
+    M = N = K = 4096
+    g = torch.Generator().manual_seed(7)
+    A = torch.randint(-8, 9, (M, K), generator=g).float()
+    B = torch.ones((K, N))
+    dC = torch.empty((M, N), device="cuda")
+    sg.gemm(A.cuda(), B.cuda(), dC, 1.0, 0.0)
+    want = A.double().sum(1, keepdim=True).expand(M, N)
+    assert torch.equal(dC.cpu().double(), want)
+
+
+# --------------------------------------------------------------- op/algo grid
+SHAPES = [(1, 1, 1), (7, 3, 5), (128, 128, 32), (127, 129, 33), (300, 260, 200),
+          (129, 257, 97), (64, 400, 31), (513, 70, 64), (256, 384, 1000)]
+
+
+@pytest.mark.parametrize("algo", ALL_ALGOS)
+@pytest.mark.parametrize("op", OPS, ids=["NN", "NT", "TN", "TT"])
+def test_ops_shapes(orc, algo, op):
+    ta, tb = op
+    for idx, (M, N, K) in enumerate(SHAPES):
+        seed = 1000 + idx
+        case = W.Case(f"grid_{M}x{N}x{K}", M, N, K, ta, tb, "uniform", seed, 1.25, -0.5)
+        G, (A, B, C) = run_case(case, algo=algo)
+        assert_close(G, oracle_full(orc, case, A, B, C), K, f"{algo} {op} {M}x{N}x{K}")
+        ic = case.as_int()
+        G, (A, B, C) = run_case(ic, algo=algo)
+        assert_bit_exact(G, oracle_full(orc, ic, A, B, C), f"{algo} {op} int {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("algo", GEMM_ALGOS)
+def test_random_ragged_sweep(orc, algo):
+    """A few dozen random shapes 1..300 per dimension, random ops, scalars and
+    padded leading dimensions (the pages' advice: compare many random shapes
+    with a CPU reference)."""
+    rng = np.random.default_rng(42 if algo == "simt_tma" else 43)
+    for t in range(40):
+        M, N, K = (int(x) for x in rng.integers(1, 301, size=3))
+        ta, tb = int(rng.integers(0, 2)), int(rng.integers(0, 2))
+        alpha = float(rng.choice([1.0, -0.5, 2.0, 0.75]))
+        beta = float(rng.choice([0.0, 1.0, -1.5]))
+        case = W.Case("sweep", M, N, K, ta, tb, "uniform", 5000 + t, alpha, beta)
+        A, B, C = W.make_inputs(case)
+        if algo == "simt_cpasync":   # any padding, ld usually not a multiple of 4
+            ea, eb = int(rng.integers(0, 5)), int(rng.integers(0, 5))
+        else:                        # pad each ld up to a multiple of 4 (TMA needs 16-byte rows)
+            ea = (-A.shape[1]) % 4 + 4 * int(rng.integers(0, 3))
+            eb = (-B.shape[1]) % 4 + 4 * int(rng.integers(0, 3))
+        Ad, Bd = padded(A.cuda(), ea), padded(B.cuda(), eb)
+        Cd = padded(C.cuda(), int(rng.integers(0, 3)), fill=float("nan") if beta == 0 else 0.0)
+        sg.gemm(Ad, Bd, Cd, alpha, beta, ta, tb, algo=algo)
+        torch.cuda.synchronize()
+        R = orc.sgemm_f64(ta, tb, alpha, A.numpy(), B.numpy(), beta, C.numpy() if beta else None)
+        assert_close(Cd.cpu().numpy(), R, K, f"{algo} t={t} {M}x{N}x{K} op={ta}{tb}")
+
+
+# --------------------------------------------------------------- layout edge cases
+def test_guard_bands_untouched():
+    """Nothing outside the M x N output (inside ldc) is written."""
+    M, N, K = 200, 130, 70
+    for algo in ALL_ALGOS:
+        A = torch.rand(M, K, device="cuda")
+        B = torch.rand(K, N, device="cuda")
+        big = torch.full((M + 3, N + 5), 12345.0, device="cuda")
+        C = big[:M, :N]
+        sg.gemm(A, B, C, 1.0, 0.0, algo=algo)
+        torch.cuda.synchronize()
+        assert torch.all(big[:M, N:] == 12345.0), algo
+        assert torch.all(big[M:, :] == 12345.0), algo
+
+
+@pytest.mark.parametrize("op", OPS, ids=["NN", "NT", "TN", "TT"])
+def test_misaligned_pointers_use_cpasync(orc, op):
+    ta, tb = op
+    M, N, K = 150, 140, 90
+    case = W.Case("mis", M, N, K, ta, tb, "uniform", 77, 1.0, 1.0)
+    A, B, C = W.make_inputs(case)
+    Ad, Bd = offset_view(A.cuda(), 1), offset_view(B.cuda(), 3)
+    Cd = offset_view(C.cuda(), 2)
+    assert sg.sgemm_select_algo(ta, tb, M, N, K, Ad.data_ptr(), Ad.stride(0), Bd.data_ptr(),
+                                Bd.stride(0), 1.0, 1.0, Cd.data_ptr(), N) == sg.ALGO_SIMT_CPASYNC
+    with pytest.raises(sg.SgemmError):
+        sg.gemm(Ad, Bd, Cd, 1.0, 1.0, ta, tb, algo="simt_tma")
+    sg.gemm(Ad, Bd, Cd, 1.0, 1.0, ta, tb)
+    torch.cuda.synchronize()
+    assert_close(Cd.cpu().numpy(), orc.sgemm_f64(ta, tb, 1.0, A.numpy(), B.numpy(), 1.0, C.numpy()),
+                 K, f"misaligned {op}")
+
+
+def test_odd_leading_dimensions(orc):
+    """The pages' ragged configuration: lda = K = 997, ldb = N = 1013 (TMA-ineligible)."""
+    case = W.RAGGED[0]
+    A, B, C = W.make_inputs(case)
+    assert sg.sgemm_select_algo(0, 0, case.M, case.N, case.K, 256, case.K, 256, case.N, 1.0, 1.0,
+                                512, case.N) == sg.ALGO_SIMT_CPASYNC
+
+
+# --------------------------------------------------------------- degenerate cases
+@pytest.mark.parametrize("algo", ALL_ALGOS)
+def test_beta_zero_ignores_nan_in_c(orc, algo):
+    M, N, K = 70, 90, 50
+    A = torch.rand(M, K, device="cuda")
+    B = torch.rand(K, N, device="cuda")
+    C = torch.full((M, N), float("nan"), device="cuda")
+    sg.gemm(A, B, C, 1.0, 0.0, algo=algo)
+    torch.cuda.synchronize()
+    R = orc.sgemm_f64(0, 0, 1.0, A.cpu().numpy(), B.cpu().numpy())
+    assert_close(C.cpu().numpy(), R, K, algo)
+
+
+def test_alpha_zero_and_k_zero():
+    M, N = 33, 47
+    C0 = torch.rand(M, N, device="cuda")
+    A = torch.full((M, 8), float("nan"), device="cuda")
+    B = torch.full((8, N), float("nan"), device="cuda")
+    C = C0.clone()
+    sg.gemm(A, B, C, 0.0, 2.0)
+    torch.cuda.synchronize()
+    assert torch.equal(C, 2.0 * C0)
+    C = C0.clone()
+    sg.gemm(A, B, C, 0.0, 0.0)
+    torch.cuda.synchronize()
+    assert torch.equal(C, torch.zeros_like(C))
+    C = torch.full((M, N), float("nan"), device="cuda")
+    Ak = torch.empty((M, 0), device="cuda")
+    Bk = torch.empty((0, N), device="cuda")
+    sg.gemm(Ak, Bk, C, 1.0, 0.0)
+    torch.cuda.synchronize()
+    assert torch.equal(C, torch.zeros_like(C))
+    assert sg.sgemm_last_launch_count() == 1
+
+
+def test_empty_outputs():
+    A = torch.rand(0, 5, device="cuda")
+    B = torch.rand(5, 7, device="cuda")
+    C = torch.empty(0, 7, device="cuda")
+    sg.gemm(A, B, C)
+    assert sg.sgemm_last_launch_count() == 0
+
+
+def test_denormals_are_kept():
+    """No flush-to-zero: products of normal numbers that land in the subnormal
+    range survive (2^-70 * 2^-70 = 2^-140, a subnormal float)."""
+    for algo in GEMM_ALGOS + ["naive"]:
+        A = torch.full((4, 4), 2.0 ** -70, device="cuda")
+        B = torch.full((4, 4), 2.0 ** -70, device="cuda")
+        C = torch.empty(4, 4, device="cuda")
+        sg.gemm(A, B, C, 1.0, 0.0, algo=algo)
+        torch.cuda.synchronize()
+        assert torch.all(C == 4 * 2.0 ** -140), algo
+
+
+# --------------------------------------------------------------- streams / status
+def test_runs_on_the_given_stream(orc):
+    s = torch.cuda.Stream()
+    M, N, K = 512, 512, 512
+    A = torch.rand(M, K, device="cuda")
+    B = torch.rand(K, N, device="cuda")
+    C = torch.empty(M, N, device="cuda")
+    with torch.cuda.stream(s):
+        sg.gemm(A, B, C)
+    s.synchronize()
+    R = orc.sgemm_f64(0, 0, 1.0, A.cpu().numpy(), B.cpu().numpy())
+    assert_close(C.cpu().numpy(), R, K, "side stream")
+
+
+def test_launch_count_is_one():
+    A = torch.rand(300, 200, device="cuda")
+    B = torch.rand(200, 100, device="cuda")
+    for algo in ALL_ALGOS:
+        sg.gemm(A, B, algo=algo)
+        assert sg.sgemm_last_launch_count() == 1, algo
+
+
+def test_bounded_wait_gives_up_and_context_survives(orc):
+    """A wait that nothing satisfies ends with SGEMM_ERR_DEVICE_TIMEOUT in about
+    the given budget; the next GEMM on the same context is still correct."""
+    import time
+    assert sg.sgemm_last_device_status() == 0
+    t0 = time.perf_counter()
+    sg.sgemm_selftest_wait_timeout(2_000_000)       # 2 ms
+    st = sg.sgemm_last_device_status()
+    assert st == 5, st
+    assert time.perf_counter() - t0 < 5.0
+    assert sg.sgemm_last_device_status() == 0       # cleared by the read
+    A = torch.rand(256, 256, device="cuda")
+    B = torch.rand(256, 256, device="cuda")
+    C = sg.gemm(A, B)
+    torch.cuda.synchronize()
+    assert_close(C.cpu().numpy(), orc.sgemm_f64(0, 0, 1.0, A.cpu().numpy(), B.cpu().numpy()), 256,
+                 "after timeout")
