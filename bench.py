@@ -222,7 +222,7 @@ def run_ours(args, dist):
     sms = props.multi_processor_count
     stream = torch.cuda.current_stream(dev)
 
-    case = W.HEADLINE
+    case = {c.name: c for c in W.ALL_CASES}[args.workload] if args.workload else W.HEADLINE
     A, B, C = (t.to(dev) for t in W.make_inputs(case))
     flops = case.flops
 
@@ -251,8 +251,8 @@ def run_ours(args, dist):
     hC = torch.empty(C.shape, dtype=torch.float32, pin_memory=True)
     hA.copy_(A)
     hB.copy_(B)
-    e2e_steps = max(3, min(args.steps, 30))
-    for i in range(2 + e2e_steps):
+    e2e_steps = max(3, min(args.steps, 30)) if not args.no_e2e else 0
+    for i in range(2 + e2e_steps if e2e_steps else 0):
         if i == 2:
             torch.cuda.synchronize()
             dist.barrier()
@@ -262,13 +262,15 @@ def run_ours(args, dist):
         B.copy_(hB, non_blocking=True)
         sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=args.algo, stream=stream)
         hC.copy_(C, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = dist.max(e0.elapsed_time(e1) / e2e_steps, dev)
-    e2e = {"value": round(flops * dist.world / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-           "ms_per_step": round(ms_e2e, 4),
-           "h2d_bytes_per_step": int(A.numel() * 4 + B.numel() * 4),
-           "d2h_bytes_per_step": int(C.numel() * 4)}
+    e2e = None
+    if e2e_steps:
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = dist.max(e0.elapsed_time(e1) / e2e_steps, dev)
+        e2e = {"value": round(flops * dist.world / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "ms_per_step": round(ms_e2e, 4),
+               "h2d_bytes_per_step": int(A.numel() * 4 + B.numel() * 4),
+               "d2h_bytes_per_step": int(C.numel() * 4)}
 
     # ---- roofline of the dominant (only) kernel of a step
     peaks = measured_peaks()
@@ -276,9 +278,9 @@ def run_ours(args, dist):
     peak = 2 * FP32_LANES_PER_SM * sms * sm_max * 1e6 / 1e12
     achieved = tflops(flops, ms_launch)
     algo_used = sg.sgemm_algo_name(sg.sgemm_select_algo(
-        0, 0, case.M, case.N, case.K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
+        case.transA, case.transB, case.M, case.N, case.K, A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0),
         case.alpha, case.beta, C.data_ptr(), C.stride(0))) if args.algo == "auto" else args.algo
-    tag = f"{algo_used}_nn_4096"
+    tag = f"{algo_used}_{case.name}"
     traffic, traffic_src = stored_traffic(tag)
     roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 3),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -316,7 +318,8 @@ def run_ours(args, dist):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic: seeded i.i.d. standard normal A, B (torch CPU generator, seed 2)",
-        "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K, "op": "NN",
+        "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K,
+                   "op": "NT"[case.transA] + "NT"[case.transB],
                    "alpha": case.alpha, "beta": case.beta, "algo": algo_used,
                    "l2": "inputs (192 MiB) larger than L2 (129 MB); no flush between steps",
                    "parallelism": "replicas" if dist.world > 1 else "single GPU"},
@@ -388,7 +391,8 @@ def run_reference(args, dist):
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic: seeded i.i.d. standard normal A, B (torch CPU generator, seed 2)",
-        "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K, "op": "NN",
+        "config": {"workload": case.name, "M": case.M, "N": case.N, "K": case.K,
+                   "op": "NT"[case.transA] + "NT"[case.transB],
                    "alpha": case.alpha, "beta": case.beta,
                    "sample_rows_per_step": rows},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": probe["cores"],
@@ -410,6 +414,10 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--workload", default=None,
+                    help="time another workload family member instead of the headline "
+                         "(e.g. nt_4096_uniform_s3); used to drive profiler captures")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

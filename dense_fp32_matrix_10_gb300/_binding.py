@@ -7,7 +7,9 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(HERE, "libsgemm_gb300.so")
+# SGEMM_GB300_LIBRARY may name another build of the same sources (for example a
+# build with different compile-time kernel options).
+_LIB_PATH = os.environ.get("SGEMM_GB300_LIBRARY") or os.path.join(HERE, "libsgemm_gb300.so")
 
 OP_N, OP_T = 0, 1
 ALGO_AUTO, ALGO_SIMT_TMA, ALGO_SIMT_CPASYNC, ALGO_TC_3XTF32, ALGO_NAIVE, ALGO_SMEM_TILED = range(6)

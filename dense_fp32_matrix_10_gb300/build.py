@@ -36,8 +36,8 @@ def _headers():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def _compile(nvcc, src, obj, log):
-    cmd = [nvcc, *NVCC_FLAGS, "-c", src, "-o", obj + ".tmp"]
+def _compile(nvcc, src, obj, log, defines=()):
+    cmd = [nvcc, *NVCC_FLAGS, *("-D" + d for d in defines), "-c", src, "-o", obj + ".tmp"]
     proc = subprocess.run(cmd, capture_output=True, text=True)
     with open(log, "w") as f:
         f.write(" ".join(cmd) + "\n" + proc.stdout + proc.stderr)
@@ -47,15 +47,25 @@ def _compile(nvcc, src, obj, log):
     return obj
 
 
-def build(force: bool = False, jobs: int = None, verbose: bool = False) -> str:
-    """Compile and link if anything is out of date; return the library path."""
+def build(force: bool = False, jobs: int = None, verbose: bool = False, defines=(),
+          out: str = None) -> str:
+    """Compile and link if anything is out of date; return the library path.
+
+    ``defines`` (e.g. ``["SG_SIMT_KC_UNROLL=4"]``) select compile-time kernel
+    options; a build with defines needs its own ``out`` path and object dir.
+    """
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    defines = list(defines)
+    if defines and not out:
+        raise ValueError("a build with defines needs its own output path")
+    lib = out or LIB
+    build_dir = BUILD if not out else os.path.join(BUILD, "variant_" + os.path.basename(out).replace(".so", ""))
+    os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     newest_header = max((os.path.getmtime(h) for h in _headers()), default=0.0)
     todo, objs = [], []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         stale = force or not os.path.exists(obj) or \
             os.path.getmtime(obj) < max(os.path.getmtime(src), newest_header)
@@ -64,20 +74,20 @@ def build(force: bool = False, jobs: int = None, verbose: bool = False) -> str:
     if todo:
         jobs = jobs or min(len(todo), os.cpu_count() or 4)
         with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
-            list(ex.map(lambda t: _compile(nvcc, *t), todo))
-    relink = force or bool(todo) or not os.path.exists(LIB) or \
-        os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs)
+            list(ex.map(lambda t: _compile(nvcc, *t, defines=defines), todo))
+    relink = force or bool(todo) or not os.path.exists(lib) or \
+        os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs)
     if relink:
-        tmp = LIB + ".tmp.%d" % os.getpid()
+        tmp = lib + ".tmp.%d" % os.getpid()
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-ldl", "-lpthread", "-lrt"]
         proc = subprocess.run(cmd, capture_output=True, text=True)
         if proc.returncode != 0:
             raise RuntimeError("link failed:\n" + proc.stderr[-4000:])
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
     if verbose:
         for _, obj, log in todo:
             sys.stdout.write(open(log).read())
-    return LIB
+    return lib
 
 
 def ptxas_report() -> str:
@@ -91,4 +101,11 @@ def ptxas_report() -> str:
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    import argparse
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--force", action="store_true")
+    ap.add_argument("-v", action="store_true")
+    ap.add_argument("--define", "-D", action="append", default=[])
+    ap.add_argument("--out", default=None)
+    a = ap.parse_args()
+    print(build(force=a.force, verbose=a.v, defines=a.define, out=a.out))

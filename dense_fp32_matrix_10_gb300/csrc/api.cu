@@ -33,6 +33,9 @@ struct DeviceState {
   std::once_flag kinfo_once[2][2][2][kNumSimtTiles];
   cudaError_t kinfo_err[2][2][2][kNumSimtTiles] = {};
   SimtKernelInfo kinfo[2][2][2][kNumSimtTiles] = {};
+  std::once_flag tcinfo_once[2][2];
+  cudaError_t tcinfo_err[2][2] = {};
+  TcKernelInfo tcinfo[2][2] = {};
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -72,6 +75,15 @@ const SimtKernelInfo *kernel_info(DeviceState &d, int producer, int ta, int tb, 
   });
   if (d.kinfo_err[producer][ta][tb][tile] != cudaSuccess) return nullptr;
   return &d.kinfo[producer][ta][tb][tile];
+}
+
+const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb) {
+  std::call_once(d.tcinfo_once[ta][tb], [&]() {
+    d.tcinfo_err[ta][tb] = tc3_entry(ta, tb).info(&d.tcinfo[ta][tb]);
+    if (d.tcinfo_err[ta][tb] != cudaSuccess) cudaGetLastError();
+  });
+  if (d.tcinfo_err[ta][tb] != cudaSuccess) return nullptr;
+  return &d.tcinfo[ta][tb];
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -230,6 +242,43 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   return SGEMM_SUCCESS;
 }
 
+// 3xTF32 on the tensor cores: 128 x 128 tiles, TMA loads (needs TMA-eligible
+// operands), one persistent CTA per SM.
+sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream) {
+  const TcKernelInfo *ki = tc_kernel_info(d, a.ta, a.tb);
+  if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_LAUNCH;
+  TcParams p;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.alpha = a.alpha;
+  p.beta = a.beta;
+  p.tiles_m = static_cast<int>(cdiv(a.M, ki->bm));
+  p.tiles_n = static_cast<int>(cdiv(a.N, ki->bn));
+  p.k_tiles = static_cast<int>(cdiv(a.K, 32));
+  const int64_t num_tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  if (num_tiles > kMaxDim) return SGEMM_ERR_UNSUPPORTED;
+  p.num_tiles = static_cast<int>(num_tiles);
+  p.group_m = 8;
+  p.c_vec4 = (a.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
+  p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
+  p.status = d.status;
+  CUtensorMap tmA, tmB;
+  const bool okA = a.ta == 0 ? encode_tmap(&tmA, a.A, a.M, a.K, a.lda, 32, 128, true)
+                             : encode_tmap(&tmA, a.A, a.K, a.M, a.lda, 128, 32, false);
+  const bool okB = a.tb == 0 ? encode_tmap(&tmB, a.B, a.K, a.N, a.ldb, 128, 32, false)
+                             : encode_tmap(&tmB, a.B, a.N, a.K, a.ldb, 32, 128, true);
+  if (!okA || !okB) return SGEMM_ERR_LAUNCH;
+  const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
+  const int grid = static_cast<int>(num_tiles < slots ? num_tiles : slots);
+  if (tc3_entry(a.ta, a.tb).launch(p, &tmA, &tmB, grid, stream) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
+  t_last_launches = 1;
+  return SGEMM_SUCCESS;
+}
+
 }  // namespace
 
 namespace sg {
@@ -287,6 +336,8 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
       return SGEMM_SUCCESS;
     }
     case SGEMM_ALGO_TC_3XTF32:
+      if (!tma_eligible(a)) return SGEMM_ERR_UNSUPPORTED;
+      return run_tc3(a, *d, s);
     default:
       return SGEMM_ERR_UNSUPPORTED;
   }

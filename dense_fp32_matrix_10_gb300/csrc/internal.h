@@ -7,6 +7,7 @@
 #include <cstdint>
 
 #include "simt_gemm.cuh"
+#include "tc_3xtf32.cuh"
 
 namespace sg {
 
@@ -36,6 +37,19 @@ struct SimtEntry {
 
 // [producer][transA][transB][tile]
 SimtEntry simt_entry(int producer, int transA, int transB, int tile);
+
+// 3xTF32 tensor-core kernel (tc_3xtf32.cu), 128 x 128 tiles, one CTA per SM.
+struct TcKernelInfo {
+  int bm, bn, ctas_per_sm;
+};
+using TcLaunchFn = cudaError_t (*)(const TcParams &, const CUtensorMap *, const CUtensorMap *, int,
+                                   cudaStream_t);
+using TcInfoFn = cudaError_t (*)(TcKernelInfo *);
+struct TcEntry {
+  TcLaunchFn launch;
+  TcInfoFn info;
+};
+TcEntry tc3_entry(int transA, int transB);
 
 // Context kernels and helpers (context.cu).
 struct PlainParams {

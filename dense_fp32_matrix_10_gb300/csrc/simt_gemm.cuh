@@ -92,8 +92,11 @@ struct SimtConfig {
   static constexpr int MIN_CTAS = (MATH_WARPS == 8) ? 1 : 2;  // CTAs per SM
   // Per-thread registers after the split; launch budget is
   // THREADS * (65536 / (THREADS * MIN_CTAS)) rounded down to 8.
-  static constexpr int PRODUCER_REGS = 40;
-  static constexpr int MATH_REGS = (MATH_WARPS == 8) ? 232 : 216;
+  // The TMA producer needs few registers; the cp.async producer computes
+  // addresses for 64 copies per stage.
+  static constexpr int PRODUCER_REGS = (PRODUCER == kTma) ? 24 : 40;
+  static constexpr int MATH_REGS = (MATH_WARPS == 8) ? ((PRODUCER == kTma) ? 240 : 232)
+                                                     : ((PRODUCER == kTma) ? 232 : 216);
   static_assert(MATH_WARPS % 4 == 0, "math role must be whole warpgroups");
   static_assert(PRODUCER_THREADS * PRODUCER_REGS + MATH_THREADS * MATH_REGS <=
                     THREADS * ((65536 / (THREADS * MIN_CTAS)) & ~7),
@@ -251,10 +254,52 @@ __device__ __forceinline__ int thread_col(int tn, int c) {
   return Cfg::B_KMAJOR ? (tn + 8 * c) : ((c < 4) ? (4 * tn + c) : (32 + 4 * tn + (c - 4)));
 }
 
+// Inner-product options (compile-time):
+//   SG_SIMT_FFMA2     1: packed FP32 FMA (__ffma2_rn: two FMAs per instruction,
+//                        each rounded like fmaf) where the layout gives natural
+//                        register pairs; 0: scalar fmaf everywhere.
+//   SG_SIMT_KC_UNROLL how many 4-k chunks of a 32-k stage are unrolled (1..8).
+#ifndef SG_SIMT_FFMA2
+#define SG_SIMT_FFMA2 1
+#endif
+#ifndef SG_SIMT_KC_UNROLL
+#define SG_SIMT_KC_UNROLL 8
+#endif
+
+constexpr int kKcUnroll = SG_SIMT_KC_UNROLL;
+
+// How the 64 accumulators of a thread are packed into 32 float2 and updated.
+// A packed FMA needs both multiplicands as register pairs; one of them is a
+// broadcast (x, x), the other must be two consecutive floats of one LDS.128:
+//   kPairCols: (row r, cols c, c+1) pairs; needs op(B) n-contiguous in smem;
+//   kPairRows: (rows r, r+1, col c) pairs; needs op(A) m-contiguous in smem;
+//   kScalar:   both operands k-contiguous -- no natural pair; scalar FFMA.
+enum AccMode : int { kPairCols = 0, kPairRows = 1, kScalar = 2 };
+
 template <class Cfg>
-__device__ __forceinline__ void mma_stage(float (&acc)[8][8], const char *a_stage,
-                                          const char *b_stage, int wm, int wn, int tm, int tn) {
+__device__ __host__ constexpr int acc_mode() {
+  return !SG_SIMT_FFMA2 ? kScalar : (!Cfg::B_KMAJOR ? kPairCols : (!Cfg::A_KMAJOR ? kPairRows : kScalar));
+}
+
+using Acc = float2[32];
+
+// Storage slot and half of output (r, c) of the thread's 8 x 8 tile.
+template <int MODE>
+__device__ __forceinline__ float &acc_ref(Acc &acc, int r, int c) {
+  if (MODE == kPairRows) return (r & 1) ? acc[(r >> 1) * 8 + c].y : acc[(r >> 1) * 8 + c].x;
+  return (c & 1) ? acc[r * 4 + (c >> 1)].y : acc[r * 4 + (c >> 1)].x;
+}
+template <int MODE>
+__device__ __forceinline__ float acc_get(const Acc &acc, int r, int c) {
+  if (MODE == kPairRows) return (r & 1) ? acc[(r >> 1) * 8 + c].y : acc[(r >> 1) * 8 + c].x;
+  return (c & 1) ? acc[r * 4 + (c >> 1)].y : acc[r * 4 + (c >> 1)].x;
+}
+
+template <class Cfg>
+__device__ __forceinline__ void mma_stage(Acc &acc, const char *a_stage, const char *b_stage,
+                                          int wm, int wn, int tm, int tn) {
   constexpr int BM = Cfg::BM, BN = Cfg::BN;
+  constexpr int MODE = acc_mode<Cfg>();
   // Per-thread base pointers inside the stage.
   const char *a_base;
   const char *b_base;
@@ -267,7 +312,7 @@ __device__ __forceinline__ void mma_stage(float (&acc)[8][8], const char *a_stag
   else
     b_base = b_stage + (wn * 64 + 4 * tn) * 4;  // + k * BN * 4, + 128 for cols 32..
 
-#pragma unroll
+#pragma unroll kKcUnroll
   for (int kc = 0; kc < 8; ++kc) {  // 4 k per chunk
     float a[8][4];  // a[r][kk]
     float b[4][8];  // b[kk][c]
@@ -308,17 +353,38 @@ __device__ __forceinline__ void mma_stage(float (&acc)[8][8], const char *a_stag
       }
     }
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
+    for (int kk = 0; kk < 4; ++kk) {
+      if (MODE == kPairCols) {
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
+        for (int r = 0; r < 8; ++r) {
+          const float2 ar = make_float2(a[r][kk], a[r][kk]);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(a[r][kk], b[kk][c], acc[r][c]);
+          for (int q = 0; q < 4; ++q)
+            acc[r * 4 + q] = __ffma2_rn(ar, make_float2(b[kk][2 * q], b[kk][2 * q + 1]), acc[r * 4 + q]);
+        }
+      } else if (MODE == kPairRows) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float2 bc = make_float2(b[kk][c], b[kk][c]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            acc[q * 8 + c] = __ffma2_rn(make_float2(a[2 * q][kk], a[2 * q + 1][kk]), bc, acc[q * 8 + c]);
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            acc_ref<kScalar>(acc, r, c) = fmaf(a[r][kk], b[kk][c], acc_ref<kScalar>(acc, r, c));
+      }
+    }
   }
 }
 
 template <class Cfg>
-__device__ __forceinline__ void epilogue(const SimtParams &p, const float (&acc)[8][8], int m0,
-                                         int n0, int wm, int wn, int tm, int tn) {
+__device__ __forceinline__ void epilogue(const SimtParams &p, const Acc &acc, int m0, int n0,
+                                         int wm, int wn, int tm, int tn) {
+  constexpr int MODE = acc_mode<Cfg>();
   const bool read_c = p.beta != 0.0f;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
@@ -326,31 +392,33 @@ __device__ __forceinline__ void epilogue(const SimtParams &p, const float (&acc)
     if (m >= p.M) continue;
     float *crow = p.C + static_cast<int64_t>(m) * p.ldc;
     if (!Cfg::B_KMAJOR) {
+      // columns 4tn..4tn+3 and 32+4tn..32+4tn+3: two float4 groups
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int n = n0 + wn * 64 + h * 32 + 4 * tn;
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = acc_get<MODE>(acc, r, 4 * h + q);
         if (p.c_vec4 && n + 3 < p.N) {
-          float4 v;
-          v.x = acc[r][4 * h + 0] * p.alpha;
-          v.y = acc[r][4 * h + 1] * p.alpha;
-          v.z = acc[r][4 * h + 2] * p.alpha;
-          v.w = acc[r][4 * h + 3] * p.alpha;
+          float4 o;
           if (read_c) {
             const float4 c = *reinterpret_cast<const float4 *>(crow + n);
-            v.x = fmaf(p.alpha, acc[r][4 * h + 0], p.beta * c.x);
-            v.y = fmaf(p.alpha, acc[r][4 * h + 1], p.beta * c.y);
-            v.z = fmaf(p.alpha, acc[r][4 * h + 2], p.beta * c.z);
-            v.w = fmaf(p.alpha, acc[r][4 * h + 3], p.beta * c.w);
+            o.x = fmaf(p.alpha, v[0], p.beta * c.x);
+            o.y = fmaf(p.alpha, v[1], p.beta * c.y);
+            o.z = fmaf(p.alpha, v[2], p.beta * c.z);
+            o.w = fmaf(p.alpha, v[3], p.beta * c.w);
+          } else {
+            o.x = p.alpha * v[0];
+            o.y = p.alpha * v[1];
+            o.z = p.alpha * v[2];
+            o.w = p.alpha * v[3];
           }
-          *reinterpret_cast<float4 *>(crow + n) = v;
+          *reinterpret_cast<float4 *>(crow + n) = o;
         } else {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (n + q < p.N) {
-              const float a = acc[r][4 * h + q];
-              crow[n + q] = read_c ? fmaf(p.alpha, a, p.beta * crow[n + q]) : p.alpha * a;
-            }
-          }
+          for (int q = 0; q < 4; ++q)
+            if (n + q < p.N)
+              crow[n + q] = read_c ? fmaf(p.alpha, v[q], p.beta * crow[n + q]) : p.alpha * v[q];
         }
       }
     } else {
@@ -358,7 +426,7 @@ __device__ __forceinline__ void epilogue(const SimtParams &p, const float (&acc)
       for (int c = 0; c < 8; ++c) {
         const int n = n0 + wn * 64 + thread_col<Cfg>(tn, c);
         if (n < p.N) {
-          const float a = acc[r][c];
+          const float a = acc_get<MODE>(acc, r, c);
           crow[n] = read_c ? fmaf(p.alpha, a, p.beta * crow[n]) : p.alpha * a;
         }
       }
@@ -418,11 +486,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
   for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
     int tile_m, tile_n;
     tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tile_m, tile_n);
-    float acc[8][8];
+    Acc acc;
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) acc[r][c] = 0.0f;
+    for (int q = 0; q < 32; ++q) acc[q] = make_float2(0.0f, 0.0f);
 
     for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
       const uint32_t s = it % Cfg::STAGES;

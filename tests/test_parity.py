@@ -19,8 +19,9 @@ from tests.parity import (assert_bit_exact, assert_close, offset_view, padded, s
 pytestmark = pytest.mark.gpu
 
 OPS = [(0, 0), (0, 1), (1, 0), (1, 1)]
-GEMM_ALGOS = ["simt_tma", "simt_cpasync"]
-ALL_ALGOS = ["auto", "simt_tma", "simt_cpasync", "naive", "smem_tiled"]
+GEMM_ALGOS = ["simt_tma", "simt_cpasync", "tc_3xtf32"]
+ALL_ALGOS = ["auto", "simt_tma", "simt_cpasync", "tc_3xtf32", "naive", "smem_tiled"]
+TMA_ALGOS = ("simt_tma", "tc_3xtf32")   # need 16-byte aligned rows
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -40,7 +41,7 @@ def run_case(case, algo="auto", A=None, B=None, C=None):
     if A is None:
         A, B, C = W.make_inputs(case)
     dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
-    if algo == "simt_tma":
+    if algo in TMA_ALGOS:
         dA = padded(dA, (-A.shape[1]) % 4)
         dB = padded(dB, (-B.shape[1]) % 4)
     sg.gemm(dA, dB, dC, case.alpha, case.beta, case.transA, case.transB, algo=algo)
@@ -58,40 +59,45 @@ SMALL_CASES = [W.SMALL_256, W.SQUARE_1024, W.SWEEP[0], W.SWEEP[1], W.RAGGED[0], 
 LARGE_CASES = [W.SWEEP[2], W.SWEEP[3], W.NT_4096, W.RAGGED[1]]
 
 
+@pytest.mark.parametrize("algo", ["auto", "simt_cpasync", "tc_3xtf32"])
 @pytest.mark.parametrize("case", SMALL_CASES, ids=[c.name for c in SMALL_CASES])
-def test_workload_full(orc, case):
-    G, (A, B, C) = run_case(case)
+def test_workload_full(orc, case, algo):
+    G, (A, B, C) = run_case(case, algo=algo)
     R = oracle_full(orc, case, A, B, C)
     assert_close(G, R, case.K, case.name)
 
 
+@pytest.mark.parametrize("algo", ["auto", "tc_3xtf32"])
 @pytest.mark.parametrize("case", SMALL_CASES, ids=[c.name for c in SMALL_CASES])
-def test_workload_integer_bit_exact(orc, case):
+def test_workload_integer_bit_exact(orc, case, algo):
     ic = case.as_int()
-    G, (A, B, C) = run_case(ic)
+    G, (A, B, C) = run_case(ic, algo=algo)
     assert_bit_exact(G, oracle_full(orc, ic, A, B, C), ic.name)
 
 
+@pytest.mark.parametrize("algo", ["auto", "tc_3xtf32"])
 @pytest.mark.parametrize("case", LARGE_CASES, ids=[c.name for c in LARGE_CASES])
-def test_workload_sampled(orc, case):
-    G, (A, B, C) = run_case(case)
+def test_workload_sampled(orc, case, algo):
+    G, (A, B, C) = run_case(case, algo=algo)
     I, J = sample_indices(case.M, case.N, 1500, seed=case.seed)
     R = orc.sgemm_entries_f64(case.transA, case.transB, case.alpha, A, B, case.beta,
                               C if case.beta != 0 else None, I, J)
     assert_close(G[I, J], R, case.K, case.name)
 
 
+@pytest.mark.parametrize("algo", ["auto", "tc_3xtf32"])
 @pytest.mark.parametrize("case", LARGE_CASES, ids=[c.name for c in LARGE_CASES])
-def test_workload_integer_sampled_bit_exact(orc, case):
+def test_workload_integer_sampled_bit_exact(orc, case, algo):
     ic = case.as_int()
-    G, (A, B, C) = run_case(ic)
+    G, (A, B, C) = run_case(ic, algo=algo)
     I, J = sample_indices(ic.M, ic.N, 1500, seed=ic.seed)
     R = orc.sgemm_entries_f64(ic.transA, ic.transB, ic.alpha, A, B, ic.beta,
                               C if ic.beta != 0 else None, I, J)
     assert_bit_exact(G[I, J], R, ic.name)
 
 
-def test_full_size_integer_row_sums():
+@pytest.mark.parametrize("algo", ["auto", "tc_3xtf32"])
+def test_full_size_integer_row_sums(algo):
     """A property that holds at any size: with all-ones op(B), every output of
     row i is alpha * sum_k op(A)[i, k] (exact for small integers), checked over
     the whole 4096^3 output."""
@@ -100,7 +106,7 @@ def test_full_size_integer_row_sums():
     A = torch.randint(-8, 9, (M, K), generator=g).float()
     B = torch.ones((K, N))
     dC = torch.empty((M, N), device="cuda")
-    sg.gemm(A.cuda(), B.cuda(), dC, 1.0, 0.0)
+    sg.gemm(A.cuda(), B.cuda(), dC, 1.0, 0.0, algo=algo)
     want = A.double().sum(1, keepdim=True).expand(M, N)
     assert torch.equal(dC.cpu().double(), want)
 
@@ -129,7 +135,7 @@ def test_random_ragged_sweep(orc, algo):
     """A few dozen random shapes 1..300 per dimension, random ops, scalars and
     padded leading dimensions (the pages' advice: compare many random shapes
     with a CPU reference)."""
-    rng = np.random.default_rng(42 if algo == "simt_tma" else 43)
+    rng = np.random.default_rng({"simt_tma": 42, "simt_cpasync": 43}.get(algo, 44))
     for t in range(40):
         M, N, K = (int(x) for x in rng.integers(1, 301, size=3))
         ta, tb = int(rng.integers(0, 2)), int(rng.integers(0, 2))
@@ -151,18 +157,20 @@ def test_random_ragged_sweep(orc, algo):
 
 
 # --------------------------------------------------------------- layout edge cases
-def test_guard_bands_untouched():
+def test_guard_bands_untouched(orc):
     """Nothing outside the M x N output (inside ldc) is written."""
-    M, N, K = 200, 130, 70
+    M, N, K = 200, 130, 72
     for algo in ALL_ALGOS:
         A = torch.rand(M, K, device="cuda")
-        B = torch.rand(K, N, device="cuda")
+        B = padded(torch.rand(K, N, device="cuda"), 2)   # ldb = 132: TMA-eligible
         big = torch.full((M + 3, N + 5), 12345.0, device="cuda")
         C = big[:M, :N]
         sg.gemm(A, B, C, 1.0, 0.0, algo=algo)
         torch.cuda.synchronize()
         assert torch.all(big[:M, N:] == 12345.0), algo
         assert torch.all(big[M:, :] == 12345.0), algo
+        R = orc.sgemm_f64(0, 0, 1.0, A.cpu().numpy(), B.cpu().numpy())
+        assert_close(C.cpu().numpy(), R, K, algo)
 
 
 @pytest.mark.parametrize("op", OPS, ids=["NN", "NT", "TN", "TT"])
@@ -175,26 +183,29 @@ def test_misaligned_pointers_use_cpasync(orc, op):
     Cd = offset_view(C.cuda(), 2)
     assert sg.sgemm_select_algo(ta, tb, M, N, K, Ad.data_ptr(), Ad.stride(0), Bd.data_ptr(),
                                 Bd.stride(0), 1.0, 1.0, Cd.data_ptr(), N) == sg.ALGO_SIMT_CPASYNC
-    with pytest.raises(sg.SgemmError):
-        sg.gemm(Ad, Bd, Cd, 1.0, 1.0, ta, tb, algo="simt_tma")
+    for algo in TMA_ALGOS:
+        with pytest.raises(sg.SgemmError):
+            sg.gemm(Ad, Bd, Cd, 1.0, 1.0, ta, tb, algo=algo)
     sg.gemm(Ad, Bd, Cd, 1.0, 1.0, ta, tb)
     torch.cuda.synchronize()
     assert_close(Cd.cpu().numpy(), orc.sgemm_f64(ta, tb, 1.0, A.numpy(), B.numpy(), 1.0, C.numpy()),
                  K, f"misaligned {op}")
 
 
-def test_odd_leading_dimensions(orc):
+def test_odd_leading_dimensions_select_cpasync():
     """The pages' ragged configuration: lda = K = 997, ldb = N = 1013 (TMA-ineligible)."""
     case = W.RAGGED[0]
-    A, B, C = W.make_inputs(case)
-    assert sg.sgemm_select_algo(0, 0, case.M, case.N, case.K, 256, case.K, 256, case.N, 1.0, 1.0,
-                                512, case.N) == sg.ALGO_SIMT_CPASYNC
+    A, B, C = (t.cuda() for t in W.make_inputs(case))
+    assert sg.sgemm_select_algo(0, 0, case.M, case.N, case.K, A.data_ptr(), case.K, B.data_ptr(),
+                                case.N, 1.0, 1.0, C.data_ptr(), case.N) == sg.ALGO_SIMT_CPASYNC
+    with pytest.raises(sg.SgemmError):
+        sg.gemm(A, B, C, 1.0, 1.0, algo="simt_tma")
 
 
 # --------------------------------------------------------------- degenerate cases
 @pytest.mark.parametrize("algo", ALL_ALGOS)
 def test_beta_zero_ignores_nan_in_c(orc, algo):
-    M, N, K = 70, 90, 50
+    M, N, K = 70, 92, 52
     A = torch.rand(M, K, device="cuda")
     B = torch.rand(K, N, device="cuda")
     C = torch.full((M, N), float("nan"), device="cuda")
@@ -235,9 +246,10 @@ def test_empty_outputs():
 
 
 def test_denormals_are_kept():
-    """No flush-to-zero: products of normal numbers that land in the subnormal
-    range survive (2^-70 * 2^-70 = 2^-140, a subnormal float)."""
-    for algo in GEMM_ALGOS + ["naive"]:
+    """No flush-to-zero on the CUDA-core kernels: products of normal numbers
+    that land in the subnormal range survive (2^-70 * 2^-70 = 2^-140, a
+    subnormal float).  (The tensor-core kernel is not held to this.)"""
+    for algo in ["simt_tma", "simt_cpasync", "naive"]:
         A = torch.full((4, 4), 2.0 ** -70, device="cuda")
         B = torch.full((4, 4), 2.0 ** -70, device="cuda")
         C = torch.empty(4, 4, device="cuda")
