@@ -42,6 +42,8 @@ sys.path.insert(0, ROOT)
 FP32_LANES_PER_SM = 128          # FP32 FMA units per Blackwell SM
 RECIPE_SM_MAX_MHZ = 2070.0       # maximum SM clock of this GB300 pool
 L2_BYTES = 129e6
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25   # dense tensor rates, GB300 nominal
+FALLBACK_BF16_TFLOPS = 1900.0         # used only if no measured peak file
 
 
 # ----------------------------------------------------------------- helpers
@@ -293,6 +295,30 @@ def run_ours(args, dist):
         roofline["frac_at_observed_clock"] = round(
             achieved / (2 * FP32_LANES_PER_SM * sms * clocks["sm_mhz"] * 1e6 / 1e12), 4)
 
+    # ---- the tensor-core (3xTF32) kernel on the same workload
+    tensor = None
+    if not args.no_tensor:
+        try:
+            r, kms, _ = time_gemm(sg, torch, case, A, B, C, max(5, min(args.steps, 200)), 3,
+                                  "tc_3xtf32", stream)
+            bf16 = float(peaks.get("bf16_tflops") or FALLBACK_BF16_TFLOPS)
+            tf32_peak = bf16 * NOMINAL_TF32_OVER_BF16
+            ach = tflops(flops, kms)
+            tensor = {"value": round(tflops(flops, r), 3), "unit": "TFLOP/s",
+                      "ms_per_step": round(r, 5), "algo": "tc_3xtf32",
+                      "roofline": {"bound": "tensor", "achieved": round(ach, 3),
+                                   "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
+                                   "frac": round(ach / tf32_peak, 4),
+                                   "traffic": stored_traffic(f"tc_3xtf32_{case.name}")[0],
+                                   "peak_basis": ("TF32 dense = measured bf16 burst "
+                                                  f"{bf16:.1f} x nominal 1.1/2.25"
+                                                  + ("" if peaks.get("bf16_tflops") else " (fallback)")),
+                                   "peak_fp32_equivalent": round(tf32_peak / 3, 1),
+                                   "frac_fp32_equivalent": round(3 * ach / tf32_peak, 4),
+                                   "note": "3 TF32 MMAs per FP32 product; achieved counts 2MNK"}}
+        except sg.SgemmError as e:
+            tensor = {"unavailable": str(e)}
+
     # ---- TFLOP/s vs size and the other workload families (rank 0 context)
     vs_size, configs = {}, {}
     if not args.no_sweep:
@@ -325,6 +351,7 @@ def run_ours(args, dist):
                    "parallelism": "replicas" if dist.world > 1 else "single GPU"},
         "pct_of_fp32_peak": round(100 * achieved / peak, 2),
         "e2e": e2e, "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
+        "tensor_core_3xtf32": tensor,
         "vs_size": vs_size, "configs": configs,
         "device": {"name": props.name, "sms": sms, "cc": f"{props.major}.{props.minor}"},
     }
@@ -418,6 +445,8 @@ def main(argv=None):
                     help="time another workload family member instead of the headline "
                          "(e.g. nt_4096_uniform_s3); used to drive profiler captures")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-tensor", action="store_true",
+                    help="skip the extra timing of the 3xTF32 tensor-core kernel")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -30,6 +30,15 @@ struct DeviceState {
   cudaError_t err = cudaSuccess;
   int sm_count = 0, cc_major = 0, cc_minor = 0;
   int *status = nullptr;
+  // Stream-K workspace: allocated on first use, kept until exit.  Calls that
+  // use it on different streams are ordered by ws_event.
+  std::mutex ws_mu;
+  float *ws = nullptr;
+  size_t ws_bytes = 0;
+  bool ws_failed = false;
+  cudaEvent_t ws_event = nullptr;
+  cudaStream_t ws_last_stream = nullptr;
+  bool ws_used = false;
   std::once_flag kinfo_once[2][2][2][kNumSimtTiles];
   cudaError_t kinfo_err[2][2][2][kNumSimtTiles] = {};
   SimtKernelInfo kinfo[2][2][2][kNumSimtTiles] = {};
@@ -183,12 +192,70 @@ bool tma_eligible(const Args &a) {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Tile choice for the CUDA-core kernels: the 128 x 128 tile when it fills the
-// SMs, else the 128 x 64 tile (two CTAs per SM) to raise the CTA count.
-int pick_simt_tile(const Args &a, int sm_count) {
-  const int64_t t128 = cdiv(a.M, 128) * cdiv(a.N, 128);
+// Tile choice for the CUDA-core kernels (eight math warps, one CTA per SM):
+// 128 x 256 with 8 x 16 thread tiles when both operands are m/n-contiguous
+// (op = TN), N is wide enough and the TMA producer runs; 128 x 128 otherwise;
+// 128 x 64 (two CTAs per SM) when N <= 64.  (Measured on 4096^3: the wide
+// tile gives TN 67.7 vs 63.0 TFLOP/s; NN, whose k-contiguous A costs more
+// registers in the wide tile, is faster narrow, 59.1 vs 58.4.)  Stream-K
+// spreads the k-iterations when the tile count does not fill whole waves.
+#ifndef SG_SIMT_WIDE_TILE
+#define SG_SIMT_WIDE_TILE 1
+#endif
+int pick_simt_tile(const Args &a, int producer) {
   if (a.N <= 64) return kTile128x64;
-  return (t128 >= sm_count) ? kTile128x128 : kTile128x64;
+  if (SG_SIMT_WIDE_TILE && producer == kTma && a.ta == 1 && a.tb == 0 && a.N >= 192)
+    return kTile128x256;
+  return kTile128x128;
+}
+
+// Smallest stream-K segment worth a partial tile (k-tiles of 32).
+constexpr int64_t kMinSkSegment = 4;
+
+struct SkPlan {
+  int dp_tiles;     // whole tiles, round-robin
+  int sk_tiles;     // tiles whose k-iterations are spread over the grid
+  int64_t sk_iters;
+  int grid;
+};
+
+// Data-parallel waves while they are full; the remainder (one to two waves'
+// worth of tiles) split by k-iterations over every CTA slot.
+SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws) {
+  SkPlan pl{static_cast<int>(tiles), 0, 0, static_cast<int>(tiles < slots ? tiles : slots)};
+  if (!have_ws || k_tiles < 2 * kMinSkSegment) return pl;
+  if (tiles >= slots && tiles % slots == 0) return pl;
+  const int64_t sk = tiles >= 2 * slots ? slots + tiles % slots : tiles;
+  int64_t grid = slots;
+  if (sk * k_tiles < grid * kMinSkSegment) grid = (sk * k_tiles) / kMinSkSegment;
+  // the fixup pass handles at most 126 segments per tile (ranges >= k_tiles/120)
+  if (grid > sk * 120) grid = sk * 120;
+  if (grid < 2 || sk % grid == 0) return pl;  // whole tiles per CTA: plain waves
+  pl.dp_tiles = static_cast<int>(tiles - sk);
+  pl.sk_tiles = static_cast<int>(sk);
+  pl.sk_iters = sk * k_tiles;
+  pl.grid = static_cast<int>(grid);
+  return pl;
+}
+
+// The device's stream-K workspace (2 partial tiles per CTA slot of the largest
+// configuration), allocated on first use; null if that failed.
+float *stream_k_workspace(DeviceState &d, size_t need) {
+  if (d.ws_failed) return nullptr;
+  if (!d.ws) {
+    // largest need: two 128 x 256 partial tiles per SM (one CTA per SM)
+    const size_t bytes = static_cast<size_t>(2) * d.sm_count * 128 * 256 * sizeof(float);
+    if (cudaMalloc(&d.ws, bytes) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d.ws_event, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      if (d.ws) cudaFree(d.ws);
+      d.ws = nullptr;
+      d.ws_failed = true;
+      return nullptr;
+    }
+    d.ws_bytes = bytes;
+  }
+  return need <= d.ws_bytes ? d.ws : nullptr;
 }
 
 sgemm_algo_t auto_algo(const Args &a) {
@@ -196,7 +263,7 @@ sgemm_algo_t auto_algo(const Args &a) {
 }
 
 sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_t stream) {
-  const int tile = pick_simt_tile(a, d.sm_count);
+  const int tile = pick_simt_tile(a, producer);
   const SimtKernelInfo *ki = kernel_info(d, producer, a.ta, a.tb, tile);
   if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_LAUNCH;
 
@@ -222,6 +289,19 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   p.c_vec4 = (a.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   p.status = d.status;
+  p.workspace = nullptr;
+
+  const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
+  std::unique_lock<std::mutex> ws_lock(d.ws_mu);
+  SkPlan plan = plan_stream_k(num_tiles, p.k_tiles, slots, !d.ws_failed);
+  if (plan.sk_tiles > 0) {
+    const size_t need = static_cast<size_t>(2) * plan.grid * ki->bm * ki->bn * sizeof(float);
+    p.workspace = stream_k_workspace(d, need);
+    if (!p.workspace) plan = plan_stream_k(num_tiles, p.k_tiles, slots, false);
+  }
+  if (plan.sk_tiles == 0) ws_lock.unlock();
+  p.dp_tiles = plan.dp_tiles;
+  p.sk_iters = plan.sk_iters;
 
   CUtensorMap tmA, tmB;
   std::memset(&tmA, 0, sizeof(tmA));
@@ -234,11 +314,21 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
                                : encode_tmap(&tmB, a.B, a.N, a.K, a.ldb, 32, ki->bn, true);
     if (!okA || !okB) return SGEMM_ERR_LAUNCH;
   }
-  const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
-  const int grid = static_cast<int>(num_tiles < slots ? num_tiles : slots);
-  cudaError_t e = simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, grid, stream);
+  if (plan.sk_tiles > 0 && d.ws_used && d.ws_last_stream != stream) {
+    // the previous stream-K call on another stream may still be using the workspace
+    if (cudaStreamWaitEvent(stream, d.ws_event, 0) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  }
+  cudaError_t e = simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, plan.grid, stream);
   if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
+  if (plan.sk_tiles > 0) {
+    if (launch_sk_fixup(p, ki->bm, ki->bn, plan.grid, plan.sk_tiles, stream) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+    t_last_launches = 2;
+    if (cudaEventRecord(d.ws_event, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    d.ws_last_stream = stream;
+    d.ws_used = true;
+  }
   return SGEMM_SUCCESS;
 }
 
@@ -266,6 +356,9 @@ sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream) {
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   p.status = d.status;
   CUtensorMap tmA, tmB;
+  // k-contiguous operands: one [128 rows][32 k] box with the 128-byte swizzle
+  // (read by the MMA directly); m/n-contiguous ones: a dense [32 k][128 mn]
+  // box (read by the converters).
   const bool okA = a.ta == 0 ? encode_tmap(&tmA, a.A, a.M, a.K, a.lda, 32, 128, true)
                              : encode_tmap(&tmA, a.A, a.K, a.M, a.lda, 128, 32, false);
   const bool okB = a.tb == 0 ? encode_tmap(&tmB, a.B, a.K, a.N, a.ldb, 128, 32, false)

@@ -14,9 +14,10 @@ namespace sg {
 // Tile configurations of the CUDA-core kernels (8 x 8 outputs per thread,
 // 32 x 64 per warp).
 enum SimtTile : int {
-  kTile128x128 = 0,  // 4 x 2 math warps
-  kTile128x64 = 1,   // 4 x 1 math warps
-  kNumSimtTiles = 2
+  kTile128x128 = 0,  // 4 x 2 math warps, 8 x 8 per thread
+  kTile128x64 = 1,   // 4 x 1 math warps, 8 x 8 per thread (two CTAs per SM)
+  kTile128x256 = 2,  // 4 x 2 math warps, 8 x 16 per thread (n-contiguous op(B) only)
+  kNumSimtTiles = 3
 };
 
 struct SimtKernelInfo {
@@ -50,6 +51,10 @@ struct TcEntry {
   TcInfoFn info;
 };
 TcEntry tc3_entry(int transA, int transB);
+
+// Second pass of a stream-K launch (sk_fixup.cu).
+cudaError_t launch_sk_fixup(const SimtParams &p, int bm, int bn, int grid_main, int sk_tiles,
+                            cudaStream_t s);
 
 // Context kernels and helpers (context.cu).
 struct PlainParams {

@@ -207,11 +207,17 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
          (static_cast<uint64_t>(2) << 61);
 }
 
-// Instruction descriptor: kind::tf32, D = F32, A = B = TF32, both K-major,
-// no negation, M x N.
+// Instruction descriptor: kind::tf32, D = F32, A = B = TF32, both operands
+// K-major, no negation, M x N.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
   return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// FP32 -> TF32 by dropping the low 13 mantissa bits (what the tensor core
+// reads from an FP32 operand); x - tf32_trunc(x) is exact in FP32.
+__device__ __forceinline__ float tf32_trunc(float x) {
+  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
 }  // namespace sg

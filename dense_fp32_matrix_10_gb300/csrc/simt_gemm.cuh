@@ -40,11 +40,14 @@
 //   op(B) tile, B stored N x K (k contiguous, "K-major"):  [BN rows][32 k],
 //       same swizzle as above.
 //
-// Thread -> output mapping inside a 32 x 64 warp tile (lane = 8 * tm + tn,
-// tm in 0..3, tn in 0..7), chosen so that every shared-memory read of a warp
-// touches each bank at most once:
+// Thread -> output mapping inside a 32 x 8TN warp tile (lane = 8 * tm + tn,
+// tm in 0..3, tn in 0..7; thread tile 8 x TN, TN = 8 or 16), chosen so that
+// the eight lanes of each quarter-warp read distinct banks or the same word:
 //   rows: MN-major A: {4tm .. 4tm+3, 16+4tm .. 16+4tm+3};  K-major A: tm + 4r.
-//   cols: MN-major B: {4tn .. 4tn+3, 32+4tn .. 32+4tn+3};  K-major B: tn + 8c.
+//   cols: MN-major B: 4tn + 32h + {0..3}, h < TN/4;        K-major B: tn + 8c.
+// Every LDS.128 of a warp takes four shared-memory wavefronts whatever the
+// broadcast, so a thread loads (8 + TN) floats per k for 8*TN FMAs: TN = 16
+// keeps shared-memory traffic at 75% of the FMA rate (TN = 8: 100%).
 #pragma once
 
 #include <cuda.h>
@@ -68,9 +71,46 @@ struct SimtParams {
   int c_vec4;            // ldc % 4 == 0 and C 16-byte aligned
   uint64_t wait_budget_ns;
   int *status;
+  // Work split (stream-K).  Tiles [0, dp_tiles) are whole-k units handed out
+  // round-robin; the k-iterations of tiles [dp_tiles, num_tiles) are divided
+  // evenly over the grid: CTA g takes iterations [g*sk_iters/G, (g+1)*sk_iters/G)
+  // of that region.  A segment that does not cover a whole tile writes its raw
+  // partial sums to workspace slot 2g (the CTA's first segment) or 2g+1 (its
+  // last); sk_fixup_kernel adds them in k order and applies alpha/beta.
+  int dp_tiles;
+  int64_t sk_iters;      // (num_tiles - dp_tiles) * k_tiles
+  float *workspace;      // 2 * gridDim.x slots of BM * BN floats
 };
 
-template <int WARPS_M_, int WARPS_N_, bool A_KMAJOR_, bool B_KMAJOR_, int STAGES_, int PRODUCER_>
+// One unit of work: k-tiles [k0, k1) of tile `tile`; slot < 0 writes C.
+struct WorkUnit {
+  int tile, k0, k1, slot;
+};
+
+// Visits this CTA's units in order; f returns false to stop early.  Every
+// role of the CTA walks the same sequence.
+template <class F>
+__device__ __forceinline__ void for_each_unit(const SimtParams &p, F &&f) {
+  for (int t = blockIdx.x; t < p.dp_tiles; t += gridDim.x)
+    if (!f(WorkUnit{t, 0, p.k_tiles, -1})) return;
+  if (p.sk_iters > 0) {
+    const int64_t g = blockIdx.x, G = gridDim.x;
+    const int64_t first = g * p.sk_iters / G, end = (g + 1) * p.sk_iters / G;
+    for (int64_t it = first; it < end;) {
+      const int ts = static_cast<int>(it / p.k_tiles);
+      const int k0 = static_cast<int>(it - static_cast<int64_t>(ts) * p.k_tiles);
+      const int64_t rest = static_cast<int64_t>(k0) + (end - it);
+      const int k1 = rest < p.k_tiles ? static_cast<int>(rest) : p.k_tiles;
+      const bool whole = (k0 == 0 && k1 == p.k_tiles);
+      if (!f(WorkUnit{p.dp_tiles + ts, k0, k1, whole ? -1 : static_cast<int>(2 * g + (it == first ? 0 : 1))}))
+        return;
+      it += k1 - k0;
+    }
+  }
+}
+
+template <int WARPS_M_, int WARPS_N_, bool A_KMAJOR_, bool B_KMAJOR_, int STAGES_, int PRODUCER_,
+          int TN_ = 8>
 struct SimtConfig {
   static constexpr int WARPS_M = WARPS_M_;
   static constexpr int WARPS_N = WARPS_N_;
@@ -78,8 +118,12 @@ struct SimtConfig {
   static constexpr bool B_KMAJOR = B_KMAJOR_;
   static constexpr int STAGES = STAGES_;
   static constexpr int PRODUCER = PRODUCER_;
+  // Thread tile 8 x TN (TN = 8 or 16); warp tile 32 x 8*TN; lanes 4 x 8.
+  static constexpr int TN = TN_;
+  static constexpr int WN = 8 * TN;
   static constexpr int BM = 32 * WARPS_M;
-  static constexpr int BN = 64 * WARPS_N;
+  static constexpr int BN = WN * WARPS_N;
+  static_assert(TN == 8 || (TN == 16 && !B_KMAJOR), "16-wide thread tiles need n-contiguous op(B)");
   static constexpr int BK = 32;
   static constexpr int MATH_WARPS = WARPS_M * WARPS_N;
   static constexpr int MATH_THREADS = 32 * MATH_WARPS;
@@ -136,17 +180,17 @@ __device__ __forceinline__ void produce_tma(const SimtParams &p, const CUtensorM
                                             const CUtensorMap *tmB, uint32_t smem_base,
                                             uint32_t full0, uint32_t empty0, bool &ok) {
   uint32_t it = 0;
-  for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+  for_each_unit(p, [&](const WorkUnit &u) {
     int tm, tn;
-    tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    tile_coords(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     const int m0 = tm * Cfg::BM, n0 = tn * Cfg::BN;
-    for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+    for (int kt = u.k0; kt < u.k1; ++kt, ++it) {
       const uint32_t s = it % Cfg::STAGES;
       const uint32_t round = it / Cfg::STAGES;
       if (round > 0 &&
           !wait_parity_bounded(empty0 + 8 * s, (round - 1) & 1, p.wait_budget_ns, p.status)) {
         ok = false;
-        break;
+        return false;
       }
       const uint32_t full = full0 + 8 * s;
       const uint32_t a_dst = smem_base + s * Cfg::STAGE_BYTES;
@@ -162,7 +206,8 @@ __device__ __forceinline__ void produce_tma(const SimtParams &p, const CUtensorM
       else
         tma_load_2d(b_dst, tmB, full, n0, k0);
     }
-  }
+    return true;
+  });
   if (!ok) {
     // Let the copies already issued land before the CTA can end.
     const uint32_t issued = it;
@@ -180,17 +225,17 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
   constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
   constexpr int PT = Cfg::PRODUCER_THREADS;
   uint32_t it = 0;
-  for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+  for_each_unit(p, [&](const WorkUnit &u) {
     int tm, tn;
-    tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    tile_coords(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     const int m0 = tm * BM, n0 = tn * BN;
-    for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+    for (int kt = u.k0; kt < u.k1; ++kt, ++it) {
       const uint32_t s = it % Cfg::STAGES;
       const uint32_t round = it / Cfg::STAGES;
       if (round > 0 &&
           !wait_parity_bounded(empty0 + 8 * s, (round - 1) & 1, p.wait_budget_ns, p.status)) {
         ok = false;
-        break;
+        return false;
       }
       const uint32_t a_dst = smem_base + s * Cfg::STAGE_BYTES;
       const uint32_t b_dst = a_dst + Cfg::A_STAGE_BYTES;
@@ -239,7 +284,8 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
       }
       cp_async_mbar_arrive_noinc(full0 + 8 * s);
     }
-  }
+    return true;
+  });
   // Do not leave while this thread's copies are still in flight.
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -251,22 +297,31 @@ __device__ __forceinline__ int thread_row(int tm, int r) {
 }
 template <class Cfg>
 __device__ __forceinline__ int thread_col(int tn, int c) {
-  return Cfg::B_KMAJOR ? (tn + 8 * c) : ((c < 4) ? (4 * tn + c) : (32 + 4 * tn + (c - 4)));
+  return Cfg::B_KMAJOR ? (tn + 8 * c) : (32 * (c >> 2) + 4 * tn + (c & 3));
 }
 
 // Inner-product options (compile-time):
 //   SG_SIMT_FFMA2     1: packed FP32 FMA (__ffma2_rn: two FMAs per instruction,
 //                        each rounded like fmaf) where the layout gives natural
 //                        register pairs; 0: scalar fmaf everywhere.
-//   SG_SIMT_KC_UNROLL how many 4-k chunks of a 32-k stage are unrolled (1..8).
+//   SG_SIMT_KC_UNROLL, SG_SIMT_KC_UNROLL_WIDE
+//                     how many 4-k chunks of a 32-k stage are unrolled (1..8)
+//                     for 8 x 8 and for 8 x 16 thread tiles (the wider tile
+//                     holds 128 accumulators and spills when unrolled deeper).
 #ifndef SG_SIMT_FFMA2
 #define SG_SIMT_FFMA2 1
 #endif
 #ifndef SG_SIMT_KC_UNROLL
 #define SG_SIMT_KC_UNROLL 8
 #endif
+#ifndef SG_SIMT_KC_UNROLL_WIDE
+#define SG_SIMT_KC_UNROLL_WIDE 1
+#endif
 
-constexpr int kKcUnroll = SG_SIMT_KC_UNROLL;
+template <int TN>
+__host__ __device__ constexpr int kc_unroll() {
+  return TN == 16 ? SG_SIMT_KC_UNROLL_WIDE : SG_SIMT_KC_UNROLL;
+}
 
 // How the 64 accumulators of a thread are packed into 32 float2 and updated.
 // A packed FMA needs both multiplicands as register pairs; one of them is a
@@ -281,24 +336,27 @@ __device__ __host__ constexpr int acc_mode() {
   return !SG_SIMT_FFMA2 ? kScalar : (!Cfg::B_KMAJOR ? kPairCols : (!Cfg::A_KMAJOR ? kPairRows : kScalar));
 }
 
-using Acc = float2[32];
+// 8 x TN accumulators packed as 4*TN float2.
+template <class Cfg>
+using AccT = float2[4 * Cfg::TN];
 
-// Storage slot and half of output (r, c) of the thread's 8 x 8 tile.
-template <int MODE>
-__device__ __forceinline__ float &acc_ref(Acc &acc, int r, int c) {
-  if (MODE == kPairRows) return (r & 1) ? acc[(r >> 1) * 8 + c].y : acc[(r >> 1) * 8 + c].x;
-  return (c & 1) ? acc[r * 4 + (c >> 1)].y : acc[r * 4 + (c >> 1)].x;
+// Storage slot and half of output (r, c) of the thread's 8 x TN tile
+// (kPairRows is only used with TN = 8).
+template <int MODE, int TN, class A>
+__device__ __forceinline__ float &acc_ref(A &acc, int r, int c) {
+  if (MODE == kPairRows) return (r & 1) ? acc[(r >> 1) * TN + c].y : acc[(r >> 1) * TN + c].x;
+  return (c & 1) ? acc[r * (TN / 2) + (c >> 1)].y : acc[r * (TN / 2) + (c >> 1)].x;
 }
-template <int MODE>
-__device__ __forceinline__ float acc_get(const Acc &acc, int r, int c) {
-  if (MODE == kPairRows) return (r & 1) ? acc[(r >> 1) * 8 + c].y : acc[(r >> 1) * 8 + c].x;
-  return (c & 1) ? acc[r * 4 + (c >> 1)].y : acc[r * 4 + (c >> 1)].x;
+template <int MODE, int TN, class A>
+__device__ __forceinline__ float acc_get(const A &acc, int r, int c) {
+  if (MODE == kPairRows) return (r & 1) ? acc[(r >> 1) * TN + c].y : acc[(r >> 1) * TN + c].x;
+  return (c & 1) ? acc[r * (TN / 2) + (c >> 1)].y : acc[r * (TN / 2) + (c >> 1)].x;
 }
 
 template <class Cfg>
-__device__ __forceinline__ void mma_stage(Acc &acc, const char *a_stage, const char *b_stage,
+__device__ __forceinline__ void mma_stage(AccT<Cfg> &acc, const char *a_stage, const char *b_stage,
                                           int wm, int wn, int tm, int tn) {
-  constexpr int BM = Cfg::BM, BN = Cfg::BN;
+  constexpr int BM = Cfg::BM, BN = Cfg::BN, TN = Cfg::TN;
   constexpr int MODE = acc_mode<Cfg>();
   // Per-thread base pointers inside the stage.
   const char *a_base;
@@ -308,83 +366,101 @@ __device__ __forceinline__ void mma_stage(Acc &acc, const char *a_stage, const c
   else
     a_base = a_stage + (wm * 32 + 4 * tm) * 4;  // + k * BM * 4, + 64 for rows 16..
   if (Cfg::B_KMAJOR)
-    b_base = b_stage + (wn * 64 + tn) * 128;  // row tn + 8c -> + c * 1024
+    b_base = b_stage + (wn * Cfg::WN + tn) * 128;  // row tn + 8c -> + c * 1024
   else
-    b_base = b_stage + (wn * 64 + 4 * tn) * 4;  // + k * BN * 4, + 128 for cols 32..
+    b_base = b_stage + (wn * Cfg::WN + 4 * tn) * 4;  // + k * BN * 4, + 128 per column group
 
-#pragma unroll kKcUnroll
+  constexpr int KC_UNROLL = kc_unroll<TN>();
+#pragma unroll KC_UNROLL
   for (int kc = 0; kc < 8; ++kc) {  // 4 k per chunk
-    float a[8][4];  // a[r][kk]
-    float b[4][8];  // b[kk][c]
-    if (Cfg::A_KMAJOR) {
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        // row = wm*32 + tm + 4r: (row & 7) = tm | 4*(r&1)
-        const int sw = (kc ^ (tm | ((r & 1) << 2))) << 4;
-        const float4 v = *reinterpret_cast<const float4 *>(a_base + r * 512 + sw);
-        a[r][0] = v.x; a[r][1] = v.y; a[r][2] = v.z; a[r][3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const char *row = a_base + (kc * 4 + kk) * BM * 4;
-        const float4 v0 = *reinterpret_cast<const float4 *>(row);
-        const float4 v1 = *reinterpret_cast<const float4 *>(row + 64);
-        a[0][kk] = v0.x; a[1][kk] = v0.y; a[2][kk] = v0.z; a[3][kk] = v0.w;
-        a[4][kk] = v1.x; a[5][kk] = v1.y; a[6][kk] = v1.z; a[7][kk] = v1.w;
-      }
-    }
+    float bk[4][8];  // k-contiguous op(B) (TN == 8): bk[kk][c]
     if (Cfg::B_KMAJOR) {
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         // row = wn*64 + tn + 8c: (row & 7) = tn
         const int sw = (kc ^ tn) << 4;
         const float4 v = *reinterpret_cast<const float4 *>(b_base + c * 1024 + sw);
-        b[0][c] = v.x; b[1][c] = v.y; b[2][c] = v.z; b[3][c] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const char *row = b_base + (kc * 4 + kk) * BN * 4;
-        const float4 v0 = *reinterpret_cast<const float4 *>(row);
-        const float4 v1 = *reinterpret_cast<const float4 *>(row + 128);
-        b[kk][0] = v0.x; b[kk][1] = v0.y; b[kk][2] = v0.z; b[kk][3] = v0.w;
-        b[kk][4] = v1.x; b[kk][5] = v1.y; b[kk][6] = v1.z; b[kk][7] = v1.w;
+        bk[0][c] = v.x; bk[1][c] = v.y; bk[2][c] = v.z; bk[3][c] = v.w;
       }
     }
+    // op(A) values are loaded KA k at a time (k-contiguous: one LDS of KA floats
+    // per row; the wavefront count is the same for KA = 2 and 4, KA = 2 holds
+    // half the registers, which the 8 x 16 tile needs).
+    constexpr int KA = (TN == 16) ? 2 : 4;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      if (MODE == kPairCols) {
+    for (int kg = 0; kg < 4 / KA; ++kg) {
+      float a[8][KA];  // a[r][j] = op(A)(row r, k = kc*4 + kg*KA + j)
+      if (Cfg::A_KMAJOR) {
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-          const float2 ar = make_float2(a[r][kk], a[r][kk]);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            acc[r * 4 + q] = __ffma2_rn(ar, make_float2(b[kk][2 * q], b[kk][2 * q + 1]), acc[r * 4 + q]);
-        }
-      } else if (MODE == kPairRows) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float2 bc = make_float2(b[kk][c], b[kk][c]);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            acc[q * 8 + c] = __ffma2_rn(make_float2(a[2 * q][kk], a[2 * q + 1][kk]), bc, acc[q * 8 + c]);
+          // row = wm*32 + tm + 4r: (row & 7) = tm | 4*(r&1)
+          const char *src = a_base + r * 512 + ((kc ^ (tm | ((r & 1) << 2))) << 4) + kg * KA * 4;
+          if constexpr (KA == 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(src);
+            a[r][0] = v.x; a[r][1] = v.y; a[r][2] = v.z; a[r][3] = v.w;
+          } else {
+            const float2 v = *reinterpret_cast<const float2 *>(src);
+            a[r][0] = v.x; a[r][1] = v.y;
+          }
         }
       } else {
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+        for (int j = 0; j < KA; ++j) {
+          const char *row = a_base + (kc * 4 + kg * KA + j) * BM * 4;
+          const float4 v0 = *reinterpret_cast<const float4 *>(row);
+          const float4 v1 = *reinterpret_cast<const float4 *>(row + 64);
+          a[0][j] = v0.x; a[1][j] = v0.y; a[2][j] = v0.z; a[3][j] = v0.w;
+          a[4][j] = v1.x; a[5][j] = v1.y; a[6][j] = v1.z; a[7][j] = v1.w;
+        }
+      }
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            acc_ref<kScalar>(acc, r, c) = fmaf(a[r][kk], b[kk][c], acc_ref<kScalar>(acc, r, c));
+      for (int j = 0; j < KA; ++j) {
+        const int kk = kg * KA + j;
+        float b[TN];
+        if (Cfg::B_KMAJOR) {
+#pragma unroll
+          for (int c = 0; c < TN; ++c) b[c] = bk[kk][c];
+        } else {
+          const char *row = b_base + (kc * 4 + kk) * BN * 4;
+#pragma unroll
+          for (int h = 0; h < TN / 4; ++h) {
+            const float4 v = *reinterpret_cast<const float4 *>(row + h * 128);
+            b[4 * h + 0] = v.x; b[4 * h + 1] = v.y; b[4 * h + 2] = v.z; b[4 * h + 3] = v.w;
+          }
+        }
+        if (MODE == kPairCols) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const float2 ar = make_float2(a[r][j], a[r][j]);
+#pragma unroll
+            for (int q = 0; q < TN / 2; ++q)
+              acc[r * (TN / 2) + q] =
+                  __ffma2_rn(ar, make_float2(b[2 * q], b[2 * q + 1]), acc[r * (TN / 2) + q]);
+          }
+        } else if (MODE == kPairRows) {
+#pragma unroll
+          for (int c = 0; c < TN; ++c) {
+            const float2 bc = make_float2(b[c], b[c]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              acc[q * TN + c] = __ffma2_rn(make_float2(a[2 * q][j], a[2 * q + 1][j]), bc, acc[q * TN + c]);
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int c = 0; c < TN; ++c)
+              acc_ref<kScalar, TN>(acc, r, c) = fmaf(a[r][j], b[c], acc_ref<kScalar, TN>(acc, r, c));
+        }
       }
     }
   }
 }
 
 template <class Cfg>
-__device__ __forceinline__ void epilogue(const SimtParams &p, const Acc &acc, int m0, int n0,
-                                         int wm, int wn, int tm, int tn) {
-  constexpr int MODE = acc_mode<Cfg>();
+__device__ __forceinline__ void epilogue(const SimtParams &p, const AccT<Cfg> &acc, int m0,
+                                         int n0, int wm, int wn, int tm, int tn) {
+  constexpr int MODE = acc_mode<Cfg>(), TN = Cfg::TN;
   const bool read_c = p.beta != 0.0f;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
@@ -392,13 +468,13 @@ __device__ __forceinline__ void epilogue(const SimtParams &p, const Acc &acc, in
     if (m >= p.M) continue;
     float *crow = p.C + static_cast<int64_t>(m) * p.ldc;
     if (!Cfg::B_KMAJOR) {
-      // columns 4tn..4tn+3 and 32+4tn..32+4tn+3: two float4 groups
+      // columns 32h + 4tn .. +3: TN/4 float4 groups
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int n = n0 + wn * 64 + h * 32 + 4 * tn;
+      for (int h = 0; h < TN / 4; ++h) {
+        const int n = n0 + wn * Cfg::WN + h * 32 + 4 * tn;
         float v[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = acc_get<MODE>(acc, r, 4 * h + q);
+        for (int q = 0; q < 4; ++q) v[q] = acc_get<MODE, TN>(acc, r, 4 * h + q);
         if (p.c_vec4 && n + 3 < p.N) {
           float4 o;
           if (read_c) {
@@ -423,13 +499,38 @@ __device__ __forceinline__ void epilogue(const SimtParams &p, const Acc &acc, in
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int n = n0 + wn * 64 + thread_col<Cfg>(tn, c);
+      for (int c = 0; c < TN; ++c) {
+        const int n = n0 + wn * Cfg::WN + thread_col<Cfg>(tn, c);
         if (n < p.N) {
-          const float a = acc_get<MODE>(acc, r, c);
+          const float a = acc_get<MODE, TN>(acc, r, c);
           crow[n] = read_c ? fmaf(p.alpha, a, p.beta * crow[n]) : p.alpha * a;
         }
       }
+    }
+  }
+}
+
+// Raw sums of a k-segment (no alpha/beta) to a dense BM x BN workspace tile.
+template <class Cfg>
+__device__ __forceinline__ void store_partial(float *ws, const AccT<Cfg> &acc, int wm, int wn,
+                                              int tm, int tn) {
+  constexpr int MODE = acc_mode<Cfg>(), TN = Cfg::TN;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    float *row = ws + static_cast<int64_t>(wm * 32 + thread_row<Cfg>(tm, r)) * Cfg::BN + wn * Cfg::WN;
+    if (!Cfg::B_KMAJOR) {
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h) {
+        float4 o;
+        o.x = acc_get<MODE, TN>(acc, r, 4 * h + 0);
+        o.y = acc_get<MODE, TN>(acc, r, 4 * h + 1);
+        o.z = acc_get<MODE, TN>(acc, r, 4 * h + 2);
+        o.w = acc_get<MODE, TN>(acc, r, 4 * h + 3);
+        *reinterpret_cast<float4 *>(row + h * 32 + 4 * tn) = o;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < TN; ++c) row[thread_col<Cfg>(tn, c)] = acc_get<MODE, TN>(acc, r, c);
     }
   }
 }
@@ -483,28 +584,29 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
   const int tm = lane >> 3;
   const int tn = lane & 7;
   uint32_t it = 0;
-  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+  for_each_unit(p, [&](const WorkUnit &u) {
     int tile_m, tile_n;
-    tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tile_m, tile_n);
-    Acc acc;
+    tile_coords(u.tile, p.tiles_m, p.tiles_n, p.group_m, tile_m, tile_n);
+    AccT<Cfg> acc;
 #pragma unroll
-    for (int q = 0; q < 32; ++q) acc[q] = make_float2(0.0f, 0.0f);
+    for (int q = 0; q < 4 * Cfg::TN; ++q) acc[q] = make_float2(0.0f, 0.0f);
 
-    for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+    for (int kt = u.k0; kt < u.k1; ++kt, ++it) {
       const uint32_t s = it % Cfg::STAGES;
       const uint32_t round = it / Cfg::STAGES;
-      if (!wait_parity_bounded(full0 + 8 * s, round & 1, p.wait_budget_ns, p.status)) {
-        ok = false;
-        break;
-      }
+      if (!wait_parity_bounded(full0 + 8 * s, round & 1, p.wait_budget_ns, p.status)) return false;
       const char *a_stage = reinterpret_cast<const char *>(smem) + s * Cfg::STAGE_BYTES;
       mma_stage<Cfg>(acc, a_stage, a_stage + Cfg::A_STAGE_BYTES, wm, wn, tm, tn);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
-    if (!ok) break;
-    epilogue<Cfg>(p, acc, tile_m * Cfg::BM, tile_n * Cfg::BN, wm, wn, tm, tn);
-  }
+    if (u.slot < 0)
+      epilogue<Cfg>(p, acc, tile_m * Cfg::BM, tile_n * Cfg::BN, wm, wn, tm, tn);
+    else
+      store_partial<Cfg>(p.workspace + static_cast<int64_t>(u.slot) * Cfg::BM * Cfg::BN, acc, wm, wn,
+                         tm, tn);
+    return true;
+  });
 }
 
 }  // namespace sg

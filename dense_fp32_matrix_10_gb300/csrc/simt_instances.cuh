@@ -51,6 +51,10 @@ template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR>
 struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x64> {
   using Cfg = SimtConfig<4, 1, A_KMAJOR, B_KMAJOR, 4, PRODUCER>;
 };
+template <int PRODUCER, bool A_KMAJOR>
+struct SimtPick<PRODUCER, A_KMAJOR, false, kTile128x256> {
+  using Cfg = SimtConfig<4, 2, A_KMAJOR, false, 4, PRODUCER, 16>;
+};
 
 template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR, int TILE>
 SimtEntry simt_make_entry() {
@@ -60,15 +64,18 @@ SimtEntry simt_make_entry() {
 
 // A stored M x K (transA = N) is the k-contiguous ("K-major") layout; B stored
 // N x K (transB = T) likewise.
+// The 128 x 256 tile exists only for n-contiguous op(B) (transB = N); a
+// request for it with transB = T gets the 128 x 128 tile.
 #define SG_DEFINE_SIMT_FAMILY(PROD, TA)                                                  \
   SimtEntry simt_entry_##PROD##_##TA(int transB, int tile) {                             \
     constexpr bool AK = (TA == 0);                                                       \
     if (transB == 0) {                                                                   \
+      if (tile == kTile128x256) return simt_make_entry<PROD, AK, false, kTile128x256>(); \
       return tile == kTile128x128 ? simt_make_entry<PROD, AK, false, kTile128x128>()     \
                                   : simt_make_entry<PROD, AK, false, kTile128x64>();      \
     }                                                                                    \
-    return tile == kTile128x128 ? simt_make_entry<PROD, AK, true, kTile128x128>()        \
-                                : simt_make_entry<PROD, AK, true, kTile128x64>();         \
+    return tile == kTile128x64 ? simt_make_entry<PROD, AK, true, kTile128x64>()          \
+                               : simt_make_entry<PROD, AK, true, kTile128x128>();        \
   }
 
 }  // namespace sg

@@ -1,0 +1,84 @@
+// sk_fixup.cu -- second pass of a stream-K launch of the CUDA-core kernel.
+//
+// The k-iterations of the last sk tiles were divided evenly over the G CTAs of
+// the main kernel; a tile whose iterations were spread over several CTAs left
+// one raw partial sum per CTA segment in the workspace.  One block per such
+// tile adds the partials in increasing k order (so the result is the same on
+// every run) and writes C = alpha * sum + beta * C (C not read when beta == 0).
+#include "internal.h"
+
+namespace sg {
+
+constexpr int kMaxSkSegments = 128;  // the host keeps every tile below this
+
+__device__ __forceinline__ int64_t sk_start(int64_t g, int64_t S, int64_t G) { return g * S / G; }
+
+__global__ void __launch_bounds__(256) sk_fixup_kernel(const SimtParams p, int bm, int bn,
+                                                       int grid_main) {
+  __shared__ int s_slot[kMaxSkSegments];
+  __shared__ int s_count;
+  if (threadIdx.x == 0) {
+    const int64_t KT = p.k_tiles, S = p.sk_iters, G = grid_main;
+    const int64_t it0 = static_cast<int64_t>(blockIdx.x) * KT, it1 = it0 + KT;
+    // CTAs whose iteration ranges meet [it0, it1), in increasing k order
+    int64_t g = it0 * G / S;
+    while (g + 1 < G && sk_start(g + 1, S, G) <= it0) ++g;
+    while (g > 0 && sk_start(g, S, G) > it0) --g;
+    int n = 0;
+    for (; g < G; ++g) {
+      const int64_t a = sk_start(g, S, G), b = sk_start(g + 1, S, G);
+      if (a >= it1) break;
+      if ((a > it0 ? a : it0) >= (b < it1 ? b : it1)) continue;  // empty segment
+      if (n < kMaxSkSegments) s_slot[n] = static_cast<int>(2 * g + (a >= it0 ? 0 : 1));
+      ++n;
+    }
+    // one segment: that CTA covered the whole tile and wrote C itself
+    s_count = (n <= 1 || n > kMaxSkSegments) ? 0 : n;
+  }
+  __syncthreads();
+  const int n = s_count;
+  if (n == 0) return;
+
+  int tm, tn;
+  tile_coords(p.dp_tiles + blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+  const int64_t tile_elems = static_cast<int64_t>(bm) * bn;
+  const bool read_c = p.beta != 0.0f;
+  // 4 consecutive columns per thread step (bn is a multiple of 64)
+  for (int e = 4 * threadIdx.x; e < bm * bn; e += 4 * blockDim.x) {
+    float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int i = 0; i < n; ++i) {
+      const float4 v = *reinterpret_cast<const float4 *>(p.workspace + s_slot[i] * tile_elems + e);
+      sum.x += v.x;
+      sum.y += v.y;
+      sum.z += v.z;
+      sum.w += v.w;
+    }
+    const int row = tm * bm + e / bn, col = tn * bn + e % bn;
+    if (row >= p.M) continue;
+    float *c = p.C + static_cast<int64_t>(row) * p.ldc + col;
+    const float s4[4] = {sum.x, sum.y, sum.z, sum.w};
+    if (p.c_vec4 && col + 3 < p.N) {
+      float4 o;
+      if (read_c) {
+        const float4 cv = *reinterpret_cast<const float4 *>(c);
+        o = make_float4(fmaf(p.alpha, s4[0], p.beta * cv.x), fmaf(p.alpha, s4[1], p.beta * cv.y),
+                        fmaf(p.alpha, s4[2], p.beta * cv.z), fmaf(p.alpha, s4[3], p.beta * cv.w));
+      } else {
+        o = make_float4(p.alpha * s4[0], p.alpha * s4[1], p.alpha * s4[2], p.alpha * s4[3]);
+      }
+      *reinterpret_cast<float4 *>(c) = o;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (col + q < p.N) c[q] = read_c ? fmaf(p.alpha, s4[q], p.beta * c[q]) : p.alpha * s4[q];
+    }
+  }
+}
+
+cudaError_t launch_sk_fixup(const SimtParams &p, int bm, int bn, int grid_main, int sk_tiles,
+                            cudaStream_t s) {
+  sk_fixup_kernel<<<sk_tiles, 256, 0, s>>>(p, bm, bn, grid_main);
+  return cudaGetLastError();
+}
+
+}  // namespace sg

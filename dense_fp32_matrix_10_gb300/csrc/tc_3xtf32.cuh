@@ -1,38 +1,37 @@
 // tc_3xtf32.cuh -- FP32 GEMM on the 5th-generation tensor cores (tcgen05,
 // TMEM accumulators) with the 3xTF32 split.
 //
-// Every FP32 operand x is split into two TF32 values,
-//     x_big = tf32(x)            (round to nearest, 10 explicit mantissa bits)
-//     x_small = tf32(x - x_big)  (x - x_big is exact in FP32)
-// and each product is taken as a_small*b_big + a_big*b_small + a_big*b_big,
-// three kind::tf32 MMAs accumulating in FP32 in tensor memory.  The dropped
-// a_small*b_small term and the rounding of the small parts are ~2^-21 relative
-// to |a*b|, below the FP32 accumulation error of a long dot product, so the
-// result meets the same tolerance as the CUDA-core kernels; integers of at most
-// 11 significant bits split exactly (small part 0), so integer-valued products
-// stay exact.
+// Every FP32 operand x is taken as the sum of two TF32 values,
+//     x_big   = x with its low 13 mantissa bits dropped (what the tensor core
+//               reads when handed the FP32 word itself),
+//     x_small = tf32(x - x_big)   (x - x_big is exact in FP32; rounded to nearest),
+// and each product as a_small*b_big + a_big*b_small + a_big*b_big: three
+// kind::tf32 MMAs accumulating in FP32 in tensor memory.  The dropped
+// a_small*b_small term and the rounding of the small parts are ~2^-20 relative
+// to |a*b|, below the FP32 accumulation error of a long dot product;
+// integer-valued inputs of at most 11 significant bits have small = 0, so
+// integer products stay exact.  Non-finite inputs get small = 0.
 //
+// Both MMA operands are read K-major (128-byte rows of 32 k, 128 B swizzle).
 // Roles (one persistent CTA of 12 warps per SM, 128 x 128 output tiles, k in
 // slices of 32):
-//   warp 0       TMA producer: FP32 op(A), op(B) k-slices into a 2-stage raw ring
-//                (k-contiguous operands with the 128 B swizzle, m/n-contiguous
-//                ones dense);
-//   warps 8..11  converters: raw FP32 -> big and small TF32 tiles in the
-//                K-major 128 B-swizzled layout the MMA reads (transposing the
-//                m/n-contiguous operands on the way), 2-stage ring;
-//   warp 1       allocates 256 TMEM columns (two 128-column accumulators) and
-//                one thread issues 3 x 4 MMAs (128 x 128 x 8) per k-slice,
-//                committing each slice to its ring barrier and each finished
-//                tile to the epilogue;
-//   warps 4..7   epilogue: tcgen05.ld of the accumulator (warp 4+q owns TMEM
-//                lanes 32q..32q+31 = tile rows), alpha/beta, stores to C;
-//                the other accumulator is being filled meanwhile.
+//   warp 0       TMA producer.  A k-contiguous operand (A stored M x K, B stored
+//                N x K) lands straight in the MMA ring as a [128][32] box and
+//                serves as its own big part.  An m/n-contiguous operand lands in
+//                a 2-stage raw ring as a dense [32 k][128 mn] box;
+//   warps 8..11  converters: for a k-contiguous operand write small = tf32(x -
+//                x_big) beside the raw tile (elementwise, same layout); for an
+//                m/n-contiguous one build both x_big and x_small tiles K-major
+//                from the raw ring (a transpose through shared memory);
+//   warp 1       allocates 256 TMEM columns (two 128-column accumulators); one
+//                thread issues 3 MMAs (128 x 128 x 8) per k8;
+//   warps 4..7   epilogue (warp 4+q owns TMEM lanes 32q..32q+31 = tile rows).
 // Accuracy: the tensor core's FP32 accumulator rounds toward zero on every MMA
-// (measured: the error of a 4096-long accumulation grows to ~3e-5 relative,
-// linearly in K).  So TMEM accumulates only CHUNK_KTILES k-slices (256 k) at a
-// time; the epilogue warps add each finished chunk into FP32 registers with
-// round-to-nearest adds, and write C after the last chunk.  The directed
-// error then stays at the size of one chunk's, independent of K.
+// (measured: a 4096-long accumulation drifts to ~3e-5 relative, linearly in K).
+// So TMEM accumulates only CHUNK_KTILES k-slices (256 k) at a time; the
+// epilogue warps add each finished chunk into FP32 registers with
+// round-to-nearest adds and write C after the last chunk.  The directed error
+// stays at the size of one chunk's, independent of K.
 // All waits are bounded; on give-up every role leaves its loop, in-flight
 // copies and MMAs are drained (bounded) and TMEM is freed before the CTA ends.
 #pragma once
@@ -62,16 +61,25 @@ struct TcConfig {
   static constexpr bool A_KMAJOR = A_KMAJOR_;
   static constexpr bool B_KMAJOR = B_KMAJOR_;
   static constexpr int BM = 128, BN = 128, BK = 32;
-  static constexpr int RAW_STAGES = 2, CONV_STAGES = 2;
-  static constexpr int TILE_BYTES = 128 * 32 * 4;          // one 128 x 32 FP32 tile
-  static constexpr int RAW_STAGE_BYTES = 2 * TILE_BYTES;   // A, B
-  static constexpr int CONV_STAGE_BYTES = 4 * TILE_BYTES;  // A big, A small, B big, B small
-  static constexpr int RAW_OFFSET = 0;
-  static constexpr int CONV_OFFSET = RAW_STAGES * RAW_STAGE_BYTES;
-  static constexpr int BAR_OFFSET = CONV_OFFSET + CONV_STAGES * CONV_STAGE_BYTES;
-  // raw_full, raw_empty, conv_full, conv_empty, acc_full[2], acc_empty[2], drain
-  static constexpr int NUM_BARS = 2 * RAW_STAGES + 2 * CONV_STAGES + 4 + 1;
+  static constexpr int TILE_BYTES = 128 * 32 * 4;  // one 128 x 32 FP32 tile
+  // MMA ring stage: A big, A small, B big, B small (K-major, 128 B swizzle).
+  // A k-contiguous operand's big tile is its raw TMA tile.
+  static constexpr int STAGE_BYTES = 4 * TILE_BYTES;
+  static constexpr int A_BIG = 0, A_SMALL = TILE_BYTES, B_BIG = 2 * TILE_BYTES,
+                       B_SMALL = 3 * TILE_BYTES;
+  // Raw ring: the m/n-contiguous operands' FP32 slices, dense [32 k][128 mn].
+  static constexpr int RAW_OPERANDS = (A_KMAJOR ? 0 : 1) + (B_KMAJOR ? 0 : 1);
+  static constexpr int RAW_STAGES = RAW_OPERANDS ? 2 : 0;
+  static constexpr int RAW_STAGE_BYTES = RAW_OPERANDS * TILE_BYTES;
+  static constexpr int STAGES = (RAW_OPERANDS == 2) ? 2 : 3;
+  static constexpr int RAW_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int RAW_A = 0, RAW_B = A_KMAJOR ? 0 : TILE_BYTES;  // within a raw stage
+  static constexpr int BAR_OFFSET = RAW_OFFSET + RAW_STAGES * RAW_STAGE_BYTES;
+  // full, conv_full, empty per stage; raw_full, raw_empty per raw stage;
+  // acc_full[2], acc_empty[2]; drain
+  static constexpr int NUM_BARS = 3 * STAGES + 2 * 2 + 4 + 1;
   static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
+  static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
   static constexpr int THREADS = 384;
   static constexpr int TMEM_COLS = 256;
   static constexpr uint32_t IDESC = idesc_tf32(128, 128);
@@ -88,19 +96,14 @@ struct TcConfig {
 template <class Cfg>
 struct TcBars {
   uint32_t base;
-  __device__ uint32_t raw_full(uint32_t s) const { return base + 8 * s; }
-  __device__ uint32_t raw_empty(uint32_t s) const { return base + 8 * (Cfg::RAW_STAGES + s); }
-  __device__ uint32_t conv_full(uint32_t s) const { return base + 8 * (2 * Cfg::RAW_STAGES + s); }
-  __device__ uint32_t conv_empty(uint32_t s) const {
-    return base + 8 * (2 * Cfg::RAW_STAGES + Cfg::CONV_STAGES + s);
-  }
-  __device__ uint32_t acc_full(uint32_t b) const {
-    return base + 8 * (2 * Cfg::RAW_STAGES + 2 * Cfg::CONV_STAGES + b);
-  }
-  __device__ uint32_t acc_empty(uint32_t b) const {
-    return base + 8 * (2 * Cfg::RAW_STAGES + 2 * Cfg::CONV_STAGES + 2 + b);
-  }
-  __device__ uint32_t drain() const { return base + 8 * (2 * Cfg::RAW_STAGES + 2 * Cfg::CONV_STAGES + 4); }
+  __device__ uint32_t full(uint32_t s) const { return base + 8 * s; }
+  __device__ uint32_t conv_full(uint32_t s) const { return base + 8 * (Cfg::STAGES + s); }
+  __device__ uint32_t empty(uint32_t s) const { return base + 8 * (2 * Cfg::STAGES + s); }
+  __device__ uint32_t raw_full(uint32_t r) const { return base + 8 * (3 * Cfg::STAGES + r); }
+  __device__ uint32_t raw_empty(uint32_t r) const { return base + 8 * (3 * Cfg::STAGES + 2 + r); }
+  __device__ uint32_t acc_full(uint32_t b) const { return base + 8 * (3 * Cfg::STAGES + 4 + b); }
+  __device__ uint32_t acc_empty(uint32_t b) const { return base + 8 * (3 * Cfg::STAGES + 6 + b); }
+  __device__ uint32_t drain() const { return base + 8 * (3 * Cfg::STAGES + 8); }
 };
 
 // ------------------------------------------------------------------ producer
@@ -108,110 +111,140 @@ template <class Cfg>
 __device__ __forceinline__ void tc_produce(const TcParams &p, const CUtensorMap *tmA,
                                            const CUtensorMap *tmB, uint32_t sbase,
                                            const TcBars<Cfg> &bar) {
-  uint32_t it = 0;
+  constexpr bool ANY_K = Cfg::A_KMAJOR || Cfg::B_KMAJOR;
+  constexpr uint32_t K_BYTES = ((Cfg::A_KMAJOR ? 1 : 0) + (Cfg::B_KMAJOR ? 1 : 0)) * Cfg::TILE_BYTES;
+  uint32_t it = 0;        // k-slices whose copies are all issued
+  bool k_issued = false;  // the k-contiguous part of slice `it` is issued
   bool ok = true;
   for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
     int tm, tn;
     tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     const int m0 = tm * Cfg::BM, n0 = tn * Cfg::BN;
-    for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
-      const uint32_t s = it % Cfg::RAW_STAGES, round = it / Cfg::RAW_STAGES;
-      if (round > 0 &&
-          !wait_parity_bounded(bar.raw_empty(s), (round - 1) & 1, p.wait_budget_ns, p.status)) {
-        ok = false;
-        break;
-      }
-      const uint32_t a_dst = sbase + Cfg::RAW_OFFSET + s * Cfg::RAW_STAGE_BYTES;
-      const uint32_t b_dst = a_dst + Cfg::TILE_BYTES;
-      mbar_arrive_expect_tx(bar.raw_full(s), Cfg::RAW_STAGE_BYTES);
+    for (int kt = 0; kt < p.k_tiles; ++kt, ++it, k_issued = false) {
       const int k0 = kt * Cfg::BK;
-      if (Cfg::A_KMAJOR)
-        tma_load_2d(a_dst, tmA, bar.raw_full(s), k0, m0);
-      else
-        tma_load_2d(a_dst, tmA, bar.raw_full(s), m0, k0);
-      if (Cfg::B_KMAJOR)
-        tma_load_2d(b_dst, tmB, bar.raw_full(s), k0, n0);
-      else
-        tma_load_2d(b_dst, tmB, bar.raw_full(s), n0, k0);
+      if (ANY_K) {  // k-contiguous operands straight into the MMA ring
+        const uint32_t s = it % Cfg::STAGES, round = it / Cfg::STAGES;
+        if (round > 0 &&
+            !wait_parity_bounded(bar.empty(s), (round - 1) & 1, p.wait_budget_ns, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t st = sbase + s * Cfg::STAGE_BYTES;
+        mbar_arrive_expect_tx(bar.full(s), K_BYTES);
+        if (Cfg::A_KMAJOR) tma_load_2d(st + Cfg::A_BIG, tmA, bar.full(s), k0, m0);
+        if (Cfg::B_KMAJOR) tma_load_2d(st + Cfg::B_BIG, tmB, bar.full(s), k0, n0);
+        k_issued = true;
+      }
+      if (Cfg::RAW_OPERANDS) {  // m/n-contiguous operands into the raw ring
+        const uint32_t r = it % 2, rround = it / 2;
+        if (rround > 0 &&
+            !wait_parity_bounded(bar.raw_empty(r), (rround - 1) & 1, p.wait_budget_ns, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t rs = sbase + Cfg::RAW_OFFSET + r * Cfg::RAW_STAGE_BYTES;
+        mbar_arrive_expect_tx(bar.raw_full(r), Cfg::RAW_STAGE_BYTES);
+        if (!Cfg::A_KMAJOR) tma_load_2d(rs + Cfg::RAW_A, tmA, bar.raw_full(r), m0, k0);
+        if (!Cfg::B_KMAJOR) tma_load_2d(rs + Cfg::RAW_B, tmB, bar.raw_full(r), n0, k0);
+      }
     }
   }
-  if (!ok) {  // let issued copies land before the CTA can end
-    const uint32_t first = it > Cfg::RAW_STAGES ? it - Cfg::RAW_STAGES : 0;
-    for (uint32_t j = first; j < it; ++j)
-      wait_parity_bounded(bar.raw_full(j % Cfg::RAW_STAGES), (j / Cfg::RAW_STAGES) & 1,
-                          p.wait_budget_ns, nullptr);
+  if (!ok) {  // let issued copies land before the CTA can end (bounded waits)
+    const uint32_t first = it > 3 ? it - 3 : 0;
+    for (uint32_t j = first; j < it; ++j) {
+      if (ANY_K)
+        wait_parity_bounded(bar.full(j % Cfg::STAGES), (j / Cfg::STAGES) & 1, p.wait_budget_ns,
+                            nullptr);
+      if (Cfg::RAW_OPERANDS)
+        wait_parity_bounded(bar.raw_full(j % 2), (j / 2) & 1, p.wait_budget_ns, nullptr);
+    }
+    if (k_issued)
+      wait_parity_bounded(bar.full(it % Cfg::STAGES), (it / Cfg::STAGES) & 1, p.wait_budget_ns,
+                          nullptr);
   }
 }
 
 // ------------------------------------------------------------------ converters
-__device__ __forceinline__ void split4(const float4 x, float4 &big, float4 &small) {
-  big.x = to_tf32(x.x);
-  big.y = to_tf32(x.y);
-  big.z = to_tf32(x.z);
-  big.w = to_tf32(x.w);
-  small.x = to_tf32(x.x - big.x);
-  small.y = to_tf32(x.y - big.y);
-  small.z = to_tf32(x.z - big.z);
-  small.w = to_tf32(x.w - big.w);
+__device__ __forceinline__ float small_part(float x, float big) {
+  return isfinite(x) ? to_tf32(x - big) : 0.0f;
 }
 
-// One 128 x 32 operand tile: raw FP32 (as the TMA left it) -> big and small
-// TF32 tiles, K-major with the 128 B swizzle.  ct = converter thread 0..127.
-template <bool KMAJOR>
-__device__ __forceinline__ void convert_tile(const unsigned char *raw, unsigned char *big,
-                                             unsigned char *small, int ct) {
-  if (KMAJOR) {
-    // Raw tile already has the destination layout: elementwise, chunk by chunk.
+// k-contiguous operand: small = tf32(x - x_big) beside the raw tile, elementwise
+// (same layout, so the small tile shares the raw tile's descriptor geometry).
+__device__ __forceinline__ void small_of_kmajor(const unsigned char *raw, unsigned char *small,
+                                                int ct) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int off = (ct + 128 * i) * 16;
-      const float4 x = *reinterpret_cast<const float4 *>(raw + off);
-      float4 b, s;
-      split4(x, b, s);
-      *reinterpret_cast<float4 *>(big + off) = b;
-      *reinterpret_cast<float4 *>(small + off) = s;
-    }
-  } else {
-    // Raw tile is [32 k][128 mn] (512 B rows); thread ct builds row mn = ct.
-    const float *r = reinterpret_cast<const float *>(raw);
+  for (int i = 0; i < 8; ++i) {
+    const int off = (ct + 128 * i) * 16;
+    const float4 x = *reinterpret_cast<const float4 *>(raw + off);
+    float4 s;
+    s.x = small_part(x.x, tf32_trunc(x.x));
+    s.y = small_part(x.y, tf32_trunc(x.y));
+    s.z = small_part(x.z, tf32_trunc(x.z));
+    s.w = small_part(x.w, tf32_trunc(x.w));
+    *reinterpret_cast<float4 *>(small + off) = s;
+  }
+}
+
+// m/n-contiguous operand: raw [32 k][128 mn] -> K-major big and small tiles
+// (128-byte rows of 32 k, 128 B swizzle); converter thread ct builds row ct.
+__device__ __forceinline__ void split_of_mnmajor(const unsigned char *raw, unsigned char *big,
+                                                 unsigned char *small, int ct) {
+  const float *r = reinterpret_cast<const float *>(raw);
 #pragma unroll
-    for (int kc = 0; kc < 8; ++kc) {
-      float4 x;
-      x.x = r[(4 * kc + 0) * 128 + ct];
-      x.y = r[(4 * kc + 1) * 128 + ct];
-      x.z = r[(4 * kc + 2) * 128 + ct];
-      x.w = r[(4 * kc + 3) * 128 + ct];
-      float4 b, s;
-      split4(x, b, s);
-      const int off = ct * 128 + ((kc ^ (ct & 7)) << 4);
-      *reinterpret_cast<float4 *>(big + off) = b;
-      *reinterpret_cast<float4 *>(small + off) = s;
-    }
+  for (int kc = 0; kc < 8; ++kc) {
+    float4 x;
+    x.x = r[(4 * kc + 0) * 128 + ct];
+    x.y = r[(4 * kc + 1) * 128 + ct];
+    x.z = r[(4 * kc + 2) * 128 + ct];
+    x.w = r[(4 * kc + 3) * 128 + ct];
+    float4 b, s;
+    b.x = tf32_trunc(x.x);
+    b.y = tf32_trunc(x.y);
+    b.z = tf32_trunc(x.z);
+    b.w = tf32_trunc(x.w);
+    s.x = small_part(x.x, b.x);
+    s.y = small_part(x.y, b.y);
+    s.z = small_part(x.z, b.z);
+    s.w = small_part(x.w, b.w);
+    const int off = ct * 128 + ((kc ^ (ct & 7)) << 4);
+    *reinterpret_cast<float4 *>(big + off) = b;
+    *reinterpret_cast<float4 *>(small + off) = s;
   }
 }
 
 template <class Cfg>
 __device__ __forceinline__ void tc_convert(const TcParams &p, unsigned char *smem,
                                            const TcBars<Cfg> &bar, int ct, int lane) {
+  constexpr bool ANY_K = Cfg::A_KMAJOR || Cfg::B_KMAJOR;
   uint32_t it = 0;
   for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
     for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
-      const uint32_t rs = it % Cfg::RAW_STAGES, rr = it / Cfg::RAW_STAGES;
-      const uint32_t cs = it % Cfg::CONV_STAGES, cr = it / Cfg::CONV_STAGES;
-      if (!wait_parity_bounded(bar.raw_full(rs), rr & 1, p.wait_budget_ns, p.status)) return;
-      if (cr > 0 &&
-          !wait_parity_bounded(bar.conv_empty(cs), (cr - 1) & 1, p.wait_budget_ns, p.status))
+      const uint32_t s = it % Cfg::STAGES, round = it / Cfg::STAGES;
+      const uint32_t r = it % 2, rround = it / 2;
+      // the stage is free once the MMAs of its previous round finished
+      if (round > 0 &&
+          !wait_parity_bounded(bar.empty(s), (round - 1) & 1, p.wait_budget_ns, p.status))
         return;
-      const unsigned char *raw_a = smem + Cfg::RAW_OFFSET + rs * Cfg::RAW_STAGE_BYTES;
-      const unsigned char *raw_b = raw_a + Cfg::TILE_BYTES;
-      unsigned char *cv = smem + Cfg::CONV_OFFSET + cs * Cfg::CONV_STAGE_BYTES;
-      convert_tile<Cfg::A_KMAJOR>(raw_a, cv, cv + Cfg::TILE_BYTES, ct);
-      convert_tile<Cfg::B_KMAJOR>(raw_b, cv + 2 * Cfg::TILE_BYTES, cv + 3 * Cfg::TILE_BYTES, ct);
+      if (ANY_K && !wait_parity_bounded(bar.full(s), round & 1, p.wait_budget_ns, p.status)) return;
+      if (Cfg::RAW_OPERANDS &&
+          !wait_parity_bounded(bar.raw_full(r), rround & 1, p.wait_budget_ns, p.status))
+        return;
+      unsigned char *st = smem + s * Cfg::STAGE_BYTES;
+      const unsigned char *rs = smem + Cfg::RAW_OFFSET + r * Cfg::RAW_STAGE_BYTES;
+      if (Cfg::A_KMAJOR)
+        small_of_kmajor(st + Cfg::A_BIG, st + Cfg::A_SMALL, ct);
+      else
+        split_of_mnmajor(rs + Cfg::RAW_A, st + Cfg::A_BIG, st + Cfg::A_SMALL, ct);
+      if (Cfg::B_KMAJOR)
+        small_of_kmajor(st + Cfg::B_BIG, st + Cfg::B_SMALL, ct);
+      else
+        split_of_mnmajor(rs + Cfg::RAW_B, st + Cfg::B_BIG, st + Cfg::B_SMALL, ct);
       fence_proxy_async_smem();  // the MMA reads these through the async proxy
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar.raw_empty(rs));
-        mbar_arrive(bar.conv_full(cs));
+        mbar_arrive(bar.conv_full(s));
+        if (Cfg::RAW_OPERANDS) mbar_arrive(bar.raw_empty(r));
       }
     }
   }
@@ -235,24 +268,25 @@ __device__ __forceinline__ void tc_issue(const TcParams &p, uint32_t sbase, uint
       const uint32_t d = tmem_base + b * 128;
       const int kc1 = min(kc0 + Cfg::CHUNK_KTILES, p.k_tiles);
       for (int kt = kc0; kt < kc1; ++kt, ++it) {
-        const uint32_t cs = it % Cfg::CONV_STAGES, cr = it / Cfg::CONV_STAGES;
-        if (!wait_parity_bounded(bar.conv_full(cs), cr & 1, p.wait_budget_ns, p.status)) {
+        const uint32_t s = it % Cfg::STAGES, round = it / Cfg::STAGES;
+        if (!wait_parity_bounded(bar.conv_full(s), round & 1, p.wait_budget_ns, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t cv = sbase + Cfg::CONV_OFFSET + cs * Cfg::CONV_STAGE_BYTES;
+        const uint32_t st = sbase + s * Cfg::STAGE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
-          const uint64_t a_big = desc_kmajor_sw128(cv + kk * 32);
-          const uint64_t a_small = desc_kmajor_sw128(cv + Cfg::TILE_BYTES + kk * 32);
-          const uint64_t b_big = desc_kmajor_sw128(cv + 2 * Cfg::TILE_BYTES + kk * 32);
-          const uint64_t b_small = desc_kmajor_sw128(cv + 3 * Cfg::TILE_BYTES + kk * 32);
+          // k8 step kk: 32 bytes along the 128-byte K-major rows
+          const uint64_t a_big = desc_kmajor_sw128(st + Cfg::A_BIG + kk * 32);
+          const uint64_t a_small = desc_kmajor_sw128(st + Cfg::A_SMALL + kk * 32);
+          const uint64_t b_big = desc_kmajor_sw128(st + Cfg::B_BIG + kk * 32);
+          const uint64_t b_small = desc_kmajor_sw128(st + Cfg::B_SMALL + kk * 32);
           mma_tf32(d, a_small, b_big, Cfg::IDESC, (kt > kc0 || kk > 0) ? 1u : 0u);
           mma_tf32(d, a_big, b_small, Cfg::IDESC, 1u);
           mma_tf32(d, a_big, b_big, Cfg::IDESC, 1u);
         }
-        mma_commit(bar.conv_empty(cs));  // frees the converted stage when these MMAs finish
+        mma_commit(bar.empty(s));  // frees the stage when these MMAs finish
       }
       if (!ok) break;
       mma_commit(bar.acc_full(b));  // chunk done: hand the accumulator to the epilogue
@@ -340,13 +374,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Cfg::RAW_STAGES; ++s) {
-      mbar_init(bar.raw_full(s), 1);
-      mbar_init(bar.raw_empty(s), Cfg::CONVERTER_WARPS);
-    }
-    for (int s = 0; s < Cfg::CONV_STAGES; ++s) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(bar.full(s), 1);
       mbar_init(bar.conv_full(s), Cfg::CONVERTER_WARPS);
-      mbar_init(bar.conv_empty(s), 1);
+      mbar_init(bar.empty(s), 1);
+    }
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(bar.raw_full(r), 1);
+      mbar_init(bar.raw_empty(r), Cfg::CONVERTER_WARPS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar.acc_full(b), 1);

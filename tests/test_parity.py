@@ -272,7 +272,7 @@ def test_runs_on_the_given_stream(orc):
     assert_close(C.cpu().numpy(), R, K, "side stream")
 
 
-def test_launch_count_is_one():
+def test_launch_count_small_is_one():
     A = torch.rand(300, 200, device="cuda")
     B = torch.rand(200, 100, device="cuda")
     for algo in ALL_ALGOS:
@@ -297,3 +297,56 @@ def test_bounded_wait_gives_up_and_context_survives(orc):
     torch.cuda.synchronize()
     assert_close(C.cpu().numpy(), orc.sgemm_f64(0, 0, 1.0, A.cpu().numpy(), B.cpu().numpy()), 256,
                  "after timeout")
+
+
+# --------------------------------------------------------------- stream-K split
+SK_SHAPES = [(1024, 1024, 1024), (2048, 2048, 2048), (8192, 64, 4096), (256, 384, 1000),
+             (4096, 4096, 4096)]
+
+
+@pytest.mark.parametrize("shape", SK_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in SK_SHAPES])
+def test_stream_k_is_deterministic(shape):
+    """Tiles whose k-iterations are spread over several CTAs are summed in a
+    fixed order: repeated runs give bit-identical results."""
+    M, N, K = shape
+    g = torch.Generator().manual_seed(99)
+    A = torch.randn(M, K, generator=g).cuda()
+    B = torch.randn(K, N, generator=g).cuda()
+    C0 = torch.randn(M, N, generator=g).cuda()
+    outs = []
+    for _ in range(3):
+        C = C0.clone()
+        sg.gemm(A, B, C, 0.5, 2.0)
+        outs.append(C)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_stream_k_uses_two_launches():
+    A = torch.randn(2048, 2048, device="cuda")
+    B = torch.randn(2048, 2048, device="cuda")
+    sg.gemm(A, B)
+    assert sg.sgemm_last_launch_count() == 2   # main kernel + fixup
+    A = torch.randn(128 * 152, 256, device="cuda")
+    B = torch.randn(256, 128, device="cuda")
+    sg.gemm(A, B)                               # exactly one wave of whole tiles
+    assert sg.sgemm_last_launch_count() == 1
+
+
+def test_stream_k_on_two_streams(orc):
+    """Stream-K calls on different streams share the device workspace; the
+    library orders them, so both results are right."""
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    g = torch.Generator().manual_seed(5)
+    mats = [(torch.randn(1024, 1024, generator=g), torch.randn(1024, 1024, generator=g))
+            for _ in range(2)]
+    dev = [(a.cuda(), b.cuda(), torch.empty(1024, 1024, device="cuda")) for a, b in mats]
+    torch.cuda.synchronize()
+    for _ in range(5):
+        with torch.cuda.stream(s1):
+            sg.gemm(*dev[0])
+        with torch.cuda.stream(s2):
+            sg.gemm(*dev[1])
+    torch.cuda.synchronize()
+    for (a, b), (_, _, c) in zip(mats, dev):
+        assert_close(c.cpu().numpy(), orc.sgemm_f64(0, 0, 1.0, a.numpy(), b.numpy()), 1024, "two streams")
