@@ -9,44 +9,21 @@
 #include <cstring>
 #include <mutex>
 
+#include "dispatch.h"
 #include "internal.h"
 #include "sgemm.h"
 
 namespace {
-
-using namespace sg;
-
 // Device status word: a kernel that gives up a bounded wait records
 // SGEMM_ERR_DEVICE_TIMEOUT here (one copy per device that loads the library).
 __device__ int g_device_status;
+sg::DeviceState g_dev[sg::kMaxDevices];
+}  // namespace
 
-constexpr int kMaxDevices = 64;
-constexpr uint64_t kDefaultWaitBudgetNs = 2000000000ull;  // 2 s
+namespace sg {
+
 std::atomic<uint64_t> g_wait_budget_ns{kDefaultWaitBudgetNs};
 thread_local int t_last_launches = 0;
-
-struct DeviceState {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
-  int sm_count = 0, cc_major = 0, cc_minor = 0;
-  int *status = nullptr;
-  // Stream-K workspace: allocated on first use, kept until exit.  Calls that
-  // use it on different streams are ordered by ws_event.
-  std::mutex ws_mu;
-  float *ws = nullptr;
-  size_t ws_bytes = 0;
-  bool ws_failed = false;
-  cudaEvent_t ws_event = nullptr;
-  cudaStream_t ws_last_stream = nullptr;
-  bool ws_used = false;
-  std::once_flag kinfo_once[2][2][2][kNumSimtTiles];
-  cudaError_t kinfo_err[2][2][2][kNumSimtTiles] = {};
-  SimtKernelInfo kinfo[2][2][2][kNumSimtTiles] = {};
-  std::once_flag tcinfo_once[2][2];
-  cudaError_t tcinfo_err[2][2] = {};
-  TcKernelInfo tcinfo[2][2] = {};
-};
-DeviceState g_dev[kMaxDevices];
 
 // Returns the current device's state (initialised once per device) or null.
 DeviceState *device_state(sgemm_status_t *why) {
@@ -95,7 +72,7 @@ const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb) {
   return &d.tcinfo[ta][tb];
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, []() {
@@ -137,29 +114,12 @@ int norm_op(int t) {
 }
 
 // [lo, hi) byte range of a stored rows x cols matrix with leading dim ld.
-void byte_range(const void *p, int64_t rows, int64_t cols, int64_t ld, uintptr_t *lo, uintptr_t *hi) {
+static void byte_range(const void *p, int64_t rows, int64_t cols, int64_t ld, uintptr_t *lo, uintptr_t *hi) {
   *lo = reinterpret_cast<uintptr_t>(p);
   *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 4);
 }
 
-bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
-
-// Indices are 32-bit inside the kernels; tile origins may run up to one tile
-// past the end of a dimension.
-constexpr int64_t kMaxDim = 0x7fffffff - 1024;
-constexpr int64_t kMaxLd = int64_t(1) << 40;  // keeps every byte offset in int64
-
-struct Args {
-  int ta, tb;
-  int64_t M, N, K;
-  float alpha, beta;
-  const float *A;
-  int64_t lda;
-  const float *B;
-  int64_t ldb;
-  float *C;
-  int64_t ldc;
-};
+static bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
 
 // Host-side validation shared by sgemm_ex and sgemm_select_algo.
 sgemm_status_t validate(const Args &a, bool c_writable) {
@@ -209,16 +169,6 @@ int pick_simt_tile(const Args &a, int producer) {
   return kTile128x128;
 }
 
-// Smallest stream-K segment worth a partial tile (k-tiles of 32).
-constexpr int64_t kMinSkSegment = 4;
-
-struct SkPlan {
-  int dp_tiles;     // whole tiles, round-robin
-  int sk_tiles;     // tiles whose k-iterations are spread over the grid
-  int64_t sk_iters;
-  int grid;
-};
-
 // Data-parallel waves while they are full; the remainder (one to two waves'
 // worth of tiles) split by k-iterations over every CTA slot.
 SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws) {
@@ -237,6 +187,12 @@ SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws
   pl.grid = static_cast<int>(grid);
   return pl;
 }
+
+}  // namespace sg
+
+namespace {
+
+using namespace sg;
 
 // The device's stream-K workspace (2 partial tiles per CTA slot of the largest
 // configuration), allocated on first use; null if that failed.

@@ -1,0 +1,93 @@
+// dispatch.h -- host-side helpers of the C ABI shared between its translation
+// units: argument checks, per-device state, kernel attributes, TMA descriptor
+// encoding and the stream-K planner (defined in api.cu).  Not part of the
+// public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "sgemm.h"
+
+namespace sg {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitBudgetNs = 2000000000ull;  // 2 s
+extern std::atomic<uint64_t> g_wait_budget_ns;
+extern thread_local int t_last_launches;
+
+struct DeviceState {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  int sm_count = 0, cc_major = 0, cc_minor = 0;
+  int *status = nullptr;
+  // Stream-K workspace: allocated on first use, kept until exit.  Calls that
+  // use it on different streams are ordered by ws_event.
+  std::mutex ws_mu;
+  float *ws = nullptr;
+  size_t ws_bytes = 0;
+  bool ws_failed = false;
+  cudaEvent_t ws_event = nullptr;
+  cudaStream_t ws_last_stream = nullptr;
+  bool ws_used = false;
+  std::once_flag kinfo_once[2][2][2][kNumSimtTiles];
+  cudaError_t kinfo_err[2][2][2][kNumSimtTiles] = {};
+  SimtKernelInfo kinfo[2][2][2][kNumSimtTiles] = {};
+  std::once_flag tcinfo_once[2][2];
+  cudaError_t tcinfo_err[2][2] = {};
+  TcKernelInfo tcinfo[2][2] = {};
+};
+// Indices are 32-bit inside the kernels; tile origins may run up to one tile
+// past the end of a dimension.
+constexpr int64_t kMaxDim = 0x7fffffff - 1024;
+constexpr int64_t kMaxLd = int64_t(1) << 40;  // keeps every byte offset in int64
+
+struct Args {
+  int ta, tb;
+  int64_t M, N, K;
+  float alpha, beta;
+  const float *A;
+  int64_t lda;
+  const float *B;
+  int64_t ldb;
+  float *C;
+  int64_t ldc;
+};
+
+// Host-side validation shared by the entry points (status codes, no launch).
+sgemm_status_t validate(const Args &a, bool c_writable);
+bool tma_eligible(const Args &a);
+int64_t cdiv(int64_t a, int64_t b);
+int norm_op(int t);
+
+// The current device's state (initialised once per device) or null with the
+// reason in *why.
+DeviceState *device_state(sgemm_status_t *why);
+const SimtKernelInfo *kernel_info(DeviceState &d, int producer, int ta, int tb, int tile);
+const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb);
+
+// 2-D FP32 tensor map over a row-major rows x cols matrix (row stride ld
+// elements), box box_cols x box_rows, zero fill outside; false on failure.
+bool encode_tmap(CUtensorMap *m, const float *base, int64_t rows, int64_t cols, int64_t ld,
+                 int box_cols, int box_rows, bool swizzle128);
+
+int pick_simt_tile(const Args &a, int producer);
+
+// Smallest stream-K segment worth a partial tile (k-tiles of 32).
+constexpr int64_t kMinSkSegment = 4;
+
+struct SkPlan {
+  int dp_tiles;     // whole tiles, round-robin
+  int sk_tiles;     // tiles whose k-iterations are spread over the grid
+  int64_t sk_iters;
+  int grid;
+};
+
+SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws);
+
+}  // namespace sg
