@@ -16,7 +16,8 @@ ALGO_AUTO, ALGO_SIMT_TMA, ALGO_SIMT_CPASYNC, ALGO_TC_3XTF32, ALGO_NAIVE, ALGO_SM
 ALGOS = {"auto": ALGO_AUTO, "simt_tma": ALGO_SIMT_TMA, "simt_cpasync": ALGO_SIMT_CPASYNC,
          "tc_3xtf32": ALGO_TC_3XTF32, "naive": ALGO_NAIVE, "smem_tiled": ALGO_SMEM_TILED}
 STATUS = {0: "SGEMM_SUCCESS", 1: "SGEMM_ERR_INVALID_VALUE", 2: "SGEMM_ERR_ALIASING",
-          3: "SGEMM_ERR_UNSUPPORTED", 4: "SGEMM_ERR_LAUNCH", 5: "SGEMM_ERR_DEVICE_TIMEOUT"}
+          3: "SGEMM_ERR_UNSUPPORTED", 4: "SGEMM_ERR_LAUNCH", 5: "SGEMM_ERR_DEVICE_TIMEOUT",
+          6: "SGEMM_ERR_SCRATCH_LIMIT"}
 
 _lib = None
 _I64 = ctypes.c_int64
@@ -50,6 +51,8 @@ def load_library():
     lib.sgemm.restype = ctypes.c_int
     lib.sgemm_ex.argtypes = gemm_args + [ctypes.c_int]
     lib.sgemm_ex.restype = ctypes.c_int
+    lib.sgemm_noalloc.argtypes = gemm_args
+    lib.sgemm_noalloc.restype = ctypes.c_int
     lib.sgemm_select_algo.argtypes = [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64, _VP, _I64,
                                       _VP, _I64, ctypes.c_float, ctypes.c_float, _VP, _I64]
     lib.sgemm_select_algo.restype = ctypes.c_int
@@ -96,6 +99,13 @@ def sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, strea
     algo = ALGOS[algo] if isinstance(algo, str) else int(algo)
     _check(load_library().sgemm_ex(_op(transA), _op(transB), M, N, K, alpha, A, lda, B, ldb,
                                    beta, C, ldc, stream, algo), "sgemm_ex")
+
+
+def sgemm_noalloc(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    """As sgemm, for callers that may not let the library allocate device
+    memory: the scratch is a fixed array loaded with the library."""
+    _check(load_library().sgemm_noalloc(_op(transA), _op(transB), M, N, K, alpha, A, lda, B, ldb,
+                                        beta, C, ldc, stream), "sgemm_noalloc")
 
 
 def sgemm_select_algo(transA, transB, M, N, K, A, lda, B, ldb, alpha, beta, C, ldc) -> int:

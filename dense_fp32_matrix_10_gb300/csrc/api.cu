@@ -454,6 +454,7 @@ const char *sgemm_status_string(sgemm_status_t status) {
     case SGEMM_ERR_UNSUPPORTED: return "unsupported device or arguments";
     case SGEMM_ERR_LAUNCH: return "CUDA launch failure";
     case SGEMM_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    case SGEMM_ERR_SCRATCH_LIMIT: return "needs more scratch than the fixed no-allocation array holds";
     default: return "unknown status";
   }
 }

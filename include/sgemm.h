@@ -74,8 +74,10 @@ typedef enum sgemm_status {
                                    or the requested algorithm cannot take these
                                    arguments (e.g. TMA with an unaligned ld) */
   SGEMM_ERR_LAUNCH = 4,         /* a CUDA call failed while queuing the work */
-  SGEMM_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up a bounded wait (reported
+  SGEMM_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up a bounded wait (reported
                                    by sgemm_last_device_status) */
+  SGEMM_ERR_SCRATCH_LIMIT = 6   /* sgemm_noalloc: the product's split tiles need
+                                   more scratch than its fixed array holds */
 } sgemm_status_t;
 
 /*
@@ -160,6 +162,43 @@ SGEMM_API void sgemm_set_wait_budget_ns(uint64_t budget_ns);
  * faulting or hanging anything.  Returns SGEMM_ERR_LAUNCH if queuing failed.
  */
 SGEMM_API sgemm_status_t sgemm_selftest_wait_timeout(uint64_t budget_ns, void *stream);
+
+/*
+ * Size of the fixed device array that sgemm_noalloc uses as scratch: 20 MiB,
+ * i.e. two 128 x 128 FP32 partial tiles for each of up to 160 CTAs.
+ */
+#define SGEMM_NOALLOC_SCRATCH_BYTES (20u * 1024u * 1024u)
+
+/*
+ * sgemm_noalloc -- the same product as sgemm(), guaranteed not to allocate
+ * device memory.  (The pages have no counterpart; this is an entry point for
+ * callers that may not let a library allocate.)
+ *
+ * sgemm() allocates its stream-K workspace with cudaMalloc the first time a
+ * product needs one.  Callers that cannot allow that -- programs whose own
+ * pool or caching allocator owns the device memory, latency-sensitive loops
+ * (cudaMalloc may synchronise the device and can fail under memory pressure),
+ * services with a fixed, audited memory footprint -- call this instead.  Its
+ * scratch is a __device__ array of SGEMM_NOALLOC_SCRATCH_BYTES that every GPU
+ * loading the library holds until the process exits; the call itself makes no
+ * cudaMalloc, cudaFree or other allocating call.
+ *
+ * Arguments, layout, numerics and degenerate cases are those of sgemm(); it
+ * runs the CUDA-core kernels (128 x 128 or 128 x 64 tiles) and updates
+ * sgemm_last_launch_count() like sgemm().
+ * Errors: as sgemm(), plus SGEMM_ERR_SCRATCH_LIMIT (nothing queued) when the
+ * product's split tiles would need more than the array holds (more than 160
+ * CTAs' worth on this device).
+ * First call on a device: looks up the array's device address on that device
+ * (once); make it before any stream capture starts.
+ * Sharing: all calls use the one array and leave its contents behind; nothing
+ * in it needs clearing between calls, but calls that overlap on the GPU (on
+ * streams not ordered with each other) race on it.
+ */
+SGEMM_API sgemm_status_t sgemm_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                       float alpha, const float *A, int64_t lda,
+                                       const float *B, int64_t ldb,
+                                       float beta, float *C, int64_t ldc, void *stream);
 
 /* Static English text for a status code (never NULL). */
 SGEMM_API const char *sgemm_status_string(sgemm_status_t status);
