@@ -26,7 +26,11 @@
  * Pointers: A, B and C are DEVICE pointers (cudaMalloc'd, or any allocation the
  * device can address) on the current device.  The caller owns all of them; the
  * library never frees, keeps or reallocates them.  C must not overlap A or B.
- * The library allocates no device memory for any call declared here.
+ * Device memory of the library's own: sgemm()/sgemm_ex() allocate, once per
+ * device and the first time a product is split by stream-K, a workspace of
+ * two 128 x 256 FP32 tiles per SM (~40 MB on 152 SMs), kept until exit; calls
+ * on different streams that use it are ordered by an event.  sgemm_noalloc()
+ * never allocates (see there).
  *
  * Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
  * default stream).  Every call returns as soon as its work is queued; results
