@@ -162,15 +162,18 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 #ifndef SG_SIMT_WIDE_TILE
 #define SG_SIMT_WIDE_TILE 1
 #endif
-int pick_simt_tile(const Args &a, int producer) {
+int pick_simt_tile(const Args &a, int producer, int sm_count) {
   if (a.N <= 64) return kTile128x64;
-  if (SG_SIMT_WIDE_TILE && producer == kTma && a.ta == 1 && a.tb == 0 && a.N >= 192)
-    return kTile128x256;
+  // the math warps read A m-contiguous when it is stored K x M, or when the
+  // TMA producer transposes a k-contiguous A in shared memory
+  const bool a_mn_in_smem = a.ta == 1 || (producer == kTma && SG_SIMT_TRANSPOSE_A);
+  // the wide tile only once it gives every SM at least one whole tile: below
+  // that, stream-K would cut its k-loop into short, fixup-heavy segments
+  const bool fills = cdiv(a.M, 128) * cdiv(a.N, 256) >= sm_count;
+  if (SG_SIMT_WIDE_TILE && producer == kTma && a_mn_in_smem && a.tb == 0 && fills) return kTile128x256;
   return kTile128x128;
 }
 
-// Data-parallel waves while they are full; the remainder (one to two waves'
-// worth of tiles) split by k-iterations over every CTA slot.
 SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws) {
   SkPlan pl{static_cast<int>(tiles), 0, 0, static_cast<int>(tiles < slots ? tiles : slots)};
   if (!have_ws || k_tiles < 2 * kMinSkSegment) return pl;
@@ -219,7 +222,7 @@ sgemm_algo_t auto_algo(const Args &a) {
 }
 
 sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_t stream) {
-  const int tile = pick_simt_tile(a, producer);
+  const int tile = pick_simt_tile(a, producer, d.sm_count);
   const SimtKernelInfo *ki = kernel_info(d, producer, a.ta, a.tb, tile);
   if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_LAUNCH;
 

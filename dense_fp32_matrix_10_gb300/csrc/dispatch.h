@@ -76,7 +76,7 @@ const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb);
 bool encode_tmap(CUtensorMap *m, const float *base, int64_t rows, int64_t cols, int64_t ld,
                  int box_cols, int box_rows, bool swizzle128);
 
-int pick_simt_tile(const Args &a, int producer);
+int pick_simt_tile(const Args &a, int producer, int sm_count);
 
 // Smallest stream-K segment worth a partial tile (k-tiles of 32).
 constexpr int64_t kMinSkSegment = 4;

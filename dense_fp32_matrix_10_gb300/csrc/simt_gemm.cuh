@@ -110,14 +110,19 @@ __device__ __forceinline__ void for_each_unit(const SimtParams &p, F &&f) {
 }
 
 template <int WARPS_M_, int WARPS_N_, bool A_KMAJOR_, bool B_KMAJOR_, int STAGES_, int PRODUCER_,
-          int TN_ = 8>
+          int TN_ = 8, bool A_TRANS_ = false>
 struct SimtConfig {
   static constexpr int WARPS_M = WARPS_M_;
   static constexpr int WARPS_N = WARPS_N_;
-  static constexpr bool A_KMAJOR = A_KMAJOR_;
+  static constexpr bool A_KMAJOR = A_KMAJOR_;  // layout of A in global memory
   static constexpr bool B_KMAJOR = B_KMAJOR_;
   static constexpr int STAGES = STAGES_;
   static constexpr int PRODUCER = PRODUCER_;
+  // A_TRANS: the TMA lands a k-contiguous A tile in a raw ring and producer
+  // warps rewrite it m-contiguous into the stage.
+  static constexpr bool A_TRANS = A_TRANS_;
+  static_assert(!A_TRANS || (A_KMAJOR && PRODUCER == kTma), "A transpose: k-contiguous A, TMA");
+  static constexpr bool A_SMEM_KMAJOR = A_KMAJOR && !A_TRANS;  // layout the math warps read
   // Thread tile 8 x TN (TN = 8 or 16); warp tile 32 x 8*TN; lanes 4 x 8.
   static constexpr int TN = TN_;
   static constexpr int WN = 8 * TN;
@@ -132,15 +137,17 @@ struct SimtConfig {
   // sub-partition: a 9-warp CTA would cap every thread at 168 registers).
   static constexpr int PRODUCER_WARPS = 4;
   static constexpr int PRODUCER_THREADS = 32 * PRODUCER_WARPS;
+  static constexpr int TRANSPOSER_WARPS = 3;  // producer warps 1..3 when A_TRANS
   static constexpr int THREADS = MATH_THREADS + PRODUCER_THREADS;
   static constexpr int MIN_CTAS = (MATH_WARPS == 8) ? 1 : 2;  // CTAs per SM
   // Per-thread registers after the split; launch budget is
   // THREADS * (65536 / (THREADS * MIN_CTAS)) rounded down to 8.
-  // The TMA producer needs few registers; the cp.async producer computes
-  // addresses for 64 copies per stage.
-  static constexpr int PRODUCER_REGS = (PRODUCER == kTma) ? 24 : 40;
-  static constexpr int MATH_REGS = (MATH_WARPS == 8) ? ((PRODUCER == kTma) ? 240 : 232)
-                                                     : ((PRODUCER == kTma) ? 232 : 216);
+  // The bare TMA producer needs few registers; the cp.async producer and the
+  // transposing producer warps need more.
+  static constexpr bool LEAN_PRODUCER = (PRODUCER == kTma) && !A_TRANS;
+  static constexpr int PRODUCER_REGS = LEAN_PRODUCER ? 24 : 40;
+  static constexpr int MATH_REGS = (MATH_WARPS == 8) ? (LEAN_PRODUCER ? 240 : 232)
+                                                     : (LEAN_PRODUCER ? 232 : 216);
   static_assert(MATH_WARPS % 4 == 0, "math role must be whole warpgroups");
   static_assert(PRODUCER_THREADS * PRODUCER_REGS + MATH_THREADS * MATH_REGS <=
                     THREADS * ((65536 / (THREADS * MIN_CTAS)) & ~7),
@@ -148,9 +155,17 @@ struct SimtConfig {
   static constexpr int A_STAGE_BYTES = BM * BK * 4;
   static constexpr int B_STAGE_BYTES = BN * BK * 4;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-  // stages first (1024-byte aligned for the 128 B swizzle), barriers after
-  static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFFSET + 2 * STAGES * 8 + 1024;  // + alignment slack
+  // stages first (1024-byte aligned for the 128 B swizzle), then the raw A
+  // ring (A_TRANS), then the barriers
+  static constexpr int RAW_A_STAGES = A_TRANS ? 2 : 0;
+  static constexpr int RAW_A_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFFSET = RAW_A_OFFSET + RAW_A_STAGES * A_STAGE_BYTES;
+  // full[STAGES], empty[STAGES], raw_full[2], raw_empty[2]
+  static constexpr int SMEM_BYTES = BAR_OFFSET + (2 * STAGES + 4) * 8 + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
+  // arrivals that complete a stage's `full` barrier
+  static constexpr int FULL_COUNT =
+      (PRODUCER == kTma) ? (A_TRANS ? 1 + TRANSPOSER_WARPS : 1) : PRODUCER_THREADS;
   static_assert(BM <= 256 && BN <= 256, "TMA box extent is at most 256");
   static_assert(A_STAGE_BYTES % 1024 == 0 && B_STAGE_BYTES % 1024 == 0, "swizzle atom alignment");
 };
@@ -178,15 +193,30 @@ __device__ __forceinline__ uint32_t kmajor_offset(int row, int k) {
 template <class Cfg>
 __device__ __forceinline__ void produce_tma(const SimtParams &p, const CUtensorMap *tmA,
                                             const CUtensorMap *tmB, uint32_t smem_base,
-                                            uint32_t full0, uint32_t empty0, bool &ok) {
-  uint32_t it = 0;
+                                            uint32_t full0, uint32_t empty0, uint32_t raw_full0,
+                                            uint32_t raw_empty0, bool &ok) {
+  uint32_t it = 0;        // k-slices whose stage copies are issued
+  uint32_t raw_it = 0;    // k-slices whose raw A copies are issued
   for_each_unit(p, [&](const WorkUnit &u) {
     int tm, tn;
     tile_coords(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     const int m0 = tm * Cfg::BM, n0 = tn * Cfg::BN;
-    for (int kt = u.k0; kt < u.k1; ++kt, ++it) {
+    for (int kt = u.k0; kt < u.k1; ++kt) {
       const uint32_t s = it % Cfg::STAGES;
       const uint32_t round = it / Cfg::STAGES;
+      const int k0 = kt * Cfg::BK;
+      if (Cfg::A_TRANS) {  // A: raw k-contiguous tile into the raw ring
+        const uint32_t r = raw_it % 2, rr = raw_it / 2;
+        if (rr > 0 &&
+            !wait_parity_bounded(raw_empty0 + 8 * r, (rr - 1) & 1, p.wait_budget_ns, p.status)) {
+          ok = false;
+          return false;
+        }
+        mbar_arrive_expect_tx(raw_full0 + 8 * r, Cfg::A_STAGE_BYTES);
+        tma_load_2d(smem_base + Cfg::RAW_A_OFFSET + r * Cfg::A_STAGE_BYTES, tmA, raw_full0 + 8 * r,
+                    k0, m0);
+        ++raw_it;
+      }
       if (round > 0 &&
           !wait_parity_bounded(empty0 + 8 * s, (round - 1) & 1, p.wait_budget_ns, p.status)) {
         ok = false;
@@ -195,27 +225,72 @@ __device__ __forceinline__ void produce_tma(const SimtParams &p, const CUtensorM
       const uint32_t full = full0 + 8 * s;
       const uint32_t a_dst = smem_base + s * Cfg::STAGE_BYTES;
       const uint32_t b_dst = a_dst + Cfg::A_STAGE_BYTES;
-      mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
-      const int k0 = kt * Cfg::BK;
-      if (Cfg::A_KMAJOR)
-        tma_load_2d(a_dst, tmA, full, k0, m0);
-      else
-        tma_load_2d(a_dst, tmA, full, m0, k0);
+      mbar_arrive_expect_tx(full, Cfg::A_TRANS ? Cfg::B_STAGE_BYTES : Cfg::STAGE_BYTES);
+      if (!Cfg::A_TRANS) {
+        if (Cfg::A_KMAJOR)
+          tma_load_2d(a_dst, tmA, full, k0, m0);
+        else
+          tma_load_2d(a_dst, tmA, full, m0, k0);
+      }
       if (Cfg::B_KMAJOR)
         tma_load_2d(b_dst, tmB, full, k0, n0);
       else
         tma_load_2d(b_dst, tmB, full, n0, k0);
+      ++it;
     }
     return true;
   });
   if (!ok) {
     // Let the copies already issued land before the CTA can end.
-    const uint32_t issued = it;
-    const uint32_t first = issued > Cfg::STAGES ? issued - Cfg::STAGES : 0;
-    for (uint32_t j = first; j < issued; ++j)
+    const uint32_t first = it > Cfg::STAGES ? it - Cfg::STAGES : 0;
+    for (uint32_t j = first; j < it; ++j)
       wait_parity_bounded(full0 + 8 * (j % Cfg::STAGES), (j / Cfg::STAGES) & 1,
                           p.wait_budget_ns, nullptr);
+    const uint32_t rfirst = raw_it > 2 ? raw_it - 2 : 0;
+    for (uint32_t j = rfirst; j < raw_it; ++j)
+      wait_parity_bounded(raw_full0 + 8 * (j % 2), (j / 2) & 1, p.wait_budget_ns, nullptr);
   }
+}
+
+// Producer warps 1..3 when A_TRANS: raw k-contiguous A tile (128-byte rows,
+// 128 B swizzle) -> m-contiguous [32 k][BM m] in the stage.  Lane l handles
+// row m = 32*mb + l: its LDS.128 of chunk c and the 4 stores of the quarter
+// warp both touch every bank once.
+template <class Cfg>
+__device__ __forceinline__ void transpose_a(const SimtParams &p, unsigned char *smem,
+                                            uint32_t full0, uint32_t empty0, uint32_t raw_full0,
+                                            uint32_t raw_empty0, int tw, int lane, bool &ok) {
+  constexpr int BM = Cfg::BM, ITEMS = (BM / 32) * 8;
+  uint32_t it = 0;
+  for_each_unit(p, [&](const WorkUnit &u) {
+    for (int kt = u.k0; kt < u.k1; ++kt, ++it) {
+      const uint32_t s = it % Cfg::STAGES, round = it / Cfg::STAGES;
+      const uint32_t r = it % 2, rr = it / 2;
+      if (!wait_parity_bounded(raw_full0 + 8 * r, rr & 1, p.wait_budget_ns, p.status) ||
+          (round > 0 &&
+           !wait_parity_bounded(empty0 + 8 * s, (round - 1) & 1, p.wait_budget_ns, p.status))) {
+        ok = false;
+        return false;
+      }
+      const unsigned char *raw = smem + Cfg::RAW_A_OFFSET + r * Cfg::A_STAGE_BYTES;
+      float *dst = reinterpret_cast<float *>(smem + s * Cfg::STAGE_BYTES);
+#pragma unroll 4
+      for (int item = tw; item < ITEMS; item += Cfg::TRANSPOSER_WARPS) {
+        const int c = item & 7, m = (item >> 3) * 32 + lane;
+        const float4 v = *reinterpret_cast<const float4 *>(raw + m * 128 + ((c ^ (m & 7)) << 4));
+        dst[(4 * c + 0) * BM + m] = v.x;
+        dst[(4 * c + 1) * BM + m] = v.y;
+        dst[(4 * c + 2) * BM + m] = v.z;
+        dst[(4 * c + 3) * BM + m] = v.w;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(full0 + 8 * s);
+        mbar_arrive(raw_empty0 + 8 * r);
+      }
+    }
+    return true;
+  });
 }
 
 template <class Cfg>
@@ -293,7 +368,7 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
 // ------------------------------------------------------------------ consumer
 template <class Cfg>
 __device__ __forceinline__ int thread_row(int tm, int r) {
-  return Cfg::A_KMAJOR ? (tm + 4 * r) : ((r < 4) ? (4 * tm + r) : (16 + 4 * tm + (r - 4)));
+  return Cfg::A_SMEM_KMAJOR ? (tm + 4 * r) : ((r < 4) ? (4 * tm + r) : (16 + 4 * tm + (r - 4)));
 }
 template <class Cfg>
 __device__ __forceinline__ int thread_col(int tn, int c) {
@@ -318,6 +393,16 @@ __device__ __forceinline__ int thread_col(int tn, int c) {
 #define SG_SIMT_KC_UNROLL_WIDE 1
 #endif
 
+// SG_SIMT_TRANSPOSE_A  1: with the TMA producer, a k-contiguous op(A) tile is
+//                        rewritten m-contiguous in shared memory by three
+//                        producer warps, so the math warps always read A as
+//                        [k][m] (conflict-free float4 rows, fewer registers,
+//                        the 8 x 16 tile becomes usable); 0: math warps read
+//                        the swizzled k-contiguous tile directly.
+#ifndef SG_SIMT_TRANSPOSE_A
+#define SG_SIMT_TRANSPOSE_A 1
+#endif
+
 template <int TN>
 __host__ __device__ constexpr int kc_unroll() {
   return TN == 16 ? SG_SIMT_KC_UNROLL_WIDE : SG_SIMT_KC_UNROLL;
@@ -333,7 +418,8 @@ enum AccMode : int { kPairCols = 0, kPairRows = 1, kScalar = 2 };
 
 template <class Cfg>
 __device__ __host__ constexpr int acc_mode() {
-  return !SG_SIMT_FFMA2 ? kScalar : (!Cfg::B_KMAJOR ? kPairCols : (!Cfg::A_KMAJOR ? kPairRows : kScalar));
+  return !SG_SIMT_FFMA2 ? kScalar
+                        : (!Cfg::B_KMAJOR ? kPairCols : (!Cfg::A_SMEM_KMAJOR ? kPairRows : kScalar));
 }
 
 // 8 x TN accumulators packed as 4*TN float2.
@@ -361,7 +447,7 @@ __device__ __forceinline__ void mma_stage(AccT<Cfg> &acc, const char *a_stage, c
   // Per-thread base pointers inside the stage.
   const char *a_base;
   const char *b_base;
-  if (Cfg::A_KMAJOR)
+  if (Cfg::A_SMEM_KMAJOR)
     a_base = a_stage + (wm * 32 + tm) * 128;  // row tm + 4r -> + r * 512
   else
     a_base = a_stage + (wm * 32 + 4 * tm) * 4;  // + k * BM * 4, + 64 for rows 16..
@@ -390,7 +476,7 @@ __device__ __forceinline__ void mma_stage(AccT<Cfg> &acc, const char *a_stage, c
 #pragma unroll
     for (int kg = 0; kg < 4 / KA; ++kg) {
       float a[8][KA];  // a[r][j] = op(A)(row r, k = kc*4 + kg*KA + j)
-      if (Cfg::A_KMAJOR) {
+      if (Cfg::A_SMEM_KMAJOR) {
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           // row = wm*32 + tm + 4r: (row & 7) = tm | 4*(r&1)
@@ -547,14 +633,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
   const uint32_t smem_base = smem_u32(smem);
   const uint32_t full0 = smem_base + Cfg::BAR_OFFSET;
   const uint32_t empty0 = full0 + 8 * Cfg::STAGES;
+  const uint32_t raw_full0 = empty0 + 8 * Cfg::STAGES;
+  const uint32_t raw_empty0 = raw_full0 + 16;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) {
-      mbar_init(full0 + 8 * s, Cfg::PRODUCER == kTma ? 1 : Cfg::PRODUCER_THREADS);
+      mbar_init(full0 + 8 * s, Cfg::FULL_COUNT);
       mbar_init(empty0 + 8 * s, Cfg::MATH_WARPS);
+    }
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(raw_full0 + 8 * r, 1);
+      mbar_init(raw_empty0 + 8 * r, Cfg::TRANSPOSER_WARPS);
     }
     fence_mbar_init();
   }
@@ -570,7 +662,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::PRODUCER_REGS));
     if (Cfg::PRODUCER == kTma) {
       if (threadIdx.x == Cfg::MATH_THREADS)
-        produce_tma<Cfg>(p, &tmA, &tmB, smem_base, full0, empty0, ok);
+        produce_tma<Cfg>(p, &tmA, &tmB, smem_base, full0, empty0, raw_full0, raw_empty0, ok);
+      else if (Cfg::A_TRANS && warp > Cfg::MATH_WARPS)
+        transpose_a<Cfg>(p, smem, full0, empty0, raw_full0, raw_empty0, warp - Cfg::MATH_WARPS - 1,
+                         lane, ok);
     } else {
       produce_cpasync<Cfg>(p, smem_base, full0, empty0, threadIdx.x - Cfg::MATH_THREADS, ok);
     }

@@ -43,17 +43,22 @@ cudaError_t simt_info(SimtKernelInfo *info) {
 
 template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR, int TILE>
 struct SimtPick;
+// With the TMA producer a k-contiguous A is transposed in shared memory
+// (SG_SIMT_TRANSPOSE_A).
+template <int PRODUCER, bool A_KMAJOR>
+constexpr bool kTransA = (PRODUCER == kTma) && A_KMAJOR && SG_SIMT_TRANSPOSE_A;
+
 template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR>
 struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x128> {
-  using Cfg = SimtConfig<4, 2, A_KMAJOR, B_KMAJOR, 4, PRODUCER>;
+  using Cfg = SimtConfig<4, 2, A_KMAJOR, B_KMAJOR, 4, PRODUCER, 8, kTransA<PRODUCER, A_KMAJOR>>;
 };
 template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR>
 struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x64> {
-  using Cfg = SimtConfig<4, 1, A_KMAJOR, B_KMAJOR, 4, PRODUCER>;
+  using Cfg = SimtConfig<4, 1, A_KMAJOR, B_KMAJOR, 4, PRODUCER, 8, kTransA<PRODUCER, A_KMAJOR>>;
 };
 template <int PRODUCER, bool A_KMAJOR>
 struct SimtPick<PRODUCER, A_KMAJOR, false, kTile128x256> {
-  using Cfg = SimtConfig<4, 2, A_KMAJOR, false, 4, PRODUCER, 16>;
+  using Cfg = SimtConfig<4, 2, A_KMAJOR, false, 4, PRODUCER, 16, kTransA<PRODUCER, A_KMAJOR>>;
 };
 
 template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR, int TILE>

@@ -162,16 +162,16 @@ def test_register_split_fits_launch_budget(lib):
     report = build.ptxas_report().splitlines()
     checked = 0
     for i, ln in enumerate(report):
-        m = re.search(r"SimtConfigILi(\d+)ELi(\d+)ELb[01]ELb[01]ELi\d+ELi(\d)E", ln)
+        m = re.search(r"SimtConfigILi(\d+)ELi(\d+)ELb[01]ELb[01]ELi\d+ELi(\d)ELi\d+ELb([01])E", ln)
         if not m or "Compiling entry" not in ln:
             continue
         regs = next(int(re.search(r"Used (\d+) registers", x).group(1))
                     for x in report[i + 1:] if "Used" in x)
         math_warps = int(m.group(1)) * int(m.group(2))
-        tma = m.group(3) == "0"
+        lean = m.group(3) == "0" and m.group(4) == "0"   # TMA producer without A transpose
         threads = 32 * math_warps + 128
-        prod_regs = 24 if tma else 40
-        math_regs = (240 if tma else 232) if math_warps == 8 else (232 if tma else 216)
+        prod_regs = 24 if lean else 40
+        math_regs = (240 if lean else 232) if math_warps == 8 else (232 if lean else 216)
         assert regs * threads >= 128 * prod_regs + 32 * math_warps * math_regs, (ln, regs)
         checked += 1
     assert checked >= 8
