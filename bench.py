@@ -47,21 +47,29 @@ FALLBACK_BF16_TFLOPS = 1900.0         # used only if no measured peak file
 
 
 # ----------------------------------------------------------------- helpers
-def kernel_source_hash() -> str:
-    """sha256 over the CUDA sources; a stored ncu traffic figure is only used
-    while it matches (otherwise the kernel changed since the capture)."""
+# Sources each kernel family is built from; a stored ncu traffic figure is
+# only used while the hash of its family's sources still matches.
+KERNEL_SOURCES = {
+    "simt": ["ptx.cuh", "internal.h", "simt_gemm.cuh", "simt_instances.cuh", "simt_tma_an.cu",
+             "simt_tma_at.cu", "simt_cpasync_an.cu", "simt_cpasync_at.cu", "sk_fixup.cu"],
+    "tc_3xtf32": ["ptx.cuh", "tc_3xtf32.cuh", "tc_3xtf32.cu"],
+}
+
+
+def kernel_source_hash(family: str) -> str:
     h = hashlib.sha256()
-    for path in sorted(glob.glob(os.path.join(ROOT, "dense_fp32_matrix_10_gb300", "csrc", "*"))):
-        if path.endswith((".cu", ".cuh", ".h")):
-            h.update(os.path.basename(path).encode())
-            h.update(open(path, "rb").read())
+    for name in KERNEL_SOURCES[family]:
+        path = os.path.join(ROOT, "dense_fp32_matrix_10_gb300", "csrc", name)
+        h.update(name.encode())
+        h.update(open(path, "rb").read())
     return h.hexdigest()[:16]
 
 
 def stored_traffic(kernel_tag: str):
     """(bytes per launch, note) from profiles/*.md lines
-    'traffic <kernel_tag> <bytes> <source hash>' if the hash matches."""
-    want = kernel_source_hash()
+    'traffic <kernel_tag> <bytes> <source hash>' if the hash still matches."""
+    family = "tc_3xtf32" if kernel_tag.startswith("tc_3xtf32") else "simt"
+    want = kernel_source_hash(family)
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         for ln in open(path, encoding="utf-8"):
             m = re.match(r"^traffic\s+(\S+)\s+(\d+)\s+(\w+)\s*$", ln.strip())

@@ -23,7 +23,7 @@ static cudaError_t tc3_info(TcKernelInfo *info) {
   cudaFuncAttributes attr;
   e = cudaFuncGetAttributes(&attr, tc3_gemm_kernel<Cfg>);
   if (e != cudaSuccess) return e;
-  if (attr.numRegs * Cfg::THREADS < 128 * (Cfg::REGS_WG0 + Cfg::REGS_EPI + Cfg::REGS_CONV))
+  if (attr.numRegs * Cfg::THREADS < 128 * (Cfg::REGS_WG0 + Cfg::REGS_EPI + 2 * Cfg::REGS_CONV))
     return cudaErrorInvalidConfiguration;
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, tc3_gemm_kernel<Cfg>, Cfg::THREADS,

@@ -13,13 +13,13 @@
 // integer products stay exact.  Non-finite inputs get small = 0.
 //
 // Both MMA operands are read K-major (128-byte rows of 32 k, 128 B swizzle).
-// Roles (one persistent CTA of 12 warps per SM, 128 x 128 output tiles, k in
+// Roles (one persistent CTA of 16 warps per SM, 128 x 128 output tiles, k in
 // slices of 32):
 //   warp 0       TMA producer.  A k-contiguous operand (A stored M x K, B stored
 //                N x K) lands straight in the MMA ring as a [128][32] box and
 //                serves as its own big part.  An m/n-contiguous operand lands in
 //                a 2-stage raw ring as a dense [32 k][128 mn] box;
-//   warps 8..11  converters: for a k-contiguous operand write small = tf32(x -
+//   warps 8..15  converters: for a k-contiguous operand write small = tf32(x -
 //                x_big) beside the raw tile (elementwise, same layout); for an
 //                m/n-contiguous one build both x_big and x_small tiles K-major
 //                from the raw ring (a transpose through shared memory);
@@ -80,16 +80,20 @@ struct TcConfig {
   static constexpr int NUM_BARS = 3 * STAGES + 2 * 2 + 4 + 1;
   static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
-  static constexpr int THREADS = 384;
+  static constexpr int THREADS = 512;
   static constexpr int TMEM_COLS = 256;
   static constexpr uint32_t IDESC = idesc_tf32(128, 128);
-  static constexpr int CONVERTER_WARPS = 4;
+  // Two converter warpgroups: the conversion is ~250 dependent instructions
+  // per thread and k-slice with one warpgroup, more than the 768 tensor-core
+  // cycles of the slice's 12 MMAs.
+  static constexpr int CONVERTER_WARPS = 8;
+  static constexpr int CONVERTER_THREADS = 32 * CONVERTER_WARPS;
   static constexpr int EPILOGUE_WARPS = 4;
   static constexpr int CHUNK_KTILES = 8;  // k-slices accumulated in TMEM per promotion
   // setmaxnreg split by warpgroup: {producer, MMA, idle}, epilogue (holds a
-  // 128-float row of the tile), converters.
-  static constexpr int REGS_WG0 = 56, REGS_EPI = 240, REGS_CONV = 200;
-  static_assert(128 * (REGS_WG0 + REGS_EPI + REGS_CONV) <= THREADS * ((65536 / THREADS) & ~7),
+  // 128-float row of the tile), two converter warpgroups.
+  static constexpr int REGS_WG0 = 56, REGS_EPI = 240, REGS_CONV = 104;
+  static_assert(128 * (REGS_WG0 + REGS_EPI + 2 * REGS_CONV) <= THREADS * ((65536 / THREADS) & ~7),
                 "register split exceeds the launch budget");
 };
 
@@ -171,11 +175,12 @@ __device__ __forceinline__ float small_part(float x, float big) {
 
 // k-contiguous operand: small = tf32(x - x_big) beside the raw tile, elementwise
 // (same layout, so the small tile shares the raw tile's descriptor geometry).
+// ct = converter thread 0..255; 1024 16-byte chunks, 4 per thread.
 __device__ __forceinline__ void small_of_kmajor(const unsigned char *raw, unsigned char *small,
                                                 int ct) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int off = (ct + 128 * i) * 16;
+  for (int i = 0; i < 4; ++i) {
+    const int off = (ct + 256 * i) * 16;
     const float4 x = *reinterpret_cast<const float4 *>(raw + off);
     float4 s;
     s.x = small_part(x.x, tf32_trunc(x.x));
@@ -187,12 +192,15 @@ __device__ __forceinline__ void small_of_kmajor(const unsigned char *raw, unsign
 }
 
 // m/n-contiguous operand: raw [32 k][128 mn] -> K-major big and small tiles
-// (128-byte rows of 32 k, 128 B swizzle); converter thread ct builds row ct.
+// (128-byte rows of 32 k, 128 B swizzle); converter thread ct builds half of
+// row ct % 128 (k chunks 4*(ct / 128) .. +3).
 __device__ __forceinline__ void split_of_mnmajor(const unsigned char *raw, unsigned char *big,
-                                                 unsigned char *small, int ct) {
+                                                 unsigned char *small, int ct0) {
   const float *r = reinterpret_cast<const float *>(raw);
+  const int ct = ct0 & 127, half = ct0 >> 7;
 #pragma unroll
-  for (int kc = 0; kc < 8; ++kc) {
+  for (int kq = 0; kq < 4; ++kq) {
+    const int kc = 4 * half + kq;
     float4 x;
     x.x = r[(4 * kc + 0) * 128 + ct];
     x.y = r[(4 * kc + 1) * 128 + ct];
@@ -222,8 +230,10 @@ __device__ __forceinline__ void tc_convert(const TcParams &p, unsigned char *sme
     for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
       const uint32_t s = it % Cfg::STAGES, round = it / Cfg::STAGES;
       const uint32_t r = it % 2, rround = it / 2;
-      // the stage is free once the MMAs of its previous round finished
-      if (round > 0 &&
+      // The stage is free once the MMAs of its previous round finished.  With
+      // a k-contiguous operand the producer waited for that before its copy,
+      // so the stage's `full` phase already implies it.
+      if (!ANY_K && round > 0 &&
           !wait_parity_bounded(bar.empty(s), (round - 1) & 1, p.wait_budget_ns, p.status))
         return;
       if (ANY_K && !wait_parity_bounded(bar.full(s), round & 1, p.wait_budget_ns, p.status)) return;
@@ -412,7 +422,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::REGS_EPI));
     tc_epilogue<Cfg>(p, tmem_base, bar, warp & 3, lane);
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::REGS_CONV));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::REGS_CONV));
     tc_convert<Cfg>(p, smem, bar, threadIdx.x - 256, lane);
   }
 
