@@ -51,6 +51,10 @@ def load_library():
     lib.sgemm.restype = ctypes.c_int
     lib.sgemm_ex.argtypes = gemm_args + [ctypes.c_int]
     lib.sgemm_ex.restype = ctypes.c_int
+    lib.sgemm_strided_batched.argtypes = [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64,
+                                          ctypes.c_float, _VP, _I64, _I64, _VP, _I64, _I64,
+                                          ctypes.c_float, _VP, _I64, _I64, _I64, _VP]
+    lib.sgemm_strided_batched.restype = ctypes.c_int
     lib.sgemm_noalloc.argtypes = gemm_args
     lib.sgemm_noalloc.restype = ctypes.c_int
     lib.sgemm_select_algo.argtypes = [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64, _VP, _I64,
@@ -101,6 +105,15 @@ def sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, strea
                                    beta, C, ldc, stream, algo), "sgemm_ex")
 
 
+def sgemm_strided_batched(transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
+                          beta, C, ldc, strideC, batch, stream=None):
+    """C_b = alpha*op(A_b)*op(B_b) + beta*C_b for b < batch (pointers as ints,
+    strides in elements; 0 shares an operand across the batch)."""
+    _check(load_library().sgemm_strided_batched(
+        _op(transA), _op(transB), M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+        strideC, batch, stream), "sgemm_strided_batched")
+
+
 def sgemm_noalloc(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
     """As sgemm, for callers that may not let the library allocate device
     memory: the scratch is a fixed array loaded with the library."""
@@ -144,6 +157,19 @@ def sgemm_version() -> str:
 
 
 # ------------------------------------------------------------------ torch
+def _batched(t, name):
+    """(pointer, batch, rows, cols, ld, stride) of a 3-D float32 CUDA tensor whose
+    last dimension is contiguous (stride(0) may be 0: one matrix shared)."""
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.dim() != 3:
+        raise TypeError(f"{name} must be a 3-D torch.float32 tensor")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    b, rows, cols = t.shape
+    if cols > 1 and t.stride(2) != 1:
+        raise ValueError(f"{name} must have unit column stride")
+    ld = t.stride(1) if (rows > 1 or t.stride(1) >= cols) else cols
+    return t.data_ptr(), b, rows, cols, max(ld, 1), t.stride(0) if b > 1 else 0
 def _matrix(t, name):
     """(pointer, rows, cols, ld) of a 2-D float32 CUDA tensor with unit column stride."""
     import torch
@@ -158,6 +184,36 @@ def _matrix(t, name):
     if ld < cols:
         raise ValueError(f"{name} has overlapping rows")
     return t.data_ptr(), rows, cols, max(ld, 1)
+
+
+def gemm_strided_batched(A, B, C=None, alpha=1.0, beta=0.0, transA=False, transB=False,
+                         stream=None):
+    """Batched C[b] = alpha * op(A[b]) @ op(B[b]) + beta * C[b] on 3-D torch CUDA
+    tensors (a batch dimension of stride 0, e.g. from expand(), shares that
+    operand).  If C is None a new (batch, M, N) tensor is allocated."""
+    import torch
+    pa, ba, ra, ca, lda, sa = _batched(A, "A")
+    pb, bb, rb, cb, ldb, sb = _batched(B, "B")
+    batch = max(ba, bb)
+    if ba not in (1, batch) or bb not in (1, batch):
+        raise ValueError("batch sizes differ")
+    M, Ka = (ca, ra) if transA else (ra, ca)
+    Kb, N = (cb, rb) if transB else (rb, cb)
+    if Ka != Kb:
+        raise ValueError(f"inner dimensions differ: {Ka} vs {Kb}")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        C = torch.empty((batch, M, N), dtype=torch.float32, device=A.device)
+    pc, bc, rc, cc, ldc, sc = _batched(C, "C")
+    if (bc, rc, cc) != (batch, M, N):
+        raise ValueError(f"C must be {batch} x {M} x {N}")
+    s = stream if stream is not None else torch.cuda.current_stream(A.device)
+    with torch.cuda.device(A.device):
+        sgemm_strided_batched(int(bool(transA)), int(bool(transB)), M, N, Ka, float(alpha), pa, lda,
+                              sa if ba > 1 else 0, pb, ldb, sb if bb > 1 else 0, float(beta), pc,
+                              ldc, sc, batch, s.cuda_stream)
+    return C
 
 
 def gemm(A, B, C=None, alpha=1.0, beta=0.0, transA=False, transB=False, algo=ALGO_AUTO,

@@ -105,6 +105,24 @@ bool encode_tmap(CUtensorMap *m, const float *base, int64_t rows, int64_t cols, 
   return r == CUDA_SUCCESS;
 }
 
+// 3-D form for a strided batch: dims {cols, rows, batch}, strides {ld, stride}
+// elements, box box_cols x box_rows x 1.
+bool encode_tmap_batched(CUtensorMap *m, const float *base, int64_t rows, int64_t cols, int64_t ld,
+                         int64_t batch, int64_t stride, int box_cols, int box_rows, bool swizzle128) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4u, static_cast<cuuint64_t>(stride) * 4u};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int norm_op(int t) {
   switch (t) {
     case 0: case 'N': case 'n': return 0;
@@ -122,7 +140,7 @@ static void byte_range(const void *p, int64_t rows, int64_t cols, int64_t ld, ui
 static bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
 
 // Host-side validation shared by sgemm_ex and sgemm_select_algo.
-sgemm_status_t validate(const Args &a, bool c_writable) {
+sgemm_status_t validate_shape(const Args &a) {
   if (a.ta < 0 || a.tb < 0) return SGEMM_ERR_INVALID_VALUE;
   if (a.M < 0 || a.N < 0 || a.K < 0) return SGEMM_ERR_INVALID_VALUE;
   if (a.M > kMaxDim || a.N > kMaxDim || a.K > kMaxDim) return SGEMM_ERR_INVALID_VALUE;
@@ -130,6 +148,13 @@ sgemm_status_t validate(const Args &a, bool c_writable) {
   if (a.lda < (a_cols > 1 ? a_cols : 1) || a.lda > kMaxLd) return SGEMM_ERR_INVALID_VALUE;
   if (a.ldb < (b_cols > 1 ? b_cols : 1) || a.ldb > kMaxLd) return SGEMM_ERR_INVALID_VALUE;
   if (a.ldc < (a.N > 1 ? a.N : 1) || a.ldc > kMaxLd) return SGEMM_ERR_INVALID_VALUE;
+  return SGEMM_SUCCESS;
+}
+
+sgemm_status_t validate(const Args &a, bool c_writable) {
+  const sgemm_status_t shape = validate_shape(a);
+  if (shape != SGEMM_SUCCESS) return shape;
+  const int64_t a_cols = a.ta ? a.M : a.K, b_cols = a.tb ? a.K : a.N;
   if (a.M == 0 || a.N == 0) return SGEMM_SUCCESS;
   if (c_writable && a.C == nullptr) return SGEMM_ERR_INVALID_VALUE;
   const bool need_ab = a.K > 0 && a.alpha != 0.0f;
@@ -221,7 +246,13 @@ sgemm_algo_t auto_algo(const Args &a) {
   return tma_eligible(a) ? SGEMM_ALGO_SIMT_TMA : SGEMM_ALGO_SIMT_CPASYNC;
 }
 
-sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_t stream) {
+// A strided batch of products (count 1 for a plain product).
+struct Batch {
+  int64_t count, sa, sb, sc;
+};
+
+sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_t stream,
+                        const Batch &bt = Batch{1, 0, 0, 0}) {
   const int tile = pick_simt_tile(a, producer, d.sm_count);
   const SimtKernelInfo *ki = kernel_info(d, producer, a.ta, a.tb, tile);
   if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_LAUNCH;
@@ -241,14 +272,46 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   p.tiles_m = static_cast<int>(cdiv(a.M, ki->bm));
   p.tiles_n = static_cast<int>(cdiv(a.N, ki->bn));
   p.k_tiles = static_cast<int>(cdiv(a.K, 32));
-  const int64_t num_tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  const int64_t tiles_per_batch = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  const int64_t num_tiles = tiles_per_batch * bt.count;
   if (num_tiles > kMaxDim) return SGEMM_ERR_UNSUPPORTED;
   p.num_tiles = static_cast<int>(num_tiles);
+  p.tiles_per_batch = static_cast<int>(tiles_per_batch);
+  p.strideA = bt.sa;
+  p.strideB = bt.sb;
+  p.strideC = bt.sc;
+  p.a_map3d = producer == kTma && bt.count > 1 && bt.sa != 0;
+  p.b_map3d = producer == kTma && bt.count > 1 && bt.sb != 0;
   p.group_m = 8;
-  p.c_vec4 = (a.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
+  p.c_vec4 = (a.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) &&
+             (bt.count == 1 || bt.sc % 4 == 0);
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   p.status = d.status;
   p.workspace = nullptr;
+
+  CUtensorMap tmA, tmB;
+  std::memset(&tmA, 0, sizeof(tmA));
+  std::memset(&tmB, 0, sizeof(tmB));
+  if (producer == kTma) {
+    // op(A): K-major when stored M x K, MN-major when stored K x M; a strided
+    // operand of a batch gets a third (batch) dimension.
+    const int64_t ar = a.ta == 0 ? a.M : a.K, ac = a.ta == 0 ? a.K : a.M;
+    const int abc = a.ta == 0 ? 32 : ki->bm, abr = a.ta == 0 ? ki->bm : 32;
+    const int64_t br = a.tb == 0 ? a.K : a.N, bc = a.tb == 0 ? a.N : a.K;
+    const int bbc = a.tb == 0 ? ki->bn : 32, bbr = a.tb == 0 ? 32 : ki->bn;
+    const bool okA = p.a_map3d
+                         ? encode_tmap_batched(&tmA, a.A, ar, ac, a.lda, bt.count, bt.sa, abc, abr, a.ta == 0)
+                         : encode_tmap(&tmA, a.A, ar, ac, a.lda, abc, abr, a.ta == 0);
+    const bool okB = p.b_map3d
+                         ? encode_tmap_batched(&tmB, a.B, br, bc, a.ldb, bt.count, bt.sb, bbc, bbr, a.tb == 1)
+                         : encode_tmap(&tmB, a.B, br, bc, a.ldb, bbc, bbr, a.tb == 1);
+    if (!okA || !okB) {
+      // a batch layout the tensor-map encoder refuses is still a valid batch:
+      // load it with cp.async instead
+      if (bt.count > 1) return run_simt(a, d, kCpAsync, stream, bt);
+      return SGEMM_ERR_LAUNCH;
+    }
+  }
 
   const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
   std::unique_lock<std::mutex> ws_lock(d.ws_mu);
@@ -262,17 +325,6 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   p.dp_tiles = plan.dp_tiles;
   p.sk_iters = plan.sk_iters;
 
-  CUtensorMap tmA, tmB;
-  std::memset(&tmA, 0, sizeof(tmA));
-  std::memset(&tmB, 0, sizeof(tmB));
-  if (producer == kTma) {
-    // op(A): K-major when stored M x K, MN-major when stored K x M.
-    const bool okA = a.ta == 0 ? encode_tmap(&tmA, a.A, a.M, a.K, a.lda, 32, ki->bm, true)
-                               : encode_tmap(&tmA, a.A, a.K, a.M, a.lda, ki->bm, 32, false);
-    const bool okB = a.tb == 0 ? encode_tmap(&tmB, a.B, a.K, a.N, a.ldb, ki->bn, 32, false)
-                               : encode_tmap(&tmB, a.B, a.N, a.K, a.ldb, 32, ki->bn, true);
-    if (!okA || !okB) return SGEMM_ERR_LAUNCH;
-  }
   if (plan.sk_tiles > 0 && d.ws_used && d.ws_last_stream != stream) {
     // the previous stream-K call on another stream may still be using the workspace
     if (cudaStreamWaitEvent(stream, d.ws_event, 0) != cudaSuccess) return SGEMM_ERR_LAUNCH;
@@ -400,6 +452,58 @@ sgemm_status_t sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K, fl
                      int64_t ldc, void *stream) {
   return sgemm_ex(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream,
                   SGEMM_ALGO_AUTO);
+}
+
+sgemm_status_t sgemm_strided_batched(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                     float alpha, const float *A, int64_t lda, int64_t strideA,
+                                     const float *B, int64_t ldb, int64_t strideB, float beta,
+                                     float *C, int64_t ldc, int64_t strideC, int64_t batch,
+                                     void *stream) {
+  Args a{norm_op(transA), norm_op(transB), M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
+  if (batch < 0 || batch > kMaxDim || strideA < 0 || strideB < 0 || strideC < 0 ||
+      strideA > kMaxLd || strideB > kMaxLd || strideC > kMaxLd)
+    return SGEMM_ERR_INVALID_VALUE;
+  t_last_launches = 0;
+  sgemm_status_t st = batch == 0 ? validate_shape(a) : validate(a, true);
+  if (st != SGEMM_SUCCESS || batch == 0 || M == 0 || N == 0) return st;
+  const bool need_ab = K > 0 && alpha != 0.0f;
+  using u128 = unsigned __int128;
+  // elements spanned by one stored operand of rows x cols with leading dimension ld
+  auto span = [](int64_t rows, int64_t cols, int64_t ld) -> u128 {
+    return static_cast<u128>(rows - 1) * static_cast<u128>(ld) + static_cast<u128>(cols);
+  };
+  const int64_t ar = a.ta ? K : M, ac = a.ta ? M : K, br = a.tb ? N : K, bc = a.tb ? K : N;
+  if (batch > 1) {
+    // the C_b must not overlap one another, and the byte range of all C_b must
+    // not overlap that of all A_b or all B_b
+    if (static_cast<u128>(strideC) < span(M, N, ldc)) return SGEMM_ERR_ALIASING;
+    auto range = [&](const void *ptr, u128 one, int64_t stride, u128 *lo, u128 *hi) {
+      *lo = reinterpret_cast<uintptr_t>(ptr);
+      *hi = *lo + 4 * (one + static_cast<u128>(batch - 1) * static_cast<u128>(stride));
+    };
+    if (need_ab) {
+      u128 c0, c1, x0, x1;
+      range(C, span(M, N, ldc), strideC, &c0, &c1);
+      range(A, span(ar, ac, lda), strideA, &x0, &x1);
+      if (c0 < x1 && x0 < c1) return SGEMM_ERR_ALIASING;
+      range(B, span(br, bc, ldb), strideB, &x0, &x1);
+      if (c0 < x1 && x0 < c1) return SGEMM_ERR_ALIASING;
+    }
+  }
+  sgemm_status_t why = SGEMM_SUCCESS;
+  DeviceState *d = device_state(&why);
+  if (!d) return why;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!need_ab) {
+    if (launch_scale_c_batched(C, ldc, strideC, static_cast<int>(M), static_cast<int>(N), batch,
+                               beta, s) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+    t_last_launches = 1;
+    return SGEMM_SUCCESS;
+  }
+  // TMA: 16-byte aligned bases, rows and batch strides
+  const bool tma = tma_eligible(a) && (batch == 1 || (strideA % 4 == 0 && strideB % 4 == 0));
+  return run_simt(a, *d, tma ? kTma : kCpAsync, s, Batch{batch, strideA, strideB, strideC});
 }
 
 int sgemm_select_algo(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A,

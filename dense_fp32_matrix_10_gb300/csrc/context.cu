@@ -58,12 +58,15 @@ __global__ void smem_tiled_kernel(const PlainParams p) {
   if (i < p.M && j < p.N) store_out(p, i, j, acc);
 }
 
-__global__ void scale_c_kernel(float *C, int64_t ldc, int M, int N, float beta) {
-  const int64_t total = static_cast<int64_t>(M) * N;
+// C_b = beta * C_b for b < batch (C_b = C + b * strideC).
+__global__ void scale_c_kernel(float *C, int64_t ldc, int64_t strideC, int M, int N, int64_t batch,
+                               float beta) {
+  const int64_t per = static_cast<int64_t>(M) * N, total = per * batch;
   for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t i = e / N, j = e - i * N;
-    float *c = C + i * ldc + j;
+    const int64_t b = e / per, r = e - b * per;
+    const int64_t i = r / N, j = r - i * N;
+    float *c = C + b * strideC + i * ldc + j;
     *c = (beta != 0.0f) ? beta * *c : 0.0f;
   }
 }
@@ -94,11 +97,16 @@ cudaError_t launch_smem_tiled(const PlainParams &p, cudaStream_t s) {
 }
 
 cudaError_t launch_scale_c(float *C, int64_t ldc, int M, int N, float beta, cudaStream_t s) {
-  const int64_t total = static_cast<int64_t>(M) * N;
+  return launch_scale_c_batched(C, ldc, 0, M, N, 1, beta, s);
+}
+
+cudaError_t launch_scale_c_batched(float *C, int64_t ldc, int64_t strideC, int M, int N,
+                                   int64_t batch, float beta, cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(M) * N * batch;
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 152 * 16) blocks = 152 * 16;  // grid-stride beyond 16 waves of 152 SMs
-  scale_c_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(C, ldc, M, N, beta);
+  scale_c_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(C, ldc, strideC, M, N, batch, beta);
   return cudaGetLastError();
 }
 

@@ -60,6 +60,8 @@ struct Args {
 };
 
 // Host-side validation shared by the entry points (status codes, no launch).
+// Dimension and leading-dimension checks only (no pointers).
+sgemm_status_t validate_shape(const Args &a);
 sgemm_status_t validate(const Args &a, bool c_writable);
 bool tma_eligible(const Args &a);
 int64_t cdiv(int64_t a, int64_t b);

@@ -69,6 +69,8 @@ struct PlainParams {
 cudaError_t launch_naive(const PlainParams &p, cudaStream_t s);
 cudaError_t launch_smem_tiled(const PlainParams &p, cudaStream_t s);
 cudaError_t launch_scale_c(float *C, int64_t ldc, int M, int N, float beta, cudaStream_t s);
+cudaError_t launch_scale_c_batched(float *C, int64_t ldc, int64_t strideC, int M, int N,
+                                   int64_t batch, float beta, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint64_t budget_ns, int *status, cudaStream_t s);
 
 }  // namespace sg

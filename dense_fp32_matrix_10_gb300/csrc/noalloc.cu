@@ -121,6 +121,9 @@ extern "C" sgemm_status_t sgemm_noalloc(int transA, int transB, int64_t M, int64
   const int64_t num_tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
   if (num_tiles > kMaxDim) return SGEMM_ERR_UNSUPPORTED;
   p.num_tiles = static_cast<int>(num_tiles);
+  p.tiles_per_batch = p.num_tiles;  // one product
+  p.strideA = p.strideB = p.strideC = 0;
+  p.a_map3d = p.b_map3d = 0;
   p.group_m = 8;
   p.c_vec4 = (ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0);
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);

@@ -93,6 +93,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *desc, uint
       : "memory");
 }
 
+// 3-D form: c2 is the outermost coordinate (the batch index of a strided
+// batch of matrices).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *desc, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 4-byte asynchronous copy global -> shared; src_bytes = 0 writes a zero and
 // reads nothing (the source address must still be a valid generic address).

@@ -80,7 +80,22 @@ struct SimtParams {
   int dp_tiles;
   int64_t sk_iters;      // (num_tiles - dp_tiles) * k_tiles
   float *workspace;      // 2 * gridDim.x slots of BM * BN floats
+  // Strided batch: product b uses A + b*strideA, B + b*strideB, C + b*strideC
+  // (elements; a zero stride shares one operand across the batch).  Tiles are
+  // numbered batch-major: num_tiles = batch * tiles_per_batch.  With the TMA
+  // producer a strided operand's tensor map has a third (batch) dimension.
+  int tiles_per_batch;
+  int64_t strideA, strideB, strideC;
+  int a_map3d, b_map3d;
 };
+
+// Batch index and (tile_m, tile_n) of linear tile t.
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m,
+                                            int &tm, int &tn);
+__device__ __forceinline__ void unit_coords(const SimtParams &p, int t, int &b, int &tm, int &tn) {
+  b = t / p.tiles_per_batch;
+  tile_coords(t - b * p.tiles_per_batch, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+}
 
 // One unit of work: k-tiles [k0, k1) of tile `tile`; slot < 0 writes C.
 struct WorkUnit {
@@ -198,8 +213,8 @@ __device__ __forceinline__ void produce_tma(const SimtParams &p, const CUtensorM
   uint32_t it = 0;        // k-slices whose stage copies are issued
   uint32_t raw_it = 0;    // k-slices whose raw A copies are issued
   for_each_unit(p, [&](const WorkUnit &u) {
-    int tm, tn;
-    tile_coords(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    int bi, tm, tn;
+    unit_coords(p, u.tile, bi, tm, tn);
     const int m0 = tm * Cfg::BM, n0 = tn * Cfg::BN;
     for (int kt = u.k0; kt < u.k1; ++kt) {
       const uint32_t s = it % Cfg::STAGES;
@@ -213,8 +228,11 @@ __device__ __forceinline__ void produce_tma(const SimtParams &p, const CUtensorM
           return false;
         }
         mbar_arrive_expect_tx(raw_full0 + 8 * r, Cfg::A_STAGE_BYTES);
-        tma_load_2d(smem_base + Cfg::RAW_A_OFFSET + r * Cfg::A_STAGE_BYTES, tmA, raw_full0 + 8 * r,
-                    k0, m0);
+        const uint32_t raw_dst = smem_base + Cfg::RAW_A_OFFSET + r * Cfg::A_STAGE_BYTES;
+        if (p.a_map3d)
+          tma_load_3d(raw_dst, tmA, raw_full0 + 8 * r, k0, m0, bi);
+        else
+          tma_load_2d(raw_dst, tmA, raw_full0 + 8 * r, k0, m0);
         ++raw_it;
       }
       if (round > 0 &&
@@ -227,15 +245,19 @@ __device__ __forceinline__ void produce_tma(const SimtParams &p, const CUtensorM
       const uint32_t b_dst = a_dst + Cfg::A_STAGE_BYTES;
       mbar_arrive_expect_tx(full, Cfg::A_TRANS ? Cfg::B_STAGE_BYTES : Cfg::STAGE_BYTES);
       if (!Cfg::A_TRANS) {
-        if (Cfg::A_KMAJOR)
-          tma_load_2d(a_dst, tmA, full, k0, m0);
+        const int c0 = Cfg::A_KMAJOR ? k0 : m0, c1 = Cfg::A_KMAJOR ? m0 : k0;
+        if (p.a_map3d)
+          tma_load_3d(a_dst, tmA, full, c0, c1, bi);
         else
-          tma_load_2d(a_dst, tmA, full, m0, k0);
+          tma_load_2d(a_dst, tmA, full, c0, c1);
       }
-      if (Cfg::B_KMAJOR)
-        tma_load_2d(b_dst, tmB, full, k0, n0);
-      else
-        tma_load_2d(b_dst, tmB, full, n0, k0);
+      {
+        const int c0 = Cfg::B_KMAJOR ? k0 : n0, c1 = Cfg::B_KMAJOR ? n0 : k0;
+        if (p.b_map3d)
+          tma_load_3d(b_dst, tmB, full, c0, c1, bi);
+        else
+          tma_load_2d(b_dst, tmB, full, c0, c1);
+      }
       ++it;
     }
     return true;
@@ -301,9 +323,11 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
   constexpr int PT = Cfg::PRODUCER_THREADS;
   uint32_t it = 0;
   for_each_unit(p, [&](const WorkUnit &u) {
-    int tm, tn;
-    tile_coords(u.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    int bi, tm, tn;
+    unit_coords(p, u.tile, bi, tm, tn);
     const int m0 = tm * BM, n0 = tn * BN;
+    const float *Ab = p.A + static_cast<int64_t>(bi) * p.strideA;
+    const float *Bb = p.B + static_cast<int64_t>(bi) * p.strideB;
     for (int kt = u.k0; kt < u.k1; ++kt, ++it) {
       const uint32_t s = it % Cfg::STAGES;
       const uint32_t round = it / Cfg::STAGES;
@@ -332,8 +356,8 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
         const int gm = m0 + m, gk = k0 + k;
         const bool in = gm < p.M && gk < p.K;
         const float *src = p.A;
-        if (in) src = Cfg::A_KMAJOR ? p.A + static_cast<int64_t>(gm) * p.lda + gk
-                                    : p.A + static_cast<int64_t>(gk) * p.lda + gm;
+        if (in) src = Cfg::A_KMAJOR ? Ab + static_cast<int64_t>(gm) * p.lda + gk
+                                    : Ab + static_cast<int64_t>(gk) * p.lda + gm;
         cp_async_4(a_dst + off, src, in ? 4u : 0u);
       }
       // op(B) tile: 32 x BN elements
@@ -353,8 +377,8 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
         const int gn = n0 + n, gk = k0 + k;
         const bool in = gn < p.N && gk < p.K;
         const float *src = p.B;
-        if (in) src = Cfg::B_KMAJOR ? p.B + static_cast<int64_t>(gn) * p.ldb + gk
-                                    : p.B + static_cast<int64_t>(gk) * p.ldb + gn;
+        if (in) src = Cfg::B_KMAJOR ? Bb + static_cast<int64_t>(gn) * p.ldb + gk
+                                    : Bb + static_cast<int64_t>(gk) * p.ldb + gn;
         cp_async_4(b_dst + off, src, in ? 4u : 0u);
       }
       cp_async_mbar_arrive_noinc(full0 + 8 * s);
@@ -544,15 +568,15 @@ __device__ __forceinline__ void mma_stage(AccT<Cfg> &acc, const char *a_stage, c
 }
 
 template <class Cfg>
-__device__ __forceinline__ void epilogue(const SimtParams &p, const AccT<Cfg> &acc, int m0,
-                                         int n0, int wm, int wn, int tm, int tn) {
+__device__ __forceinline__ void epilogue(const SimtParams &p, float *Cb, const AccT<Cfg> &acc,
+                                         int m0, int n0, int wm, int wn, int tm, int tn) {
   constexpr int MODE = acc_mode<Cfg>(), TN = Cfg::TN;
   const bool read_c = p.beta != 0.0f;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const int m = m0 + wm * 32 + thread_row<Cfg>(tm, r);
     if (m >= p.M) continue;
-    float *crow = p.C + static_cast<int64_t>(m) * p.ldc;
+    float *crow = Cb + static_cast<int64_t>(m) * p.ldc;
     if (!Cfg::B_KMAJOR) {
       // columns 32h + 4tn .. +3: TN/4 float4 groups
 #pragma unroll
@@ -680,8 +704,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
   const int tn = lane & 7;
   uint32_t it = 0;
   for_each_unit(p, [&](const WorkUnit &u) {
-    int tile_m, tile_n;
-    tile_coords(u.tile, p.tiles_m, p.tiles_n, p.group_m, tile_m, tile_n);
     AccT<Cfg> acc;
 #pragma unroll
     for (int q = 0; q < 4 * Cfg::TN; ++q) acc[q] = make_float2(0.0f, 0.0f);
@@ -695,9 +717,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
-    if (u.slot < 0)
-      epilogue<Cfg>(p, acc, tile_m * Cfg::BM, tile_n * Cfg::BN, wm, wn, tm, tn);
-    else
+    if (u.slot < 0) {
+      // tile coordinates only now: nothing but acc stays live across the k-loop
+      int bi, tile_m, tile_n;
+      unit_coords(p, u.tile, bi, tile_m, tile_n);
+      epilogue<Cfg>(p, p.C + static_cast<int64_t>(bi) * p.strideC, acc, tile_m * Cfg::BM,
+                    tile_n * Cfg::BN, wm, wn, tm, tn);
+    } else
       store_partial<Cfg>(p.workspace + static_cast<int64_t>(u.slot) * Cfg::BM * Cfg::BN, acc, wm, wn,
                          tm, tn);
     return true;

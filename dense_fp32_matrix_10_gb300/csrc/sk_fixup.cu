@@ -39,8 +39,9 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const SimtParams p, int b
   const int n = s_count;
   if (n == 0) return;
 
-  int tm, tn;
-  tile_coords(p.dp_tiles + blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+  int bi, tm, tn;
+  unit_coords(p, p.dp_tiles + blockIdx.x, bi, tm, tn);
+  float *Cb = p.C + static_cast<int64_t>(bi) * p.strideC;
   const int64_t tile_elems = static_cast<int64_t>(bm) * bn;
   const bool read_c = p.beta != 0.0f;
   // 4 consecutive columns per thread step (bn is a multiple of 64)
@@ -55,7 +56,7 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const SimtParams p, int b
     }
     const int row = tm * bm + e / bn, col = tn * bn + e % bn;
     if (row >= p.M) continue;
-    float *c = p.C + static_cast<int64_t>(row) * p.ldc + col;
+    float *c = Cb + static_cast<int64_t>(row) * p.ldc + col;
     const float s4[4] = {sum.x, sum.y, sum.z, sum.w};
     if (p.c_vec4 && col + 3 < p.N) {
       float4 o;

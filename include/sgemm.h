@@ -128,6 +128,33 @@ SGEMM_API sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, 
                         sgemm_algo_t algo);
 
 /*
+ * Strided batch: for b = 0 .. batch-1,
+ *     C_b = alpha * op(A_b) * op(B_b) + beta * C_b,
+ * with A_b = A + b*strideA, B_b = B + b*strideB, C_b = C + b*strideC (strides
+ * in elements, >= 0).  Attention's Q K^T, which the cloud.baidu.com article
+ * 9456745 (introduction) names among the main uses of a GEMM kernel, is such
+ * a batch of small products, one per head -- here one launch for the whole
+ * batch instead of one per product.  A stride of 0 shares that operand
+ * across the batch (e.g. one weight matrix for every product).
+ * Layout and leading dimensions per product are as for sgemm().  When batch > 1
+ * the C_b must not overlap one another (strideC >= (M-1)*ldc + N), and the
+ * address range covered by all C_b must not meet the range covered by all A_b
+ * or all B_b (else SGEMM_ERR_ALIASING; inputs may overlap each other, e.g.
+ * sliding windows).  batch < 0 or a negative stride is SGEMM_ERR_INVALID_VALUE;
+ * batch == 0, M == 0 or N == 0 do nothing; K == 0 or alpha == 0 scale every
+ * C_b by beta.  Runs the CUDA-core kernels -- TMA loads (a 3-D tensor map per
+ * strided operand) when bases, leading dimensions and strides are multiples of
+ * 16 bytes and the map encodes, cp.async otherwise -- with the k-iterations of
+ * the batch's tiles spread by stream-K like a single product's.  batch * tiles per product must stay below 2^31
+ * (SGEMM_ERR_UNSUPPORTED).
+ */
+SGEMM_API sgemm_status_t sgemm_strided_batched(int transA, int transB, int64_t M, int64_t N,
+                                               int64_t K, float alpha, const float *A, int64_t lda,
+                                               int64_t strideA, const float *B, int64_t ldb,
+                                               int64_t strideB, float beta, float *C, int64_t ldc,
+                                               int64_t strideC, int64_t batch, void *stream);
+
+/*
  * The family SGEMM_ALGO_AUTO would run for these arguments, or -1 if the
  * arguments are invalid.  Host only: queues nothing and touches no device
  * memory (it reads the device's SM count once).

@@ -107,6 +107,48 @@ class Oracle:
         """The FP64 result rounded once to FP32 (round to nearest even)."""
         return self.sgemm_f64(transA, transB, alpha, A, B, beta, C, threads).astype(np.float32)
 
+    def sgemm_strided_batched_f64(self, transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb,
+                                  strideB, beta, C, ldc, strideC, batch, threads=None):
+        """(batch, M, N) float64: product b is alpha*op(A_b)*op(B_b) + beta*C_b,
+        where X_b is the stored matrix that starts b*strideX elements into the
+        flat float32 buffer X, with leading dimension ldX (the strided-batch
+        layout of BLAS-style interfaces; a stride of 0 repeats one matrix).
+        Each product is one call of the single-product oracle on that offset;
+        C may be None when beta == 0."""
+        ta, tb = _op(transA), _op(transB)
+        flats = []
+        for x, name in ((A, "A"), (B, "B"), (C, "C")):
+            if x is None:
+                flats.append(None)
+                continue
+            if not isinstance(x, np.ndarray) or x.dtype != np.float32 or x.ndim != 1 \
+                    or (x.size and x.strides[0] != 4):
+                raise TypeError(f"{name} must be a contiguous 1-D float32 numpy array")
+            flats.append(x)
+        A, B, C = flats
+        need = [(A, lda, strideA, K if ta else M, M if ta else K, "A"),
+                (B, ldb, strideB, N if tb else K, K if tb else N, "B")]
+        if C is not None:
+            need.append((C, ldc, strideC, M, N, "C"))
+        for x, ld, stride, rows, cols, name in need:
+            if stride < 0 or ld < max(cols, 1):
+                raise ValueError(f"{name}: bad stride or leading dimension")
+            if batch > 0 and rows > 0 and cols > 0 and \
+                    (batch - 1) * stride + (rows - 1) * ld + cols > x.size:
+                raise ValueError(f"{name} buffer is too small for the batch")
+        R = np.empty((batch, M, N), dtype=np.float64)
+        nth = int(threads or default_threads())
+        for b in range(batch):
+            pa = ctypes.cast(A.ctypes.data + 4 * b * strideA, _F32P) if A is not None and A.size else None
+            pb = ctypes.cast(B.ctypes.data + 4 * b * strideB, _F32P) if B is not None and B.size else None
+            pc = ctypes.cast(C.ctypes.data + 4 * b * strideC, _F32P) if C is not None and C.size else None
+            st = self.lib.oracle_sgemm_f64(
+                ta, tb, M, N, K, float(alpha), pa, lda, pb, ldb, float(beta), pc, ldc,
+                R[b].ctypes.data_as(_F64P), max(N, 1), nth)
+            if st != 0:
+                raise ValueError(f"oracle_sgemm_f64 rejected product {b} (status {st})")
+        return R
+
     def sgemm_entries_f64(self, transA, transB, alpha, A, B, beta, C, I, J):
         """float64 values of the (I[e], J[e]) outputs of the same product."""
         ta, tb = _op(transA), _op(transB)
@@ -147,3 +189,7 @@ def sgemm_f32(*args, **kw):
 
 def sgemm_entries_f64(*args, **kw):
     return default().sgemm_entries_f64(*args, **kw)
+
+
+def sgemm_strided_batched_f64(*args, **kw):
+    return default().sgemm_strided_batched_f64(*args, **kw)

@@ -328,8 +328,78 @@ def pin_threads_invariant(orc):
     assert np.array_equal(r1, r7)
 
 
+# ------------------------------------------------------------ strided batch
+def _strided_view(flat, batch, rows, cols, ld, stride):
+    """numpy's own view of the strided-batch layout: element (b, r, c) at
+    flat[b*stride + r*ld + c]."""
+    return np.lib.stride_tricks.as_strided(flat, shape=(batch, rows, cols),
+                                           strides=(4 * stride, 4 * ld, 4), writeable=False)
+
+
+def pin_batched_closed_form(orc):
+    """A_b = (b+1) * I (square, K = M): product b is exactly (b+1) * op(B_b);
+    with transB the transposed B_b, so a swapped stride or op shows."""
+    M = K = 6
+    N, batch = 5, 4
+    rng = _rng(31)
+    eye = np.eye(M, dtype=np.float32)
+    A = np.concatenate([(b + 1) * eye.ravel() for b in range(batch)]).astype(np.float32)
+    for tb in (0, 1):
+        rows, cols = (N, K) if tb else (K, N)
+        B = _stored(rng, (batch * rows * cols,), "int")
+        R = orc.sgemm_strided_batched_f64(0, tb, M, N, K, 1.0, A, M, M * M, B, cols, rows * cols,
+                                          0.0, None, N, M * N, batch)
+        Bv = _strided_view(B, batch, rows, cols, cols, rows * cols)
+        for b in range(batch):
+            Bb = Bv[b].T if tb else Bv[b]
+            assert np.array_equal(R[b], (b + 1) * Bb.astype(np.float64)), (tb, b)
+
+
+def pin_batched_broadcast_and_interleaved(orc):
+    """Head-interleaved inputs (lda = heads * K, strideA = K: the packed Q K^T
+    layout of attention) and a shared operand (strideB = 0), against numpy's
+    float64 matmul on numpy's own strided views; integer data, so exact."""
+    heads, M, N, K = 3, 5, 4, 7
+    rng = _rng(32)
+    A = _stored(rng, (M * heads * K,), "int")
+    B = _stored(rng, (K * N,), "int")
+    C = _stored(rng, (heads * M * N,), "int")
+    R = orc.sgemm_strided_batched_f64(0, 0, M, N, K, 2.0, A, heads * K, K, B, N, 0, -1.0, C, N,
+                                      M * N, heads)
+    Av = _strided_view(A, heads, M, K, heads * K, K).astype(np.float64)
+    Bv = _strided_view(B, heads, K, N, N, 0).astype(np.float64)
+    Cv = _strided_view(C, heads, M, N, N, M * N).astype(np.float64)
+    assert np.array_equal(R, 2.0 * np.matmul(Av, Bv) - Cv)
+    # transposed A read from the same interleaved buffer (op(A) = A_b^T: K x M stored)
+    At = _stored(rng, (K * heads * M,), "int")
+    R = orc.sgemm_strided_batched_f64(1, 0, M, N, K, 1.0, At, heads * M, M, B, N, 0, 0.0, None, N,
+                                      M * N, heads)
+    Atv = _strided_view(At, heads, K, M, heads * M, M).astype(np.float64)
+    assert np.array_equal(R, np.matmul(np.swapaxes(Atv, 1, 2), Bv))
+
+
+def pin_batched_gaps_unread(orc):
+    """Elements between the matrices of a padded batch (NaN here) are never
+    read, and beta == 0 reads no C at all."""
+    batch, M, N, K = 3, 4, 3, 5
+    rng = _rng(33)
+    sa, sb = M * K + 9, K * N + 2
+    A = np.full(batch * sa, np.nan, np.float32)
+    B = np.full(batch * sb, np.nan, np.float32)
+    for b in range(batch):
+        A[b * sa: b * sa + M * K] = _stored(rng, (M * K,), "dyadic")
+        B[b * sb: b * sb + K * N] = _stored(rng, (K * N,), "dyadic")
+    C = np.full(batch * M * N, np.nan, np.float32)
+    R = orc.sgemm_strided_batched_f64(0, 0, M, N, K, 1.0, A, K, sa, B, N, sb, 0.0, C, N, M * N, batch)
+    assert np.all(np.isfinite(R))
+    Av = _strided_view(A, batch, M, K, K, sa).astype(np.float64)
+    Bv = _strided_view(B, batch, K, N, N, sb).astype(np.float64)
+    assert np.array_equal(R, np.matmul(Av, Bv))
+
+
 ALL_PINS = [
     pin_golden, pin_fraction_dyadic, pin_fraction_float, pin_identity, pin_all_ones,
     pin_integer_vs_numpy, pin_numpy_float64, pin_transpose_identities, pin_scaling,
     pin_degenerate, pin_padded_ld, pin_entries_match_full, pin_threads_invariant,
+    pin_batched_closed_form, pin_batched_broadcast_and_interleaved, pin_batched_gaps_unread,
 ]
