@@ -220,6 +220,14 @@ def tflops(flops, ms):
     return flops / (ms * 1e-3) / 1e12
 
 
+def job_rate(dist, flops_per_rank: float, ms_this_rank: float, device=None):
+    """Whole-job rate over replicas: every rank did `flops_per_rank`, the job
+    took as long as its slowest rank.  Returns (max ms over ranks, TFLOP/s of
+    all ranks together)."""
+    ms = dist.max(ms_this_rank, device)
+    return ms, flops_per_rank * dist.world / (ms * 1e-3) / 1e12
+
+
 def run_ours(args, dist):
     import torch
     import dense_fp32_matrix_10_gb300 as sg
@@ -252,8 +260,7 @@ def run_ours(args, dist):
     dist.barrier()
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
-    ms_step = dist.max(ms_region, dev)
-    value = flops * dist.world / (ms_step * 1e-3) / 1e12
+    ms_step, value = job_rate(dist, flops, ms_region, dev)
 
     # ---- end to end through the C ABI: pinned host operands in, result out
     hA = torch.empty(A.shape, dtype=torch.float32, pin_memory=True)
@@ -276,8 +283,8 @@ def run_ours(args, dist):
     if e2e_steps:
         e1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = dist.max(e0.elapsed_time(e1) / e2e_steps, dev)
-        e2e = {"value": round(flops * dist.world / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        ms_e2e, e2e_rate = job_rate(dist, flops, e0.elapsed_time(e1) / e2e_steps, dev)
+        e2e = {"value": round(e2e_rate, 3), "unit": "TFLOP/s",
                "ms_per_step": round(ms_e2e, 4),
                "h2d_bytes_per_step": int(A.numel() * 4 + B.numel() * 4),
                "d2h_bytes_per_step": int(C.numel() * 4)}
