@@ -58,6 +58,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not yet complete may stay
+// suspended up to `hint_ns` (it still wakes when the phase completes), so a
+// waiting warp takes fewer issue slots from the warps doing the math.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Suspend-time hint of the bounded waits' retries (0: the hardware default).
+#ifndef SG_WAIT_HINT_NS
+#define SG_WAIT_HINT_NS 0
+#endif
+
 // Error codes a kernel records in the device status word.
 enum : int { kDevOk = 0, kDevTimeout = 5 };
 
@@ -69,7 +89,9 @@ __device__ __forceinline__ bool wait_parity_bounded(uint32_t bar, uint32_t parit
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (SG_WAIT_HINT_NS > 0 ? mbar_try_wait_hint(bar, parity, SG_WAIT_HINT_NS)
+                            : mbar_try_wait(bar, parity))
+      return true;
     if (globaltimer_ns() - t0 > budget_ns) {
       if (status) atomicExch(status, kDevTimeout);
       return false;

@@ -124,6 +124,19 @@ __device__ __forceinline__ void for_each_unit(const SimtParams &p, F &&f) {
   }
 }
 
+// SG_SIMT_TRANSPOSERS  producer warps (1..3) that share the A transpose;
+// SG_SIMT_TRANSPOSER_REGS their registers per thread (the math warps get the
+// rest of the launch budget); SG_SIMT_TRANSPOSE_UNROLL rows in flight.
+#ifndef SG_SIMT_TRANSPOSERS
+#define SG_SIMT_TRANSPOSERS 3
+#endif
+#ifndef SG_SIMT_TRANSPOSER_REGS
+#define SG_SIMT_TRANSPOSER_REGS 56
+#endif
+#ifndef SG_SIMT_TRANSPOSE_UNROLL
+#define SG_SIMT_TRANSPOSE_UNROLL 4
+#endif
+
 template <int WARPS_M_, int WARPS_N_, bool A_KMAJOR_, bool B_KMAJOR_, int STAGES_, int PRODUCER_,
           int TN_ = 8, bool A_TRANS_ = false>
 struct SimtConfig {
@@ -152,7 +165,7 @@ struct SimtConfig {
   // sub-partition: a 9-warp CTA would cap every thread at 168 registers).
   static constexpr int PRODUCER_WARPS = 4;
   static constexpr int PRODUCER_THREADS = 32 * PRODUCER_WARPS;
-  static constexpr int TRANSPOSER_WARPS = 3;  // producer warps 1..3 when A_TRANS
+  static constexpr int TRANSPOSER_WARPS = SG_SIMT_TRANSPOSERS;  // producer warps 1.. when A_TRANS
   static constexpr int THREADS = MATH_THREADS + PRODUCER_THREADS;
   static constexpr int MIN_CTAS = (MATH_WARPS == 8) ? 1 : 2;  // CTAs per SM
   // Per-thread registers after the split; launch budget is
@@ -160,9 +173,12 @@ struct SimtConfig {
   // The bare TMA producer needs few registers; the cp.async producer and the
   // transposing producer warps need more.
   static constexpr bool LEAN_PRODUCER = (PRODUCER == kTma) && !A_TRANS;
-  static constexpr int PRODUCER_REGS = LEAN_PRODUCER ? 24 : 40;
-  static constexpr int MATH_REGS = (MATH_WARPS == 8) ? (LEAN_PRODUCER ? 240 : 232)
-                                                     : (LEAN_PRODUCER ? 232 : 216);
+  static constexpr int LAUNCH_REGS = (65536 / (THREADS * MIN_CTAS)) & ~7;
+  static constexpr int PRODUCER_REGS =
+      LEAN_PRODUCER ? 24 : (A_TRANS ? SG_SIMT_TRANSPOSER_REGS : 40);
+  static constexpr int MATH_REGS_FIT =
+      ((THREADS * LAUNCH_REGS - PRODUCER_THREADS * PRODUCER_REGS) / MATH_THREADS) & ~7;
+  static constexpr int MATH_REGS = MATH_REGS_FIT < 240 ? MATH_REGS_FIT : 240;
   static_assert(MATH_WARPS % 4 == 0, "math role must be whole warpgroups");
   static_assert(PRODUCER_THREADS * PRODUCER_REGS + MATH_THREADS * MATH_REGS <=
                     THREADS * ((65536 / (THREADS * MIN_CTAS)) & ~7),
@@ -296,7 +312,8 @@ __device__ __forceinline__ void transpose_a(const SimtParams &p, unsigned char *
       }
       const unsigned char *raw = smem + Cfg::RAW_A_OFFSET + r * Cfg::A_STAGE_BYTES;
       float *dst = reinterpret_cast<float *>(smem + s * Cfg::STAGE_BYTES);
-#pragma unroll 4
+      constexpr int UNROLL = SG_SIMT_TRANSPOSE_UNROLL;
+#pragma unroll UNROLL
       for (int item = tw; item < ITEMS; item += Cfg::TRANSPOSER_WARPS) {
         const int c = item & 7, m = (item >> 3) * 32 + lane;
         const float4 v = *reinterpret_cast<const float4 *>(raw + m * 128 + ((c ^ (m & 7)) << 4));
@@ -687,7 +704,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     if (Cfg::PRODUCER == kTma) {
       if (threadIdx.x == Cfg::MATH_THREADS)
         produce_tma<Cfg>(p, &tmA, &tmB, smem_base, full0, empty0, raw_full0, raw_empty0, ok);
-      else if (Cfg::A_TRANS && warp > Cfg::MATH_WARPS)
+      else if (Cfg::A_TRANS && warp > Cfg::MATH_WARPS && warp <= Cfg::MATH_WARPS + Cfg::TRANSPOSER_WARPS)
         transpose_a<Cfg>(p, smem, full0, empty0, raw_full0, raw_empty0, warp - Cfg::MATH_WARPS - 1,
                          lane, ok);
     } else {

@@ -160,18 +160,24 @@ def test_register_split_fits_launch_budget(lib):
     forever.  The library re-checks this at run time before any launch."""
     from dense_fp32_matrix_10_gb300 import build
     report = build.ptxas_report().splitlines()
+    src = open(os.path.join(ROOT, "dense_fp32_matrix_10_gb300", "csrc", "simt_gemm.cuh")).read()
+    trans_regs = int(re.search(r"#define SG_SIMT_TRANSPOSER_REGS (\d+)", src).group(1))
     checked = 0
     for i, ln in enumerate(report):
-        m = re.search(r"SimtConfigILi(\d+)ELi(\d+)ELb[01]ELb[01]ELi\d+ELi(\d)ELi\d+ELb([01])E", ln)
+        m = re.search(r"SimtConfigILi(\d+)ELi(\d+)ELb[01]ELb[01]ELi\d+ELi(\d)ELi(\d+)ELb([01])E", ln)
         if not m or "Compiling entry" not in ln:
             continue
         regs = next(int(re.search(r"Used (\d+) registers", x).group(1))
                     for x in report[i + 1:] if "Used" in x)
         math_warps = int(m.group(1)) * int(m.group(2))
-        lean = m.group(3) == "0" and m.group(4) == "0"   # TMA producer without A transpose
+        tma, tn, a_trans = m.group(3) == "0", int(m.group(4)), m.group(5) == "1"
         threads = 32 * math_warps + 128
-        prod_regs = 24 if lean else 40
-        math_regs = (240 if lean else 232) if math_warps == 8 else (232 if lean else 216)
+        min_ctas = 1 if math_warps == 8 else 2
+        launch = (65536 // (threads * min_ctas)) & ~7
+        prod_regs = 24 if (tma and not a_trans) else (trans_regs if a_trans else 40)
+        math_regs = min(240, ((threads * launch - 128 * prod_regs) // (32 * math_warps)) & ~7)
         assert regs * threads >= 128 * prod_regs + 32 * math_warps * math_regs, (ln, regs)
+        # room for the 8 x TN accumulators, fragments and addresses
+        assert math_regs >= (216 if tn == 16 else 168), (ln, math_regs)
         checked += 1
     assert checked >= 8
