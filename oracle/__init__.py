@@ -6,7 +6,9 @@ GPU library never imports or calls it, and it shares no code with the GPU path.
 
 The arithmetic lives in ``oracle_sgemm.c`` (plain C, FP64 accumulation in
 ascending k; its header comment gives the definition it follows and the pages
-it cites).  This module is only ctypes marshalling of numpy arrays.
+it cites).  This module is only ctypes marshalling of numpy arrays.  The library also
+holds the transpose (``oracle_transpose_f32``) that the GPU transpose kernel
+is checked against.
 
 Matrices are 2-D numpy float32 arrays in their *stored* (row-major) layout:
 A is M x K (op N) or K x M (op T); B is K x N (op N) or N x K (op T); C is M x N.
@@ -76,6 +78,8 @@ class Oracle:
             ctypes.c_int, ctypes.c_int, _I64, _I64, _I64,
             ctypes.c_float, _F32P, _I64, _F32P, _I64,
             ctypes.c_float, _F32P, _I64, _F64P, _I64, ctypes.c_int]
+        lib.oracle_transpose_f32.restype = ctypes.c_int
+        lib.oracle_transpose_f32.argtypes = [_I64, _I64, _F32P, _I64, _F32P, _I64]
         lib.oracle_sgemm_entries_f64.restype = ctypes.c_int
         lib.oracle_sgemm_entries_f64.argtypes = [
             ctypes.c_int, ctypes.c_int, _I64, _I64, _I64,
@@ -149,6 +153,22 @@ class Oracle:
                 raise ValueError(f"oracle_sgemm_f64 rejected product {b} (status {st})")
         return R
 
+    def transpose_f32(self, X, out=None):
+        """X^T of a 2-D float32 array (cols x rows, float32).  With `out` (a
+        float32 array of that shape, possibly a view with a longer row) the
+        result is written there and only there."""
+        rows, cols = X.shape
+        px, ldx = _mat(X, "X")
+        if out is None:
+            out = np.empty((cols, rows), dtype=np.float32)
+        if out.shape != (cols, rows):
+            raise ValueError("out has the wrong shape")
+        po, ldo = _mat(out, "out")
+        st = self.lib.oracle_transpose_f32(rows, cols, px, ldx, po, ldo)
+        if st != 0:
+            raise ValueError(f"oracle_transpose_f32 rejected its arguments (status {st})")
+        return out
+
     def sgemm_entries_f64(self, transA, transB, alpha, A, B, beta, C, I, J):
         """float64 values of the (I[e], J[e]) outputs of the same product."""
         ta, tb = _op(transA), _op(transB)
@@ -193,3 +213,7 @@ def sgemm_entries_f64(*args, **kw):
 
 def sgemm_strided_batched_f64(*args, **kw):
     return default().sgemm_strided_batched_f64(*args, **kw)
+
+
+def transpose_f32(*args, **kw):
+    return default().transpose_f32(*args, **kw)

@@ -231,3 +231,25 @@ int oracle_sgemm_entries_f64(int transA, int transB, int64_t M, int64_t N, int64
   }
   return ORACLE_OK;
 }
+
+/*
+ * Matrix transpose, the workload of "现代 CUDA 工具箱实战：从朴素代码到硬件极限的优化之路"
+ * (hankli.space; its naive kernel in "代码实现 / Baseline" reads element
+ * (y, x) of the N x N input and writes it to (x, y) of the output):
+ *
+ *   out[c * ld_out + r] = in[r * ld_in + c]     for r < rows, c < cols,
+ *
+ * widened from a square N x N matrix to a rows x cols input with leading
+ * dimensions (out is cols x rows).  A copy of each value: no arithmetic, so
+ * the result is bit-exact by construction.  Elements of out outside the
+ * cols x rows block are not touched.
+ */
+int oracle_transpose_f32(int64_t rows, int64_t cols, const float *in, int64_t ld_in,
+                         float *out, int64_t ld_out) {
+  if (rows < 0 || cols < 0) return ORACLE_EINVAL;
+  if (rows == 0 || cols == 0) return ORACLE_OK;
+  if (in == NULL || out == NULL || ld_in < cols || ld_out < rows) return ORACLE_EINVAL;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) out[c * ld_out + r] = in[r * ld_in + c];
+  return ORACLE_OK;
+}

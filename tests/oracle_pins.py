@@ -328,6 +328,54 @@ def pin_threads_invariant(orc):
     assert np.array_equal(r1, r7)
 
 
+# ------------------------------------------------------------ transpose
+TRANSPOSE_GOLDEN_DIR = os.path.join(GOLDEN_DIR, "transpose")
+
+
+def _bits(x):
+    return np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+
+
+def pin_transpose_golden(orc):
+    files = sorted(glob.glob(os.path.join(TRANSPOSE_GOLDEN_DIR, "*.txt")))
+    assert len(files) >= 2
+    for f in files:
+        g = load_golden(f)
+        X = g["in"].astype(np.float32)
+        out = orc.transpose_f32(X)
+        assert np.array_equal(_bits(out), _bits(g["expect"])), os.path.basename(f)
+
+
+def pin_transpose_numpy_and_involution(orc):
+    """Bit-exact equal to numpy's own transpose (NaN payloads, signed zeros,
+    infinities and subnormals included) on ragged shapes, and transposing
+    twice gives the input back."""
+    rng = _rng(41)
+    for rows, cols in [(1, 1), (1, 7), (7, 1), (5, 3), (33, 17), (64, 130)]:
+        X = rng.standard_normal((rows, cols)).astype(np.float32)
+        flat = X.reshape(-1)
+        flat[:: 5] = np.float32(-0.0)
+        flat[1:: 7] = np.float32(np.inf)
+        flat[2:: 11] = np.float32(1e-42)            # subnormal
+        bits = flat.view(np.uint32)
+        bits[3:: 13] = 0x7FC0ABCD                   # NaN with a payload
+        T = orc.transpose_f32(X)
+        assert np.array_equal(_bits(T), _bits(X.T)), (rows, cols)
+        assert np.array_equal(_bits(orc.transpose_f32(T)), _bits(X)), (rows, cols)
+
+
+def pin_transpose_leading_dimensions(orc):
+    """Padded input rows are not read and padded output rows not written."""
+    rng = _rng(42)
+    rows, cols = 9, 6
+    big_in = np.full((rows, cols + 3), np.nan, np.float32)
+    big_in[:, :cols] = _stored(rng, (rows, cols), "dyadic")
+    big_out = np.full((cols, rows + 5), 7.0, np.float32)
+    orc.transpose_f32(big_in[:, :cols], out=big_out[:, :rows])
+    assert np.array_equal(big_out[:, :rows], big_in[:, :cols].T)
+    assert np.all(big_out[:, rows:] == 7.0)
+
+
 # ------------------------------------------------------------ strided batch
 def _strided_view(flat, batch, rows, cols, ld, stride):
     """numpy's own view of the strided-batch layout: element (b, r, c) at
@@ -402,4 +450,5 @@ ALL_PINS = [
     pin_integer_vs_numpy, pin_numpy_float64, pin_transpose_identities, pin_scaling,
     pin_degenerate, pin_padded_ld, pin_entries_match_full, pin_threads_invariant,
     pin_batched_closed_form, pin_batched_broadcast_and_interleaved, pin_batched_gaps_unread,
+    pin_transpose_golden, pin_transpose_numpy_and_involution, pin_transpose_leading_dimensions,
 ]

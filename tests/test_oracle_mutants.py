@@ -67,6 +67,15 @@ MUTANTS = [
     ("entries_drop_beta",
      "if (beta != 0.0f) r += (double)beta * (double)C[i * ldc + j];",
      "(void)ldc;"),
+    ("transpose_copies_instead",
+     "out[c * ld_out + r] = in[r * ld_in + c];",
+     "out[r * ld_out + c] = in[r * ld_in + c];"),
+    ("transpose_uses_ld_in_for_out",
+     "out[c * ld_out + r] = in[r * ld_in + c];",
+     "out[c * ld_in + r] = in[r * ld_in + c];"),
+    ("transpose_last_column_dropped",
+     "for (int64_t c = 0; c < cols; ++c) out[c * ld_out + r]",
+     "for (int64_t c = 0; c + 1 < cols; ++c) out[c * ld_out + r]"),
     ("row_block_short_by_one",
      "j->row_end = j->row_begin + per < M ? j->row_begin + per : M;",
      "j->row_end = j->row_begin + per - 1 < M ? j->row_begin + per - 1 : M;"),
