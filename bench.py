@@ -16,8 +16,11 @@ timed region), ``roofline`` (the dominant kernel's FLOP rate against the FP32
 CUDA-core peak 2 * 128 * SMs * f_SM, at the 2070 MHz maximum SM clock),
 ``cpu_baseline`` (the CPU oracle timed on a bounded sample of the same product
 on this host's cores), ``clocks`` (nvidia-smi samples taken during the timed
-region), ``vs_size`` (TFLOP/s of the 512..4096 square sweep) and ``configs``
-(TFLOP/s of the other workload families).
+region), ``vs_size`` (TFLOP/s of the 512..4096 square sweep), ``configs``
+(TFLOP/s of the other workload families), ``tensor_core_3xtf32`` (the
+tensor-core kernel on the headline product), ``transpose`` (the transpose
+kernel's HBM bandwidth at 4096 x 4096 and 16384 x 16384) and
+``library_context`` (cuBLAS FP32 on the headline product, for context).
 
 ``--impl reference`` times the CPU oracle instead (the only other use of the
 oracle here), on a bounded sample per step, and prints the same JSON line with
@@ -44,6 +47,7 @@ RECIPE_SM_MAX_MHZ = 2070.0       # maximum SM clock of this GB300 pool
 L2_BYTES = 129e6
 NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25   # dense tensor rates, GB300 nominal
 FALLBACK_BF16_TFLOPS = 1900.0         # used only if no measured peak file
+FALLBACK_HBM_GBS = 6800.0
 
 
 # ----------------------------------------------------------------- helpers
@@ -53,6 +57,7 @@ KERNEL_SOURCES = {
     "simt": ["ptx.cuh", "internal.h", "simt_gemm.cuh", "simt_instances.cuh", "simt_tma_an.cu",
              "simt_tma_at.cu", "simt_cpasync_an.cu", "simt_cpasync_at.cu", "sk_fixup.cu"],
     "tc_3xtf32": ["ptx.cuh", "tc_3xtf32.cuh", "tc_3xtf32.cu"],
+    "transpose": ["transpose.cu"],
 }
 
 
@@ -68,7 +73,7 @@ def kernel_source_hash(family: str) -> str:
 def stored_traffic(kernel_tag: str):
     """(bytes per launch, note) from profiles/*.md lines
     'traffic <kernel_tag> <bytes> <source hash>' if the hash still matches."""
-    family = "tc_3xtf32" if kernel_tag.startswith("tc_3xtf32") else "simt"
+    family = next((f for f in ("tc_3xtf32", "transpose") if kernel_tag.startswith(f)), "simt")
     want = kernel_source_hash(family)
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         for ln in open(path, encoding="utf-8"):
@@ -216,6 +221,30 @@ def time_gemm(sg, torch, case, A, B, C, steps, warmup, algo, stream, record_laun
     return region, per_launch, launches
 
 
+def time_transpose(sg, torch, rows, cols, reps, stream, flush=None):
+    """Mean per-launch ms of sgemm_transpose on a rows x cols matrix (CUDA
+    events around each launch on `stream`; `flush`, a buffer larger than L2,
+    is rewritten between launches, outside the events)."""
+    X = torch.randn(rows, cols, device=stream.device)
+    Y = torch.empty(cols, rows, device=stream.device)
+    for _ in range(3):
+        sg.transpose(X, Y, stream=stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            if flush is not None:
+                flush.fill_(1.0)
+            a.record(stream)
+            sg.transpose(X, Y, stream=stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    ok = bool(torch.equal(Y, X.t()))
+    ms = sum(a.elapsed_time(b) for a, b in ev) / reps
+    del X, Y
+    return ms, ok
+
+
 def tflops(flops, ms):
     return flops / (ms * 1e-3) / 1e12
 
@@ -334,6 +363,50 @@ def run_ours(args, dist):
         except sg.SgemmError as e:
             tensor = {"unavailable": str(e)}
 
+    # ---- the transpose kernel (the transpose page's 4096 x 4096 case, L2
+    # flushed between launches, and a 1 GiB case larger than L2)
+    transpose = None
+    if not args.no_transpose:
+        hbm = float(peaks.get("hbm_gbs") or FALLBACK_HBM_GBS)
+        flush = torch.empty(64 * 1024 * 1024, device=dev)    # 256 MiB > L2
+        transpose = {}
+        for rows, cols, fl in ((4096, 4096, flush), (16384, 16384, None)):
+            ms, ok = time_transpose(sg, torch, rows, cols, 20, stream, fl)
+            gbs = 8.0 * rows * cols / (ms * 1e-3) / 1e9
+            transpose[f"{rows}x{cols}"] = {
+                "ms": round(ms, 5), "same_as_torch_t": ok,
+                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
+                             "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                             "traffic": stored_traffic(f"transpose_{rows}x{cols}")[0],
+                             "algorithmic_bytes_per_launch": 8 * rows * cols,
+                             "peak_basis": "measured copy bandwidth" if peaks.get("hbm_gbs")
+                                           else "fallback",
+                             "l2": "flushed (256 MiB write) between launches" if fl is not None
+                                   else "2 GiB per launch, larger than L2"}}
+        del flush
+
+    # ---- library context: cuBLAS FP32 (TF32 off) on the headline product
+    library_context = None
+    if not args.no_library_context:
+        prev = torch.backends.cuda.matmul.allow_tf32
+        torch.backends.cuda.matmul.allow_tf32 = False
+        opA = A.t() if case.transA else A
+        opB = B.t() if case.transB else B
+        out = torch.empty(case.M, case.N, device=dev)
+        for _ in range(3):
+            torch.mm(opA, opB, out=out)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(20):
+            torch.mm(opA, opB, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        torch.backends.cuda.matmul.allow_tf32 = prev
+        library_context = {"cublas_fp32_tflops": round(tflops(flops, e0.elapsed_time(e1) / 20), 3),
+                           "what": "torch.mm FP32, TF32 off (cuBLAS), same product; context only"}
+        del out
+
     # ---- TFLOP/s vs size and the other workload families (rank 0 context)
     vs_size, configs = {}, {}
     if not args.no_sweep:
@@ -366,7 +439,8 @@ def run_ours(args, dist):
                    "parallelism": "replicas" if dist.world > 1 else "single GPU"},
         "pct_of_fp32_peak": round(100 * achieved / peak, 2),
         "e2e": e2e, "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
-        "tensor_core_3xtf32": tensor,
+        "tensor_core_3xtf32": tensor, "transpose": transpose,
+        "library_context": library_context,
         "vs_size": vs_size, "configs": configs,
         "device": {"name": props.name, "sms": sms, "cc": f"{props.major}.{props.minor}"},
     }
@@ -462,6 +536,10 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-tensor", action="store_true",
                     help="skip the extra timing of the 3xTF32 tensor-core kernel")
+    ap.add_argument("--no-transpose", action="store_true",
+                    help="skip the extra timing of the transpose kernel")
+    ap.add_argument("--no-library-context", action="store_true",
+                    help="skip the cuBLAS FP32 context number")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -55,6 +55,8 @@ def load_library():
                                           ctypes.c_float, _VP, _I64, _I64, _VP, _I64, _I64,
                                           ctypes.c_float, _VP, _I64, _I64, _I64, _VP]
     lib.sgemm_strided_batched.restype = ctypes.c_int
+    lib.sgemm_transpose.argtypes = [_I64, _I64, _VP, _I64, _VP, _I64, _VP]
+    lib.sgemm_transpose.restype = ctypes.c_int
     lib.sgemm_noalloc.argtypes = gemm_args
     lib.sgemm_noalloc.restype = ctypes.c_int
     lib.sgemm_select_algo.argtypes = [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64, _VP, _I64,
@@ -114,6 +116,12 @@ def sgemm_strided_batched(transA, transB, M, N, K, alpha, A, lda, strideA, B, ld
         strideC, batch, stream), "sgemm_strided_batched")
 
 
+def sgemm_transpose(rows, cols, inp, ld_in, out, ld_out, stream=None):
+    """out (cols x rows) = in (rows x cols) transposed; pointers as ints."""
+    _check(load_library().sgemm_transpose(rows, cols, inp, ld_in, out, ld_out, stream),
+           "sgemm_transpose")
+
+
 def sgemm_noalloc(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
     """As sgemm, for callers that may not let the library allocate device
     memory: the scratch is a fixed array loaded with the library."""
@@ -170,6 +178,8 @@ def _batched(t, name):
         raise ValueError(f"{name} must have unit column stride")
     ld = t.stride(1) if (rows > 1 or t.stride(1) >= cols) else cols
     return t.data_ptr(), b, rows, cols, max(ld, 1), t.stride(0) if b > 1 else 0
+
+
 def _matrix(t, name):
     """(pointer, rows, cols, ld) of a 2-D float32 CUDA tensor with unit column stride."""
     import torch
@@ -184,6 +194,23 @@ def _matrix(t, name):
     if ld < cols:
         raise ValueError(f"{name} has overlapping rows")
     return t.data_ptr(), rows, cols, max(ld, 1)
+
+
+def transpose(X, out=None, stream=None):
+    """X^T of a 2-D float32 CUDA tensor (unit column stride, any row stride)
+    through sgemm_transpose; `out` (cols x rows, unit column stride) is
+    allocated when not given."""
+    import torch
+    px, rows, cols, ldx = _matrix(X, "X")
+    if out is None:
+        out = torch.empty((cols, rows), dtype=torch.float32, device=X.device)
+    po, orow, ocol, ldo = _matrix(out, "out")
+    if (orow, ocol) != (cols, rows):
+        raise ValueError(f"out must be {cols} x {rows}")
+    s = stream if stream is not None else torch.cuda.current_stream(X.device)
+    with torch.cuda.device(X.device):
+        sgemm_transpose(rows, cols, px, ldx, po, ldo, s.cuda_stream)
+    return out
 
 
 def gemm_strided_batched(A, B, C=None, alpha=1.0, beta=0.0, transA=False, transB=False,

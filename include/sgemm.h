@@ -155,6 +155,22 @@ SGEMM_API sgemm_status_t sgemm_strided_batched(int transA, int transB, int64_t M
                                                int64_t strideC, int64_t batch, void *stream);
 
 /*
+ * Matrix transpose: out[c * ld_out + r] = in[r * ld_in + c] for r < rows,
+ * c < cols -- the workload of "现代 CUDA 工具箱实战：从朴素代码到硬件极限的优化之路"
+ * (hankli.space, widened from N x N to rows x cols with leading dimensions).
+ * in is rows x cols (ld_in >= cols), out is cols x rows (ld_out >= rows), both
+ * row-major device memory owned by the caller; elements of out outside the
+ * cols x rows block are not written.  Values are copied bit for bit.
+ * Errors: negative sizes or short leading dimensions -> INVALID_VALUE; in and
+ * out overlapping (including in place) -> ALIASING; rows == 0 or cols == 0 do
+ * nothing.  One launch, queued on `stream`; memory-bound (2 * rows * cols * 4
+ * bytes), 16-byte vector accesses when both bases and leading dimensions are
+ * 16-byte aligned.
+ */
+SGEMM_API sgemm_status_t sgemm_transpose(int64_t rows, int64_t cols, const float *in,
+                                         int64_t ld_in, float *out, int64_t ld_out, void *stream);
+
+/*
  * The family SGEMM_ALGO_AUTO would run for these arguments, or -1 if the
  * arguments are invalid.  Host only: queues nothing and touches no device
  * memory (it reads the device's SM count once).
