@@ -343,6 +343,117 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   return SGEMM_SUCCESS;
 }
 
+// Products whose op(A) is k-contiguous (A stored M x K) or whose op(B) is
+// k-contiguous (B stored N x K) can instead have that operand transposed once
+// into library scratch by the transpose kernel, after which the product runs
+// with A m-contiguous and B n-contiguous -- the layout whose tiles need no
+// shared-memory rewrite and take the 128 x 256 tile.  The math is the same
+// as the in-kernel transpose's (same shared-memory tiles, same k order), so
+// the result is bit-identical; the cost is 8 bytes of HBM traffic per
+// transposed element, small against 2 * M * N * K FLOP once the other
+// dimension is large.  Measured on GB300 at 4096^3 (TFLOP/s, in-kernel ->
+// transposed ahead): NN 63.9 -> 66.8, NT 54.0 -> 64.2, TT 58.2 -> 66.9
+// (TN 67.6 needs nothing).
+#ifndef SG_PRETRANSPOSE
+#define SG_PRETRANSPOSE 1
+#endif
+constexpr int64_t kPretransposeMinOther = 1024;        // the other dimension
+constexpr int64_t kPretransposeMinWork = int64_t(1) << 30;   // M * N * K
+constexpr size_t kPretransposeMaxBytes = size_t(2) << 30;    // 2 GiB of scratch
+
+struct Pretranspose {
+  bool a, b;
+};
+
+Pretranspose pretranspose_plan(const Args &a, int sm_count) {
+  Pretranspose t{false, false};
+  if (!SG_PRETRANSPOSE || !tma_eligible(a)) return t;
+  const double work = static_cast<double>(a.M) * static_cast<double>(a.N) * static_cast<double>(a.K);
+  if (work < static_cast<double>(kPretransposeMinWork)) return t;
+  // only where the transposed product fills the GPU with 128 x 256 tiles:
+  // below that both layouts run 128 x 128 tiles and the extra launch loses
+  // (measured at 2048^3 NN: 57.4 in-kernel vs 56.2 TFLOP/s transposed ahead)
+  if (cdiv(a.M, 128) * cdiv(a.N, 256) < sm_count) return t;
+  t.a = a.ta == 0 && a.N >= kPretransposeMinOther;
+  t.b = a.tb == 1 && a.M >= kPretransposeMinOther;
+  return t;
+}
+
+int64_t round4(int64_t x) { return (x + 3) & ~int64_t(3); }
+
+// Scratch of at least `bytes` (grown in 64 MiB steps), or null.
+float *pretranspose_scratch(DeviceState &d, size_t bytes) {
+  if (d.tr_failed || bytes > kPretransposeMaxBytes) return nullptr;
+  if (!d.tr_event && cudaEventCreateWithFlags(&d.tr_event, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    d.tr_failed = true;
+    return nullptr;
+  }
+  if (bytes > d.tr_bytes) {
+    const size_t step = size_t(64) << 20;
+    const size_t want = (bytes + step - 1) / step * step;
+    if (d.tr) {
+      // cudaFree waits for work still using the old buffer
+      cudaFree(d.tr);
+      d.tr = nullptr;
+      d.tr_bytes = 0;
+      d.tr_used = false;
+    }
+    if (cudaMalloc(&d.tr, want) != cudaSuccess) {
+      cudaGetLastError();
+      d.tr = nullptr;
+      return nullptr;   // not fatal: this product takes the in-kernel transpose
+    }
+    d.tr_bytes = want;
+  }
+  return d.tr;
+}
+
+// Runs the product with the planned operands transposed into scratch.
+// Returns SGEMM_ERR_UNSUPPORTED (and queues nothing) when no scratch can be
+// had, so that the caller runs the product as it is.
+sgemm_status_t run_pretransposed(const Args &a, DeviceState &d, cudaStream_t s, Pretranspose t) {
+  const int64_t lda2 = round4(a.M), ldb2 = round4(a.N);
+  const size_t a_elems = t.a ? static_cast<size_t>(a.K) * lda2 : 0;
+  const size_t a_bytes = (a_elems * sizeof(float) + 255) & ~size_t(255);
+  const size_t bytes = a_bytes + (t.b ? static_cast<size_t>(a.K) * ldb2 * sizeof(float) : 0);
+  std::lock_guard<std::mutex> lock(d.tr_mu);
+  float *scratch = pretranspose_scratch(d, bytes);
+  if (!scratch) return SGEMM_ERR_UNSUPPORTED;
+  if (d.tr_used && d.tr_last_stream != s) {
+    // a call on another stream may still be reading the scratch
+    if (cudaStreamWaitEvent(s, d.tr_event, 0) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  }
+  Args b = a;
+  int launches = 0;
+  if (t.a) {   // A is M x K (lda): A^T is K x M (lda2)
+    if (launch_transpose(a.A, a.lda, scratch, lda2, static_cast<int>(a.M), static_cast<int>(a.K),
+                         d.sm_count, d.status, s) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+    b.A = scratch;
+    b.ta = 1;
+    b.lda = lda2;
+    ++launches;
+  }
+  if (t.b) {   // B is N x K (ldb): B^T is K x N (ldb2)
+    float *bt = reinterpret_cast<float *>(reinterpret_cast<char *>(scratch) + a_bytes);
+    if (launch_transpose(a.B, a.ldb, bt, ldb2, static_cast<int>(a.N), static_cast<int>(a.K),
+                         d.sm_count, d.status, s) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+    b.B = bt;
+    b.tb = 0;
+    b.ldb = ldb2;
+    ++launches;
+  }
+  const sgemm_status_t st = run_simt(b, d, kTma, s);
+  if (st != SGEMM_SUCCESS) return st;
+  t_last_launches += launches;
+  if (cudaEventRecord(d.tr_event, s) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  d.tr_last_stream = s;
+  d.tr_used = true;
+  return SGEMM_SUCCESS;
+}
+
 // 3xTF32 on the tensor cores: 128 x 128 tiles, TMA loads (needs TMA-eligible
 // operands), one persistent CTA per SM.
 sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream) {
@@ -424,9 +535,15 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
 
   if (algo == SGEMM_ALGO_AUTO) algo = auto_algo(a);
   switch (algo) {
-    case SGEMM_ALGO_SIMT_TMA:
+    case SGEMM_ALGO_SIMT_TMA: {
       if (!tma_eligible(a)) return SGEMM_ERR_UNSUPPORTED;
+      const Pretranspose t = pretranspose_plan(a, d->sm_count);
+      if (t.a || t.b) {
+        const sgemm_status_t st = run_pretransposed(a, *d, s, t);
+        if (st != SGEMM_ERR_UNSUPPORTED) return st;
+      }
       return run_simt(a, *d, kTma, s);
+    }
     case SGEMM_ALGO_SIMT_CPASYNC:
       return run_simt(a, *d, kCpAsync, s);
     case SGEMM_ALGO_NAIVE:

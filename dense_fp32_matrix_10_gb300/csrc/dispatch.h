@@ -35,6 +35,16 @@ struct DeviceState {
   cudaEvent_t ws_event = nullptr;
   cudaStream_t ws_last_stream = nullptr;
   bool ws_used = false;
+  // Scratch for operands transposed ahead of a product (see run_pretransposed):
+  // grown on demand up to kPretransposeMaxBytes, kept until exit; calls on
+  // different streams that use it are ordered by tr_event.
+  std::mutex tr_mu;
+  float *tr = nullptr;
+  size_t tr_bytes = 0;
+  bool tr_failed = false;
+  cudaEvent_t tr_event = nullptr;
+  cudaStream_t tr_last_stream = nullptr;
+  bool tr_used = false;
   std::once_flag kinfo_once[2][2][2][kNumSimtTiles];
   cudaError_t kinfo_err[2][2][2][kNumSimtTiles] = {};
   SimtKernelInfo kinfo[2][2][2][kNumSimtTiles] = {};

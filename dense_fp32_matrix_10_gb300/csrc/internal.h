@@ -69,6 +69,10 @@ struct PlainParams {
 cudaError_t launch_naive(const PlainParams &p, cudaStream_t s);
 cudaError_t launch_smem_tiled(const PlainParams &p, cudaStream_t s);
 cudaError_t launch_scale_c(float *C, int64_t ldc, int M, int N, float beta, cudaStream_t s);
+// out (cols x rows, ld_out) = in (rows x cols, ld_in) transposed (transpose.cu);
+// `status` is the device status word the bounded waits report to.
+cudaError_t launch_transpose(const float *in, int64_t ld_in, float *out, int64_t ld_out, int rows,
+                             int cols, int sm_count, int *status, cudaStream_t s);
 cudaError_t launch_scale_c_batched(float *C, int64_t ldc, int64_t strideC, int M, int N,
                                    int64_t batch, float beta, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint64_t budget_ns, int *status, cudaStream_t s);

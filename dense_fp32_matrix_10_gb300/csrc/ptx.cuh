@@ -126,6 +126,47 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *desc, uint
       : "memory");
 }
 
+// 2-D tiled bulk tensor store shared -> global (this thread's bulk group).
+// Box elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void *desc, uint32_t src, int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(desc)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Close this thread's current bulk group.
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_group_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Named barrier over `count` threads that also ANDs a predicate across them:
+// every participant gets true only if all passed true.
+__device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
+
 // ---------------------------------------------------------------- cp.async
 // 4-byte asynchronous copy global -> shared; src_bytes = 0 writes a zero and
 // reads nothing (the source address must still be a valid generic address).

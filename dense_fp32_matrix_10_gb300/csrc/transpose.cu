@@ -12,8 +12,8 @@
 //   * each load instruction reads 4 input rows x 128 contiguous bytes (whole
 //     128-byte lines), and
 //   * each store instruction writes 8 output rows x 64 contiguous bytes (whole
-//     32-byte sectors; the eight warps of a CTA, stacked down the input,
-//     complete 512 contiguous bytes of every output row they touch).
+//     32-byte sectors; a CTA's 64 x 64 tile completes 256 contiguous bytes of
+//     each of its 64 output rows).
 // Loads and stores use the streaming cache hint: nothing is read twice.
 //
 // Edges: a thread whose 4 x 4 block is not entirely inside the matrix, or any
@@ -22,6 +22,7 @@
 //
 // Roofline: HBM, 2 * rows * cols * 4 bytes per launch.
 #include <cstdint>
+#include <mutex>
 
 #include "dispatch.h"
 #include "internal.h"
@@ -30,55 +31,292 @@
 namespace sg {
 namespace {
 
-constexpr int kWarps = 8;                       // CTA: 8 warps stacked along the rows
-constexpr int kCtaRows = kWarps * 16;           // 16 input rows per warp
-constexpr int kCtaCols = 32;                    // 8 lanes x 4 columns
+// CTA tile: 64 x 64 input elements; its 8 warps are 4 (down) x 2 (across),
+// each warp 16 rows x 32 columns of 4 x 4 thread blocks.
+constexpr int kWarps = 8;
+constexpr int kTile = 64;
 constexpr int kCtasPerSm = 8;                   // 2048 threads per SM
+// Tiles are visited in groups of kGroup tile-rows, column by column inside a
+// group, so the CTAs in flight cover a compact band: long contiguous runs of
+// both the input rows and the output rows (DRAM page locality).
+#ifndef SG_TRANSPOSE_GROUP
+#define SG_TRANSPOSE_GROUP 16
+#endif
+constexpr int kGroup = SG_TRANSPOSE_GROUP;
+// 1: streaming (evict-first) cache hints on the loads and stores.
+#ifndef SG_TRANSPOSE_STREAMING
+#define SG_TRANSPOSE_STREAMING 1
+#endif
+
+__device__ __forceinline__ float4 load4(const float *p) {
+  if (SG_TRANSPOSE_STREAMING) return __ldcs(reinterpret_cast<const float4 *>(p));
+  return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ void store4(float *p, float4 v) {
+  if (SG_TRANSPOSE_STREAMING)
+    __stcs(reinterpret_cast<float4 *>(p), v);
+  else
+    *reinterpret_cast<float4 *>(p) = v;
+}
 
 struct TransposeParams {
   const float *in;
   float *out;
   int64_t ld_in, ld_out;
   int rows, cols;
-  int64_t row_blocks;   // ceil(rows / kCtaRows)
-  int64_t num_blocks;   // row_blocks * ceil(cols / kCtaCols)
-  int vec;              // 16-byte aligned bases and leading dimensions
+  int tiles_r, tiles_c;   // ceil(rows / 64), ceil(cols / 64)
+  int64_t num_tiles;
+  int vec;                // 16-byte aligned bases and leading dimensions
 };
+
+// SG_TRANSPOSE_ILP tiles per loop trip: all their loads are issued before
+// any store, so each thread keeps ILP * 64 bytes of reads in flight.
+#ifndef SG_TRANSPOSE_ILP
+#define SG_TRANSPOSE_ILP 1
+#endif
+constexpr int kIlp = SG_TRANSPOSE_ILP;
+
+// Origin (r, c) of this thread's 4 x 4 block in tile t, or r = -1 past the end.
+__device__ __forceinline__ void block_origin(const TransposeParams &p, int64_t t, int r_in, int c_in,
+                                             int &r, int &c) {
+  r = -1;
+  c = 0;
+  if (t >= p.num_tiles) return;
+  const int64_t per_group = static_cast<int64_t>(kGroup) * p.tiles_c;
+  const int64_t g = t / per_group, i = t - g * per_group;
+  const int64_t first = g * kGroup;
+  const int64_t rows_here = (p.tiles_r - first < kGroup) ? p.tiles_r - first : kGroup;
+  const int64_t tr = first + i % rows_here, tc = i / rows_here;
+  r = static_cast<int>(tr * kTile) + r_in;
+  c = static_cast<int>(tc * kTile) + c_in;
+  if (r >= p.rows || c >= p.cols) r = -1;
+}
+
+__device__ __forceinline__ void copy_block_scalar(const TransposeParams &p, int r, int c) {
+  const int ra = min(4, p.rows - r), cb = min(4, p.cols - c);
+  for (int a = 0; a < ra; ++a)
+    for (int b = 0; b < cb; ++b)
+      p.out[static_cast<int64_t>(c + b) * p.ld_out + r + a] = p.in[static_cast<int64_t>(r + a) * p.ld_in + c + b];
+}
 
 __global__ void __launch_bounds__(kWarps * 32) transpose_kernel(const TransposeParams p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int bi = lane >> 3, bj = lane & 7;   // this thread's 4 x 4 block within the warp's 16 x 32
-  for (int64_t blk = blockIdx.x; blk < p.num_blocks; blk += gridDim.x) {
-    // consecutive CTAs walk down the rows of one 32-column strip, so the
-    // output rows of that strip fill contiguously
-    const int64_t strip = blk / p.row_blocks, rb = blk - strip * p.row_blocks;
-    const int r = static_cast<int>(rb * kCtaRows) + warp * 16 + 4 * bi;
-    const int c = static_cast<int>(strip * kCtaCols) + 4 * bj;
-    if (r >= p.rows || c >= p.cols) continue;
-    if (p.vec && r + 4 <= p.rows && c + 4 <= p.cols) {
-      float4 v[4];
+  const int r_in = (warp >> 1) * 16 + 4 * (lane >> 3);   // thread block origin inside the tile
+  const int c_in = (warp & 1) * 32 + 4 * (lane & 7);
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kIlp;
+  for (int64_t t0 = blockIdx.x; t0 < p.num_tiles; t0 += step) {
+    int r[kIlp], c[kIlp];
+    bool fast = p.vec != 0;
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
-        v[a] = __ldcs(reinterpret_cast<const float4 *>(p.in + static_cast<int64_t>(r + a) * p.ld_in + c));
-      __stcs(reinterpret_cast<float4 *>(p.out + static_cast<int64_t>(c + 0) * p.ld_out + r),
-             make_float4(v[0].x, v[1].x, v[2].x, v[3].x));
-      __stcs(reinterpret_cast<float4 *>(p.out + static_cast<int64_t>(c + 1) * p.ld_out + r),
-             make_float4(v[0].y, v[1].y, v[2].y, v[3].y));
-      __stcs(reinterpret_cast<float4 *>(p.out + static_cast<int64_t>(c + 2) * p.ld_out + r),
-             make_float4(v[0].z, v[1].z, v[2].z, v[3].z));
-      __stcs(reinterpret_cast<float4 *>(p.out + static_cast<int64_t>(c + 3) * p.ld_out + r),
-             make_float4(v[0].w, v[1].w, v[2].w, v[3].w));
+    for (int u = 0; u < kIlp; ++u) {
+      block_origin(p, t0 + static_cast<int64_t>(u) * gridDim.x, r_in, c_in, r[u], c[u]);
+      fast = fast && r[u] >= 0 && r[u] + 4 <= p.rows && c[u] + 4 <= p.cols;
+    }
+    if (fast) {
+      float4 v[kIlp][4];
+#pragma unroll
+      for (int u = 0; u < kIlp; ++u)
+#pragma unroll
+        for (int a = 0; a < 4; ++a) v[u][a] = load4(p.in + static_cast<int64_t>(r[u] + a) * p.ld_in + c[u]);
+#pragma unroll
+      for (int u = 0; u < kIlp; ++u) {
+        float *o = p.out + static_cast<int64_t>(c[u]) * p.ld_out + r[u];
+        store4(o, make_float4(v[u][0].x, v[u][1].x, v[u][2].x, v[u][3].x));
+        store4(o + p.ld_out, make_float4(v[u][0].y, v[u][1].y, v[u][2].y, v[u][3].y));
+        store4(o + 2 * p.ld_out, make_float4(v[u][0].z, v[u][1].z, v[u][2].z, v[u][3].z));
+        store4(o + 3 * p.ld_out, make_float4(v[u][0].w, v[u][1].w, v[u][2].w, v[u][3].w));
+      }
     } else {
-      const int ra = min(4, p.rows - r), cb = min(4, p.cols - c);
-      for (int a = 0; a < ra; ++a)
-        for (int b = 0; b < cb; ++b)
-          p.out[static_cast<int64_t>(c + b) * p.ld_out + r + a] =
-              p.in[static_cast<int64_t>(r + a) * p.ld_in + c + b];
+      for (int u = 0; u < kIlp; ++u)
+        if (r[u] >= 0) copy_block_scalar(p, r[u], c[u]);
     }
   }
 }
 
+// ------------------------------------------------------------ TMA-staged form
+// For 16-byte aligned layouts.  A tile is 128 input rows x 32 input columns.
+// One producer thread loads it with a TMA box (32 x 128, 128-byte swizzle:
+// 16-byte chunk j of row r sits at chunk j ^ (r mod 8)) into a 4-deep ring;
+// four consumer warps read it column-wise -- thread t takes row t, one
+// 16-byte chunk (4 columns) per LDS.128, conflict-free thanks to the swizzle
+// -- and write the 32 x 128 output tile densely (a warp's 32 stores of one
+// output row are consecutive words); one consumer thread then stores it with
+// a TMA box (128 x 32), which also clips the ragged edges.  Shared memory,
+// not registers, holds the bytes in flight: up to 4 input and 2 output tiles
+// (96 KiB) per CTA, two CTAs per SM.
+constexpr int kTmRows = 128, kTmCols = 32;
+constexpr int kTmTileBytes = kTmRows * kTmCols * 4;   // 16 KiB, same for in and out
+constexpr int kTmInStages = 4, kTmOutStages = 2;
+constexpr int kTmConsumers = 128;                     // warps 1..4
+constexpr int kTmThreads = 32 + kTmConsumers;
+constexpr int kTmSmem = (kTmInStages + kTmOutStages) * kTmTileBytes + 1024 /*align*/ + 64 /*barriers*/;
+#ifndef SG_TRANSPOSE_TMA_GROUP
+#define SG_TRANSPOSE_TMA_GROUP 8
+#endif
+
+struct TmaTransposeParams {
+  int rows, cols;
+  int tiles_r, tiles_c;          // ceil(rows / 128), ceil(cols / 32)
+  int64_t num_tiles;
+  uint64_t wait_budget_ns;
+  int *status;
+};
+
+// Input-tile origin (r0, c0) of linear tile t: groups of G 32-column strips,
+// walked down the rows inside a group.
+__device__ __forceinline__ void tma_tile_origin(const TmaTransposeParams &p, int64_t t, int &r0, int &c0) {
+  constexpr int G = SG_TRANSPOSE_TMA_GROUP;
+  const int64_t per_group = static_cast<int64_t>(G) * p.tiles_r;
+  const int64_t g = t / per_group, i = t - g * per_group;
+  const int64_t first = g * G;
+  const int64_t cols_here = (p.tiles_c - first < G) ? p.tiles_c - first : G;
+  const int64_t tc = first + i % cols_here, tr = i / cols_here;
+  r0 = static_cast<int>(tr * kTmRows);
+  c0 = static_cast<int>(tc * kTmCols);
+}
+
+__global__ void __launch_bounds__(kTmThreads) transpose_tma_kernel(const __grid_constant__ CUtensorMap in_map,
+                                                                   const __grid_constant__ CUtensorMap out_map,
+                                                                   const TmaTransposeParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;   // 128-byte swizzle wants 1 KiB
+  const uint32_t in0 = base, out0 = base + kTmInStages * kTmTileBytes;
+  const uint32_t bars = out0 + kTmOutStages * kTmTileBytes;
+  const uint32_t full0 = bars, empty0 = bars + 8 * kTmInStages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTmInStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kTmConsumers / 32);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&in_map);
+    tma_prefetch_desc(&out_map);
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---- producer: one thread issues the tile loads
+    if (lane != 0) return;
+    uint32_t i = 0;
+    for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
+      const uint32_t s = i % kTmInStages, round = i / kTmInStages;
+      if (round > 0 && !wait_parity_bounded(empty0 + 8 * s, (round - 1) & 1, p.wait_budget_ns, p.status))
+        break;   // consumers give up on their own bounded waits
+      int r0, c0;
+      tma_tile_origin(p, t, r0, c0);
+      mbar_arrive_expect_tx(full0 + 8 * s, kTmTileBytes);
+      tma_load_2d(in0 + s * kTmTileBytes, &in_map, full0 + 8 * s, c0, r0);
+    }
+    // do not let the CTA end with a load of ours still landing: wait (bounded)
+    // for the last loads issued in each stage
+    for (uint32_t k = (i > kTmInStages ? i - kTmInStages : 0); k < i; ++k)
+      wait_parity_bounded(full0 + 8 * (k % kTmInStages), (k / kTmInStages) & 1, p.wait_budget_ns, p.status);
+    return;
+  }
+
+  // ---- consumers: thread ct owns input row ct of every tile
+  const int ct = threadIdx.x - 32;
+  uint32_t i = 0;
+  for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
+    const uint32_t s = i % kTmInStages, round = i / kTmInStages, o = i % kTmOutStages;
+    bool ok = wait_parity_bounded(full0 + 8 * s, round & 1, p.wait_budget_ns, p.status);
+    // the output buffer is free once the store issued kTmOutStages tiles ago
+    // has read it (only the issuing thread can wait for its bulk groups)
+    if (ct == 0) bulk_wait_group_read<kTmOutStages - 1>();
+    if (!bar_and(1, kTmConsumers, ok)) break;   // all consumers leave together
+    const uint32_t src = in0 + s * kTmTileBytes + ct * 128;
+    const uint32_t dst = out0 + o * kTmTileBytes + ct * 4;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 v = lds128(src + ((j ^ (ct & 7)) << 4));
+      // output row 4j + q, column ct
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + (4 * j + 0) * 512), "f"(v.x) : "memory");
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + (4 * j + 1) * 512), "f"(v.y) : "memory");
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + (4 * j + 2) * 512), "f"(v.z) : "memory");
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + (4 * j + 3) * 512), "f"(v.w) : "memory");
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    fence_proxy_async_smem();                     // make the tile visible to the TMA store
+    bar_and(1, kTmConsumers, true);
+    if (ct == 0) {
+      int r0, c0;
+      tma_tile_origin(p, t, r0, c0);
+      tma_store_2d(&out_map, out0 + o * kTmTileBytes, r0, c0);   // out: x = input row, y = input col
+      bulk_commit_group();
+    }
+  }
+  if (ct == 0) bulk_wait_group_all();
+}
+
+// Per device: dynamic shared memory of the TMA form set once.
+std::once_flag g_tma_attr_once[kMaxDevices];
+cudaError_t g_tma_attr_err[kMaxDevices];
+
+cudaError_t launch_transpose_tma(const float *in, int64_t ld_in, float *out, int64_t ld_out, int rows,
+                                 int cols, int sm_count, int *status, cudaStream_t s, bool *used) {
+  *used = false;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaGetLastError();
+  std::call_once(g_tma_attr_once[dev], [dev]() {
+    g_tma_attr_err[dev] = cudaFuncSetAttribute(transpose_tma_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kTmSmem);
+    if (g_tma_attr_err[dev] != cudaSuccess) cudaGetLastError();
+  });
+  if (g_tma_attr_err[dev] != cudaSuccess) return cudaSuccess;   // not used: caller takes the other form
+  CUtensorMap in_map, out_map;
+  if (!encode_tmap(&in_map, in, rows, cols, ld_in, kTmCols, kTmRows, true) ||
+      !encode_tmap(&out_map, out, cols, rows, ld_out, kTmRows, kTmCols, false))
+    return cudaSuccess;                                            // likewise
+  TmaTransposeParams p;
+  p.rows = rows;
+  p.cols = cols;
+  p.tiles_r = static_cast<int>(cdiv(rows, kTmRows));
+  p.tiles_c = static_cast<int>(cdiv(cols, kTmCols));
+  p.num_tiles = static_cast<int64_t>(p.tiles_r) * p.tiles_c;
+  p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
+  p.status = status;
+  const int64_t slots = static_cast<int64_t>(sm_count) * 2;
+  const int64_t grid = p.num_tiles < slots ? p.num_tiles : slots;
+  transpose_tma_kernel<<<static_cast<unsigned>(grid), kTmThreads, kTmSmem, s>>>(in_map, out_map, p);
+  *used = true;
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+#ifndef SG_TRANSPOSE_TMA
+#define SG_TRANSPOSE_TMA 1
+#endif
+
+cudaError_t launch_transpose(const float *in, int64_t ld_in, float *out, int64_t ld_out, int rows,
+                             int cols, int sm_count, int *status, cudaStream_t s) {
+  const bool aligned = (reinterpret_cast<uintptr_t>(in) % 16 == 0) &&
+                       (reinterpret_cast<uintptr_t>(out) % 16 == 0) && (ld_in % 4 == 0) &&
+                       (ld_out % 4 == 0);
+  if (SG_TRANSPOSE_TMA && aligned) {
+    bool used = false;
+    const cudaError_t e = launch_transpose_tma(in, ld_in, out, ld_out, rows, cols, sm_count, status, s, &used);
+    if (used || e != cudaSuccess) return e;
+  }
+  TransposeParams p;
+  p.in = in;
+  p.out = out;
+  p.ld_in = ld_in;
+  p.ld_out = ld_out;
+  p.rows = rows;
+  p.cols = cols;
+  p.tiles_r = static_cast<int>(cdiv(rows, kTile));
+  p.tiles_c = static_cast<int>(cdiv(cols, kTile));
+  p.num_tiles = static_cast<int64_t>(p.tiles_r) * p.tiles_c;
+  p.vec = aligned;
+  const int64_t slots = static_cast<int64_t>(sm_count) * kCtasPerSm;
+  const int64_t grid = p.num_tiles < slots ? p.num_tiles : slots;
+  transpose_kernel<<<static_cast<unsigned>(grid), kWarps * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace sg
 
 using namespace sg;
@@ -103,22 +341,9 @@ extern "C" sgemm_status_t sgemm_transpose(int64_t rows, int64_t cols, const floa
   DeviceState *d = device_state(&why);
   if (!d) return why;
 
-  TransposeParams p;
-  p.in = in;
-  p.out = out;
-  p.ld_in = ld_in;
-  p.ld_out = ld_out;
-  p.rows = static_cast<int>(rows);
-  p.cols = static_cast<int>(cols);
-  p.row_blocks = cdiv(rows, kCtaRows);
-  p.num_blocks = p.row_blocks * cdiv(cols, kCtaCols);
-  p.vec = (reinterpret_cast<uintptr_t>(in) % 16 == 0) && (reinterpret_cast<uintptr_t>(out) % 16 == 0) &&
-          (ld_in % 4 == 0) && (ld_out % 4 == 0);
-  const int64_t slots = static_cast<int64_t>(d->sm_count) * kCtasPerSm;
-  const int64_t grid = p.num_blocks < slots ? p.num_blocks : slots;
-  transpose_kernel<<<static_cast<unsigned>(grid), kWarps * 32, 0,
-                     reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  if (launch_transpose(in, ld_in, out, ld_out, static_cast<int>(rows), static_cast<int>(cols),
+                       d->sm_count, d->status, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
   return SGEMM_SUCCESS;
 }

@@ -325,12 +325,65 @@ def test_stream_k_is_deterministic(shape):
 def test_stream_k_uses_two_launches():
     A = torch.randn(2048, 2048, device="cuda")
     B = torch.randn(2048, 2048, device="cuda")
-    sg.gemm(A, B)
+    sg.gemm(A, B, transA=True)                  # TN: no operand transposed ahead
     assert sg.sgemm_last_launch_count() == 2   # main kernel + fixup
     A = torch.randn(128 * 152, 256, device="cuda")
     B = torch.randn(256, 128, device="cuda")
     sg.gemm(A, B)                               # exactly one wave of whole tiles
     assert sg.sgemm_last_launch_count() == 1
+
+
+# --------------------------------------------------------------- operands transposed ahead
+PRE_SHAPES = [(2048, 4864, 256), (2502, 4100, 300), (2048, 2048, 2048)]
+
+
+@pytest.mark.parametrize("op", [(0, 0), (0, 1), (1, 1)], ids=["NN", "NT", "TT"])
+@pytest.mark.parametrize("shape", PRE_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in PRE_SHAPES])
+def test_pretransposed_matches_tn_bit_for_bit(shape, op):
+    """Large NN / NT / TT products (TMA-eligible, at least one 128 x 256 tile
+    per SM) have their k-contiguous operand(s) transposed into scratch first
+    and then run as TN: the result must equal, bit for bit, the TN call on
+    operands transposed by torch (same kernel, same tiles, same k order), with
+    one extra launch per transposed operand (2048^3 stays in-kernel)."""
+    M, N, K = shape
+    ta, tb = op
+    g = torch.Generator().manual_seed(M + N + K + 2 * ta + tb)
+    A = torch.randn((K, M) if ta else (M, K), generator=g).cuda()
+    B = torch.randn((N, K) if tb else (K, N), generator=g).cuda()
+    C0 = torch.randn(M, N, generator=g).cuda()
+    C1 = C0.clone()
+    sg.gemm(A, B, C1, 0.75, 0.5, ta, tb)
+    n1 = sg.sgemm_last_launch_count()
+    At = A if ta else A.t().contiguous()        # K x M
+    Bn = B.t().contiguous() if tb else B        # K x N
+    C2 = C0.clone()
+    sg.gemm(At, Bn, C2, 0.75, 0.5, 1, 0)
+    n2 = sg.sgemm_last_launch_count()
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+    # only TMA-eligible layouts (16-byte rows) of GPU-filling size
+    eligible = (A.stride(0) % 4 == 0 and B.stride(0) % 4 == 0 and M * N * K >= 2 ** 30
+                and -(-M // 128) * -(-N // 256) >= torch.cuda.get_device_properties(0).multi_processor_count)
+    assert n1 == n2 + eligible * ((ta == 0 and N >= 1024) + (tb == 1 and M >= 1024))
+
+
+def test_pretransposed_on_two_streams(orc):
+    """Calls on different streams share the transposed-operand scratch; the
+    library orders them, so every result is right."""
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    g = torch.Generator().manual_seed(6)
+    mats = [(torch.randn(2048, 512, generator=g), torch.randn(512, 4864, generator=g))
+            for _ in range(2)]
+    dev = [(a.cuda(), b.cuda(), torch.empty(2048, 4864, device="cuda")) for a, b in mats]
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for (A, B, C), s in zip(dev, (s1, s2)):
+            with torch.cuda.stream(s):
+                sg.gemm(A, B, C, stream=s)
+            assert sg.sgemm_last_launch_count() >= 2
+    torch.cuda.synchronize()
+    for (a, b), (_, _, C) in zip(mats, dev):
+        assert_close(C.cpu().numpy(), orc.sgemm_f64(0, 0, 1.0, a.numpy(), b.numpy()), 512, "stream")
 
 
 def test_stream_k_on_two_streams(orc):
