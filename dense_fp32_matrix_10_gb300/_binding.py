@@ -265,6 +265,14 @@ def gemm(A, B, C=None, alpha=1.0, beta=0.0, transA=False, transB=False, algo=ALG
     pc, rc, cc, ldc = _matrix(C, "C")
     if (rc, cc) != (M, N):
         raise ValueError(f"C must be {M} x {N}")
+    algo = ALGOS[algo] if isinstance(algo, str) else int(algo)
+    dev = A.device.index
+    if dev is None or dev == torch.cuda.current_device():
+        s = stream if stream is not None else torch.cuda.current_stream()
+        _check(load_library().sgemm_ex(int(bool(transA)), int(bool(transB)), M, N, Ka, float(alpha),
+                                       pa, lda, pb, ldb, float(beta), pc, ldc, s.cuda_stream, algo),
+               "sgemm_ex")
+        return C
     s = stream if stream is not None else torch.cuda.current_stream(A.device)
     with torch.cuda.device(A.device):
         sgemm_ex(int(bool(transA)), int(bool(transB)), M, N, Ka, float(alpha), pa, lda, pb, ldb,
