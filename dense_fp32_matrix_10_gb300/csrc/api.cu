@@ -50,6 +50,7 @@ DeviceState *device_state(sgemm_status_t *why) {
     *why = SGEMM_ERR_UNSUPPORTED;
     return nullptr;
   }
+  cudaGetLastError();   // a stale error of someone else's call is not ours
   return &d;
 }
 
@@ -199,11 +200,18 @@ int pick_simt_tile(const Args &a, int producer, int sm_count) {
   return kTile128x128;
 }
 
+#ifndef SG_SK_REMAINDER
+#define SG_SK_REMAINDER 0
+#endif
 SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws) {
   SkPlan pl{static_cast<int>(tiles), 0, 0, static_cast<int>(tiles < slots ? tiles : slots)};
   if (!have_ws || k_tiles < 2 * kMinSkSegment) return pl;
   if (tiles >= slots && tiles % slots == 0) return pl;
-  const int64_t sk = tiles >= 2 * slots ? slots + tiles % slots : tiles;
+  // SG_SK_REMAINDER 1: split only the tiles beyond whole waves; 0: the last
+  // one to two waves' worth
+  const int64_t sk = tiles < slots ? tiles
+                     : SG_SK_REMAINDER ? tiles % slots
+                     : (tiles >= 2 * slots ? slots + tiles % slots : tiles);
   int64_t grid = slots;
   if (sk * k_tiles < grid * kMinSkSegment) grid = (sk * k_tiles) / kMinSkSegment;
   // the fixup pass handles at most 126 segments per tile (ranges >= k_tiles/120)
@@ -216,6 +224,31 @@ SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws
   return pl;
 }
 
+bool stream_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return cs == cudaStreamCaptureStatusActive;
+}
+
+cudaError_t order_before_use(BufferOrder &o, cudaStream_t s, bool capturing) {
+  if (!o.used) return cudaSuccess;
+  if (capturing) return cudaStreamWaitEvent(s, o.ev, cudaEventWaitExternal);
+  if (o.in_graph || o.last != s) return cudaStreamWaitEvent(s, o.ev, 0);
+  return cudaSuccess;
+}
+
+cudaError_t order_after_use(BufferOrder &o, cudaStream_t s, bool capturing) {
+  const cudaError_t e = capturing ? cudaEventRecordWithFlags(o.ev, s, cudaEventRecordExternal)
+                                  : cudaEventRecord(o.ev, s);
+  o.used = true;
+  o.last = s;
+  o.in_graph = o.in_graph || capturing;
+  return e;
+}
+
 }  // namespace sg
 
 namespace {
@@ -223,14 +256,16 @@ namespace {
 using namespace sg;
 
 // The device's stream-K workspace (2 partial tiles per CTA slot of the largest
-// configuration), allocated on first use; null if that failed.
-float *stream_k_workspace(DeviceState &d, size_t need) {
+// configuration), allocated on first use; null if that failed, or if it does
+// not exist yet and `capturing` (no allocation inside a stream capture).
+float *stream_k_workspace(DeviceState &d, size_t need, bool capturing) {
   if (d.ws_failed) return nullptr;
   if (!d.ws) {
+    if (capturing) return nullptr;
     // largest need: two 128 x 256 partial tiles per SM (one CTA per SM)
     const size_t bytes = static_cast<size_t>(2) * d.sm_count * 128 * 256 * sizeof(float);
     if (cudaMalloc(&d.ws, bytes) != cudaSuccess ||
-        cudaEventCreateWithFlags(&d.ws_event, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventCreateWithFlags(&d.ws_order.ev, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
       if (d.ws) cudaFree(d.ws);
       d.ws = nullptr;
@@ -314,21 +349,22 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   }
 
   const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
+  const bool capturing = stream_capturing(stream);
   std::unique_lock<std::mutex> ws_lock(d.ws_mu);
   SkPlan plan = plan_stream_k(num_tiles, p.k_tiles, slots, !d.ws_failed);
   if (plan.sk_tiles > 0) {
     const size_t need = static_cast<size_t>(2) * plan.grid * ki->bm * ki->bn * sizeof(float);
-    p.workspace = stream_k_workspace(d, need);
+    p.workspace = stream_k_workspace(d, need, capturing);
     if (!p.workspace) plan = plan_stream_k(num_tiles, p.k_tiles, slots, false);
   }
   if (plan.sk_tiles == 0) ws_lock.unlock();
   p.dp_tiles = plan.dp_tiles;
   p.sk_iters = plan.sk_iters;
 
-  if (plan.sk_tiles > 0 && d.ws_used && d.ws_last_stream != stream) {
-    // the previous stream-K call on another stream may still be using the workspace
-    if (cudaStreamWaitEvent(stream, d.ws_event, 0) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-  }
+  // the previous stream-K call (another stream, or a graph) may still be
+  // using the workspace
+  if (plan.sk_tiles > 0 && order_before_use(d.ws_order, stream, capturing) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
   cudaError_t e = simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, plan.grid, stream);
   if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
@@ -336,9 +372,7 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
     if (launch_sk_fixup(p, ki->bm, ki->bn, plan.grid, plan.sk_tiles, stream) != cudaSuccess)
       return SGEMM_ERR_LAUNCH;
     t_last_launches = 2;
-    if (cudaEventRecord(d.ws_event, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-    d.ws_last_stream = stream;
-    d.ws_used = true;
+    if (order_after_use(d.ws_order, stream, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
   }
   return SGEMM_SUCCESS;
 }
@@ -381,10 +415,12 @@ Pretranspose pretranspose_plan(const Args &a, int sm_count) {
 
 int64_t round4(int64_t x) { return (x + 3) & ~int64_t(3); }
 
-// Scratch of at least `bytes` (grown in 64 MiB steps), or null.
-float *pretranspose_scratch(DeviceState &d, size_t bytes) {
+// Scratch of at least `bytes` (grown in 64 MiB steps), or null (also when it
+// would have to be allocated or grown inside a stream capture).
+float *pretranspose_scratch(DeviceState &d, size_t bytes, bool capturing) {
   if (d.tr_failed || bytes > kPretransposeMaxBytes) return nullptr;
-  if (!d.tr_event && cudaEventCreateWithFlags(&d.tr_event, cudaEventDisableTiming) != cudaSuccess) {
+  if (capturing) return bytes <= d.tr_bytes ? d.tr : nullptr;
+  if (!d.tr_order.ev && cudaEventCreateWithFlags(&d.tr_order.ev, cudaEventDisableTiming) != cudaSuccess) {
     cudaGetLastError();
     d.tr_failed = true;
     return nullptr;
@@ -397,7 +433,6 @@ float *pretranspose_scratch(DeviceState &d, size_t bytes) {
       cudaFree(d.tr);
       d.tr = nullptr;
       d.tr_bytes = 0;
-      d.tr_used = false;
     }
     if (cudaMalloc(&d.tr, want) != cudaSuccess) {
       cudaGetLastError();
@@ -417,13 +452,12 @@ sgemm_status_t run_pretransposed(const Args &a, DeviceState &d, cudaStream_t s, 
   const size_t a_elems = t.a ? static_cast<size_t>(a.K) * lda2 : 0;
   const size_t a_bytes = (a_elems * sizeof(float) + 255) & ~size_t(255);
   const size_t bytes = a_bytes + (t.b ? static_cast<size_t>(a.K) * ldb2 * sizeof(float) : 0);
+  const bool capturing = stream_capturing(s);
   std::lock_guard<std::mutex> lock(d.tr_mu);
-  float *scratch = pretranspose_scratch(d, bytes);
+  float *scratch = pretranspose_scratch(d, bytes, capturing);
   if (!scratch) return SGEMM_ERR_UNSUPPORTED;
-  if (d.tr_used && d.tr_last_stream != s) {
-    // a call on another stream may still be reading the scratch
-    if (cudaStreamWaitEvent(s, d.tr_event, 0) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-  }
+  // a call on another stream (or a graph) may still be reading the scratch
+  if (order_before_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
   Args b = a;
   int launches = 0;
   if (t.a) {   // A is M x K (lda): A^T is K x M (lda2)
@@ -448,9 +482,7 @@ sgemm_status_t run_pretransposed(const Args &a, DeviceState &d, cudaStream_t s, 
   const sgemm_status_t st = run_simt(b, d, kTma, s);
   if (st != SGEMM_SUCCESS) return st;
   t_last_launches += launches;
-  if (cudaEventRecord(d.tr_event, s) != cudaSuccess) return SGEMM_ERR_LAUNCH;
-  d.tr_last_stream = s;
-  d.tr_used = true;
+  if (order_after_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
   return SGEMM_SUCCESS;
 }
 

@@ -21,30 +21,47 @@ constexpr uint64_t kDefaultWaitBudgetNs = 2000000000ull;  // 2 s
 extern std::atomic<uint64_t> g_wait_budget_ns;
 extern thread_local int t_last_launches;
 
+// Orders the users of one library-owned device buffer (stream-K workspace,
+// transposed-operand scratch) across streams and captured CUDA graphs: every
+// use waits for the previous use's event and records its own.  Eager uses on
+// the stream that used the buffer last need no wait; uses inside a stream
+// capture wait and record through external event nodes, which take effect
+// each time the graph is launched (a graph launch records the event like
+// cudaEventRecord would); after the first captured use, eager uses always
+// wait, since graph launches do not pass through this library.
+struct BufferOrder {
+  cudaEvent_t ev = nullptr;
+  cudaStream_t last = nullptr;
+  bool used = false;
+  // a use has been captured into a graph at some point: its launches are
+  // invisible to the host-side bookkeeping, so every later use waits
+  bool in_graph = false;
+};
+cudaError_t order_before_use(BufferOrder &o, cudaStream_t s, bool capturing);
+cudaError_t order_after_use(BufferOrder &o, cudaStream_t s, bool capturing);
+// True while `s` is being captured into a CUDA graph.
+bool stream_capturing(cudaStream_t s);
+
 struct DeviceState {
   std::once_flag once;
   cudaError_t err = cudaSuccess;
   int sm_count = 0, cc_major = 0, cc_minor = 0;
   int *status = nullptr;
   // Stream-K workspace: allocated on first use, kept until exit.  Calls that
-  // use it on different streams are ordered by ws_event.
+  // use it on different streams or in graphs are ordered by ws_order.
   std::mutex ws_mu;
   float *ws = nullptr;
   size_t ws_bytes = 0;
   bool ws_failed = false;
-  cudaEvent_t ws_event = nullptr;
-  cudaStream_t ws_last_stream = nullptr;
-  bool ws_used = false;
+  BufferOrder ws_order;
   // Scratch for operands transposed ahead of a product (see run_pretransposed):
   // grown on demand up to kPretransposeMaxBytes, kept until exit; calls on
-  // different streams that use it are ordered by tr_event.
+  // different streams or in graphs that use it are ordered by tr_order.
   std::mutex tr_mu;
   float *tr = nullptr;
   size_t tr_bytes = 0;
   bool tr_failed = false;
-  cudaEvent_t tr_event = nullptr;
-  cudaStream_t tr_last_stream = nullptr;
-  bool tr_used = false;
+  BufferOrder tr_order;
   std::once_flag kinfo_once[2][2][2][kNumSimtTiles];
   cudaError_t kinfo_err[2][2][2][kNumSimtTiles] = {};
   SimtKernelInfo kinfo[2][2][2][kNumSimtTiles] = {};
@@ -78,7 +95,8 @@ int64_t cdiv(int64_t a, int64_t b);
 int norm_op(int t);
 
 // The current device's state (initialised once per device) or null with the
-// reason in *why.
+// reason in *why.  Also clears a pending error left by earlier, unrelated
+// runtime calls, so that the launches that follow report only their own.
 DeviceState *device_state(sgemm_status_t *why);
 const SimtKernelInfo *kernel_info(DeviceState &d, int producer, int ta, int tb, int tile);
 const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb);

@@ -28,14 +28,25 @@
  * library never frees, keeps or reallocates them.  C must not overlap A or B.
  * Device memory of the library's own: sgemm()/sgemm_ex() allocate, once per
  * device and the first time a product is split by stream-K, a workspace of
- * two 128 x 256 FP32 tiles per SM (~40 MB on 152 SMs), kept until exit; calls
- * on different streams that use it are ordered by an event.  sgemm_noalloc()
- * never allocates (see there).
+ * two 128 x 256 FP32 tiles per SM (~40 MB on 152 SMs), and, the first time a
+ * large NN/NT/TT product transposes an operand ahead (see sgemm()), a scratch
+ * buffer for it (grown in 64 MiB steps, at most 2 GiB); both are kept until
+ * exit.  Calls on different streams that use them are ordered by events.
+ * sgemm_noalloc() never allocates (see there).
  *
  * Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
  * default stream).  Every call returns as soon as its work is queued; results
  * are ready once the stream reaches that point.  Argument errors are detected
- * on the host before anything is queued, and then nothing is launched.
+ * on the host before anything is queued, and then nothing is launched.  A
+ * pending error left by earlier, unrelated CUDA runtime calls is cleared
+ * before the call's launches, so it does not fail this call.
+ *
+ * CUDA graphs: sgemm(), sgemm_ex(), sgemm_strided_batched() and
+ * sgemm_transpose() may be captured.  Inside a capture the library allocates
+ * nothing: a product whose stream-K workspace or transpose scratch does not
+ * exist yet (or is too small) runs without it.  Uses of these buffers inside
+ * graphs are ordered against every other use through external event nodes,
+ * so graph launches and eager calls on other streams may be mixed freely.
  *
  * Numerics: FP32 inputs and outputs; each output's K products are accumulated
  * in FP32 (FFMA) by the CUDA-core kernels, or from TF32 splits in FP32 by the
@@ -110,6 +121,11 @@ typedef enum sgemm_algo {
  * C = alpha * op(A) * op(B) + beta * C, kernel chosen automatically.
  * Returns SGEMM_SUCCESS once the work is queued on `stream`, or an error code
  * (see sgemm_status_t) with nothing queued.  Thread-safe.
+ * Large products whose op(A) or op(B) is k-contiguous (A stored M x K, or B
+ * stored N x K) and that fill the GPU with 128 x 256 tiles first copy that
+ * operand transposed into library scratch (one transpose launch each) and
+ * then run with both operands m/n-contiguous; the result is bit-identical to
+ * the in-kernel path.  sgemm_last_launch_count() reports all launches.
  */
 SGEMM_API sgemm_status_t sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
                      float alpha, const float *A, int64_t lda,

@@ -1,0 +1,135 @@
+"""Products captured into CUDA graphs.
+
+The library's stream-K workspace and transpose scratch are shared by every
+call on a device.  Inside a capture the library allocates nothing and orders
+its uses of those buffers through external event nodes, so graph launches
+and eager calls on other streams can be mixed.  These tests replay graphs
+interleaved with eager stream-K / transposing calls on another stream and
+require every result to be bit-identical to the same product run alone (a
+race on the shared buffers would corrupt partial sums), plus a capture made
+before any workspace exists (fresh process).
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+import dense_fp32_matrix_10_gb300 as sg
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_fp32_matrix_10_gb300 import build
+    build.build()
+    torch.cuda.init()
+    yield
+    assert sg.sgemm_last_device_status() == 0
+
+
+def _operands(M, N, K, seed, ta=0, tb=0):
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randn((K, M) if ta else (M, K), generator=g).cuda()
+    B = torch.randn((N, K) if tb else (K, N), generator=g).cuda()
+    return A, B
+
+
+def _alone(A, B, M, N, ta=0, tb=0):
+    C = torch.empty(M, N, device="cuda")
+    sg.gemm(A, B, C, transA=ta, transB=tb)
+    torch.cuda.synchronize()
+    return C.clone()
+
+
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (2048, 4864, 256)],
+                         ids=["stream_k_1024", "pretransposed_2048x4864x256"])
+def test_graph_replays_interleaved_with_eager_calls(shape):
+    M, N, K = shape
+    A1, B1 = _operands(M, N, K, 1)
+    A2, B2 = _operands(M, N, K, 2)
+    ref1, ref2 = _alone(A1, B1, M, N), _alone(A2, B2, M, N)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    C1 = torch.empty(M, N, device="cuda")
+    C2 = torch.empty(M, N, device="cuda")
+    with torch.cuda.stream(s1):
+        sg.gemm(A1, B1, C1, stream=s1)                 # buffers exist before capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s1):
+        for _ in range(3):
+            sg.gemm(A1, B1, C1, stream=s1)
+    for _ in range(5):
+        C1.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        with torch.cuda.stream(s2):
+            for _ in range(2):
+                sg.gemm(A2, B2, C2, stream=s2)         # same shared buffers, other stream
+        torch.cuda.synchronize()
+        assert torch.equal(C1, ref1)
+        assert torch.equal(C2, ref2)
+
+
+def test_batched_and_transpose_capture():
+    s = torch.cuda.Stream()
+    A = torch.randn(16, 256, 64, device="cuda")
+    B = torch.randn(16, 64, 256, device="cuda")
+    X = torch.randn(3000, 1000, device="cuda")
+    refC = sg.gemm_strided_batched(A, B)
+    refT = sg.transpose(X)
+    torch.cuda.synchronize()
+    C = torch.empty_like(refC)
+    T = torch.empty_like(refT)
+    with torch.cuda.stream(s):
+        sg.gemm_strided_batched(A, B, C, stream=s)
+        sg.transpose(X, T, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        sg.gemm_strided_batched(A, B, C, stream=s)
+        sg.transpose(X, T, stream=s)
+    C.zero_()
+    T.zero_()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(C, refC) and torch.equal(T, refT)
+
+
+CHILD = r"""
+import sys, torch
+sys.path.insert(0, {root!r})
+import dense_fp32_matrix_10_gb300 as sg
+M = N = K = 1024
+g0 = torch.Generator().manual_seed(3)
+A = torch.randn(M, K, generator=g0).cuda(); B = torch.randn(K, N, generator=g0).cuda()
+C = torch.empty(M, N, device="cuda")
+s = torch.cuda.Stream()
+torch.cuda.synchronize()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):          # first call of the process: no workspace yet
+    sg.gemm(A, B, C, stream=s)
+g.replay(); torch.cuda.synchronize()
+inside = C.clone()
+C2 = sg.gemm(A, B)                           # eager afterwards: allocates, splits by stream-K
+torch.cuda.synchronize()
+ref = (A.double() @ B.double())
+for X in (inside, C2):
+    err = ((X.double() - ref).norm() / ref.norm()).item()
+    assert err < 1e-5, err
+assert sg.sgemm_last_device_status() == 0
+print("ok")
+"""
+
+
+def test_capture_before_any_workspace_exists():
+    p = subprocess.run([sys.executable, "-c", CHILD.format(root=ROOT)], capture_output=True,
+                       text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-3000:]
+    assert p.stdout.strip().endswith("ok")
