@@ -286,8 +286,10 @@ struct Batch {
   int64_t count, sa, sb, sc;
 };
 
+// pdl: the product directly follows another kernel of the same call on the
+// stream (an operand transpose) and may be scheduled before it ends.
 sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_t stream,
-                        const Batch &bt = Batch{1, 0, 0, 0}) {
+                        const Batch &bt = Batch{1, 0, 0, 0}, bool pdl = false) {
   const int tile = pick_simt_tile(a, producer, d.sm_count);
   const SimtKernelInfo *ki = kernel_info(d, producer, a.ta, a.tb, tile);
   if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_LAUNCH;
@@ -343,7 +345,7 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
     if (!okA || !okB) {
       // a batch layout the tensor-map encoder refuses is still a valid batch:
       // load it with cp.async instead
-      if (bt.count > 1) return run_simt(a, d, kCpAsync, stream, bt);
+      if (bt.count > 1) return run_simt(a, d, kCpAsync, stream, bt, pdl);
       return SGEMM_ERR_LAUNCH;
     }
   }
@@ -365,7 +367,7 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   // using the workspace
   if (plan.sk_tiles > 0 && order_before_use(d.ws_order, stream, capturing) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
-  cudaError_t e = simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, plan.grid, stream);
+  cudaError_t e = simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, plan.grid, stream, pdl);
   if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
   if (plan.sk_tiles > 0) {
@@ -398,8 +400,18 @@ constexpr size_t kPretransposeMaxBytes = size_t(2) << 30;    // 2 GiB of scratch
 struct Pretranspose {
   bool a, b;
 };
+// The tensor-core product after a transpose is launched the ordinary way:
+// as a programmatic dependent it ran slower (4096^3 NN 140.8 vs 167.8
+// TFLOP/s on GB300), while the CUDA-core kernel gains a little from it.
+#ifndef SG_TC_PDL
+#define SG_TC_PDL 0
+#endif
 
-Pretranspose pretranspose_plan(const Args &a, int sm_count) {
+sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream, bool pdl = false);
+
+// tile_n: the N extent of the tiles the transposed product runs with (256
+// for the CUDA-core kernel's wide tile, 128 for the tensor-core kernel).
+Pretranspose pretranspose_plan(const Args &a, int sm_count, int64_t tile_n) {
   Pretranspose t{false, false};
   if (!SG_PRETRANSPOSE || !tma_eligible(a)) return t;
   const double work = static_cast<double>(a.M) * static_cast<double>(a.N) * static_cast<double>(a.K);
@@ -407,7 +419,7 @@ Pretranspose pretranspose_plan(const Args &a, int sm_count) {
   // only where the transposed product fills the GPU with 128 x 256 tiles:
   // below that both layouts run 128 x 128 tiles and the extra launch loses
   // (measured at 2048^3 NN: 57.4 in-kernel vs 56.2 TFLOP/s transposed ahead)
-  if (cdiv(a.M, 128) * cdiv(a.N, 256) < sm_count) return t;
+  if (cdiv(a.M, 128) * cdiv(a.N, tile_n) < sm_count) return t;
   t.a = a.ta == 0 && a.N >= kPretransposeMinOther;
   t.b = a.tb == 1 && a.M >= kPretransposeMinOther;
   return t;
@@ -447,7 +459,8 @@ float *pretranspose_scratch(DeviceState &d, size_t bytes, bool capturing) {
 // Runs the product with the planned operands transposed into scratch.
 // Returns SGEMM_ERR_UNSUPPORTED (and queues nothing) when no scratch can be
 // had, so that the caller runs the product as it is.
-sgemm_status_t run_pretransposed(const Args &a, DeviceState &d, cudaStream_t s, Pretranspose t) {
+sgemm_status_t run_pretransposed(const Args &a, DeviceState &d, cudaStream_t s, Pretranspose t,
+                                 bool tensor) {
   const int64_t lda2 = round4(a.M), ldb2 = round4(a.N);
   const size_t a_elems = t.a ? static_cast<size_t>(a.K) * lda2 : 0;
   const size_t a_bytes = (a_elems * sizeof(float) + 255) & ~size_t(255);
@@ -479,7 +492,8 @@ sgemm_status_t run_pretransposed(const Args &a, DeviceState &d, cudaStream_t s, 
     b.ldb = ldb2;
     ++launches;
   }
-  const sgemm_status_t st = run_simt(b, d, kTma, s);
+  const sgemm_status_t st = tensor ? run_tc3(b, d, s, /*pdl=*/SG_TC_PDL != 0)
+                                   : run_simt(b, d, kTma, s, Batch{1, 0, 0, 0}, /*pdl=*/true);
   if (st != SGEMM_SUCCESS) return st;
   t_last_launches += launches;
   if (order_after_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
@@ -488,7 +502,7 @@ sgemm_status_t run_pretransposed(const Args &a, DeviceState &d, cudaStream_t s, 
 
 // 3xTF32 on the tensor cores: 128 x 128 tiles, TMA loads (needs TMA-eligible
 // operands), one persistent CTA per SM.
-sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream) {
+sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream, bool pdl) {
   const TcKernelInfo *ki = tc_kernel_info(d, a.ta, a.tb);
   if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_LAUNCH;
   TcParams p;
@@ -520,7 +534,7 @@ sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream) {
   if (!okA || !okB) return SGEMM_ERR_LAUNCH;
   const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
   const int grid = static_cast<int>(num_tiles < slots ? num_tiles : slots);
-  if (tc3_entry(a.ta, a.tb).launch(p, &tmA, &tmB, grid, stream) != cudaSuccess)
+  if (tc3_entry(a.ta, a.tb).launch(p, &tmA, &tmB, grid, stream, pdl) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
   return SGEMM_SUCCESS;
@@ -569,9 +583,9 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
   switch (algo) {
     case SGEMM_ALGO_SIMT_TMA: {
       if (!tma_eligible(a)) return SGEMM_ERR_UNSUPPORTED;
-      const Pretranspose t = pretranspose_plan(a, d->sm_count);
+      const Pretranspose t = pretranspose_plan(a, d->sm_count, 256);
       if (t.a || t.b) {
-        const sgemm_status_t st = run_pretransposed(a, *d, s, t);
+        const sgemm_status_t st = run_pretransposed(a, *d, s, t, false);
         if (st != SGEMM_ERR_UNSUPPORTED) return st;
       }
       return run_simt(a, *d, kTma, s);
@@ -588,9 +602,18 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
       t_last_launches = 1;
       return SGEMM_SUCCESS;
     }
-    case SGEMM_ALGO_TC_3XTF32:
+    case SGEMM_ALGO_TC_3XTF32: {
       if (!tma_eligible(a)) return SGEMM_ERR_UNSUPPORTED;
+      // the tensor-core kernel is fastest with both operands m/n-contiguous
+      // (they pass through its raw ring, which decouples TMA from the MMA
+      // stages), so large products transpose k-contiguous operands ahead too
+      const Pretranspose t = pretranspose_plan(a, d->sm_count, 128);
+      if (t.a || t.b) {
+        const sgemm_status_t st = run_pretransposed(a, *d, s, t, true);
+        if (st != SGEMM_ERR_UNSUPPORTED) return st;
+      }
       return run_tc3(a, *d, s);
+    }
     default:
       return SGEMM_ERR_UNSUPPORTED;
   }

@@ -109,7 +109,10 @@ bool encode_tmap(CUtensorMap *m, const float *base, int64_t rows, int64_t cols, 
 int pick_simt_tile(const Args &a, int producer, int sm_count);
 
 // Smallest stream-K segment worth a partial tile (k-tiles of 32).
-constexpr int64_t kMinSkSegment = 4;
+#ifndef SG_MIN_SK_SEGMENT
+#define SG_MIN_SK_SEGMENT 1
+#endif
+constexpr int64_t kMinSkSegment = SG_MIN_SK_SEGMENT;
 
 struct SkPlan {
   int dp_tiles;     // whole tiles, round-robin

@@ -20,13 +20,34 @@ enum SimtTile : int {
   kNumSimtTiles = 3
 };
 
+// Launches `kernel`; with `pdl` it may be scheduled before the previous
+// kernel on the stream has finished (the kernel must call griddep_wait()
+// before touching memory that kernel writes).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, bool pdl, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 struct SimtKernelInfo {
   int bm, bn, threads, smem_bytes, ctas_per_sm;
 };
 
 // Launches one instantiation; grid = number of persistent CTAs.
+// pdl: launch with programmatic stream serialization (it directly follows
+// another kernel of the same call on the stream).
 using SimtLaunchFn = cudaError_t (*)(const SimtParams &, const CUtensorMap *, const CUtensorMap *,
-                                     int grid, cudaStream_t);
+                                     int grid, cudaStream_t, bool pdl);
 // Sets the kernel's shared-memory attribute on the current device (once) and
 // reports its shape and occupancy.
 using SimtInfoFn = cudaError_t (*)(SimtKernelInfo *);
@@ -44,7 +65,7 @@ struct TcKernelInfo {
   int bm, bn, ctas_per_sm;
 };
 using TcLaunchFn = cudaError_t (*)(const TcParams &, const CUtensorMap *, const CUtensorMap *, int,
-                                   cudaStream_t);
+                                   cudaStream_t, bool pdl);
 using TcInfoFn = cudaError_t (*)(TcKernelInfo *);
 struct TcEntry {
   TcLaunchFn launch;

@@ -167,6 +167,17 @@ __device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
   return out != 0;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel on its stream is still running; griddep_wait() blocks
+// until that kernel has completed and its memory operations are visible (a
+// no-op for a kernel launched the ordinary way).  griddep_launch_dependents()
+// lets the next such kernel on the stream be scheduled early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cp.async
 // 4-byte asynchronous copy global -> shared; src_bytes = 0 writes a zero and
 // reads nothing (the source address must still be a valid generic address).

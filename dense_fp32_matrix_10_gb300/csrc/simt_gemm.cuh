@@ -696,6 +696,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     tma_prefetch_desc(&tmB);
   }
   __syncthreads();
+  // Everything above overlaps the previous kernel of the same call (the
+  // transpose of an operand) when this one was launched as its dependent; the
+  // operands and C are touched only after it has finished.  The fixup pass
+  // that follows may be scheduled as soon as CTA slots free up.
+  griddep_wait();
+  griddep_launch_dependents();
 
   bool ok = true;
   if (warp >= Cfg::MATH_WARPS) {

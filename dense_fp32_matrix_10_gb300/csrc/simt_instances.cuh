@@ -10,9 +10,9 @@ namespace sg {
 
 template <class Cfg>
 cudaError_t simt_launch(const SimtParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
-                        int grid, cudaStream_t stream) {
-  simt_gemm_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(*tmA, *tmB, p);
-  return cudaGetLastError();
+                        int grid, cudaStream_t stream, bool pdl) {
+  return launch_maybe_pdl(simt_gemm_kernel<Cfg>, dim3(grid), dim3(Cfg::THREADS), Cfg::SMEM_BYTES,
+                          stream, pdl, *tmA, *tmB, p);
 }
 
 template <class Cfg>

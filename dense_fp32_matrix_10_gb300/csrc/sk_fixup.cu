@@ -2,24 +2,32 @@
 //
 // The k-iterations of the last sk tiles were divided evenly over the G CTAs of
 // the main kernel; a tile whose iterations were spread over several CTAs left
-// one raw partial sum per CTA segment in the workspace.  One block per such
-// tile adds the partials in increasing k order (so the result is the same on
-// every run) and writes C = alpha * sum + beta * C (C not read when beta == 0).
+// one raw partial sum per CTA segment in the workspace.  Each block takes one
+// 1024-element chunk of such a tile (one float4 per thread, so even a handful
+// of split tiles spreads over many SMs and no thread waits on a chain of
+// loads), adds the partials in increasing k order (so the result is the same
+// on every run) and writes C = alpha * sum + beta * C (C not read when
+// beta == 0).
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace sg {
 
 constexpr int kMaxSkSegments = 128;  // the host keeps every tile below this
+constexpr int kFixupThreads = 256;
+constexpr int kChunk = 4 * kFixupThreads;  // elements per block
 
 __device__ __forceinline__ int64_t sk_start(int64_t g, int64_t S, int64_t G) { return g * S / G; }
 
-__global__ void __launch_bounds__(256) sk_fixup_kernel(const SimtParams p, int bm, int bn,
-                                                       int grid_main) {
+__global__ void __launch_bounds__(kFixupThreads) sk_fixup_kernel(const SimtParams p, int bm, int bn,
+                                                                 int grid_main) {
+  const int chunks = bm * bn / kChunk;   // bm * bn is a multiple of 8192
+  const int tile = blockIdx.x / chunks, chunk = blockIdx.x - tile * chunks;
   __shared__ int s_slot[kMaxSkSegments];
   __shared__ int s_count;
   if (threadIdx.x == 0) {
     const int64_t KT = p.k_tiles, S = p.sk_iters, G = grid_main;
-    const int64_t it0 = static_cast<int64_t>(blockIdx.x) * KT, it1 = it0 + KT;
+    const int64_t it0 = static_cast<int64_t>(tile) * KT, it1 = it0 + KT;
     // CTAs whose iteration ranges meet [it0, it1), in increasing k order
     int64_t g = it0 * G / S;
     while (g + 1 < G && sk_start(g + 1, S, G) <= it0) ++g;
@@ -38,14 +46,18 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const SimtParams p, int b
   __syncthreads();
   const int n = s_count;
   if (n == 0) return;
+  // launched as the main kernel's dependent: its partials and C are complete
+  // and visible only after this
+  griddep_wait();
 
   int bi, tm, tn;
-  unit_coords(p, p.dp_tiles + blockIdx.x, bi, tm, tn);
+  unit_coords(p, p.dp_tiles + tile, bi, tm, tn);
   float *Cb = p.C + static_cast<int64_t>(bi) * p.strideC;
   const int64_t tile_elems = static_cast<int64_t>(bm) * bn;
   const bool read_c = p.beta != 0.0f;
-  // 4 consecutive columns per thread step (bn is a multiple of 64)
-  for (int e = 4 * threadIdx.x; e < bm * bn; e += 4 * blockDim.x) {
+  // 4 consecutive columns per thread (bn is a multiple of 64)
+  {
+    const int e = chunk * kChunk + 4 * threadIdx.x;
     float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     for (int i = 0; i < n; ++i) {
       const float4 v = *reinterpret_cast<const float4 *>(p.workspace + s_slot[i] * tile_elems + e);
@@ -55,7 +67,7 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const SimtParams p, int b
       sum.w += v.w;
     }
     const int row = tm * bm + e / bn, col = tn * bn + e % bn;
-    if (row >= p.M) continue;
+    if (row >= p.M) return;
     float *c = Cb + static_cast<int64_t>(row) * p.ldc + col;
     const float s4[4] = {sum.x, sum.y, sum.z, sum.w};
     if (p.c_vec4 && col + 3 < p.N) {
@@ -78,8 +90,8 @@ __global__ void __launch_bounds__(256) sk_fixup_kernel(const SimtParams p, int b
 
 cudaError_t launch_sk_fixup(const SimtParams &p, int bm, int bn, int grid_main, int sk_tiles,
                             cudaStream_t s) {
-  sk_fixup_kernel<<<sk_tiles, 256, 0, s>>>(p, bm, bn, grid_main);
-  return cudaGetLastError();
+  return launch_maybe_pdl(sk_fixup_kernel, dim3(sk_tiles * (bm * bn / kChunk)), dim3(kFixupThreads), 0,
+                          s, true, p, bm, bn, grid_main);
 }
 
 }  // namespace sg

@@ -7,9 +7,9 @@ namespace sg {
 
 template <class Cfg>
 static cudaError_t tc3_launch(const TcParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
-                              int grid, cudaStream_t stream) {
-  tc3_gemm_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(*tmA, *tmB, p);
-  return cudaGetLastError();
+                              int grid, cudaStream_t stream, bool pdl) {
+  return launch_maybe_pdl(tc3_gemm_kernel<Cfg>, dim3(grid), dim3(Cfg::THREADS), Cfg::SMEM_BYTES,
+                          stream, pdl, *tmA, *tmB, p);
 }
 
 template <class Cfg>

@@ -408,6 +408,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base =
       *reinterpret_cast<volatile uint32_t *>(smem + Cfg::BAR_OFFSET + Cfg::NUM_BARS * 8);
+  // launched as the dependent of an operand transpose: set-up above overlaps
+  // it, operands and C are touched only after it has finished
+  griddep_wait();
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::REGS_WG0));

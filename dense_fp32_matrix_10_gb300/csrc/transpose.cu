@@ -100,6 +100,7 @@ __device__ __forceinline__ void copy_block_scalar(const TransposeParams &p, int 
 }
 
 __global__ void __launch_bounds__(kWarps * 32) transpose_kernel(const TransposeParams p) {
+  griddep_launch_dependents();   // a product that reads our output may be scheduled
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r_in = (warp >> 1) * 16 + 4 * (lane >> 3);   // thread block origin inside the tile
   const int c_in = (warp & 1) * 32 + 4 * (lane & 7);
@@ -178,6 +179,7 @@ __device__ __forceinline__ void tma_tile_origin(const TmaTransposeParams &p, int
 __global__ void __launch_bounds__(kTmThreads) transpose_tma_kernel(const __grid_constant__ CUtensorMap in_map,
                                                                    const __grid_constant__ CUtensorMap out_map,
                                                                    const TmaTransposeParams p) {
+  griddep_launch_dependents();   // a product that reads our output may be scheduled
   extern __shared__ unsigned char smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;   // 128-byte swizzle wants 1 KiB
   const uint32_t in0 = base, out0 = base + kTmInStages * kTmTileBytes;

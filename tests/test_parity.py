@@ -272,9 +272,10 @@ def test_runs_on_the_given_stream(orc):
     assert_close(C.cpu().numpy(), R, K, "side stream")
 
 
-def test_launch_count_small_is_one():
-    A = torch.rand(300, 200, device="cuda")
-    B = torch.rand(200, 100, device="cuda")
+def test_launch_count_single_k_slice_is_one():
+    """K = 32 is one k-slice: nothing to split, one launch for every family."""
+    A = torch.rand(300, 32, device="cuda")
+    B = torch.rand(32, 100, device="cuda")
     for algo in ALL_ALGOS:
         sg.gemm(A, B, algo=algo)
         assert sg.sgemm_last_launch_count() == 1, algo
@@ -367,6 +368,28 @@ def test_pretransposed_matches_tn_bit_for_bit(shape, op):
     eligible = (A.stride(0) % 4 == 0 and B.stride(0) % 4 == 0 and M * N * K >= 2 ** 30
                 and -(-M // 128) * -(-N // 256) >= torch.cuda.get_device_properties(0).multi_processor_count)
     assert n1 == n2 + eligible * ((ta == 0 and N >= 1024) + (tb == 1 and M >= 1024))
+
+
+@pytest.mark.parametrize("op", [(0, 0), (0, 1), (1, 1)], ids=["NN", "NT", "TT"])
+def test_tensor_core_pretransposed_matches_tn_bit_for_bit(op):
+    """The 3xTF32 kernel, too, runs large NN / NT / TT products in the TN
+    layout after transposing k-contiguous operands ahead: bit-identical to
+    the TN call on operands transposed by torch."""
+    M, N, K = 2048, 2560, 512
+    ta, tb = op
+    g = torch.Generator().manual_seed(11 + 2 * ta + tb)
+    A = torch.randn((K, M) if ta else (M, K), generator=g).cuda()
+    B = torch.randn((N, K) if tb else (K, N), generator=g).cuda()
+    C1 = torch.empty(M, N, device="cuda")
+    sg.gemm(A, B, C1, 1.0, 0.0, ta, tb, algo="tc_3xtf32")
+    n1 = sg.sgemm_last_launch_count()
+    At = A if ta else A.t().contiguous()
+    Bn = B.t().contiguous() if tb else B
+    C2 = torch.empty(M, N, device="cuda")
+    sg.gemm(At, Bn, C2, 1.0, 0.0, 1, 0, algo="tc_3xtf32")
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+    assert n1 == 1 + (ta == 0) + (tb == 1)
 
 
 def test_pretransposed_on_two_streams(orc):
