@@ -20,7 +20,10 @@ region), ``vs_size`` (TFLOP/s of the 512..4096 square sweep), ``configs``
 (TFLOP/s of the other workload families), ``tensor_core_3xtf32`` (the
 tensor-core kernel on the headline product), ``transpose`` (the transpose
 kernel's HBM bandwidth at 4096 x 4096 and 16384 x 16384) and
-``library_context`` (cuBLAS FP32 on the headline product, for context).
+``library_context`` (cuBLAS FP32 on the headline product, for context),
+``strided_batched`` (a per-head attention Q K^T batch through
+sgemm_strided_batched) and ``ladder`` (the pages' naive and 16 x 16
+shared-memory-tiled kernels against the default path at 2048^3).
 
 ``--impl reference`` times the CPU oracle instead (the only other use of the
 oracle here), on a bounded sample per step, and prints the same JSON line with
@@ -385,6 +388,50 @@ def run_ours(args, dist):
                                    else "2 GiB per launch, larger than L2"}}
         del flush
 
+    # ---- strided batch (attention Q K^T shape) and the pages' kernel ladder
+    batched = None
+    if not args.no_batched:
+        bt, bm_, bn_, bk_ = 96, 512, 512, 64
+        Q = torch.randn(bt, bm_, bk_, device=dev)
+        Kt = torch.randn(bt, bn_, bk_, device=dev)
+        S = torch.empty(bt, bm_, bn_, device=dev)
+        for _ in range(3):
+            sg.gemm_strided_batched(Q, Kt, S, transB=True, stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(50):
+            sg.gemm_strided_batched(Q, Kt, S, transB=True, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        bms = e0.elapsed_time(e1) / 50
+        bach = tflops(2.0 * bt * bm_ * bn_ * bk_, bms)
+        batched = {"workload": f"{bt} x ({bm_}x{bk_}) . ({bk_}x{bn_})^T, NT (per-head Q K^T)",
+                   "value": round(bach, 3), "unit": "TFLOP/s", "ms": round(bms, 5),
+                   "roofline": {"bound": "alu", "achieved": round(bach, 3), "peak": round(peak, 3),
+                                "unit": "TFLOP/s", "frac": round(bach / peak, 4)}}
+        del Q, Kt, S
+    ladder = None
+    if not args.no_ladder:
+        n = 2048
+        La, Lb = torch.randn(n, n, device=dev), torch.randn(n, n, device=dev)
+        Lc = torch.empty(n, n, device=dev)
+        ladder = {"workload": f"{n}^3 NN", "unit": "TFLOP/s"}
+        for algo_name in ("naive", "smem_tiled", "auto"):
+            sg.gemm(La, Lb, Lc, algo=algo_name, stream=stream)
+            reps = 3 if algo_name != "auto" else 20
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                sg.gemm(La, Lb, Lc, algo=algo_name, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ladder[algo_name] = round(tflops(2.0 * n ** 3, e0.elapsed_time(e1) / reps), 3)
+        ladder["speedup_auto_over_naive"] = round(ladder["auto"] / ladder["naive"], 1)
+        ladder["speedup_smem_tiled_over_naive"] = round(ladder["smem_tiled"] / ladder["naive"], 2)
+        del La, Lb, Lc
+
     # ---- library context: cuBLAS FP32 (TF32 off) on the headline product
     library_context = None
     if not args.no_library_context:
@@ -440,6 +487,7 @@ def run_ours(args, dist):
         "pct_of_fp32_peak": round(100 * achieved / peak, 2),
         "e2e": e2e, "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
         "tensor_core_3xtf32": tensor, "transpose": transpose,
+        "strided_batched": batched, "ladder": ladder,
         "library_context": library_context,
         "vs_size": vs_size, "configs": configs,
         "device": {"name": props.name, "sms": sms, "cc": f"{props.major}.{props.minor}"},
@@ -540,6 +588,10 @@ def main(argv=None):
                     help="skip the extra timing of the transpose kernel")
     ap.add_argument("--no-library-context", action="store_true",
                     help="skip the cuBLAS FP32 context number")
+    ap.add_argument("--no-batched", action="store_true",
+                    help="skip the extra timing of a strided batch")
+    ap.add_argument("--no-ladder", action="store_true",
+                    help="skip the naive / shared-memory-tiled comparison kernels")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
