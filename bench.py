@@ -455,7 +455,7 @@ def run_ours(args, dist):
         del out
 
     # ---- TFLOP/s vs size and the other workload families (rank 0 context)
-    vs_size, configs = {}, {}
+    vs_size, families = {}, {}
     if not args.no_sweep:
         for sc in W.SWEEP:
             sA, sB, sC = (t.to(dev) for t in W.make_inputs(sc))
@@ -470,7 +470,7 @@ def run_ours(args, dist):
             # beta != 0 updates C in place each call; the values drift but the
             # work per call is identical.
             r, _, _ = time_gemm(sg, torch, sc, sA, sB, sC, n, 3, args.algo, stream)
-            configs[sc.name] = round(tflops(sc.flops, r), 3)
+            families[sc.name] = round(tflops(sc.flops, r), 3)
             del sA, sB, sC, sC0
 
     result = {
@@ -489,7 +489,7 @@ def run_ours(args, dist):
         "tensor_core_3xtf32": tensor, "transpose": transpose,
         "strided_batched": batched, "ladder": ladder,
         "library_context": library_context,
-        "vs_size": vs_size, "configs": configs,
+        "vs_size": vs_size, "configs": families,
         "device": {"name": props.name, "sms": sms, "cc": f"{props.major}.{props.minor}"},
     }
     if dist.rank == 0 and not args.no_cpu_baseline:

@@ -438,6 +438,10 @@ float *pretranspose_scratch(DeviceState &d, size_t bytes, bool capturing) {
     return nullptr;
   }
   if (bytes > d.tr_bytes) {
+    // a captured graph holds the current buffer's address: once one exists
+    // the buffer is never freed or moved (larger products then take the
+    // in-kernel transpose)
+    if (d.tr_order.in_graph) return nullptr;
     const size_t step = size_t(64) << 20;
     const size_t want = (bytes + step - 1) / step * step;
     if (d.tr) {

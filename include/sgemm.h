@@ -44,7 +44,9 @@
  * CUDA graphs: sgemm(), sgemm_ex(), sgemm_strided_batched() and
  * sgemm_transpose() may be captured.  Inside a capture the library allocates
  * nothing: a product whose stream-K workspace or transpose scratch does not
- * exist yet (or is too small) runs without it.  Uses of these buffers inside
+ * exist yet (or is too small) runs without it; and once a capture has used
+ * the transpose scratch it is never reallocated (graphs hold its address), so
+ * later products that would need a larger one run without it.  Uses of these buffers inside
  * graphs are ordered against every other use through external event nodes,
  * so graph launches and eager calls on other streams may be mixed freely.
  *

@@ -102,6 +102,51 @@ def test_batched_and_transpose_capture():
     assert torch.equal(C, refC) and torch.equal(T, refT)
 
 
+GROW_CHILD = r"""
+import sys, torch
+sys.path.insert(0, {root!r})
+import dense_fp32_matrix_10_gb300 as sg
+def ops(M, N, K, seed):
+    g0 = torch.Generator().manual_seed(seed)
+    return torch.randn(M, K, generator=g0).cuda(), torch.randn(K, N, generator=g0).cuda()
+# a transposed-ahead product (scratch of K x M floats), captured
+A, B = ops(2048, 4864, 256, 1)
+C = torch.empty(2048, 4864, device="cuda")
+s = torch.cuda.Stream()
+with torch.cuda.stream(s):
+    sg.gemm(A, B, C, stream=s)
+    assert sg.sgemm_last_launch_count() >= 2          # transpose + product
+torch.cuda.synchronize()
+ref = C.clone()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):
+    sg.gemm(A, B, C, stream=s)
+# an eager product needing a larger scratch (A^T of 8192 x 4096 floats, 128 MiB,
+# against the 64 MiB allocated so far): must not move the graph's buffer
+A2, B2 = ops(4096, 4096, 8192, 2)
+C2 = sg.gemm(A2, B2)
+torch.cuda.synchronize()
+C.zero_()
+g.replay()
+torch.cuda.synchronize()
+assert torch.equal(C, ref)
+r2 = A2.double() @ B2.double()
+assert ((C2.double() - r2).norm() / r2.norm()).item() < 1e-5
+assert sg.sgemm_last_device_status() == 0
+print("ok")
+"""
+
+
+def test_captured_scratch_is_never_moved():
+    """After a capture used the transpose scratch, a larger product must not
+    reallocate it (the graph holds its address): the graph still replays
+    correctly after such a product, which itself runs correctly."""
+    p = subprocess.run([sys.executable, "-c", GROW_CHILD.format(root=ROOT)], capture_output=True,
+                       text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-3000:]
+    assert p.stdout.strip().endswith("ok")
+
+
 CHILD = r"""
 import sys, torch
 sys.path.insert(0, {root!r})
