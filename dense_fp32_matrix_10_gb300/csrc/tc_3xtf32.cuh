@@ -12,7 +12,11 @@
 // integer-valued inputs of at most 11 significant bits have small = 0, so
 // integer products stay exact.  Non-finite inputs get small = 0.
 //
-// Both MMA operands are read K-major (128-byte rows of 32 k, 128 B swizzle).
+// B is read K-major from shared memory (128-byte rows of 32 k, 128 B swizzle);
+// A too when it is k-contiguous, while an m-contiguous A (the layout the
+// dispatcher gives every large product) is converted straight into tensor
+// memory and read from there (measured on GB300 at 4096^3 TN: converters
+// 172 -> 189 TFLOP/s with the paired split below, 217 with A in TMEM).
 // Roles (one persistent CTA of 16 warps per SM, 128 x 128 output tiles, k in
 // slices of 32):
 //   warp 0       TMA producer.  A k-contiguous operand (A stored M x K, B stored
@@ -23,8 +27,9 @@
 //                x_big) beside the raw tile (elementwise, same layout); for an
 //                m/n-contiguous one build both x_big and x_small tiles K-major
 //                from the raw ring (a transpose through shared memory);
-//   warp 1       allocates 256 TMEM columns (two 128-column accumulators); one
-//                thread issues 3 MMAs (128 x 128 x 8) per k8;
+//   warp 1       allocates 256 TMEM columns (two 128-column accumulators; 512
+//                with A's parts in TMEM too); one thread issues 3 MMAs
+//                (128 x 128 x 8) per k8;
 //   warps 4..7   epilogue (warp 4+q owns TMEM lanes 32q..32q+31 = tile rows).
 // Accuracy: the tensor core's FP32 accumulator rounds toward zero on every MMA
 // (measured: a 4096-long accumulation drifts to ~3e-5 relative, linearly in K).
@@ -41,6 +46,19 @@
 
 #include "ptx.cuh"
 #include "simt_gemm.cuh"  // tile_coords
+
+#ifndef SG_TC_A_TMEM
+#define SG_TC_A_TMEM 1
+#endif
+#ifndef SG_TC_RAW_STAGES
+#define SG_TC_RAW_STAGES 2
+#endif
+#ifndef SG_TC_ATMEM_STAGES
+#define SG_TC_ATMEM_STAGES 3
+#endif
+#ifndef SG_TC_ATMEM_RAW_STAGES
+#define SG_TC_ATMEM_RAW_STAGES 3
+#endif
 
 namespace sg {
 
@@ -62,26 +80,37 @@ struct TcConfig {
   static constexpr bool B_KMAJOR = B_KMAJOR_;
   static constexpr int BM = 128, BN = 128, BK = 32;
   static constexpr int TILE_BYTES = 128 * 32 * 4;  // one 128 x 32 FP32 tile
-  // MMA ring stage: A big, A small, B big, B small (K-major, 128 B swizzle).
-  // A k-contiguous operand's big tile is its raw TMA tile.
-  static constexpr int STAGE_BYTES = 4 * TILE_BYTES;
-  static constexpr int A_BIG = 0, A_SMALL = TILE_BYTES, B_BIG = 2 * TILE_BYTES,
-                       B_SMALL = 3 * TILE_BYTES;
+  // A_TMEM: an m-contiguous A (through the raw ring) is converted straight
+  // into tensor memory and the MMAs read it from there, so shared memory
+  // carries only B for them (its bandwidth bounds this kernel).
+  static constexpr bool A_TMEM = !A_KMAJOR && SG_TC_A_TMEM;
+  // MMA ring stage: A big, A small (unless A_TMEM), B big, B small (K-major,
+  // 128 B swizzle).  A k-contiguous operand's big tile is its raw TMA tile.
+  static constexpr int STAGE_BYTES = (A_TMEM ? 2 : 4) * TILE_BYTES;
+  static constexpr int A_BIG = 0, A_SMALL = TILE_BYTES, B_BIG = A_TMEM ? 0 : 2 * TILE_BYTES,
+                       B_SMALL = B_BIG + TILE_BYTES;
   // Raw ring: the m/n-contiguous operands' FP32 slices, dense [32 k][128 mn].
   static constexpr int RAW_OPERANDS = (A_KMAJOR ? 0 : 1) + (B_KMAJOR ? 0 : 1);
-  static constexpr int RAW_STAGES = RAW_OPERANDS ? 2 : 0;
+  // Raw-ring depth: a TMA load must land within RAW_STAGES k-slices of MMA
+  // work; with A in TMEM the smaller MMA stages leave room for a deeper ring.
+  static constexpr int RAW_STAGES = RAW_OPERANDS ? (A_TMEM ? SG_TC_ATMEM_RAW_STAGES : SG_TC_RAW_STAGES) : 0;
   static constexpr int RAW_STAGE_BYTES = RAW_OPERANDS * TILE_BYTES;
-  static constexpr int STAGES = (RAW_OPERANDS == 2) ? 2 : 3;
+  static constexpr int STAGES = A_TMEM ? SG_TC_ATMEM_STAGES : ((RAW_OPERANDS == 2) ? 2 : 3);
+  // TMEM columns: two 128-column accumulators, then (A_TMEM) per stage A big
+  // (32 columns = 32 k) and A small (32 more).
+  static constexpr int A_TMEM_COL = 256;
+  static constexpr int TMEM_COLS = A_TMEM ? 512 : 256;
+  static_assert(!A_TMEM || A_TMEM_COL + 64 * STAGES <= TMEM_COLS, "A stages exceed TMEM");
   static constexpr int RAW_OFFSET = STAGES * STAGE_BYTES;
   static constexpr int RAW_A = 0, RAW_B = A_KMAJOR ? 0 : TILE_BYTES;  // within a raw stage
   static constexpr int BAR_OFFSET = RAW_OFFSET + RAW_STAGES * RAW_STAGE_BYTES;
   // full, conv_full, empty per stage; raw_full, raw_empty per raw stage;
   // acc_full[2], acc_empty[2]; drain
-  static constexpr int NUM_BARS = 3 * STAGES + 2 * 2 + 4 + 1;
+  static constexpr int RAW_BARS = RAW_STAGES > 0 ? RAW_STAGES : 1;
+  static constexpr int NUM_BARS = 3 * STAGES + 2 * RAW_BARS + 4 + 1;
   static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
   static constexpr int THREADS = 512;
-  static constexpr int TMEM_COLS = 256;
   static constexpr uint32_t IDESC = idesc_tf32(128, 128);
   // Two converter warpgroups: the conversion is ~250 dependent instructions
   // per thread and k-slice with one warpgroup, more than the 768 tensor-core
@@ -104,10 +133,16 @@ struct TcBars {
   __device__ uint32_t conv_full(uint32_t s) const { return base + 8 * (Cfg::STAGES + s); }
   __device__ uint32_t empty(uint32_t s) const { return base + 8 * (2 * Cfg::STAGES + s); }
   __device__ uint32_t raw_full(uint32_t r) const { return base + 8 * (3 * Cfg::STAGES + r); }
-  __device__ uint32_t raw_empty(uint32_t r) const { return base + 8 * (3 * Cfg::STAGES + 2 + r); }
-  __device__ uint32_t acc_full(uint32_t b) const { return base + 8 * (3 * Cfg::STAGES + 4 + b); }
-  __device__ uint32_t acc_empty(uint32_t b) const { return base + 8 * (3 * Cfg::STAGES + 6 + b); }
-  __device__ uint32_t drain() const { return base + 8 * (3 * Cfg::STAGES + 8); }
+  __device__ uint32_t raw_empty(uint32_t r) const {
+    return base + 8 * (3 * Cfg::STAGES + Cfg::RAW_BARS + r);
+  }
+  __device__ uint32_t acc_full(uint32_t b) const {
+    return base + 8 * (3 * Cfg::STAGES + 2 * Cfg::RAW_BARS + b);
+  }
+  __device__ uint32_t acc_empty(uint32_t b) const {
+    return base + 8 * (3 * Cfg::STAGES + 2 * Cfg::RAW_BARS + 2 + b);
+  }
+  __device__ uint32_t drain() const { return base + 8 * (3 * Cfg::STAGES + 2 * Cfg::RAW_BARS + 4); }
 };
 
 // ------------------------------------------------------------------ producer
@@ -140,7 +175,7 @@ __device__ __forceinline__ void tc_produce(const TcParams &p, const CUtensorMap 
         k_issued = true;
       }
       if (Cfg::RAW_OPERANDS) {  // m/n-contiguous operands into the raw ring
-        const uint32_t r = it % 2, rround = it / 2;
+        const uint32_t r = it % Cfg::RAW_STAGES, rround = it / Cfg::RAW_STAGES;
         if (rround > 0 &&
             !wait_parity_bounded(bar.raw_empty(r), (rround - 1) & 1, p.wait_budget_ns, p.status)) {
           ok = false;
@@ -154,13 +189,15 @@ __device__ __forceinline__ void tc_produce(const TcParams &p, const CUtensorMap 
     }
   }
   if (!ok) {  // let issued copies land before the CTA can end (bounded waits)
-    const uint32_t first = it > 3 ? it - 3 : 0;
+    constexpr uint32_t DEPTH = Cfg::STAGES > Cfg::RAW_STAGES ? Cfg::STAGES : Cfg::RAW_STAGES;
+    const uint32_t first = it > DEPTH ? it - DEPTH : 0;
     for (uint32_t j = first; j < it; ++j) {
       if (ANY_K)
         wait_parity_bounded(bar.full(j % Cfg::STAGES), (j / Cfg::STAGES) & 1, p.wait_budget_ns,
                             nullptr);
       if (Cfg::RAW_OPERANDS)
-        wait_parity_bounded(bar.raw_full(j % 2), (j / 2) & 1, p.wait_budget_ns, nullptr);
+        wait_parity_bounded(bar.raw_full(j % Cfg::RAW_STAGES), (j / Cfg::RAW_STAGES) & 1,
+                            p.wait_budget_ns, nullptr);
     }
     if (k_issued)
       wait_parity_bounded(bar.full(it % Cfg::STAGES), (it / Cfg::STAGES) & 1, p.wait_budget_ns,
@@ -173,6 +210,26 @@ __device__ __forceinline__ float small_part(float x, float big) {
   return isfinite(x) ? to_tf32(x - big) : 0.0f;
 }
 
+// Big and small TF32 parts of two values at once: big = x with its low 13
+// mantissa bits cleared; small = x - big (exact in FP32, one packed FMA for
+// the pair) rounded to the nearest TF32 value, ties away from zero -- adding
+// half of the last kept bit (1 << 12) to the magnitude bits and clearing the
+// low 13 bits does exactly that, subnormals included; small = 0 when x is not
+// finite, which is exactly when x - big is NaN.
+__device__ __forceinline__ void split_pair(float x0, float x1, float &b0, float &b1, float &s0,
+                                           float &s1) {
+  b0 = __uint_as_float(__float_as_uint(x0) & 0xFFFFE000u);
+  b1 = __uint_as_float(__float_as_uint(x1) & 0xFFFFE000u);
+  const float2 d = __ffma2_rn(make_float2(b0, b1), make_float2(-1.0f, -1.0f), make_float2(x0, x1));
+  const float r0 = __uint_as_float((__float_as_uint(d.x) + 0x1000u) & 0xFFFFE000u);
+  const float r1 = __uint_as_float((__float_as_uint(d.y) + 0x1000u) & 0xFFFFE000u);
+  s0 = (d.x == d.x) ? r0 : 0.0f;
+  s1 = (d.y == d.y) ? r1 : 0.0f;
+}
+#ifndef SG_TC_SPLIT_PAIR
+#define SG_TC_SPLIT_PAIR 1
+#endif
+
 // k-contiguous operand: small = tf32(x - x_big) beside the raw tile, elementwise
 // (same layout, so the small tile shares the raw tile's descriptor geometry).
 // ct = converter thread 0..255; 1024 16-byte chunks, 4 per thread.
@@ -183,10 +240,16 @@ __device__ __forceinline__ void small_of_kmajor(const unsigned char *raw, unsign
     const int off = (ct + 256 * i) * 16;
     const float4 x = *reinterpret_cast<const float4 *>(raw + off);
     float4 s;
-    s.x = small_part(x.x, tf32_trunc(x.x));
-    s.y = small_part(x.y, tf32_trunc(x.y));
-    s.z = small_part(x.z, tf32_trunc(x.z));
-    s.w = small_part(x.w, tf32_trunc(x.w));
+    if (SG_TC_SPLIT_PAIR) {
+      float b0, b1, b2, b3;
+      split_pair(x.x, x.y, b0, b1, s.x, s.y);
+      split_pair(x.z, x.w, b2, b3, s.z, s.w);
+    } else {
+      s.x = small_part(x.x, tf32_trunc(x.x));
+      s.y = small_part(x.y, tf32_trunc(x.y));
+      s.z = small_part(x.z, tf32_trunc(x.z));
+      s.w = small_part(x.w, tf32_trunc(x.w));
+    }
     *reinterpret_cast<float4 *>(small + off) = s;
   }
 }
@@ -207,29 +270,61 @@ __device__ __forceinline__ void split_of_mnmajor(const unsigned char *raw, unsig
     x.z = r[(4 * kc + 2) * 128 + ct];
     x.w = r[(4 * kc + 3) * 128 + ct];
     float4 b, s;
-    b.x = tf32_trunc(x.x);
-    b.y = tf32_trunc(x.y);
-    b.z = tf32_trunc(x.z);
-    b.w = tf32_trunc(x.w);
-    s.x = small_part(x.x, b.x);
-    s.y = small_part(x.y, b.y);
-    s.z = small_part(x.z, b.z);
-    s.w = small_part(x.w, b.w);
+    if (SG_TC_SPLIT_PAIR) {
+      split_pair(x.x, x.y, b.x, b.y, s.x, s.y);
+      split_pair(x.z, x.w, b.z, b.w, s.z, s.w);
+    } else {
+      b.x = tf32_trunc(x.x);
+      b.y = tf32_trunc(x.y);
+      b.z = tf32_trunc(x.z);
+      b.w = tf32_trunc(x.w);
+      s.x = small_part(x.x, b.x);
+      s.y = small_part(x.y, b.y);
+      s.z = small_part(x.z, b.z);
+      s.w = small_part(x.w, b.w);
+    }
     const int off = ct * 128 + ((kc ^ (ct & 7)) << 4);
     *reinterpret_cast<float4 *>(big + off) = b;
     *reinterpret_cast<float4 *>(small + off) = s;
   }
 }
 
+// m-contiguous A slice, raw [32 k][128 m] -> TF32 big and small parts in
+// tensor memory (A_TMEM): thread ct handles tile row m = ct % 128, which is
+// lane l of its warp in TMEM lane quarter warp % 4 (m = 32 * (warp % 4) + l);
+// the two converter warpgroups take k 0..15 and 16..31.
+template <class Cfg>
+__device__ __forceinline__ void a_to_tmem(const unsigned char *raw, uint32_t a_col, int ct, int warp) {
+  const float *r = reinterpret_cast<const float *>(raw);
+  const int m = ct & 127, kh = ct >> 7;
+  uint32_t big[16], small[16];
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const float x0 = r[(16 * kh + j) * 128 + m], x1 = r[(16 * kh + j + 1) * 128 + m];
+    float b0, b1, s0, s1;
+    split_pair(x0, x1, b0, b1, s0, s1);
+    big[j] = __float_as_uint(b0);
+    big[j + 1] = __float_as_uint(b1);
+    small[j] = __float_as_uint(s0);
+    small[j + 1] = __float_as_uint(s1);
+  }
+  const uint32_t lanes = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  tmem_st_32x32b_x16(a_col + lanes + 16 * kh, big);
+  tmem_st_32x32b_x16(a_col + lanes + 32 + 16 * kh, small);
+  tmem_st_wait();
+}
+
 template <class Cfg>
 __device__ __forceinline__ void tc_convert(const TcParams &p, unsigned char *smem,
-                                           const TcBars<Cfg> &bar, int ct, int lane) {
+                                           const TcBars<Cfg> &bar, uint32_t tmem_base, int ct,
+                                           int warp, int lane) {
   constexpr bool ANY_K = Cfg::A_KMAJOR || Cfg::B_KMAJOR;
   uint32_t it = 0;
   for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
     for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
       const uint32_t s = it % Cfg::STAGES, round = it / Cfg::STAGES;
-      const uint32_t r = it % 2, rround = it / 2;
+      const uint32_t r = Cfg::RAW_OPERANDS ? it % Cfg::RAW_STAGES : 0;
+      const uint32_t rround = Cfg::RAW_OPERANDS ? it / Cfg::RAW_STAGES : 0;
       // The stage is free once the MMAs of its previous round finished.  With
       // a k-contiguous operand the producer waited for that before its copy,
       // so the stage's `full` phase already implies it.
@@ -242,15 +337,20 @@ __device__ __forceinline__ void tc_convert(const TcParams &p, unsigned char *sme
         return;
       unsigned char *st = smem + s * Cfg::STAGE_BYTES;
       const unsigned char *rs = smem + Cfg::RAW_OFFSET + r * Cfg::RAW_STAGE_BYTES;
-      if (Cfg::A_KMAJOR)
+      if (Cfg::A_TMEM) {
+        tc_fence_after_sync();   // the MMAs that read this A stage have finished
+        a_to_tmem<Cfg>(rs + Cfg::RAW_A, tmem_base + Cfg::A_TMEM_COL + 64 * s, ct, warp);
+      } else if (Cfg::A_KMAJOR) {
         small_of_kmajor(st + Cfg::A_BIG, st + Cfg::A_SMALL, ct);
-      else
+      } else {
         split_of_mnmajor(rs + Cfg::RAW_A, st + Cfg::A_BIG, st + Cfg::A_SMALL, ct);
+      }
       if (Cfg::B_KMAJOR)
         small_of_kmajor(st + Cfg::B_BIG, st + Cfg::B_SMALL, ct);
       else
         split_of_mnmajor(rs + Cfg::RAW_B, st + Cfg::B_BIG, st + Cfg::B_SMALL, ct);
       fence_proxy_async_smem();  // the MMA reads these through the async proxy
+      if (Cfg::A_TMEM) tc_fence_before_sync();   // ... and A's tensor-memory parts
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(bar.conv_full(s));
@@ -287,14 +387,22 @@ __device__ __forceinline__ void tc_issue(const TcParams &p, uint32_t sbase, uint
         const uint32_t st = sbase + s * Cfg::STAGE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < Cfg::BK / 8; ++kk) {
-          // k8 step kk: 32 bytes along the 128-byte K-major rows
-          const uint64_t a_big = desc_kmajor_sw128(st + Cfg::A_BIG + kk * 32);
-          const uint64_t a_small = desc_kmajor_sw128(st + Cfg::A_SMALL + kk * 32);
+          // k8 step kk: 32 bytes along the 128-byte K-major rows (8 TMEM columns)
           const uint64_t b_big = desc_kmajor_sw128(st + Cfg::B_BIG + kk * 32);
           const uint64_t b_small = desc_kmajor_sw128(st + Cfg::B_SMALL + kk * 32);
-          mma_tf32(d, a_small, b_big, Cfg::IDESC, (kt > kc0 || kk > 0) ? 1u : 0u);
-          mma_tf32(d, a_big, b_small, Cfg::IDESC, 1u);
-          mma_tf32(d, a_big, b_big, Cfg::IDESC, 1u);
+          const uint32_t acc = (kt > kc0 || kk > 0) ? 1u : 0u;
+          if (Cfg::A_TMEM) {
+            const uint32_t a_big = tmem_base + Cfg::A_TMEM_COL + 64 * s + 8 * kk;
+            mma_tf32_a_tmem(d, a_big + 32, b_big, Cfg::IDESC, acc);   // a_small * b_big
+            mma_tf32_a_tmem(d, a_big, b_small, Cfg::IDESC, 1u);
+            mma_tf32_a_tmem(d, a_big, b_big, Cfg::IDESC, 1u);
+          } else {
+            const uint64_t a_big = desc_kmajor_sw128(st + Cfg::A_BIG + kk * 32);
+            const uint64_t a_small = desc_kmajor_sw128(st + Cfg::A_SMALL + kk * 32);
+            mma_tf32(d, a_small, b_big, Cfg::IDESC, acc);
+            mma_tf32(d, a_big, b_small, Cfg::IDESC, 1u);
+            mma_tf32(d, a_big, b_big, Cfg::IDESC, 1u);
+          }
         }
         mma_commit(bar.empty(s));  // frees the stage when these MMAs finish
       }
@@ -389,7 +497,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       mbar_init(bar.conv_full(s), Cfg::CONVERTER_WARPS);
       mbar_init(bar.empty(s), 1);
     }
-    for (int r = 0; r < 2; ++r) {
+    for (int r = 0; r < Cfg::RAW_BARS; ++r) {
       mbar_init(bar.raw_full(r), 1);
       mbar_init(bar.raw_empty(r), Cfg::CONVERTER_WARPS);
     }
@@ -426,7 +534,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_epilogue<Cfg>(p, tmem_base, bar, warp & 3, lane);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::REGS_CONV));
-    tc_convert<Cfg>(p, smem, bar, threadIdx.x - 256, lane);
+    tc_convert<Cfg>(p, smem, bar, tmem_base, threadIdx.x - 256, warp, lane);
   }
 
   tc_fence_before_sync();
