@@ -73,6 +73,14 @@ const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb) {
   return &d.tcinfo[ta][tb];
 }
 
+const TcKernelInfo *tc_kernel_info_presplit(DeviceState &d) {
+  std::call_once(d.tcpre_once, [&]() {
+    d.tcpre_err = tc3_presplit_entry().info(&d.tcpre);
+    if (d.tcpre_err != cudaSuccess) cudaGetLastError();
+  });
+  return d.tcpre_err == cudaSuccess ? &d.tcpre : nullptr;
+}
+
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -427,6 +435,14 @@ Pretranspose pretranspose_plan(const Args &a, int sm_count, int64_t tile_n) {
 
 int64_t round4(int64_t x) { return (x + 3) & ~int64_t(3); }
 
+// Products large enough for the split pass of the tensor-core path: the size
+// rule of pretranspose_plan with 128 x 128 tiles, any layout.
+bool presplit_size_ok(const Args &a, int sm_count) {
+  const double work = static_cast<double>(a.M) * static_cast<double>(a.N) * static_cast<double>(a.K);
+  return tma_eligible(a) && work >= static_cast<double>(kPretransposeMinWork) &&
+         cdiv(a.M, 128) * cdiv(a.N, 128) >= sm_count;
+}
+
 // Scratch of at least `bytes` (grown in 64 MiB steps), or null (also when it
 // would have to be allocated or grown inside a stream capture).
 float *pretranspose_scratch(DeviceState &d, size_t bytes, bool capturing) {
@@ -538,9 +554,88 @@ sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream, bool 
   if (!okA || !okB) return SGEMM_ERR_LAUNCH;
   const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
   const int grid = static_cast<int>(num_tiles < slots ? num_tiles : slots);
-  if (tc3_entry(a.ta, a.tb).launch(p, &tmA, &tmB, grid, stream, pdl) != cudaSuccess)
+  if (tc3_entry(a.ta, a.tb).launch(p, &tmA, &tmB, &tmA, &tmB, grid, stream, pdl) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
+  return SGEMM_SUCCESS;
+}
+
+// 3xTF32 with the split done ahead: a memory-bound pass writes each operand's
+// TF32 small parts K-major into library scratch (and, for an m/n-contiguous
+// operand, the operand itself transposed, which serves as its big parts);
+// the tensor-core kernel then loads big and small tiles with TMA and converts
+// nothing.  Every block of A and B is split once per product instead of once
+// per output tile that uses it.  Returns SGEMM_ERR_UNSUPPORTED with nothing
+// queued when the scratch or a pass is unavailable.
+#ifndef SG_TC_PRESPLIT
+#define SG_TC_PRESPLIT 1
+#endif
+sgemm_status_t run_tc3_presplit(const Args &a, DeviceState &d, cudaStream_t s) {
+  const TcKernelInfo *ki = tc_kernel_info_presplit(d);
+  if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_UNSUPPORTED;
+  const int64_t ldk = a.K;   // K % 4 == 0 on this path
+  const size_t mat_a = (static_cast<size_t>(a.M) * ldk * sizeof(float) + 255) & ~size_t(255);
+  const size_t mat_b = (static_cast<size_t>(a.N) * ldk * sizeof(float) + 255) & ~size_t(255);
+  const bool tA = a.ta == 1, tB = a.tb == 0;   // operands to transpose to K-major
+  const size_t bytes = mat_a * (tA ? 2 : 1) + mat_b * (tB ? 2 : 1);
+  const bool capturing = stream_capturing(s);
+  std::lock_guard<std::mutex> lock(d.tr_mu);
+  float *scratch = pretranspose_scratch(d, bytes, capturing);
+  if (!scratch) return SGEMM_ERR_UNSUPPORTED;
+  char *cur = reinterpret_cast<char *>(scratch);
+  auto take = [&cur](size_t n) {
+    float *q = reinterpret_cast<float *>(cur);
+    cur += n;
+    return q;
+  };
+  float *a_small = take(mat_a), *a_big = tA ? take(mat_a) : nullptr;
+  float *b_small = take(mat_b), *b_big = tB ? take(mat_b) : nullptr;
+  if (order_before_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  bool done = false;
+  // A: stored M x K (k along rows) or K x M
+  if (launch_tf32_split(a.A, a.lda, tA ? static_cast<int>(a.K) : static_cast<int>(a.M),
+                        tA ? static_cast<int>(a.M) : static_cast<int>(a.K), tA, a_big, a_small, ldk,
+                        d.sm_count, d.status, s, &done) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
+  if (!done) return SGEMM_ERR_UNSUPPORTED;   // nothing queued yet
+  // B: stored N x K or K x N
+  if (launch_tf32_split(a.B, a.ldb, tB ? static_cast<int>(a.K) : static_cast<int>(a.N),
+                        tB ? static_cast<int>(a.N) : static_cast<int>(a.K), tB, b_big, b_small, ldk,
+                        d.sm_count, d.status, s, &done) != cudaSuccess || !done)
+    return SGEMM_ERR_LAUNCH;   // the A pass is queued: failing here is an error
+  const float *A_big = tA ? a_big : a.A, *B_big = tB ? b_big : a.B;
+  const int64_t lda_big = tA ? ldk : a.lda, ldb_big = tB ? ldk : a.ldb;
+
+  TcParams p;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.alpha = a.alpha;
+  p.beta = a.beta;
+  p.tiles_m = static_cast<int>(cdiv(a.M, ki->bm));
+  p.tiles_n = static_cast<int>(cdiv(a.N, ki->bn));
+  p.k_tiles = static_cast<int>(cdiv(a.K, 32));
+  const int64_t num_tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  if (num_tiles > kMaxDim) return SGEMM_ERR_LAUNCH;
+  p.num_tiles = static_cast<int>(num_tiles);
+  p.group_m = 8;
+  p.c_vec4 = (a.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
+  p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
+  p.status = d.status;
+  CUtensorMap tmA, tmB, tmAs, tmBs;   // all K-major [128 rows][32 k] boxes, 128-byte swizzle
+  if (!encode_tmap(&tmA, A_big, a.M, a.K, lda_big, 32, 128, true) ||
+      !encode_tmap(&tmAs, a_small, a.M, a.K, ldk, 32, 128, true) ||
+      !encode_tmap(&tmB, B_big, a.N, a.K, ldb_big, 32, 128, true) ||
+      !encode_tmap(&tmBs, b_small, a.N, a.K, ldk, 32, 128, true))
+    return SGEMM_ERR_LAUNCH;
+  const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
+  const int grid = static_cast<int>(num_tiles < slots ? num_tiles : slots);
+  if (tc3_presplit_entry().launch(p, &tmA, &tmB, &tmAs, &tmBs, grid, s, false) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
+  t_last_launches = 3;
+  if (order_after_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
   return SGEMM_SUCCESS;
 }
 
@@ -612,6 +707,11 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
       // (they pass through its raw ring, which decouples TMA from the MMA
       // stages), so large products transpose k-contiguous operands ahead too
       const Pretranspose t = pretranspose_plan(a, d->sm_count, 128);
+      // large products: split ahead (K % 4 == 0 keeps the split pass vectorised)
+      if (SG_TC_PRESPLIT && presplit_size_ok(a, d->sm_count) && a.K % 4 == 0) {
+        const sgemm_status_t st = run_tc3_presplit(a, *d, s);
+        if (st != SGEMM_ERR_UNSUPPORTED) return st;
+      }
       if (t.a || t.b) {
         const sgemm_status_t st = run_pretransposed(a, *d, s, t, true);
         if (st != SGEMM_ERR_UNSUPPORTED) return st;

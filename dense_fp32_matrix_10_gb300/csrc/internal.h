@@ -64,14 +64,20 @@ SimtEntry simt_entry(int producer, int transA, int transB, int tile);
 struct TcKernelInfo {
   int bm, bn, ctas_per_sm;
 };
-using TcLaunchFn = cudaError_t (*)(const TcParams &, const CUtensorMap *, const CUtensorMap *, int,
-                                   cudaStream_t, bool pdl);
+// Maps: op(A), op(B), and -- for the pre-split form only -- A's and B's small
+// parts (K-major); the other forms ignore the last two.
+using TcLaunchFn = cudaError_t (*)(const TcParams &, const CUtensorMap *, const CUtensorMap *,
+                                   const CUtensorMap *, const CUtensorMap *, int, cudaStream_t,
+                                   bool pdl);
 using TcInfoFn = cudaError_t (*)(TcKernelInfo *);
 struct TcEntry {
   TcLaunchFn launch;
   TcInfoFn info;
 };
 TcEntry tc3_entry(int transA, int transB);
+// The form that reads pre-split operands: A and B k-contiguous big parts plus
+// their small parts, all through TMA (no conversion in the kernel).
+TcEntry tc3_presplit_entry();
 
 // Second pass of a stream-K launch (sk_fixup.cu).
 cudaError_t launch_sk_fixup(const SimtParams &p, int bm, int bn, int grid_main, int sk_tiles,
@@ -94,6 +100,14 @@ cudaError_t launch_scale_c(float *C, int64_t ldc, int M, int N, float beta, cuda
 // `status` is the device status word the bounded waits report to.
 cudaError_t launch_transpose(const float *in, int64_t ld_in, float *out, int64_t ld_out, int rows,
                              int cols, int sm_count, int *status, cudaStream_t s);
+// The split pass of the 3xTF32 product (transpose.cu): the TF32 small parts of
+// a rows x cols operand (k along each row when !transpose, down the columns
+// when transpose), written K-major to `small` (ld_out); with `transpose` the
+// operand is also written transposed to `big` (its TF32 big parts).  *done is false when the pass
+// could not run (then nothing was queued).
+cudaError_t launch_tf32_split(const float *in, int64_t ld_in, int rows, int cols, bool transpose,
+                              float *big, float *small, int64_t ld_out, int sm_count, int *status,
+                              cudaStream_t s, bool *done);
 cudaError_t launch_scale_c_batched(float *C, int64_t ldc, int64_t strideC, int M, int N,
                                    int64_t batch, float beta, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint64_t budget_ns, int *status, cudaStream_t s);

@@ -335,4 +335,21 @@ __device__ __forceinline__ float tf32_trunc(float x) {
   return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
+// ---------------------------------------------------------------- 3xTF32 split
+// Big and small TF32 parts of two values at once: big = x with its low 13
+// mantissa bits cleared; small = x - big (exact in FP32, one packed FMA for
+// the pair) rounded to the nearest TF32 value, ties away from zero -- adding
+// half of the last kept bit (1 << 12) to the magnitude bits and clearing the
+// low 13 bits does exactly that, subnormals included; small = 0 when x is not
+// finite, which is exactly when x - big is NaN.
+__device__ __forceinline__ void split_pair(float x0, float x1, float &b0, float &b1, float &s0,
+                                           float &s1) {
+  b0 = __uint_as_float(__float_as_uint(x0) & 0xFFFFE000u);
+  b1 = __uint_as_float(__float_as_uint(x1) & 0xFFFFE000u);
+  const float2 d = __ffma2_rn(make_float2(b0, b1), make_float2(-1.0f, -1.0f), make_float2(x0, x1));
+  const float r0 = __uint_as_float((__float_as_uint(d.x) + 0x1000u) & 0xFFFFE000u);
+  const float r1 = __uint_as_float((__float_as_uint(d.y) + 0x1000u) & 0xFFFFE000u);
+  s0 = (d.x == d.x) ? r0 : 0.0f;
+  s1 = (d.y == d.y) ? r1 : 0.0f;
+}
 }  // namespace sg

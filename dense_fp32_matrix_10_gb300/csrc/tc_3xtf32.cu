@@ -7,9 +7,10 @@ namespace sg {
 
 template <class Cfg>
 static cudaError_t tc3_launch(const TcParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
-                              int grid, cudaStream_t stream, bool pdl) {
+                              const CUtensorMap *tmAs, const CUtensorMap *tmBs, int grid,
+                              cudaStream_t stream, bool pdl) {
   return launch_maybe_pdl(tc3_gemm_kernel<Cfg>, dim3(grid), dim3(Cfg::THREADS), Cfg::SMEM_BYTES,
-                          stream, pdl, *tmA, *tmB, p);
+                          stream, pdl, *tmA, *tmB, *tmAs, *tmBs, p);
 }
 
 template <class Cfg>
@@ -35,11 +36,13 @@ static cudaError_t tc3_info(TcKernelInfo *info) {
   return cudaSuccess;
 }
 
-template <bool AK, bool BK>
+template <bool AK, bool BK, bool PRESPLIT = false>
 static TcEntry tc3_make() {
-  using Cfg = TcConfig<AK, BK>;
+  using Cfg = TcConfig<AK, BK, PRESPLIT>;
   return TcEntry{&tc3_launch<Cfg>, &tc3_info<Cfg>};
 }
+
+TcEntry tc3_presplit_entry() { return tc3_make<true, true, true>(); }
 
 TcEntry tc3_entry(int transA, int transB) {
   // A stored M x K (transA = N) and B stored N x K (transB = T) are k-contiguous.

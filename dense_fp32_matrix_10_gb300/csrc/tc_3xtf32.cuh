@@ -74,10 +74,15 @@ struct TcParams {
   int *status;
 };
 
-template <bool A_KMAJOR_, bool B_KMAJOR_>
+template <bool A_KMAJOR_, bool B_KMAJOR_, bool PRESPLIT_ = false>
 struct TcConfig {
   static constexpr bool A_KMAJOR = A_KMAJOR_;
   static constexpr bool B_KMAJOR = B_KMAJOR_;
+  // PRESPLIT: the small parts come from global memory (written by a split
+  // pass before the launch) and land in the stage by TMA like the big parts;
+  // the converter warps have nothing to do.
+  static constexpr bool PRESPLIT = PRESPLIT_;
+  static_assert(!PRESPLIT || (A_KMAJOR && B_KMAJOR), "pre-split operands are K-major");
   static constexpr int BM = 128, BN = 128, BK = 32;
   static constexpr int TILE_BYTES = 128 * 32 * 4;  // one 128 x 32 FP32 tile
   // A_TMEM: an m-contiguous A (through the raw ring) is converted straight
@@ -148,10 +153,12 @@ struct TcBars {
 // ------------------------------------------------------------------ producer
 template <class Cfg>
 __device__ __forceinline__ void tc_produce(const TcParams &p, const CUtensorMap *tmA,
-                                           const CUtensorMap *tmB, uint32_t sbase,
+                                           const CUtensorMap *tmB, const CUtensorMap *tmAs,
+                                           const CUtensorMap *tmBs, uint32_t sbase,
                                            const TcBars<Cfg> &bar) {
   constexpr bool ANY_K = Cfg::A_KMAJOR || Cfg::B_KMAJOR;
-  constexpr uint32_t K_BYTES = ((Cfg::A_KMAJOR ? 1 : 0) + (Cfg::B_KMAJOR ? 1 : 0)) * Cfg::TILE_BYTES;
+  constexpr uint32_t K_BYTES =
+      ((Cfg::A_KMAJOR ? 1 : 0) + (Cfg::B_KMAJOR ? 1 : 0)) * Cfg::TILE_BYTES * (Cfg::PRESPLIT ? 2 : 1);
   uint32_t it = 0;        // k-slices whose copies are all issued
   bool k_issued = false;  // the k-contiguous part of slice `it` is issued
   bool ok = true;
@@ -172,6 +179,10 @@ __device__ __forceinline__ void tc_produce(const TcParams &p, const CUtensorMap 
         mbar_arrive_expect_tx(bar.full(s), K_BYTES);
         if (Cfg::A_KMAJOR) tma_load_2d(st + Cfg::A_BIG, tmA, bar.full(s), k0, m0);
         if (Cfg::B_KMAJOR) tma_load_2d(st + Cfg::B_BIG, tmB, bar.full(s), k0, n0);
+        if (Cfg::PRESPLIT) {
+          tma_load_2d(st + Cfg::A_SMALL, tmAs, bar.full(s), k0, m0);
+          tma_load_2d(st + Cfg::B_SMALL, tmBs, bar.full(s), k0, n0);
+        }
         k_issued = true;
       }
       if (Cfg::RAW_OPERANDS) {  // m/n-contiguous operands into the raw ring
@@ -210,22 +221,6 @@ __device__ __forceinline__ float small_part(float x, float big) {
   return isfinite(x) ? to_tf32(x - big) : 0.0f;
 }
 
-// Big and small TF32 parts of two values at once: big = x with its low 13
-// mantissa bits cleared; small = x - big (exact in FP32, one packed FMA for
-// the pair) rounded to the nearest TF32 value, ties away from zero -- adding
-// half of the last kept bit (1 << 12) to the magnitude bits and clearing the
-// low 13 bits does exactly that, subnormals included; small = 0 when x is not
-// finite, which is exactly when x - big is NaN.
-__device__ __forceinline__ void split_pair(float x0, float x1, float &b0, float &b1, float &s0,
-                                           float &s1) {
-  b0 = __uint_as_float(__float_as_uint(x0) & 0xFFFFE000u);
-  b1 = __uint_as_float(__float_as_uint(x1) & 0xFFFFE000u);
-  const float2 d = __ffma2_rn(make_float2(b0, b1), make_float2(-1.0f, -1.0f), make_float2(x0, x1));
-  const float r0 = __uint_as_float((__float_as_uint(d.x) + 0x1000u) & 0xFFFFE000u);
-  const float r1 = __uint_as_float((__float_as_uint(d.y) + 0x1000u) & 0xFFFFE000u);
-  s0 = (d.x == d.x) ? r0 : 0.0f;
-  s1 = (d.y == d.y) ? r1 : 0.0f;
-}
 #ifndef SG_TC_SPLIT_PAIR
 #define SG_TC_SPLIT_PAIR 1
 #endif
@@ -319,6 +314,7 @@ __device__ __forceinline__ void tc_convert(const TcParams &p, unsigned char *sme
                                            const TcBars<Cfg> &bar, uint32_t tmem_base, int ct,
                                            int warp, int lane) {
   constexpr bool ANY_K = Cfg::A_KMAJOR || Cfg::B_KMAJOR;
+  if (Cfg::PRESPLIT) return;   // the split pass did their work
   uint32_t it = 0;
   for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
     for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
@@ -379,7 +375,8 @@ __device__ __forceinline__ void tc_issue(const TcParams &p, uint32_t sbase, uint
       const int kc1 = min(kc0 + Cfg::CHUNK_KTILES, p.k_tiles);
       for (int kt = kc0; kt < kc1; ++kt, ++it) {
         const uint32_t s = it % Cfg::STAGES, round = it / Cfg::STAGES;
-        if (!wait_parity_bounded(bar.conv_full(s), round & 1, p.wait_budget_ns, p.status)) {
+        if (!wait_parity_bounded(Cfg::PRESPLIT ? bar.full(s) : bar.conv_full(s), round & 1,
+                                 p.wait_budget_ns, p.status)) {
           ok = false;
           break;
         }
@@ -482,6 +479,7 @@ __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_bas
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc3_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmAs, const __grid_constant__ CUtensorMap tmBs,
                     const TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -509,6 +507,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (Cfg::PRESPLIT) {
+      tma_prefetch_desc(&tmAs);
+      tma_prefetch_desc(&tmBs);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
   tc_fence_before_sync();
@@ -523,7 +525,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::REGS_WG0));
     if (warp == 0) {
-      if (lane == 0) tc_produce<Cfg>(p, &tmA, &tmB, sbase, bar);
+      if (lane == 0) tc_produce<Cfg>(p, &tmA, &tmB, &tmAs, &tmBs, sbase, bar);
       __syncwarp();
     } else if (warp == 1) {
       if (lane == 0) tc_issue<Cfg>(p, sbase, tmem_base, bar);

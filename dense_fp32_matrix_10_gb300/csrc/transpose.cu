@@ -22,6 +22,7 @@
 //
 // Roofline: HBM, 2 * rows * cols * 4 bytes per launch.
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "dispatch.h"
@@ -147,10 +148,19 @@ __global__ void __launch_bounds__(kWarps * 32) transpose_kernel(const TransposeP
 // (96 KiB) per CTA, two CTAs per SM.
 constexpr int kTmRows = 128, kTmCols = 32;
 constexpr int kTmTileBytes = kTmRows * kTmCols * 4;   // 16 KiB, same for in and out
-constexpr int kTmInStages = 4, kTmOutStages = 2;
+constexpr int kTmOutStages = 2;
 constexpr int kTmConsumers = 128;                     // warps 1..4
 constexpr int kTmThreads = 32 + kTmConsumers;
-constexpr int kTmSmem = (kTmInStages + kTmOutStages) * kTmTileBytes + 1024 /*align*/ + 64 /*barriers*/;
+// SPLIT: the split pass of the 3xTF32 product -- besides the transposed
+// values (which serve as the TF32 big parts) each output tile gets a twin
+// holding the small parts; one input stage fewer keeps two CTAs per SM.
+template <bool SPLIT>
+struct TmShape {
+  static constexpr int IN_STAGES = SPLIT ? 3 : 4;
+  static constexpr int OUT_TILES = SPLIT ? 2 : 1;   // per output stage
+  static constexpr int SMEM = (IN_STAGES + kTmOutStages * OUT_TILES) * kTmTileBytes + 1024 /*align*/ +
+                              64 /*barriers*/;
+};
 #ifndef SG_TRANSPOSE_TMA_GROUP
 #define SG_TRANSPOSE_TMA_GROUP 8
 #endif
@@ -176,14 +186,17 @@ __device__ __forceinline__ void tma_tile_origin(const TmaTransposeParams &p, int
   c0 = static_cast<int>(tc * kTmCols);
 }
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(kTmThreads) transpose_tma_kernel(const __grid_constant__ CUtensorMap in_map,
                                                                    const __grid_constant__ CUtensorMap out_map,
+                                                                   const __grid_constant__ CUtensorMap small_map,
                                                                    const TmaTransposeParams p) {
+  constexpr int kTmInStages = TmShape<SPLIT>::IN_STAGES, OUT_TILES = TmShape<SPLIT>::OUT_TILES;
   griddep_launch_dependents();   // a product that reads our output may be scheduled
   extern __shared__ unsigned char smem_raw[];
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;   // 128-byte swizzle wants 1 KiB
   const uint32_t in0 = base, out0 = base + kTmInStages * kTmTileBytes;
-  const uint32_t bars = out0 + kTmOutStages * kTmTileBytes;
+  const uint32_t bars = out0 + kTmOutStages * OUT_TILES * kTmTileBytes;
   const uint32_t full0 = bars, empty0 = bars + 8 * kTmInStages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -194,6 +207,7 @@ __global__ void __launch_bounds__(kTmThreads) transpose_tma_kernel(const __grid_
     fence_mbar_init();
     tma_prefetch_desc(&in_map);
     tma_prefetch_desc(&out_map);
+    if (SPLIT) tma_prefetch_desc(&small_map);
   }
   __syncthreads();
 
@@ -228,7 +242,7 @@ __global__ void __launch_bounds__(kTmThreads) transpose_tma_kernel(const __grid_
     if (ct == 0) bulk_wait_group_read<kTmOutStages - 1>();
     if (!bar_and(1, kTmConsumers, ok)) break;   // all consumers leave together
     const uint32_t src = in0 + s * kTmTileBytes + ct * 128;
-    const uint32_t dst = out0 + o * kTmTileBytes + ct * 4;
+    const uint32_t dst = out0 + o * OUT_TILES * kTmTileBytes + ct * 4;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float4 v = lds128(src + ((j ^ (ct & 7)) << 4));
@@ -237,6 +251,16 @@ __global__ void __launch_bounds__(kTmThreads) transpose_tma_kernel(const __grid_
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + (4 * j + 1) * 512), "f"(v.y) : "memory");
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + (4 * j + 2) * 512), "f"(v.z) : "memory");
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + (4 * j + 3) * 512), "f"(v.w) : "memory");
+      if (SPLIT) {   // the small parts into the twin tile
+        float b0, b1, b2, b3, s0, s1, s2, s3;
+        split_pair(v.x, v.y, b0, b1, s0, s1);
+        split_pair(v.z, v.w, b2, b3, s2, s3);
+        const uint32_t d2 = dst + kTmTileBytes;
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(d2 + (4 * j + 0) * 512), "f"(s0) : "memory");
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(d2 + (4 * j + 1) * 512), "f"(s1) : "memory");
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(d2 + (4 * j + 2) * 512), "f"(s2) : "memory");
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(d2 + (4 * j + 3) * 512), "f"(s3) : "memory");
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
@@ -245,31 +269,43 @@ __global__ void __launch_bounds__(kTmThreads) transpose_tma_kernel(const __grid_
     if (ct == 0) {
       int r0, c0;
       tma_tile_origin(p, t, r0, c0);
-      tma_store_2d(&out_map, out0 + o * kTmTileBytes, r0, c0);   // out: x = input row, y = input col
+      const uint32_t ob = out0 + o * OUT_TILES * kTmTileBytes;
+      tma_store_2d(&out_map, ob, r0, c0);   // out: x = input row, y = input col
+      if (SPLIT) tma_store_2d(&small_map, ob + kTmTileBytes, r0, c0);
       bulk_commit_group();
     }
   }
   if (ct == 0) bulk_wait_group_all();
 }
 
-// Per device: dynamic shared memory of the TMA form set once.
-std::once_flag g_tma_attr_once[kMaxDevices];
-cudaError_t g_tma_attr_err[kMaxDevices];
+// Per device and form: dynamic shared memory set once, CTAs per SM.
+std::once_flag g_tma_attr_once[2][kMaxDevices];
+cudaError_t g_tma_attr_err[2][kMaxDevices];
+int g_tma_ctas[2][kMaxDevices];
 
-cudaError_t launch_transpose_tma(const float *in, int64_t ld_in, float *out, int64_t ld_out, int rows,
-                                 int cols, int sm_count, int *status, cudaStream_t s, bool *used) {
+template <bool SPLIT>
+cudaError_t launch_transpose_tma(const float *in, int64_t ld_in, float *out, float *small,
+                                 int64_t ld_out, int rows, int cols, int sm_count, int *status,
+                                 cudaStream_t s, bool *used) {
   *used = false;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaGetLastError();
-  std::call_once(g_tma_attr_once[dev], [dev]() {
-    g_tma_attr_err[dev] = cudaFuncSetAttribute(transpose_tma_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kTmSmem);
-    if (g_tma_attr_err[dev] != cudaSuccess) cudaGetLastError();
+  std::call_once(g_tma_attr_once[SPLIT][dev], [dev]() {
+    cudaError_t &e = g_tma_attr_err[SPLIT][dev];
+    e = cudaFuncSetAttribute(transpose_tma_kernel<SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TmShape<SPLIT>::SMEM);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_tma_ctas[SPLIT][dev], transpose_tma_kernel<SPLIT>,
+                                                        kTmThreads, TmShape<SPLIT>::SMEM);
+    if (e == cudaSuccess && g_tma_ctas[SPLIT][dev] < 1) e = cudaErrorInvalidConfiguration;
+    if (e != cudaSuccess) cudaGetLastError();
   });
-  if (g_tma_attr_err[dev] != cudaSuccess) return cudaSuccess;   // not used: caller takes the other form
-  CUtensorMap in_map, out_map;
+  if (g_tma_attr_err[SPLIT][dev] != cudaSuccess) return cudaSuccess;   // not used: caller decides
+  CUtensorMap in_map, out_map, small_map;
+  std::memset(&small_map, 0, sizeof(small_map));
   if (!encode_tmap(&in_map, in, rows, cols, ld_in, kTmCols, kTmRows, true) ||
-      !encode_tmap(&out_map, out, cols, rows, ld_out, kTmRows, kTmCols, false))
+      !encode_tmap(&out_map, out, cols, rows, ld_out, kTmRows, kTmCols, false) ||
+      (SPLIT && !encode_tmap(&small_map, small, cols, rows, ld_out, kTmRows, kTmCols, false)))
     return cudaSuccess;                                            // likewise
   TmaTransposeParams p;
   p.rows = rows;
@@ -279,11 +315,29 @@ cudaError_t launch_transpose_tma(const float *in, int64_t ld_in, float *out, int
   p.num_tiles = static_cast<int64_t>(p.tiles_r) * p.tiles_c;
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   p.status = status;
-  const int64_t slots = static_cast<int64_t>(sm_count) * 2;
+  const int64_t slots = static_cast<int64_t>(sm_count) * g_tma_ctas[SPLIT][dev];
   const int64_t grid = p.num_tiles < slots ? p.num_tiles : slots;
-  transpose_tma_kernel<<<static_cast<unsigned>(grid), kTmThreads, kTmSmem, s>>>(in_map, out_map, p);
+  transpose_tma_kernel<SPLIT><<<static_cast<unsigned>(grid), kTmThreads, TmShape<SPLIT>::SMEM, s>>>(
+      in_map, out_map, small_map, p);
   *used = true;
   return cudaGetLastError();
+}
+
+// Small TF32 parts of a k-contiguous operand, elementwise: out[r][c] =
+// small(in[r][c]) (16-byte rows on both sides).
+__global__ void __launch_bounds__(256) tf32_small_kernel(const float *in, int64_t ld_in, float *out,
+                                                         int64_t ld_out, int rows, int cols4) {
+  griddep_launch_dependents();
+  const int64_t total = static_cast<int64_t>(rows) * cols4;
+  for (int64_t e = blockIdx.x * 256ll + threadIdx.x; e < total; e += static_cast<int64_t>(gridDim.x) * 256) {
+    const int64_t r = e / cols4, c = 4 * (e - r * cols4);
+    const float4 x = __ldcs(reinterpret_cast<const float4 *>(in + r * ld_in + c));
+    float4 sm;
+    float b0, b1, b2, b3;
+    split_pair(x.x, x.y, b0, b1, sm.x, sm.y);
+    split_pair(x.z, x.w, b2, b3, sm.z, sm.w);
+    *reinterpret_cast<float4 *>(out + r * ld_out + c) = sm;
+  }
 }
 
 }  // namespace
@@ -299,7 +353,8 @@ cudaError_t launch_transpose(const float *in, int64_t ld_in, float *out, int64_t
                        (ld_out % 4 == 0);
   if (SG_TRANSPOSE_TMA && aligned) {
     bool used = false;
-    const cudaError_t e = launch_transpose_tma(in, ld_in, out, ld_out, rows, cols, sm_count, status, s, &used);
+    const cudaError_t e =
+        launch_transpose_tma<false>(in, ld_in, out, nullptr, ld_out, rows, cols, sm_count, status, s, &used);
     if (used || e != cudaSuccess) return e;
   }
   TransposeParams p;
@@ -317,6 +372,27 @@ cudaError_t launch_transpose(const float *in, int64_t ld_in, float *out, int64_t
   const int64_t grid = p.num_tiles < slots ? p.num_tiles : slots;
   transpose_kernel<<<static_cast<unsigned>(grid), kWarps * 32, 0, s>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_tf32_split(const float *in, int64_t ld_in, int rows, int cols, bool transpose,
+                              float *big, float *small, int64_t ld_out, int sm_count, int *status,
+                              cudaStream_t s, bool *done) {
+  *done = false;
+  if (transpose) {
+    bool used = false;
+    const cudaError_t e =
+        launch_transpose_tma<true>(in, ld_in, big, small, ld_out, rows, cols, sm_count, status, s, &used);
+    *done = used && e == cudaSuccess;
+    return e;
+  }
+  const int cols4 = cols / 4;   // cols % 4 == 0 for the tensor-core layouts
+  const int64_t total = static_cast<int64_t>(rows) * cols4;
+  int64_t grid = (total + 255) / 256;
+  if (grid > sm_count * 8ll) grid = sm_count * 8ll;
+  tf32_small_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(in, ld_in, small, ld_out, rows, cols4);
+  const cudaError_t e = cudaGetLastError();
+  *done = e == cudaSuccess;
+  return e;
 }
 
 }  // namespace sg

@@ -111,7 +111,9 @@ typedef enum sgemm_algo {
                                   ring with 4-byte cp.async.  Any alignment/ld. */
   SGEMM_ALGO_TC_3XTF32 = 3,    /* tcgen05 tensor cores, TMEM accumulator, each
                                   FP32 operand split into two TF32 parts and
-                                  three products accumulated. */
+                                  three products accumulated.  Large products
+                                  split both operands ahead into library
+                                  scratch (two extra launches). */
   SGEMM_ALGO_NAIVE = 4,        /* one thread per output, operands read straight
                                   from global memory (the pages' first kernel;
                                   for comparison only) */

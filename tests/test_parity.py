@@ -372,9 +372,10 @@ def test_pretransposed_matches_tn_bit_for_bit(shape, op):
 
 @pytest.mark.parametrize("op", [(0, 0), (0, 1), (1, 1)], ids=["NN", "NT", "TT"])
 def test_tensor_core_pretransposed_matches_tn_bit_for_bit(op):
-    """The 3xTF32 kernel, too, runs large NN / NT / TT products in the TN
-    layout after transposing k-contiguous operands ahead: bit-identical to
-    the TN call on operands transposed by torch."""
+    """Large 3xTF32 products split both operands ahead (a pass per operand,
+    transposing an m/n-contiguous one to K-major) and run the converter-free
+    kernel: NN / NT / TT must equal, bit for bit, the TN call on operands
+    transposed by torch, and take three launches."""
     M, N, K = 2048, 2560, 512
     ta, tb = op
     g = torch.Generator().manual_seed(11 + 2 * ta + tb)
@@ -389,7 +390,7 @@ def test_tensor_core_pretransposed_matches_tn_bit_for_bit(op):
     sg.gemm(At, Bn, C2, 1.0, 0.0, 1, 0, algo="tc_3xtf32")
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
-    assert n1 == 1 + (ta == 0) + (tb == 1)
+    assert n1 == 3 and sg.sgemm_last_launch_count() == 3
 
 
 def test_pretransposed_on_two_streams(orc):
