@@ -393,6 +393,30 @@ def test_tensor_core_pretransposed_matches_tn_bit_for_bit(op):
     assert n1 == 3 and sg.sgemm_last_launch_count() == 3
 
 
+@pytest.mark.parametrize("op", [(0, 0), (1, 1)], ids=["NN", "TT"])
+def test_tensor_core_split_ahead_ragged(orc, op):
+    """Split ahead on a product whose M and N end in partial tiles, with alpha
+    and beta (C read): sampled outputs against the oracle; and a TMA-eligible
+    product with K % 4 != 0 (rows padded), which keeps the in-kernel split."""
+    ta, tb = op
+    for (M, N, K, pad) in [(2000, 2504, 1004, 0), (2048, 2560, 1002, 2)]:
+        g = torch.Generator().manual_seed(M + K + ta)
+        A = torch.rand((K, M) if ta else (M, K), generator=g).mul_(2).sub_(1)
+        B = torch.rand((N, K) if tb else (K, N), generator=g).mul_(2).sub_(1)
+        C0 = torch.rand(M, N, generator=g).mul_(2).sub_(1)
+        dA = padded(A.cuda(), pad) if not ta else A.cuda()
+        dB = padded(B.cuda(), pad) if tb else B.cuda()
+        dC = C0.cuda()
+        sg.gemm(dA, dB, dC, 1.25, -0.5, ta, tb, algo="tc_3xtf32")
+        n = sg.sgemm_last_launch_count()
+        torch.cuda.synchronize()
+        assert n == (3 if K % 4 == 0 else n)
+        I, J = sample_indices(M, N, 3000, seed=M)
+        R = orc.sgemm_entries_f64(ta, tb, 1.25, A.numpy(), B.numpy(), -0.5, C0.numpy(), I, J)
+        G = dC.cpu().numpy()[I, J]
+        assert_close(G, R, K, f"tc split ahead {M}x{N}x{K} {op}")
+
+
 def test_pretransposed_on_two_streams(orc):
     """Calls on different streams share the transposed-operand scratch; the
     library orders them, so every result is right."""
