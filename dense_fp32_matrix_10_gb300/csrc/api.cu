@@ -196,14 +196,23 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 #ifndef SG_SIMT_WIDE_TILE
 #define SG_SIMT_WIDE_TILE 1
 #endif
+// SG_WIDE_MIN_FILL_PCT: the 128 x 256 tile (and with it the transpose ahead)
+// is used once that many percent of the SMs get a whole tile; stream-K spreads
+// the rest.  Measured on GB300 (graph-timed): requiring a full wave left
+// 2048^3 on 128 x 128 tiles (NN 58.3, NT 54.5, TN 59.3 TFLOP/s); from 75 %
+// down to 25 % it runs wide (60.7 / 59.1 / 63.2), 3072^3 and larger
+// unchanged, 1536^3 (47 %) slightly faster.
+#ifndef SG_WIDE_MIN_FILL_PCT
+#define SG_WIDE_MIN_FILL_PCT 40
+#endif
 int pick_simt_tile(const Args &a, int producer, int sm_count) {
   if (a.N <= 64) return kTile128x64;
   // the math warps read A m-contiguous when it is stored K x M, or when the
   // TMA producer transposes a k-contiguous A in shared memory
   const bool a_mn_in_smem = a.ta == 1 || (producer == kTma && SG_SIMT_TRANSPOSE_A);
-  // the wide tile only once it gives every SM at least one whole tile: below
-  // that, stream-K would cut its k-loop into short, fixup-heavy segments
-  const bool fills = cdiv(a.M, 128) * cdiv(a.N, 256) >= sm_count;
+  // the wide tile only once enough SMs get a whole tile: far below that,
+  // stream-K would cut its k-loop into short, fixup-heavy segments
+  const bool fills = cdiv(a.M, 128) * cdiv(a.N, 256) * 100 >= SG_WIDE_MIN_FILL_PCT * sm_count;
   if (SG_SIMT_WIDE_TILE && producer == kTma && a_mn_in_smem && a.tb == 0 && fills) return kTile128x256;
   return kTile128x128;
 }
@@ -427,7 +436,8 @@ Pretranspose pretranspose_plan(const Args &a, int sm_count, int64_t tile_n) {
   // only where the transposed product fills the GPU with 128 x 256 tiles:
   // below that both layouts run 128 x 128 tiles and the extra launch loses
   // (measured at 2048^3 NN: 57.4 in-kernel vs 56.2 TFLOP/s transposed ahead)
-  if (cdiv(a.M, 128) * cdiv(a.N, tile_n) < sm_count) return t;
+  if (cdiv(a.M, 128) * cdiv(a.N, tile_n) * 100 < (tile_n == 256 ? SG_WIDE_MIN_FILL_PCT : 100) * sm_count)
+    return t;
   t.a = a.ta == 0 && a.N >= kPretransposeMinOther;
   t.b = a.tb == 1 && a.M >= kPretransposeMinOther;
   return t;

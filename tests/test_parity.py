@@ -345,7 +345,7 @@ def test_pretransposed_matches_tn_bit_for_bit(shape, op):
     per SM) have their k-contiguous operand(s) transposed into scratch first
     and then run as TN: the result must equal, bit for bit, the TN call on
     operands transposed by torch (same kernel, same tiles, same k order), with
-    one extra launch per transposed operand (2048^3 stays in-kernel)."""
+    one extra launch per transposed operand."""
     M, N, K = shape
     ta, tb = op
     g = torch.Generator().manual_seed(M + N + K + 2 * ta + tb)
@@ -365,8 +365,9 @@ def test_pretransposed_matches_tn_bit_for_bit(shape, op):
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
     # only TMA-eligible layouts (16-byte rows) of GPU-filling size
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     eligible = (A.stride(0) % 4 == 0 and B.stride(0) % 4 == 0 and M * N * K >= 2 ** 30
-                and -(-M // 128) * -(-N // 256) >= torch.cuda.get_device_properties(0).multi_processor_count)
+                and -(-M // 128) * -(-N // 256) * 100 >= 40 * sms)
     assert n1 == n2 + eligible * ((ta == 0 and N >= 1024) + (tb == 1 and M >= 1024))
 
 
