@@ -414,9 +414,24 @@ constexpr int64_t kPretransposeMinOther = 1024;        // the other dimension
 constexpr int64_t kPretransposeMinWork = int64_t(1) << 30;   // M * N * K
 constexpr size_t kPretransposeMaxBytes = size_t(2) << 30;    // 2 GiB of scratch
 
+// Operands copied into library scratch ahead of the product: transposed
+// (a, b), or repacked into 16-byte aligned rows (ra, rb) so that the TMA
+// producer can load them.
 struct Pretranspose {
   bool a, b;
+  bool ra = false, rb = false;
+  bool any() const { return a || b || ra || rb; }
 };
+// Repacking: AUTO runs a product whose A or B is not TMA-eligible (base not
+// 16-byte aligned, or a leading dimension not a multiple of 4) on the TMA
+// path after copying that operand into aligned scratch, once M * N * K
+// reaches this: the cp.async producer moves 4 bytes per instruction and is
+// far slower (GB300, NN, TFLOP/s in place -> repacked: 767 x 769 x 771
+// 16.2 -> 21.0, 2047 x 2049 x 2051 23.9 -> 50.6; below about 2^27 the extra
+// launch costs more than it saves: 383 x 385 x 387 4.5 -> 3.7).
+#ifndef SG_REPACK_MIN_WORK
+#define SG_REPACK_MIN_WORK (int64_t(1) << 27)
+#endif
 // The tensor-core product after a transpose is launched the ordinary way:
 // as a programmatic dependent it ran slower (4096^3 NN 140.8 vs 167.8
 // TFLOP/s on GB300), while the CUDA-core kernel gains a little from it.
@@ -428,9 +443,9 @@ sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream, bool 
 
 // tile_n: the N extent of the tiles the transposed product runs with (256
 // for the CUDA-core kernel's wide tile, 128 for the tensor-core kernel).
-Pretranspose pretranspose_plan(const Args &a, int sm_count, int64_t tile_n) {
+Pretranspose transpose_plan_any(const Args &a, int sm_count, int64_t tile_n) {
   Pretranspose t{false, false};
-  if (!SG_PRETRANSPOSE || !tma_eligible(a)) return t;
+  if (!SG_PRETRANSPOSE) return t;
   const double work = static_cast<double>(a.M) * static_cast<double>(a.N) * static_cast<double>(a.K);
   if (work < static_cast<double>(kPretransposeMinWork)) return t;
   // only where the transposed product fills the GPU with 128 x 256 tiles:
@@ -444,6 +459,27 @@ Pretranspose pretranspose_plan(const Args &a, int sm_count, int64_t tile_n) {
 }
 
 int64_t round4(int64_t x) { return (x + 3) & ~int64_t(3); }
+
+Pretranspose pretranspose_plan(const Args &a, int sm_count, int64_t tile_n) {
+  return tma_eligible(a) ? transpose_plan_any(a, sm_count, tile_n) : Pretranspose{false, false};
+}
+
+bool a_tma_ok(const Args &a) { return reinterpret_cast<uintptr_t>(a.A) % 16 == 0 && a.lda % 4 == 0; }
+bool b_tma_ok(const Args &a) { return reinterpret_cast<uintptr_t>(a.B) % 16 == 0 && a.ldb % 4 == 0; }
+
+// AUTO on operands that are not TMA-eligible: large enough products copy
+// each offending operand into aligned scratch -- transposed where the plan
+// transposes it anyway, else repacked as it is (same values, same layout).
+bool repack_wanted(const Args &a) {
+  const double work = static_cast<double>(a.M) * static_cast<double>(a.N) * static_cast<double>(a.K);
+  return !tma_eligible(a) && work >= static_cast<double>(SG_REPACK_MIN_WORK);
+}
+Pretranspose repack_plan(const Args &a, int sm_count) {
+  Pretranspose t = transpose_plan_any(a, sm_count, 256);
+  t.ra = !t.a && !a_tma_ok(a);
+  t.rb = !t.b && !b_tma_ok(a);
+  return t;
+}
 
 // Products large enough for the split pass of the tensor-core path: the size
 // rule of pretranspose_plan with 128 x 128 tiles, any layout.
@@ -464,23 +500,26 @@ float *pretranspose_scratch(DeviceState &d, size_t bytes, bool capturing) {
     return nullptr;
   }
   if (bytes > d.tr_bytes) {
-    // a captured graph holds the current buffer's address: once one exists
-    // the buffer is never freed or moved (larger products then take the
-    // in-kernel transpose)
-    if (d.tr_order.in_graph) return nullptr;
     const size_t step = size_t(64) << 20;
-    const size_t want = (bytes + step - 1) / step * step;
-    if (d.tr) {
+    size_t want = (bytes + step - 1) / step * step;
+    // a captured graph holds the current buffer's address: once one exists
+    // the buffer is kept for good and a new one taken (at least twice as
+    // large, so that the kept buffers add up to less than the live one)
+    const bool keep = d.tr_order.in_graph && d.tr;
+    if (keep && want < 2 * d.tr_bytes) want = 2 * d.tr_bytes;
+    if (want > kPretransposeMaxBytes) want = bytes;
+    float *fresh = nullptr;
+    if (cudaMalloc(&fresh, want) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;   // not fatal: this product runs on its operands in place
+    }
+    if (keep) {
+      d.tr_retired.push_back(d.tr);
+    } else if (d.tr) {
       // cudaFree waits for work still using the old buffer
       cudaFree(d.tr);
-      d.tr = nullptr;
-      d.tr_bytes = 0;
     }
-    if (cudaMalloc(&d.tr, want) != cudaSuccess) {
-      cudaGetLastError();
-      d.tr = nullptr;
-      return nullptr;   // not fatal: this product takes the in-kernel transpose
-    }
+    d.tr = fresh;
     d.tr_bytes = want;
   }
   return d.tr;
@@ -491,10 +530,14 @@ float *pretranspose_scratch(DeviceState &d, size_t bytes, bool capturing) {
 // had, so that the caller runs the product as it is.
 sgemm_status_t run_pretransposed(const Args &a, DeviceState &d, cudaStream_t s, Pretranspose t,
                                  bool tensor) {
-  const int64_t lda2 = round4(a.M), ldb2 = round4(a.N);
-  const size_t a_elems = t.a ? static_cast<size_t>(a.K) * lda2 : 0;
+  // stored shapes of A and B, and the leading dimension of each copy
+  const int64_t a_rows = a.ta ? a.K : a.M, a_cols = a.ta ? a.M : a.K;
+  const int64_t b_rows = a.tb ? a.N : a.K, b_cols = a.tb ? a.K : a.N;
+  const int64_t lda2 = t.a ? round4(a.M) : round4(a_cols), ldb2 = t.b ? round4(a.N) : round4(b_cols);
+  const size_t a_elems = t.a ? static_cast<size_t>(a.K) * lda2 : t.ra ? static_cast<size_t>(a_rows) * lda2 : 0;
+  const size_t b_elems = t.b ? static_cast<size_t>(a.K) * ldb2 : t.rb ? static_cast<size_t>(b_rows) * ldb2 : 0;
   const size_t a_bytes = (a_elems * sizeof(float) + 255) & ~size_t(255);
-  const size_t bytes = a_bytes + (t.b ? static_cast<size_t>(a.K) * ldb2 * sizeof(float) : 0);
+  const size_t bytes = a_bytes + b_elems * sizeof(float);
   const bool capturing = stream_capturing(s);
   std::lock_guard<std::mutex> lock(d.tr_mu);
   float *scratch = pretranspose_scratch(d, bytes, capturing);
@@ -512,14 +555,36 @@ sgemm_status_t run_pretransposed(const Args &a, DeviceState &d, cudaStream_t s, 
     b.lda = lda2;
     ++launches;
   }
+  float *b_copy = reinterpret_cast<float *>(reinterpret_cast<char *>(scratch) + a_bytes);
   if (t.b) {   // B is N x K (ldb): B^T is K x N (ldb2)
-    float *bt = reinterpret_cast<float *>(reinterpret_cast<char *>(scratch) + a_bytes);
-    if (launch_transpose(a.B, a.ldb, bt, ldb2, static_cast<int>(a.N), static_cast<int>(a.K),
+    if (launch_transpose(a.B, a.ldb, b_copy, ldb2, static_cast<int>(a.N), static_cast<int>(a.K),
                          d.sm_count, d.status, s) != cudaSuccess)
       return SGEMM_ERR_LAUNCH;
-    b.B = bt;
+    b.B = b_copy;
     b.tb = 0;
     b.ldb = ldb2;
+    ++launches;
+  }
+  // operands kept as they are but moved to aligned rows: one launch for both
+  const bool ra = t.ra && !t.a, rb = t.rb && !t.b;
+  if (ra || rb) {
+    cudaError_t e;
+    if (ra)
+      e = launch_repack(a.A, a.lda, static_cast<int>(a_rows), static_cast<int>(a_cols), scratch, lda2,
+                        rb ? a.B : nullptr, a.ldb, static_cast<int>(b_rows), static_cast<int>(b_cols),
+                        b_copy, ldb2, s);
+    else
+      e = launch_repack(a.B, a.ldb, static_cast<int>(b_rows), static_cast<int>(b_cols), b_copy, ldb2,
+                        nullptr, 0, 0, 0, nullptr, 0, s);
+    if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (ra) {
+      b.A = scratch;
+      b.lda = lda2;
+    }
+    if (rb) {
+      b.B = b_copy;
+      b.ldb = ldb2;
+    }
     ++launches;
   }
   const sgemm_status_t st = tensor ? run_tc3(b, d, s, /*pdl=*/SG_TC_PDL != 0)
@@ -688,12 +753,17 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
     return SGEMM_SUCCESS;
   }
 
+  if (algo == SGEMM_ALGO_AUTO && repack_wanted(a)) {
+    const sgemm_status_t st = run_pretransposed(a, *d, s, repack_plan(a, d->sm_count), false);
+    if (st != SGEMM_ERR_UNSUPPORTED) return st;
+    algo = SGEMM_ALGO_SIMT_CPASYNC;   // no scratch: run in place
+  }
   if (algo == SGEMM_ALGO_AUTO) algo = auto_algo(a);
   switch (algo) {
     case SGEMM_ALGO_SIMT_TMA: {
       if (!tma_eligible(a)) return SGEMM_ERR_UNSUPPORTED;
       const Pretranspose t = pretranspose_plan(a, d->sm_count, 256);
-      if (t.a || t.b) {
+      if (t.any()) {
         const sgemm_status_t st = run_pretransposed(a, *d, s, t, false);
         if (st != SGEMM_ERR_UNSUPPORTED) return st;
       }
@@ -722,7 +792,7 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
         const sgemm_status_t st = run_tc3_presplit(a, *d, s);
         if (st != SGEMM_ERR_UNSUPPORTED) return st;
       }
-      if (t.a || t.b) {
+      if (t.any()) {
         const sgemm_status_t st = run_pretransposed(a, *d, s, t, true);
         if (st != SGEMM_ERR_UNSUPPORTED) return st;
       }
@@ -798,6 +868,7 @@ int sgemm_select_algo(int transA, int transB, int64_t M, int64_t N, int64_t K, c
   Args a{norm_op(transA), norm_op(transB), M, N, K, alpha, beta, A, lda, B, ldb,
          const_cast<float *>(C), ldc};
   if (validate(a, false) != SGEMM_SUCCESS) return -1;
+  if (repack_wanted(a)) return SGEMM_ALGO_SIMT_TMA;
   return static_cast<int>(auto_algo(a));
 }
 

@@ -10,6 +10,7 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "sgemm.h"
@@ -54,12 +55,15 @@ struct DeviceState {
   size_t ws_bytes = 0;
   bool ws_failed = false;
   BufferOrder ws_order;
-  // Scratch for operands transposed ahead of a product (see run_pretransposed):
+  // Scratch for operands copied ahead of a product (see run_pretransposed):
   // grown on demand up to kPretransposeMaxBytes, kept until exit; calls on
-  // different streams or in graphs that use it are ordered by tr_order.
+  // different streams or in graphs that use it are ordered by tr_order.  A
+  // buffer that a captured graph may hold is never freed: growing past it
+  // retires it to tr_retired.
   std::mutex tr_mu;
   float *tr = nullptr;
   size_t tr_bytes = 0;
+  std::vector<float *> tr_retired;
   bool tr_failed = false;
   BufferOrder tr_order;
   std::once_flag kinfo_once[2][2][2][kNumSimtTiles];

@@ -29,9 +29,10 @@
  * Device memory of the library's own: sgemm()/sgemm_ex() allocate, once per
  * device and the first time a product is split by stream-K, a workspace of
  * two 128 x 256 FP32 tiles per SM (~40 MB on 152 SMs), and, the first time a
- * large NN/NT/TT product transposes an operand ahead (see sgemm()), a scratch
- * buffer for it (grown in 64 MiB steps, at most 2 GiB); both are kept until
- * exit.  Calls on different streams that use them are ordered by events.
+ * product copies an operand ahead (a transpose or an aligning copy, see
+ * sgemm()), a scratch buffer for it (grown in 64 MiB steps, at most 2 GiB);
+ * both are kept until exit.  Calls on different streams that use them are
+ * ordered by events.
  * sgemm_noalloc() never allocates (see there).
  *
  * Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
@@ -45,10 +46,11 @@
  * sgemm_transpose() may be captured.  Inside a capture the library allocates
  * nothing: a product whose stream-K workspace or transpose scratch does not
  * exist yet (or is too small) runs without it; and once a capture has used
- * the transpose scratch it is never reallocated (graphs hold its address), so
- * later products that would need a larger one run without it.  Uses of these buffers inside
- * graphs are ordered against every other use through external event nodes,
- * so graph launches and eager calls on other streams may be mixed freely.
+ * the scratch it is never freed (graphs hold its address): an eager product
+ * that needs a larger one gets a new buffer of at least twice the size and
+ * the old one is kept until exit.  Uses of these buffers inside graphs are
+ * ordered against every other use through external event nodes, so graph
+ * launches and eager calls on other streams may be mixed freely.
  *
  * Numerics: FP32 inputs and outputs; each output's K products are accumulated
  * in FP32 (FFMA) by the CUDA-core kernels, or from TF32 splits in FP32 by the
@@ -129,7 +131,13 @@ typedef enum sgemm_algo {
  * stored N x K) and that fill the GPU with 128 x 256 tiles first copy that
  * operand transposed into library scratch (one transpose launch each) and
  * then run with both operands m/n-contiguous; the result is bit-identical to
- * the in-kernel path.  sgemm_last_launch_count() reports all launches.
+ * the in-kernel path.  Products of M * N * K >= 2^27 whose A or B is not
+ * TMA-eligible (base not 16-byte aligned, or lda / ldb not a multiple of 4)
+ * first copy that operand into 16-byte aligned scratch rows (one launch for
+ * both; transposed instead where the rule above transposes it) and run the
+ * SGEMM_ALGO_SIMT_TMA kernel, again bit-identical to that kernel on aligned
+ * copies of the operands; smaller ones run SGEMM_ALGO_SIMT_CPASYNC in place.
+ * sgemm_last_launch_count() reports all launches.
  */
 SGEMM_API sgemm_status_t sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K,
                      float alpha, const float *A, int64_t lda,

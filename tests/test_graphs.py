@@ -47,8 +47,8 @@ def _alone(A, B, M, N, ta=0, tb=0):
     return C.clone()
 
 
-@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (2048, 4864, 256)],
-                         ids=["stream_k_1024", "pretransposed_2048x4864x256"])
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (2048, 4864, 256), (1000, 1013, 997)],
+                         ids=["stream_k_1024", "pretransposed_2048x4864x256", "repacked_1000x1013x997"])
 def test_graph_replays_interleaved_with_eager_calls(shape):
     M, N, K = shape
     A1, B1 = _operands(M, N, K, 1)
@@ -122,9 +122,11 @@ g = torch.cuda.CUDAGraph()
 with torch.cuda.graph(g, stream=s):
     sg.gemm(A, B, C, stream=s)
 # an eager product needing a larger scratch (A^T of 8192 x 4096 floats, 128 MiB,
-# against the 64 MiB allocated so far): must not move the graph's buffer
+# against the 64 MiB allocated so far): gets a new buffer (its transpose ahead
+# still runs) and must not free the graph's
 A2, B2 = ops(4096, 4096, 8192, 2)
 C2 = sg.gemm(A2, B2)
+assert sg.sgemm_last_launch_count() >= 2
 torch.cuda.synchronize()
 C.zero_()
 g.replay()
@@ -139,8 +141,8 @@ print("ok")
 
 def test_captured_scratch_is_never_moved():
     """After a capture used the transpose scratch, a larger product must not
-    reallocate it (the graph holds its address): the graph still replays
-    correctly after such a product, which itself runs correctly."""
+    free it (the graph holds its address): the larger product takes a new
+    buffer and runs correctly, and the graph still replays correctly."""
     p = subprocess.run([sys.executable, "-c", GROW_CHILD.format(root=ROOT)], capture_output=True,
                        text=True, timeout=300)
     assert p.returncode == 0, p.stderr[-3000:]

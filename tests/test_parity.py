@@ -192,14 +192,66 @@ def test_misaligned_pointers_use_cpasync(orc, op):
                  K, f"misaligned {op}")
 
 
-def test_odd_leading_dimensions_select_cpasync():
-    """The pages' ragged configuration: lda = K = 997, ldb = N = 1013 (TMA-ineligible)."""
+def test_odd_leading_dimensions_are_repacked(orc):
+    """The pages' ragged configuration: lda = K = 997, ldb = N = 1013 (TMA-ineligible).
+    Forcing the TMA family is refused; AUTO copies both operands into aligned
+    scratch (two repack launches) and runs the TMA kernel, which it reports."""
     case = W.RAGGED[0]
     A, B, C = (t.cuda() for t in W.make_inputs(case))
     assert sg.sgemm_select_algo(0, 0, case.M, case.N, case.K, A.data_ptr(), case.K, B.data_ptr(),
-                                case.N, 1.0, 1.0, C.data_ptr(), case.N) == sg.ALGO_SIMT_CPASYNC
+                                case.N, 1.0, 1.0, C.data_ptr(), case.N) == sg.ALGO_SIMT_TMA
     with pytest.raises(sg.SgemmError):
         sg.gemm(A, B, C, 1.0, 1.0, algo="simt_tma")
+    C0 = C.clone()
+    sg.gemm(A, B, C, case.alpha, case.beta)
+    n = sg.sgemm_last_launch_count()
+    torch.cuda.synchronize()
+    Ap, Bp = padded(A, (-case.K) % 4), padded(B, (-case.N) % 4)
+    C2 = C0.clone()
+    sg.gemm(Ap, Bp, C2, case.alpha, case.beta, algo="simt_tma")
+    torch.cuda.synchronize()
+    assert torch.equal(C, C2)
+    assert n == sg.sgemm_last_launch_count() + 1   # one launch repacks both
+
+
+# (M, N, K, transA, transB, A offset, B offset): odd leading dimensions and
+# misaligned bases, each operand repacked or (where the plan transposes it
+# anyway) transposed from its unaligned storage
+REPACK_CASES = [(1000, 1013, 997, 1, 1, 0, 0), (700, 1500, 999, 0, 1, 1, 0),
+                (2048, 2048, 1023, 0, 0, 0, 0), (2048, 2052, 1021, 0, 1, 3, 2),
+                (1500, 333, 2000, 1, 0, 2, 1)]
+
+
+@pytest.mark.parametrize("case", REPACK_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_repacked_operands_match_aligned_call(orc, case):
+    """An AUTO product on TMA-ineligible operands equals, bit for bit, the same
+    call on aligned copies of them (same kernel, same tiles, same k order);
+    sampled outputs also meet the FP32 tolerance against the oracle."""
+    M, N, K, ta, tb, oa, ob = case
+    g = torch.Generator().manual_seed(M + 3 * N + K)
+    A = torch.rand((K, M) if ta else (M, K), generator=g).mul_(2).sub_(1)
+    B = torch.rand((N, K) if tb else (K, N), generator=g).mul_(2).sub_(1)
+    C0 = torch.rand(M, N, generator=g).cuda()
+    dA = offset_view(A.cuda(), oa) if oa else A.cuda()
+    dB = offset_view(B.cuda(), ob) if ob else B.cuda()
+    assert sg.sgemm_select_algo(ta, tb, M, N, K, dA.data_ptr(), dA.stride(0), dB.data_ptr(),
+                                dB.stride(0), 0.5, 1.5, C0.data_ptr(), N) == sg.ALGO_SIMT_TMA
+    C1 = C0.clone()
+    sg.gemm(dA, dB, C1, 0.5, 1.5, ta, tb)
+    n1 = sg.sgemm_last_launch_count()
+    Ap = padded(A.cuda(), (-A.shape[1]) % 4)
+    Bp = padded(B.cuda(), (-B.shape[1]) % 4)
+    C2 = C0.clone()
+    sg.gemm(Ap, Bp, C2, 0.5, 1.5, ta, tb, algo="simt_tma")
+    n2 = sg.sgemm_last_launch_count()
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+    # at most one repack launch (both operands) and a transpose of a
+    # misaligned operand the aligned call transposes too
+    assert n2 <= n1 <= n2 + 1
+    I, J = sample_indices(M, N, 2000, seed=K)
+    R = orc.sgemm_entries_f64(ta, tb, 0.5, A.numpy(), B.numpy(), 1.5, C0.cpu().numpy(), I, J)
+    assert_close(C1.cpu().numpy()[I, J], R, K, f"repacked {case}")
 
 
 # --------------------------------------------------------------- degenerate cases
@@ -345,7 +397,9 @@ def test_pretransposed_matches_tn_bit_for_bit(shape, op):
     per SM) have their k-contiguous operand(s) transposed into scratch first
     and then run as TN: the result must equal, bit for bit, the TN call on
     operands transposed by torch (same kernel, same tiles, same k order), with
-    one extra launch per transposed operand."""
+    one extra launch per transposed operand.  An operand whose rows are not
+    16-byte aligned is copied into aligned scratch even when not transposed
+    (one launch too)."""
     M, N, K = shape
     ta, tb = op
     g = torch.Generator().manual_seed(M + N + K + 2 * ta + tb)
@@ -357,18 +411,21 @@ def test_pretransposed_matches_tn_bit_for_bit(shape, op):
     n1 = sg.sgemm_last_launch_count()
     # K x M and K x N, rows padded to 16 bytes as the library's scratch is, so
     # that the reference call takes the same (TMA) kernel
-    At = A if ta else padded(A.t().contiguous(), (-M) % 4)
-    Bn = padded(B.t().contiguous(), (-N) % 4) if tb else B
+    At = padded(A if ta else A.t().contiguous(), (-M) % 4)
+    Bn = padded(B.t().contiguous() if tb else B, (-N) % 4)
     C2 = C0.clone()
     sg.gemm(At, Bn, C2, 0.75, 0.5, 1, 0)
     n2 = sg.sgemm_last_launch_count()
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
-    # only TMA-eligible layouts (16-byte rows) of GPU-filling size
+    # transposed ahead at GPU-filling size; a misaligned operand is copied anyway
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    eligible = (A.stride(0) % 4 == 0 and B.stride(0) % 4 == 0 and M * N * K >= 2 ** 30
-                and -(-M // 128) * -(-N // 256) * 100 >= 40 * sms)
-    assert n1 == n2 + eligible * ((ta == 0 and N >= 1024) + (tb == 1 and M >= 1024))
+    big = M * N * K >= 2 ** 30 and -(-M // 128) * -(-N // 256) * 100 >= 40 * sms
+    t_a, t_b = big and ta == 0 and N >= 1024, big and tb == 1 and M >= 1024
+    a_ok, b_ok = A.stride(0) % 4 == 0, B.stride(0) % 4 == 0
+    # one launch per transposed operand, one for any operands only repacked
+    copies = t_a + t_b + ((not a_ok and not t_a) or (not b_ok and not t_b))
+    assert n1 == n2 + copies
 
 
 @pytest.mark.parametrize("op", [(0, 0), (0, 1), (1, 1)], ids=["NN", "NT", "TT"])
