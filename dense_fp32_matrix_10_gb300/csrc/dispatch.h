@@ -40,6 +40,12 @@ struct BufferOrder {
 };
 cudaError_t order_before_use(BufferOrder &o, cudaStream_t s, bool capturing);
 cudaError_t order_after_use(BufferOrder &o, cudaStream_t s, bool capturing);
+// Copies of one or two (in1 != nullptr) rows x cols matrices into 16-byte
+// aligned rows (ld_out % 4 == 0, out 16-byte aligned), zero-padded, in one
+// launch (repack.cu).
+cudaError_t launch_repack(const float *in0, int64_t ld_in0, int rows0, int cols0, float *out0,
+                          int64_t ld_out0, const float *in1, int64_t ld_in1, int rows1, int cols1,
+                          float *out1, int64_t ld_out1, cudaStream_t s);
 // True while `s` is being captured into a CUDA graph.
 bool stream_capturing(cudaStream_t s);
 

@@ -108,12 +108,6 @@ cudaError_t launch_transpose(const float *in, int64_t ld_in, float *out, int64_t
 cudaError_t launch_tf32_split(const float *in, int64_t ld_in, int rows, int cols, bool transpose,
                               float *big, float *small, int64_t ld_out, int sm_count, int *status,
                               cudaStream_t s, bool *done);
-// Copies of one or two (in1 != nullptr) rows x cols matrices into 16-byte
-// aligned rows (ld_out % 4 == 0, out 16-byte aligned), zero-padded, in one
-// launch (transpose.cu).
-cudaError_t launch_repack(const float *in0, int64_t ld_in0, int rows0, int cols0, float *out0,
-                          int64_t ld_out0, const float *in1, int64_t ld_in1, int rows1, int cols1,
-                          float *out1, int64_t ld_out1, cudaStream_t s);
 cudaError_t launch_scale_c_batched(float *C, int64_t ldc, int64_t strideC, int M, int N,
                                    int64_t batch, float beta, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint64_t budget_ns, int *status, cudaStream_t s);
