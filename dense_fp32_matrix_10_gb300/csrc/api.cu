@@ -205,8 +205,12 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 #ifndef SG_WIDE_MIN_FILL_PCT
 #define SG_WIDE_MIN_FILL_PCT 40
 #endif
+#ifndef SG_SMALL_TILE_WORK
+#define SG_SMALL_TILE_WORK 0
+#endif
 int pick_simt_tile(const Args &a, int producer, int sm_count) {
   if (a.N <= 64) return kTile128x64;
+  if (static_cast<double>(a.M) * a.N * a.K <= static_cast<double>(SG_SMALL_TILE_WORK)) return kTile128x64;
   // the math warps read A m-contiguous when it is stored K x M, or when the
   // TMA producer transposes a k-contiguous A in shared memory
   const bool a_mn_in_smem = a.ta == 1 || (producer == kTma && SG_SIMT_TRANSPOSE_A);
@@ -388,7 +392,7 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
   if (plan.sk_tiles > 0) {
-    if (launch_sk_fixup(p, ki->bm, ki->bn, plan.grid, plan.sk_tiles, stream) != cudaSuccess)
+    if (launch_sk_fixup(p, ki->bm, ki->bn, plan.grid, plan.sk_tiles, d.sm_count, stream) != cudaSuccess)
       return SGEMM_ERR_LAUNCH;
     t_last_launches = 2;
     if (order_after_use(d.ws_order, stream, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;

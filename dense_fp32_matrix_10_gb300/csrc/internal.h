@@ -81,7 +81,7 @@ TcEntry tc3_presplit_entry();
 
 // Second pass of a stream-K launch (sk_fixup.cu).
 cudaError_t launch_sk_fixup(const SimtParams &p, int bm, int bn, int grid_main, int sk_tiles,
-                            cudaStream_t s);
+                            int sm_count, cudaStream_t s);
 
 // Context kernels and helpers (context.cu).
 struct PlainParams {

@@ -152,7 +152,7 @@ extern "C" sgemm_status_t sgemm_noalloc(int transA, int transB, int64_t M, int64
     return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
   if (plan.sk_tiles > 0) {
-    if (launch_sk_fixup(p, ki->bm, ki->bn, plan.grid, plan.sk_tiles, s) != cudaSuccess)
+    if (launch_sk_fixup(p, ki->bm, ki->bn, plan.grid, plan.sk_tiles, d->sm_count, s) != cudaSuccess)
       return SGEMM_ERR_LAUNCH;
     t_last_launches = 2;
   }

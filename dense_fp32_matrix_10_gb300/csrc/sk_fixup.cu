@@ -19,6 +19,10 @@ constexpr int kChunk = 4 * kFixupThreads;  // elements per block
 
 __device__ __forceinline__ int64_t sk_start(int64_t g, int64_t S, int64_t G) { return g * S / G; }
 
+// BATCH: partials loaded per round (all in flight at once).  Tiles split
+// into many segments (small products) take 8, which costs registers; the
+// usual two or three segments per tile take 1 and keep eight blocks per SM.
+template <int BATCH>
 __global__ void __launch_bounds__(kFixupThreads) sk_fixup_kernel(const SimtParams p, int bm, int bn,
                                                                  int grid_main) {
   const int chunks = bm * bn / kChunk;   // bm * bn is a multiple of 8192
@@ -58,16 +62,25 @@ __global__ void __launch_bounds__(kFixupThreads) sk_fixup_kernel(const SimtParam
   // 4 consecutive columns per thread (bn is a multiple of 64)
   {
     const int e = chunk * kChunk + 4 * threadIdx.x;
-    float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int i = 0; i < n; ++i) {
-      const float4 v = *reinterpret_cast<const float4 *>(p.workspace + s_slot[i] * tile_elems + e);
-      sum.x += v.x;
-      sum.y += v.y;
-      sum.z += v.z;
-      sum.w += v.w;
-    }
     const int row = tm * bm + e / bn, col = tn * bn + e % bn;
     if (row >= p.M) return;
+    float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    // partials in groups of BATCH loads in flight, added in slot order
+    for (int i0 = 0; i0 < n; i0 += BATCH) {
+      float4 v[BATCH];
+#pragma unroll
+      for (int j = 0; j < BATCH; ++j)
+        if (i0 + j < n) v[j] = __ldcg(reinterpret_cast<const float4 *>(p.workspace + s_slot[i0 + j] * tile_elems + e));
+#pragma unroll
+      for (int j = 0; j < BATCH; ++j) {
+        if (i0 + j < n) {
+          sum.x += v[j].x;
+          sum.y += v[j].y;
+          sum.z += v[j].z;
+          sum.w += v[j].w;
+        }
+      }
+    }
     float *c = Cb + static_cast<int64_t>(row) * p.ldc + col;
     const float s4[4] = {sum.x, sum.y, sum.z, sum.w};
     if (p.c_vec4 && col + 3 < p.N) {
@@ -89,9 +102,15 @@ __global__ void __launch_bounds__(kFixupThreads) sk_fixup_kernel(const SimtParam
 }
 
 cudaError_t launch_sk_fixup(const SimtParams &p, int bm, int bn, int grid_main, int sk_tiles,
-                            cudaStream_t s) {
-  return launch_maybe_pdl(sk_fixup_kernel, dim3(sk_tiles * (bm * bn / kChunk)), dim3(kFixupThreads), 0,
-                          s, true, p, bm, bn, grid_main);
+                            int sm_count, cudaStream_t s) {
+  const dim3 grid(sk_tiles * (bm * bn / kChunk));
+  // 8 loads in flight where tiles have many segments (at most
+  // ceil(grid_main / sk_tiles) + 1) and the grid is one wave at the four
+  // blocks per SM its registers allow (GB300, graph replays: 256^3 13.2 ->
+  // 12.5 us, 768^3 29.8 -> 28.5 us; 1024^3, two waves, 49.2 -> 51.0 us)
+  if ((grid_main + sk_tiles - 1) / sk_tiles + 1 >= 4 && grid.x <= 4u * static_cast<unsigned>(sm_count))
+    return launch_maybe_pdl(sk_fixup_kernel<8>, grid, dim3(kFixupThreads), 0, s, true, p, bm, bn, grid_main);
+  return launch_maybe_pdl(sk_fixup_kernel<1>, grid, dim3(kFixupThreads), 0, s, true, p, bm, bn, grid_main);
 }
 
 }  // namespace sg
