@@ -120,7 +120,7 @@ const TcKernelInfo *tc_kernel_info_presplit(DeviceState &d);
 bool encode_tmap(CUtensorMap *m, const float *base, int64_t rows, int64_t cols, int64_t ld,
                  int box_cols, int box_rows, bool swizzle128);
 
-int pick_simt_tile(const Args &a, int producer, int sm_count);
+int pick_simt_tile(const Args &a, int producer, int sm_count, int64_t batch = 1);
 
 // Smallest stream-K segment worth a partial tile (k-tiles of 32).
 #ifndef SG_MIN_SK_SEGMENT
