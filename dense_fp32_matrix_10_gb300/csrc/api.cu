@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <mutex>
 
 #include "dispatch.h"
@@ -260,9 +261,26 @@ bool stream_capturing(cudaStream_t s) {
   return cs == cudaStreamCaptureStatusActive;
 }
 
+// Id of the capture sequence `s` is recording into, or 0.
+unsigned long long capture_id(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  unsigned long long id = 0;
+  if (cudaStreamGetCaptureInfo(s, &cs, &id) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return cs == cudaStreamCaptureStatusActive ? id : 0;
+}
+
 cudaError_t order_before_use(BufferOrder &o, cudaStream_t s, bool capturing) {
   if (!o.used) return cudaSuccess;
-  if (capturing) return cudaStreamWaitEvent(s, o.ev, cudaEventWaitExternal);
+  if (capturing) {
+    // the previous use was captured earlier on this stream into the same
+    // graph: the graph orders the two, and a wait node here would only cut
+    // the programmatic launch chain
+    if (o.last == s && o.capture != 0 && o.capture == capture_id(s)) return cudaSuccess;
+    return cudaStreamWaitEvent(s, o.ev, cudaEventWaitExternal);
+  }
   if (o.in_graph || o.last != s) return cudaStreamWaitEvent(s, o.ev, 0);
   return cudaSuccess;
 }
@@ -273,6 +291,7 @@ cudaError_t order_after_use(BufferOrder &o, cudaStream_t s, bool capturing) {
   o.used = true;
   o.last = s;
   o.in_graph = o.in_graph || capturing;
+  o.capture = capturing ? capture_id(s) : 0;
   return e;
 }
 
@@ -315,8 +334,14 @@ struct Batch {
 
 // pdl: the product directly follows another kernel of the same call on the
 // stream (an operand transpose) and may be scheduled before it ends.
+// Launches queued right before the product (the operand copies of
+// run_pretransposed): after every wait the product needs, so that the copies
+// and the product form one programmatic launch chain.
+using PreLaunch = std::function<cudaError_t()>;
+
 sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_t stream,
-                        const Batch &bt = Batch{1, 0, 0, 0}, bool pdl = false) {
+                        const Batch &bt = Batch{1, 0, 0, 0}, bool pdl = false,
+                        const PreLaunch *pre = nullptr) {
   const int tile = pick_simt_tile(a, producer, d.sm_count, bt.count);
   const SimtKernelInfo *ki = kernel_info(d, producer, a.ta, a.tb, tile);
   if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_LAUNCH;
@@ -372,7 +397,7 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
     if (!okA || !okB) {
       // a batch layout the tensor-map encoder refuses is still a valid batch:
       // load it with cp.async instead
-      if (bt.count > 1) return run_simt(a, d, kCpAsync, stream, bt, pdl);
+      if (bt.count > 1) return run_simt(a, d, kCpAsync, stream, bt, pdl, pre);
       return SGEMM_ERR_LAUNCH;
     }
   }
@@ -394,6 +419,7 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   // using the workspace
   if (plan.sk_tiles > 0 && order_before_use(d.ws_order, stream, capturing) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
+  if (pre && (*pre)() != cudaSuccess) return SGEMM_ERR_LAUNCH;
   cudaError_t e = simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, plan.grid, stream, pdl);
   if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
@@ -427,6 +453,9 @@ constexpr size_t kPretransposeMaxBytes = size_t(2) << 30;    // 2 GiB of scratch
 // Operands copied into library scratch ahead of the product: transposed
 // (a, b), or repacked into 16-byte aligned rows (ra, rb) so that the TMA
 // producer can load them.
+#ifndef SG_PRETRANSPOSE_NARROW_WORK
+#define SG_PRETRANSPOSE_NARROW_WORK 0
+#endif
 struct Pretranspose {
   bool a, b;
   bool ra = false, rb = false;
@@ -457,14 +486,20 @@ Pretranspose transpose_plan_any(const Args &a, int sm_count, int64_t tile_n) {
   Pretranspose t{false, false};
   if (!SG_PRETRANSPOSE) return t;
   const double work = static_cast<double>(a.M) * static_cast<double>(a.N) * static_cast<double>(a.K);
-  if (work < static_cast<double>(kPretransposeMinWork)) return t;
   // only where the transposed product fills the GPU with 128 x 256 tiles:
   // below that both layouts run 128 x 128 tiles and the extra launch loses
   // (measured at 2048^3 NN: 57.4 in-kernel vs 56.2 TFLOP/s transposed ahead)
-  if (cdiv(a.M, 128) * cdiv(a.N, tile_n) * 100 < (tile_n == 256 ? SG_WIDE_MIN_FILL_PCT : 100) * sm_count)
-    return t;
-  t.a = a.ta == 0 && a.N >= kPretransposeMinOther;
-  t.b = a.tb == 1 && a.M >= kPretransposeMinOther;
+  const bool fills =
+      cdiv(a.M, 128) * cdiv(a.N, tile_n) * 100 >= (tile_n == 256 ? SG_WIDE_MIN_FILL_PCT : 100) * sm_count;
+  int64_t min_other = kPretransposeMinOther;
+  if (work < static_cast<double>(kPretransposeMinWork) || !fills) {
+    if (!(SG_PRETRANSPOSE_NARROW_WORK > 0 && tile_n == 256 &&
+          work >= static_cast<double>(SG_PRETRANSPOSE_NARROW_WORK)))
+      return t;
+    min_other = 512;
+  }
+  t.a = a.ta == 0 && a.N >= min_other;
+  t.b = a.tb == 1 && a.M >= min_other;
   return t;
 }
 
@@ -554,51 +589,48 @@ sgemm_status_t run_pretransposed(const Args &a, DeviceState &d, cudaStream_t s, 
   if (!scratch) return SGEMM_ERR_UNSUPPORTED;
   // a call on another stream (or a graph) may still be reading the scratch
   if (order_before_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  // the product's operands: the copies in scratch
   Args b = a;
-  int launches = 0;
-  if (t.a) {   // A is M x K (lda): A^T is K x M (lda2)
-    if (launch_transpose(a.A, a.lda, scratch, lda2, static_cast<int>(a.M), static_cast<int>(a.K),
-                         d.sm_count, d.status, s) != cudaSuccess)
-      return SGEMM_ERR_LAUNCH;
-    b.A = scratch;
-    b.ta = 1;
-    b.lda = lda2;
-    ++launches;
-  }
   float *b_copy = reinterpret_cast<float *>(reinterpret_cast<char *>(scratch) + a_bytes);
-  if (t.b) {   // B is N x K (ldb): B^T is K x N (ldb2)
-    if (launch_transpose(a.B, a.ldb, b_copy, ldb2, static_cast<int>(a.N), static_cast<int>(a.K),
-                         d.sm_count, d.status, s) != cudaSuccess)
-      return SGEMM_ERR_LAUNCH;
+  const bool ra = t.ra && !t.a, rb = t.rb && !t.b;   // kept as they are, moved to aligned rows
+  if (t.a || ra) {
+    b.A = scratch;
+    b.lda = lda2;
+    if (t.a) b.ta = 1;
+  }
+  if (t.b || rb) {
     b.B = b_copy;
-    b.tb = 0;
     b.ldb = ldb2;
-    ++launches;
+    if (t.b) b.tb = 0;
   }
-  // operands kept as they are but moved to aligned rows: one launch for both
-  const bool ra = t.ra && !t.a, rb = t.rb && !t.b;
-  if (ra || rb) {
-    cudaError_t e;
-    if (ra)
-      e = launch_repack(a.A, a.lda, static_cast<int>(a_rows), static_cast<int>(a_cols), scratch, lda2,
-                        rb ? a.B : nullptr, a.ldb, static_cast<int>(b_rows), static_cast<int>(b_cols),
-                        b_copy, ldb2, s);
-    else
-      e = launch_repack(a.B, a.ldb, static_cast<int>(b_rows), static_cast<int>(b_cols), b_copy, ldb2,
-                        nullptr, 0, 0, 0, nullptr, 0, s);
-    if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
-    if (ra) {
-      b.A = scratch;
-      b.lda = lda2;
+  const int launches = int(t.a) + int(t.b) + int(ra || rb);
+  // the copies, queued by the product's launcher after its own waits
+  const PreLaunch copies = [&]() -> cudaError_t {
+    if (t.a) {   // A is M x K (lda): A^T is K x M (lda2)
+      const cudaError_t e = launch_transpose(a.A, a.lda, scratch, lda2, static_cast<int>(a.M),
+                                             static_cast<int>(a.K), d.sm_count, d.status, s);
+      if (e != cudaSuccess) return e;
     }
-    if (rb) {
-      b.B = b_copy;
-      b.ldb = ldb2;
+    if (t.b) {   // B is N x K (ldb): B^T is K x N (ldb2)
+      const cudaError_t e = launch_transpose(a.B, a.ldb, b_copy, ldb2, static_cast<int>(a.N),
+                                             static_cast<int>(a.K), d.sm_count, d.status, s);
+      if (e != cudaSuccess) return e;
     }
-    ++launches;
+    if (ra)   // one launch for both
+      return launch_repack(a.A, a.lda, static_cast<int>(a_rows), static_cast<int>(a_cols), scratch, lda2,
+                           rb ? a.B : nullptr, a.ldb, static_cast<int>(b_rows), static_cast<int>(b_cols),
+                           b_copy, ldb2, s);
+    if (rb)
+      return launch_repack(a.B, a.ldb, static_cast<int>(b_rows), static_cast<int>(b_cols), b_copy, ldb2,
+                           nullptr, 0, 0, 0, nullptr, 0, s);
+    return cudaSuccess;
+  };
+  sgemm_status_t st;
+  if (tensor) {
+    st = copies() == cudaSuccess ? run_tc3(b, d, s, /*pdl=*/SG_TC_PDL != 0) : SGEMM_ERR_LAUNCH;
+  } else {
+    st = run_simt(b, d, kTma, s, Batch{1, 0, 0, 0}, /*pdl=*/true, &copies);
   }
-  const sgemm_status_t st = tensor ? run_tc3(b, d, s, /*pdl=*/SG_TC_PDL != 0)
-                                   : run_simt(b, d, kTma, s, Batch{1, 0, 0, 0}, /*pdl=*/true);
   if (st != SGEMM_SUCCESS) return st;
   t_last_launches += launches;
   if (order_after_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;

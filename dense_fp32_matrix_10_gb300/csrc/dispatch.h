@@ -37,6 +37,8 @@ struct BufferOrder {
   // a use has been captured into a graph at some point: its launches are
   // invisible to the host-side bookkeeping, so every later use waits
   bool in_graph = false;
+  // capture sequence of the last use (0: an eager use)
+  unsigned long long capture = 0;
 };
 cudaError_t order_before_use(BufferOrder &o, cudaStream_t s, bool capturing);
 cudaError_t order_after_use(BufferOrder &o, cudaStream_t s, bool capturing);
