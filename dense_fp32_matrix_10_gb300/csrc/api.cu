@@ -453,9 +453,6 @@ constexpr size_t kPretransposeMaxBytes = size_t(2) << 30;    // 2 GiB of scratch
 // Operands copied into library scratch ahead of the product: transposed
 // (a, b), or repacked into 16-byte aligned rows (ra, rb) so that the TMA
 // producer can load them.
-#ifndef SG_PRETRANSPOSE_NARROW_WORK
-#define SG_PRETRANSPOSE_NARROW_WORK 0
-#endif
 struct Pretranspose {
   bool a, b;
   bool ra = false, rb = false;
@@ -489,17 +486,13 @@ Pretranspose transpose_plan_any(const Args &a, int sm_count, int64_t tile_n) {
   // only where the transposed product fills the GPU with 128 x 256 tiles:
   // below that both layouts run 128 x 128 tiles and the extra launch loses
   // (measured at 2048^3 NN: 57.4 in-kernel vs 56.2 TFLOP/s transposed ahead)
+  // (GB300, graph replays: transposing ahead into 128 x 128 tiles costs
+  // 768^3 NN 28.4 -> 38.2 us, 1024^3 49.2 -> 58.2 us)
   const bool fills =
       cdiv(a.M, 128) * cdiv(a.N, tile_n) * 100 >= (tile_n == 256 ? SG_WIDE_MIN_FILL_PCT : 100) * sm_count;
-  int64_t min_other = kPretransposeMinOther;
-  if (work < static_cast<double>(kPretransposeMinWork) || !fills) {
-    if (!(SG_PRETRANSPOSE_NARROW_WORK > 0 && tile_n == 256 &&
-          work >= static_cast<double>(SG_PRETRANSPOSE_NARROW_WORK)))
-      return t;
-    min_other = 512;
-  }
-  t.a = a.ta == 0 && a.N >= min_other;
-  t.b = a.tb == 1 && a.M >= min_other;
+  if (work < static_cast<double>(kPretransposeMinWork) || !fills) return t;
+  t.a = a.ta == 0 && a.N >= kPretransposeMinOther;
+  t.b = a.tb == 1 && a.M >= kPretransposeMinOther;
   return t;
 }
 
