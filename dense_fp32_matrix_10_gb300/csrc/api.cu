@@ -231,6 +231,9 @@ int pick_simt_tile(const Args &a, int producer, int sm_count, int64_t batch) {
 #ifndef SG_SK_REMAINDER
 #define SG_SK_REMAINDER 0
 #endif
+#ifndef SG_SK_FIXUP_LAUNCH
+#define SG_SK_FIXUP_LAUNCH 0
+#endif
 SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws) {
   SkPlan pl{static_cast<int>(tiles), 0, 0, static_cast<int>(tiles < slots ? tiles : slots)};
   if (!have_ws || k_tiles < 2 * kMinSkSegment) return pl;
@@ -308,9 +311,11 @@ float *stream_k_workspace(DeviceState &d, size_t need, bool capturing) {
   if (d.ws_failed) return nullptr;
   if (!d.ws) {
     if (capturing) return nullptr;
-    // largest need: two 128 x 256 partial tiles per SM (one CTA per SM)
+    // largest need: two 128 x 256 partial tiles per SM (one CTA per SM),
+    // then the arrival counters of the in-kernel fixup (zero between launches)
     const size_t bytes = static_cast<size_t>(2) * d.sm_count * 128 * 256 * sizeof(float);
-    if (cudaMalloc(&d.ws, bytes) != cudaSuccess ||
+    if (cudaMalloc(&d.ws, bytes + kSkCounters * sizeof(int)) != cudaSuccess ||
+        cudaMemset(reinterpret_cast<char *>(d.ws) + bytes, 0, kSkCounters * sizeof(int)) != cudaSuccess ||
         cudaEventCreateWithFlags(&d.ws_order.ev, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
       if (d.ws) cudaFree(d.ws);
@@ -319,6 +324,7 @@ float *stream_k_workspace(DeviceState &d, size_t need, bool capturing) {
       return nullptr;
     }
     d.ws_bytes = bytes;
+    d.sk_count = reinterpret_cast<int *>(reinterpret_cast<char *>(d.ws) + bytes);
   }
   return need <= d.ws_bytes ? d.ws : nullptr;
 }
@@ -414,6 +420,20 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   if (plan.sk_tiles == 0) ws_lock.unlock();
   p.dp_tiles = plan.dp_tiles;
   p.sk_iters = plan.sk_iters;
+  // Split tiles of at most about three segments (grid <= 2 * split tiles)
+  // are finished inside the TMA kernel that reads A m-contiguous (tiles of
+  // eight math warps), by the CTA
+  // that arrives last at each; otherwise sk_fixup_kernel does it, which
+  // spreads a tile of many segments over many blocks (GB300, per call: 4096^3
+  // 2042.5 -> 2034.6 us and 2048^3 TN 268.3 -> 265.3 us in-kernel, but 1536^3
+  // NN 125.3 -> 129.3 us and 256^3 11.0 -> 19.5 us).  SG_SK_FIXUP_LAUNCH 1:
+  // always the separate pass.
+  const bool in_kernel_fixup_kernel =
+      producer == kTma && !(a.ta == 0 && SG_SIMT_TRANSPOSE_A) && tile != kTile128x64;
+  p.sk_count = (plan.sk_tiles > 0 && !SG_SK_FIXUP_LAUNCH && in_kernel_fixup_kernel &&
+                plan.grid <= 2 * static_cast<int64_t>(plan.sk_tiles) && plan.sk_tiles <= kSkCounters)
+                   ? d.sk_count
+                   : nullptr;
 
   // the previous stream-K call (another stream, or a graph) may still be
   // using the workspace
@@ -424,9 +444,11 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
   if (plan.sk_tiles > 0) {
-    if (launch_sk_fixup(p, ki->bm, ki->bn, plan.grid, plan.sk_tiles, d.sm_count, stream) != cudaSuccess)
-      return SGEMM_ERR_LAUNCH;
-    t_last_launches = 2;
+    if (p.sk_count == nullptr) {
+      if (launch_sk_fixup(p, ki->bm, ki->bn, plan.grid, plan.sk_tiles, d.sm_count, stream) != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
+      t_last_launches = 2;
+    }
     if (order_after_use(d.ws_order, stream, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
   }
   return SGEMM_SUCCESS;
@@ -925,6 +947,12 @@ sgemm_status_t sgemm_last_device_status(void *stream) {
   if (v != 0) {
     const int zero = 0;
     if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      return SGEMM_ERR_LAUNCH;
+    }
+    // a kernel that gave up a wait may have left arrival counters mid-count
+    std::lock_guard<std::mutex> lock(d->ws_mu);
+    if (d->sk_count && cudaMemset(d->sk_count, 0, kSkCounters * sizeof(int)) != cudaSuccess) {
       cudaGetLastError();
       return SGEMM_ERR_LAUNCH;
     }

@@ -61,6 +61,7 @@ struct DeviceState {
   std::mutex ws_mu;
   float *ws = nullptr;
   size_t ws_bytes = 0;
+  int *sk_count = nullptr;   // kSkCounters arrival counters after the partial tiles
   bool ws_failed = false;
   BufferOrder ws_order;
   // Scratch for operands copied ahead of a product (see run_pretransposed):
@@ -87,6 +88,9 @@ struct DeviceState {
 // Indices are 32-bit inside the kernels; tile origins may run up to one tile
 // past the end of a dimension.
 constexpr int64_t kMaxDim = 0x7fffffff - 1024;
+// stream-K tiles a launch may finish in-kernel (at most two waves' worth of
+// tiles are split, far below this)
+constexpr int kSkCounters = 4096;
 constexpr int64_t kMaxLd = int64_t(1) << 40;  // keeps every byte offset in int64
 
 struct Args {

@@ -87,6 +87,11 @@ struct SimtParams {
   int tiles_per_batch;
   int64_t strideA, strideB, strideC;
   int a_map3d, b_map3d;
+  // In-kernel fixup: one arrival counter per stream-K tile (zero between
+  // launches).  Every segment stores its partial and counts itself in; the
+  // CTA that arrives last adds the tile's partials in k order and writes C.
+  // Null: sk_fixup_kernel does that in a second launch.
+  int *sk_count = nullptr;
 };
 
 // Batch index and (tile_m, tile_n) of linear tile t.
@@ -122,6 +127,28 @@ __device__ __forceinline__ void for_each_unit(const SimtParams &p, F &&f) {
       it += k1 - k0;
     }
   }
+}
+
+// Calls f(i, slot) for the CTA segments covering stream-K tile ts (its index
+// within the stream-K region) in increasing k order (i = 0, 1, ...), with the
+// workspace slot each stored its partial in (slot 2g: CTA g's first unit,
+// 2g + 1: its last); returns their number.  G = the main grid.
+template <class F>
+__device__ __forceinline__ int sk_for_each_segment(const SimtParams &p, int64_t G, int ts, F &&f) {
+  const int64_t KT = p.k_tiles, S = p.sk_iters;
+  const int64_t it0 = static_cast<int64_t>(ts) * KT, it1 = it0 + KT;
+  int64_t g = it0 * G / S;
+  while (g + 1 < G && (g + 1) * S / G <= it0) ++g;
+  while (g > 0 && g * S / G > it0) --g;
+  int n = 0;
+  for (; g < G; ++g) {
+    const int64_t a = g * S / G, b = (g + 1) * S / G;
+    if (a >= it1) break;
+    if ((a > it0 ? a : it0) >= (b < it1 ? b : it1)) continue;  // empty segment
+    f(n, static_cast<int>(2 * g + (a >= it0 ? 0 : 1)));
+    ++n;
+  }
+  return n;
 }
 
 // SG_SIMT_TRANSPOSERS  producer warps (1..3) that share the A transpose;
@@ -662,12 +689,56 @@ __device__ __forceinline__ void store_partial(float *ws, const AccT<Cfg> &acc, i
   }
 }
 
+// Kernels that can finish split tiles themselves (SimtParams::sk_count).
+template <class Cfg>
+__host__ __device__ constexpr bool kInKernelFixup() {
+  return Cfg::PRODUCER == kTma && !Cfg::A_TRANS && Cfg::MATH_WARPS == 8;
+}
+
+// Barrier of the math warps only (the producer warps never take part), on an
+// mbarrier with one arrival per math warp, so that its wait is bounded like
+// every other wait of the kernel; false if it gave up.
+__device__ __forceinline__ bool math_barrier(uint32_t bar, uint32_t &phase, int lane, const SimtParams &p) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = wait_parity_bounded(bar, phase, p.wait_budget_ns, p.status);
+  phase ^= 1u;
+  return ok;
+}
+
+// acc += a partial tile stored by store_partial (read through L2: other CTAs
+// wrote it during this launch).
+template <class Cfg>
+__device__ __forceinline__ void add_partial(AccT<Cfg> &acc, const float *ws, int wm, int wn, int tm,
+                                            int tn) {
+  constexpr int MODE = acc_mode<Cfg>(), TN = Cfg::TN;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const float *row = ws + static_cast<int64_t>(wm * 32 + thread_row<Cfg>(tm, r)) * Cfg::BN + wn * Cfg::WN;
+    if (!Cfg::B_KMAJOR) {
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h) {
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(row + h * 32 + 4 * tn));
+        acc_ref<MODE, TN>(acc, r, 4 * h + 0) += v.x;
+        acc_ref<MODE, TN>(acc, r, 4 * h + 1) += v.y;
+        acc_ref<MODE, TN>(acc, r, 4 * h + 2) += v.z;
+        acc_ref<MODE, TN>(acc, r, 4 * h + 3) += v.w;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < TN; ++c) acc_ref<MODE, TN>(acc, r, c) += __ldcg(row + thread_col<Cfg>(tn, c));
+    }
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     simt_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const SimtParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ int s_last;   // in-kernel fixup: this CTA arrived last at its tile
+  __shared__ __align__(8) uint64_t s_math_bar;
   // 1024-byte alignment of the stage ring (required by the 128 B swizzle).
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -689,6 +760,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
       mbar_init(raw_full0 + 8 * r, 1);
       mbar_init(raw_empty0 + 8 * r, Cfg::TRANSPOSER_WARPS);
     }
+    if constexpr (kInKernelFixup<Cfg>()) mbar_init(smem_u32(&s_math_bar), Cfg::MATH_WARPS);
     fence_mbar_init();
   }
   if (Cfg::PRODUCER == kTma && threadIdx.x == Cfg::MATH_THREADS) {
@@ -726,6 +798,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
   const int tm = lane >> 3;
   const int tn = lane & 7;
   uint32_t it = 0;
+  const uint32_t math_bar = smem_u32(&s_math_bar);
+  uint32_t math_phase = 0;
   for_each_unit(p, [&](const WorkUnit &u) {
     AccT<Cfg> acc;
 #pragma unroll
@@ -740,15 +814,59 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
-    if (u.slot < 0) {
-      // tile coordinates only now: nothing but acc stays live across the k-loop
-      int bi, tile_m, tile_n;
-      unit_coords(p, u.tile, bi, tile_m, tile_n);
-      epilogue<Cfg>(p, p.C + static_cast<int64_t>(bi) * p.strideC, acc, tile_m * Cfg::BM,
-                    tile_n * Cfg::BN, wm, wn, tm, tn);
-    } else
+    if constexpr (!kInKernelFixup<Cfg>()) {
+      if (u.slot < 0) {
+        // tile coordinates only now: nothing but acc stays live across the k-loop
+        int bi, tile_m, tile_n;
+        unit_coords(p, u.tile, bi, tile_m, tile_n);
+        epilogue<Cfg>(p, p.C + static_cast<int64_t>(bi) * p.strideC, acc, tile_m * Cfg::BM,
+                      tile_n * Cfg::BN, wm, wn, tm, tn);
+      } else {
+        // sk_fixup_kernel adds the partials (these kernels run the mid-size
+        // products, for which the separate pass is the faster)
+        store_partial<Cfg>(p.workspace + static_cast<int64_t>(u.slot) * Cfg::BM * Cfg::BN, acc, wm, wn,
+                           tm, tn);
+      }
+      return true;
+    }
+    if (u.slot >= 0) {
       store_partial<Cfg>(p.workspace + static_cast<int64_t>(u.slot) * Cfg::BM * Cfg::BN, acc, wm, wn,
                          tm, tn);
+      if (p.sk_count == nullptr) return true;   // sk_fixup_kernel adds the partials
+      // count this segment in; the last to arrive adds the tile's partials
+      const int ts = u.tile - p.dp_tiles;
+      int own = -1;
+      const int n = sk_for_each_segment(p, gridDim.x, ts, [&](int i, int slot) {
+        if (slot == u.slot) own = i;
+      });
+      __threadfence();
+      if (!math_barrier(math_bar, math_phase, lane, p)) return false;
+      if (threadIdx.x == 0) {
+        const bool last = atomicAdd(p.sk_count + ts, 1) == n - 1;
+        if (last) p.sk_count[ts] = 0;   // ready for the next launch
+        s_last = last;
+        __threadfence();
+      }
+      if (!math_barrier(math_bar, math_phase, lane, p)) return false;
+      if (!s_last) return true;
+      // the sum in k order, 0 + p0 + p1 + ..., as sk_fixup_kernel forms it;
+      // this CTA's own partial is still in acc when it comes first
+      constexpr int MODE = acc_mode<Cfg>(), TN = Cfg::TN;
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int c = 0; c < TN; ++c)
+          acc_ref<MODE, TN>(acc, r, c) = own == 0 ? 0.0f + acc_get<MODE, TN>(acc, r, c) : 0.0f;
+      sk_for_each_segment(p, gridDim.x, ts, [&](int i, int slot) {
+        if (i == 0 && own == 0) return;
+        add_partial<Cfg>(acc, p.workspace + static_cast<int64_t>(slot) * Cfg::BM * Cfg::BN, wm, wn, tm, tn);
+      });
+    }
+    // tile coordinates only now: nothing but acc stays live across the k-loop
+    int bi, tile_m, tile_n;
+    unit_coords(p, u.tile, bi, tile_m, tile_n);
+    epilogue<Cfg>(p, p.C + static_cast<int64_t>(bi) * p.strideC, acc, tile_m * Cfg::BM,
+                  tile_n * Cfg::BN, wm, wn, tm, tn);
     return true;
   });
 }

@@ -28,7 +28,9 @@
  * library never frees, keeps or reallocates them.  C must not overlap A or B.
  * Device memory of the library's own: sgemm()/sgemm_ex() allocate, once per
  * device and the first time a product is split by stream-K, a workspace of
- * two 128 x 256 FP32 tiles per SM (~40 MB on 152 SMs), and, the first time a
+ * two 128 x 256 FP32 tiles per SM (~40 MB on 152 SMs, plus 16 KiB of
+ * per-tile arrival counters for split tiles finished inside the product
+ * kernel), and, the first time a
  * product copies an operand ahead (a transpose or an aligning copy, see
  * sgemm()), a scratch buffer for it (grown in 64 MiB steps, at most 2 GiB);
  * both are kept until exit.  Calls on different streams that use them are
@@ -217,7 +219,8 @@ SGEMM_API int sgemm_last_launch_count(void);
  * Synchronises `stream`, then reads and clears the current device's status
  * word, in which a kernel records that it gave up a bounded wait.  Returns
  * SGEMM_SUCCESS, SGEMM_ERR_DEVICE_TIMEOUT, or SGEMM_ERR_LAUNCH if the
- * synchronisation itself failed.
+ * synchronisation itself failed.  On a timeout it also zeroes the stream-K
+ * arrival counters, which a kernel that gave up may have left mid-count.
  */
 SGEMM_API sgemm_status_t sgemm_last_device_status(void *stream);
 

@@ -375,11 +375,18 @@ def test_stream_k_is_deterministic(shape):
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
-def test_stream_k_uses_two_launches():
+def test_stream_k_launches():
+    """Large products finish split tiles inside the product kernel (the CTA
+    that arrives last at a tile adds its partials): one launch.  Tiles split
+    into many segments take the separate fixup pass: two launches."""
     A = torch.randn(2048, 2048, device="cuda")
     B = torch.randn(2048, 2048, device="cuda")
     sg.gemm(A, B, transA=True)                  # TN: no operand transposed ahead
-    assert sg.sgemm_last_launch_count() == 2   # main kernel + fixup
+    assert sg.sgemm_last_launch_count() == 1
+    A = torch.randn(1024, 1024, device="cuda")
+    B = torch.randn(1024, 1024, device="cuda")
+    sg.gemm(A, B, transA=True)                  # 64 tiles over every SM
+    assert sg.sgemm_last_launch_count() == 2
     A = torch.randn(128 * 152, 256, device="cuda")
     B = torch.randn(256, 128, device="cuda")
     sg.gemm(A, B)                               # exactly one wave of whole tiles

@@ -69,6 +69,33 @@ def test_noalloc_matches_sgemm_on_two_calls_in_a_row(case):
     assert sg.sgemm_last_device_status() == 0
 
 
+# (M, N, K, transA, transB, alpha, beta): both entry points take the 128 x 128
+# tile (A read m-contiguous) and the same stream-K split (every tile split,
+# at most three segments each)
+SAME_SPLIT = [(1536, 1024, 1024, 1, 0, 1.5, 0.5), (1280, 1280, 768, 1, 1, 1.0, 0.0)]
+
+
+@pytest.mark.parametrize("case", SAME_SPLIT, ids=["1536x1024x1024_TN", "1280x1280x768_TT"])
+def test_in_kernel_fixup_equals_fixup_launch(case):
+    """sgemm finishes split tiles inside the product kernel (the last CTA to
+    arrive adds the partials); sgemm_noalloc leaves them to sk_fixup_kernel.
+    Both add the same partials in the same k order: equal bit for bit."""
+    M, N, K, ta, tb, alpha, beta = case
+    g = torch.Generator().manual_seed(7 + M)
+    A = torch.randn((K, M) if ta else (M, K), generator=g).cuda()
+    B = torch.randn((N, K) if tb else (K, N), generator=g).cuda()
+    C0 = torch.randn((M, N), generator=g).cuda()
+    ref = C0.clone()
+    _call(sg.sgemm, ta, tb, M, N, K, alpha, A, B, beta, ref)
+    assert sg.sgemm_last_launch_count() == 1
+    out = C0.clone()
+    _call(sg.sgemm_noalloc, ta, tb, M, N, K, alpha, A, B, beta, out)
+    assert sg.sgemm_last_launch_count() == 2
+    torch.cuda.synchronize()
+    assert torch.equal(ref, out)
+    assert sg.sgemm_last_device_status() == 0
+
+
 def test_noalloc_uses_the_scratch_path_and_allocates_nothing():
     """A split (two-launch) product through sgemm_noalloc, repeated on new
     shapes, leaves the device's free memory exactly where it was."""
