@@ -188,12 +188,22 @@ def _matrix(t, name):
     if not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     rows, cols = t.shape
-    if cols > 1 and t.stride(1) != 1:
+    st0, st1 = t.stride()
+    if cols > 1 and st1 != 1:
         raise ValueError(f"{name} must have unit column stride (row-major)")
-    ld = t.stride(0) if (rows > 1 or t.stride(0) >= cols) else cols
+    ld = st0 if (rows > 1 or st0 >= cols) else cols
     if ld < cols:
         raise ValueError(f"{name} has overlapping rows")
     return t.data_ptr(), rows, cols, max(ld, 1)
+
+
+def _current_raw_stream(device_index):
+    """cudaStream_t (as int) of torch's current stream on `device_index`."""
+    import torch
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(device_index)
+    return torch.cuda.current_stream(device_index).cuda_stream
 
 
 def transpose(X, out=None, stream=None):
@@ -266,12 +276,13 @@ def gemm(A, B, C=None, alpha=1.0, beta=0.0, transA=False, transB=False, algo=ALG
     if (rc, cc) != (M, N):
         raise ValueError(f"C must be {M} x {N}")
     algo = ALGOS[algo] if isinstance(algo, str) else int(algo)
-    dev = A.device.index
-    if dev is None or dev == torch.cuda.current_device():
-        s = stream if stream is not None else torch.cuda.current_stream()
-        _check(load_library().sgemm_ex(int(bool(transA)), int(bool(transB)), M, N, Ka, float(alpha),
-                                       pa, lda, pb, ldb, float(beta), pc, ldc, s.cuda_stream, algo),
-               "sgemm_ex")
+    dev = A.get_device()
+    if dev == torch.cuda.current_device():
+        s = stream.cuda_stream if stream is not None else _current_raw_stream(dev)
+        st = (_lib or load_library()).sgemm_ex(1 if transA else 0, 1 if transB else 0, M, N, Ka,
+                                               alpha, pa, lda, pb, ldb, beta, pc, ldc, s, algo)
+        if st != 0:
+            raise SgemmError(st, "sgemm_ex")
         return C
     s = stream if stream is not None else torch.cuda.current_stream(A.device)
     with torch.cuda.device(A.device):
