@@ -47,8 +47,10 @@ def _alone(A, B, M, N, ta=0, tb=0):
     return C.clone()
 
 
-@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (2048, 4864, 256), (1000, 1013, 997)],
-                         ids=["stream_k_1024", "pretransposed_2048x4864x256", "repacked_1000x1013x997"])
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (2048, 4864, 256), (1000, 1013, 997),
+                                   (2048, 2048, 2048)],
+                         ids=["stream_k_1024", "pretransposed_2048x4864x256", "repacked_1000x1013x997",
+                              "in_kernel_fixup_2048"])
 def test_graph_replays_interleaved_with_eager_calls(shape):
     M, N, K = shape
     A1, B1 = _operands(M, N, K, 1)

@@ -28,10 +28,12 @@ def _cuda():
     assert sg.sgemm_last_device_status() == 0
 
 
-# (M, N, K, transA, transB, algo): stream-K splits, a transpose ahead, the
-# 3xTF32 split ahead, a strided batch and a transpose
+# (M, N, K, transA, transB, algo): stream-K splits (finished by the fixup
+# pass, and in-kernel), a transpose ahead, the 3xTF32 split ahead, and a
+# transpose on every thread
 JOBS = [(1024, 1024, 1024, 0, 0, "auto"), (2048, 4864, 256, 0, 0, "auto"),
-        (2048, 2560, 512, 1, 1, "tc_3xtf32"), (1536, 1024, 768, 1, 0, "auto")]
+        (2048, 2560, 512, 1, 1, "tc_3xtf32"), (1536, 1024, 768, 1, 0, "auto"),
+        (2048, 2048, 1024, 1, 0, "auto")]
 
 
 def _job_inputs(i):
