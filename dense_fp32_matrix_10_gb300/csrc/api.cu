@@ -274,6 +274,11 @@ int pick_simt_tile(const Args &a, int producer, int sm_count, int64_t batch) {
 #ifndef SG_SK_FIXUP_LAUNCH
 #define SG_SK_FIXUP_LAUNCH 0
 #endif
+// SG_EPI_TMA 1: the 128 x 128 TMA kernels write C through a staged tile and
+// TMA stores when beta == 0 (0: always from registers).
+#ifndef SG_EPI_TMA
+#define SG_EPI_TMA 1
+#endif
 SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws) {
   SkPlan pl{static_cast<int>(tiles), 0, 0, static_cast<int>(tiles < slots ? tiles : slots)};
   if (!have_ws || k_tiles < 2 * kMinSkSegment) return pl;
@@ -448,6 +453,24 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
     }
   }
 
+  // C through staged TMA stores (the 128 x 128 TMA kernels, beta == 0, C
+  // addressable by a tensor map)
+  CUtensorMap tmC;
+  std::memset(&tmC, 0, sizeof(tmC));
+  p.c_tma = 0;
+  // N % 4 == 0: a TMA store writes whole 16-byte granules at the inner edge
+  // of the tensor, so a ragged row end would get up to three floats past N
+  const bool nt_transposing = a.ta == 0 && a.tb == 1 && SG_SIMT_TRANSPOSE_A;   // no staging there
+  if (SG_EPI_TMA && producer == kTma && tile == kTile128x128 && !nt_transposing && a.beta == 0.0f &&
+      a.N % 4 == 0 && reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0) {
+    if (bt.count == 1) {
+      if (encode_tmap(&tmC, a.C, a.M, a.N, a.ldc, 32, 128, true)) p.c_tma = 1;
+    } else if (bt.sc % 4 == 0 &&
+               encode_tmap_batched(&tmC, a.C, a.M, a.N, a.ldc, bt.count, bt.sc, 32, 128, true)) {
+      p.c_tma = 2;
+    }
+  }
+
   const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
   const bool capturing = stream_capturing(stream);
   std::unique_lock<std::mutex> ws_lock(d.ws_mu);
@@ -480,7 +503,8 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   if (plan.sk_tiles > 0 && order_before_use(d.ws_order, stream, capturing) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
   if (pre && (*pre)() != cudaSuccess) return SGEMM_ERR_LAUNCH;
-  cudaError_t e = simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, plan.grid, stream, pdl);
+  cudaError_t e =
+      simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, &tmC, plan.grid, stream, pdl);
   if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
   if (plan.sk_tiles > 0) {

@@ -47,7 +47,7 @@ struct SimtKernelInfo {
 // pdl: launch with programmatic stream serialization (it directly follows
 // another kernel of the same call on the stream).
 using SimtLaunchFn = cudaError_t (*)(const SimtParams &, const CUtensorMap *, const CUtensorMap *,
-                                     int grid, cudaStream_t, bool pdl);
+                                     const CUtensorMap *, int grid, cudaStream_t, bool pdl);
 // Sets the kernel's shared-memory attribute on the current device (once) and
 // reports its shape and occupancy.
 using SimtInfoFn = cudaError_t (*)(SimtKernelInfo *);
@@ -97,9 +97,11 @@ cudaError_t launch_naive(const PlainParams &p, cudaStream_t s);
 cudaError_t launch_smem_tiled(const PlainParams &p, cudaStream_t s);
 cudaError_t launch_scale_c(float *C, int64_t ldc, int M, int N, float beta, cudaStream_t s);
 // out (cols x rows, ld_out) = in (rows x cols, ld_in) transposed (transpose.cu);
-// `status` is the device status word the bounded waits report to.
+// `status` is the device status word the bounded waits report to.  Unless
+// exact_edges, up to three floats past the end of each output row (inside
+// ld_out rounded up to 4) may be written too (library scratch).
 cudaError_t launch_transpose(const float *in, int64_t ld_in, float *out, int64_t ld_out, int rows,
-                             int cols, int sm_count, int *status, cudaStream_t s);
+                             int cols, int sm_count, int *status, cudaStream_t s, bool exact_edges = false);
 // The split pass of the 3xTF32 product (transpose.cu): the TF32 small parts of
 // a rows x cols operand (k along each row when !transpose, down the columns
 // when transpose), written K-major to `small` (ld_out); with `transpose` the

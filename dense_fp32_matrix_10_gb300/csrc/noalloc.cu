@@ -148,7 +148,9 @@ extern "C" sgemm_status_t sgemm_noalloc(int transA, int transB, int64_t M, int64
                                : encode_tmap(&tmB, B, N, K, ldb, 32, ki->bn, true);
     if (!okA || !okB) return SGEMM_ERR_LAUNCH;
   }
-  if (simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, plan.grid, s, false) != cudaSuccess)
+  CUtensorMap tmC;   // C written straight from registers (p.c_tma == 0)
+  std::memset(&tmC, 0, sizeof(tmC));
+  if (simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, &tmC, plan.grid, s, false) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
   if (plan.sk_tiles > 0) {

@@ -92,6 +92,9 @@ struct SimtParams {
   // CTA that arrives last adds the tile's partials in k order and writes C.
   // Null: sk_fixup_kernel does that in a second launch.
   int *sk_count = nullptr;
+  // C written by TMA stores (EPI_TMA kernels; beta == 0 and C addressable by
+  // the tmC tensor map: 2-D, or 3-D with the batch stride)
+  int c_tma = 0;
 };
 
 // Batch index and (tile_m, tile_n) of linear tile t.
@@ -217,7 +220,18 @@ struct SimtConfig {
   // ring (A_TRANS), then the barriers
   static constexpr int RAW_A_STAGES = A_TRANS ? 2 : 0;
   static constexpr int RAW_A_OFFSET = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFFSET = RAW_A_OFFSET + RAW_A_STAGES * A_STAGE_BYTES;
+  // EPI_TMA: the 128 x 128 TMA kernels can stage a finished tile in shared
+  // memory (four 32-column boxes, 128-byte swizzle) and write it to C with
+  // TMA stores, so the math warps go on to the next tile while it drains.
+  // Not the NT kernel (A transposed in shared memory, B k-contiguous), whose
+  // transposing warps already load shared memory heavily: there it lost
+  // (GB300, 96 x 512x512x64: NT 36.3 -> 35.6 TFLOP/s, against NN 36.3 ->
+  // 39.1, TN 38.2 -> 40.6, TT 37.3 -> 38.9).
+  static constexpr bool EPI_TMA =
+      (PRODUCER == kTma) && (MATH_WARPS == 8) && (TN == 8) && !(A_TRANS && B_KMAJOR);
+  static constexpr int STAGING_OFFSET = RAW_A_OFFSET + RAW_A_STAGES * A_STAGE_BYTES;
+  static constexpr int STAGING_BYTES = EPI_TMA ? BM * BN * 4 : 0;
+  static constexpr int BAR_OFFSET = STAGING_OFFSET + STAGING_BYTES;
   // full[STAGES], empty[STAGES], raw_full[2], raw_empty[2]
   static constexpr int SMEM_BYTES = BAR_OFFSET + (2 * STAGES + 4) * 8 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
@@ -689,6 +703,51 @@ __device__ __forceinline__ void store_partial(float *ws, const AccT<Cfg> &acc, i
   }
 }
 
+// 3-D TMA store (batch coordinate c2).
+__device__ __forceinline__ void tma_store_3d(const void *desc, uint32_t src, int32_t c0, int32_t c1,
+                                             int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(desc)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// alpha * acc into the staging tile: column block j = column / 32 holds rows
+// of 128 bytes, 16-byte chunk q of row R at chunk q ^ (R mod 8) (the layout
+// of a 128-byte-swizzled TMA box, 1024-byte aligned).
+template <class Cfg>
+__device__ __forceinline__ void stage_tile(unsigned char *staging, const AccT<Cfg> &acc, float alpha,
+                                           int wm, int wn, int tm, int tn) {
+  constexpr int MODE = acc_mode<Cfg>(), TN = Cfg::TN;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int R = wm * 32 + thread_row<Cfg>(tm, r);
+    if (!Cfg::B_KMAJOR) {
+#pragma unroll
+      for (int h = 0; h < TN / 4; ++h) {
+        const int col = wn * Cfg::WN + h * 32 + 4 * tn;
+        float4 o;
+        o.x = alpha * acc_get<MODE, TN>(acc, r, 4 * h + 0);
+        o.y = alpha * acc_get<MODE, TN>(acc, r, 4 * h + 1);
+        o.z = alpha * acc_get<MODE, TN>(acc, r, 4 * h + 2);
+        o.w = alpha * acc_get<MODE, TN>(acc, r, 4 * h + 3);
+        unsigned char *dst = staging + (col >> 5) * (Cfg::BM * 128) + R * 128 +
+                             ((((col & 31) >> 2) ^ (R & 7)) << 4);
+        *reinterpret_cast<float4 *>(dst) = o;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < TN; ++c) {
+        const int col = wn * Cfg::WN + thread_col<Cfg>(tn, c);
+        unsigned char *dst = staging + (col >> 5) * (Cfg::BM * 128) + R * 128 +
+                             ((((col & 31) >> 2) ^ (R & 7)) << 4) + ((col & 3) << 2);
+        *reinterpret_cast<float *>(dst) = alpha * acc_get<MODE, TN>(acc, r, c);
+      }
+    }
+  }
+}
+
 // Kernels that can finish split tiles themselves (SimtParams::sk_count).
 template <class Cfg>
 __host__ __device__ constexpr bool kInKernelFixup() {
@@ -735,7 +794,8 @@ __device__ __forceinline__ void add_partial(AccT<Cfg> &acc, const float *ws, int
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     simt_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const SimtParams p) {
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const SimtParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ int s_last;   // in-kernel fixup: this CTA arrived last at its tile
   __shared__ __align__(8) uint64_t s_math_bar;
@@ -760,12 +820,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
       mbar_init(raw_full0 + 8 * r, 1);
       mbar_init(raw_empty0 + 8 * r, Cfg::TRANSPOSER_WARPS);
     }
-    if constexpr (kInKernelFixup<Cfg>()) mbar_init(smem_u32(&s_math_bar), Cfg::MATH_WARPS);
+    if constexpr (kInKernelFixup<Cfg>() || Cfg::EPI_TMA) mbar_init(smem_u32(&s_math_bar), Cfg::MATH_WARPS);
     fence_mbar_init();
   }
   if (Cfg::PRODUCER == kTma && threadIdx.x == Cfg::MATH_THREADS) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (Cfg::EPI_TMA && p.c_tma) tma_prefetch_desc(&tmC);
   }
   __syncthreads();
   // Everything above overlaps the previous kernel of the same call (the
@@ -800,6 +861,41 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
   uint32_t it = 0;
   const uint32_t math_bar = smem_u32(&s_math_bar);
   uint32_t math_phase = 0;
+  // Writes a finished tile (alpha applied) to C: through the staging tile and
+  // TMA stores when p.c_tma, else straight from registers.  False if a
+  // bounded wait gave up.
+  const auto finish_tile = [&](const AccT<Cfg> &acc, int tile) -> bool {
+    // tile coordinates only now: nothing but acc stays live across the k-loop
+    int bi, tile_m, tile_n;
+    unit_coords(p, tile, bi, tile_m, tile_n);
+    if constexpr (Cfg::EPI_TMA) {
+      if (p.c_tma) {
+        // the previous tile's stores have read the staging tile
+        if (threadIdx.x == 0) bulk_wait_group_read<0>();
+        if (!math_barrier(math_bar, math_phase, lane, p)) return false;
+        stage_tile<Cfg>(smem + Cfg::STAGING_OFFSET, acc, p.alpha, wm, wn, tm, tn);
+        fence_proxy_async_smem();
+        if (!math_barrier(math_bar, math_phase, lane, p)) return false;
+        if (threadIdx.x == 0) {
+          const int m0 = tile_m * Cfg::BM, n0 = tile_n * Cfg::BN;
+#pragma unroll
+          for (int j = 0; j < Cfg::BN / 32; ++j) {
+            if (n0 + 32 * j >= p.N) break;
+            const uint32_t src = smem_base + Cfg::STAGING_OFFSET + j * (Cfg::BM * 128);
+            if (p.c_tma == 2)
+              tma_store_3d(&tmC, src, n0 + 32 * j, m0, bi);
+            else
+              tma_store_2d(&tmC, src, n0 + 32 * j, m0);
+          }
+          bulk_commit_group();
+        }
+        return true;
+      }
+    }
+    epilogue<Cfg>(p, p.C + static_cast<int64_t>(bi) * p.strideC, acc, tile_m * Cfg::BM,
+                  tile_n * Cfg::BN, wm, wn, tm, tn);
+    return true;
+  };
   for_each_unit(p, [&](const WorkUnit &u) {
     AccT<Cfg> acc;
 #pragma unroll
@@ -816,11 +912,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     }
     if constexpr (!kInKernelFixup<Cfg>()) {
       if (u.slot < 0) {
-        // tile coordinates only now: nothing but acc stays live across the k-loop
-        int bi, tile_m, tile_n;
-        unit_coords(p, u.tile, bi, tile_m, tile_n);
-        epilogue<Cfg>(p, p.C + static_cast<int64_t>(bi) * p.strideC, acc, tile_m * Cfg::BM,
-                      tile_n * Cfg::BN, wm, wn, tm, tn);
+        return finish_tile(acc, u.tile);
       } else {
         // sk_fixup_kernel adds the partials (these kernels run the mid-size
         // products, for which the separate pass is the faster)
@@ -862,13 +954,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
         add_partial<Cfg>(acc, p.workspace + static_cast<int64_t>(slot) * Cfg::BM * Cfg::BN, wm, wn, tm, tn);
       });
     }
-    // tile coordinates only now: nothing but acc stays live across the k-loop
-    int bi, tile_m, tile_n;
-    unit_coords(p, u.tile, bi, tile_m, tile_n);
-    epilogue<Cfg>(p, p.C + static_cast<int64_t>(bi) * p.strideC, acc, tile_m * Cfg::BM,
-                  tile_n * Cfg::BN, wm, wn, tm, tn);
-    return true;
+    return finish_tile(acc, u.tile);
   });
+  // the last tile's TMA stores complete before the CTA (and its shared
+  // memory) goes away
+  if constexpr (Cfg::EPI_TMA) {
+    if (threadIdx.x == 0 && p.c_tma) bulk_wait_group_all();
+  }
 }
 
 }  // namespace sg

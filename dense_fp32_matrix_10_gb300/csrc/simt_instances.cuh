@@ -10,9 +10,9 @@ namespace sg {
 
 template <class Cfg>
 cudaError_t simt_launch(const SimtParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
-                        int grid, cudaStream_t stream, bool pdl) {
+                        const CUtensorMap *tmC, int grid, cudaStream_t stream, bool pdl) {
   return launch_maybe_pdl(simt_gemm_kernel<Cfg>, dim3(grid), dim3(Cfg::THREADS), Cfg::SMEM_BYTES,
-                          stream, pdl, *tmA, *tmB, p);
+                          stream, pdl, *tmA, *tmB, *tmC, p);
 }
 
 template <class Cfg>

@@ -347,11 +347,16 @@ __global__ void __launch_bounds__(256) tf32_small_kernel(const float *in, int64_
 #endif
 
 cudaError_t launch_transpose(const float *in, int64_t ld_in, float *out, int64_t ld_out, int rows,
-                             int cols, int sm_count, int *status, cudaStream_t s) {
+                             int cols, int sm_count, int *status, cudaStream_t s, bool exact_edges) {
   const bool aligned = (reinterpret_cast<uintptr_t>(in) % 16 == 0) &&
                        (reinterpret_cast<uintptr_t>(out) % 16 == 0) && (ld_in % 4 == 0) &&
                        (ld_out % 4 == 0);
-  if (SG_TRANSPOSE_TMA && aligned) {
+  // A TMA store writes whole 16-byte granules at the inner edge of the
+  // tensor: an output row of `rows` floats, rows % 4 != 0, gets up to three
+  // floats written past its end (into the row's padding, or past the last
+  // row).  Where nothing outside the rows may change, such shapes take the
+  // register kernel.
+  if (SG_TRANSPOSE_TMA && aligned && (!exact_edges || rows % 4 == 0)) {
     bool used = false;
     const cudaError_t e =
         launch_transpose_tma<false>(in, ld_in, out, nullptr, ld_out, rows, cols, sm_count, status, s, &used);
@@ -420,7 +425,8 @@ extern "C" sgemm_status_t sgemm_transpose(int64_t rows, int64_t cols, const floa
   if (!d) return why;
 
   if (launch_transpose(in, ld_in, out, ld_out, static_cast<int>(rows), static_cast<int>(cols),
-                       d->sm_count, d->status, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+                       d->sm_count, d->status, reinterpret_cast<cudaStream_t>(stream),
+                       /*exact_edges=*/true) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
   return SGEMM_SUCCESS;

@@ -229,6 +229,20 @@ def test_overlapping_inputs(_cuda, orc):
 
 
 @gpu
+def test_staged_epilogue_batch_gaps(_cuda, orc):
+    """128 x 128 tiles of a batch written by 3-D TMA stores (beta = 0): C_b
+    ragged in M and N (N % 4 == 0), with NaN-filled gaps inside ldc and
+    between the C_b that must stay untouched."""
+    run_batched(orc, 1, 0, 300, 260, 128, 16, alpha=0.75, ldb=264, sb=128 * 264, ldc=268,
+                sc=300 * 268 + 36, seed=21)
+    run_batched(orc, 0, 0, 257, 132, 64, 72, ldb=132, sb=64 * 132, ldc=136, sc=257 * 136 + 8,
+                seed=22)
+    # N % 4 != 0: the register epilogue (exact at the row ends)
+    run_batched(orc, 1, 0, 300, 261, 128, 16, alpha=0.75, ldb=264, sb=128 * 264, ldc=268,
+                sc=300 * 268 + 36, seed=23)
+
+
+@gpu
 def test_stream_k_batch(_cuda, orc):
     """A batch whose tiles outnumber the SMs once but not twice: the k-loop
     of the last wave is split and summed by the fixup pass."""

@@ -173,6 +173,34 @@ def test_guard_bands_untouched(orc):
         assert_close(C.cpu().numpy(), R, K, algo)
 
 
+# (M, N, K, transA, transB): 128 x 128 tiles with beta = 0, ragged in M;
+# N % 4 == 0 takes the staged TMA stores, the odd N the register epilogue
+# (a TMA store would write the rest of the last 16-byte granule of a row)
+STAGED = [(1000, 700, 300, 0, 0), (1003, 1004, 512, 1, 0), (777, 1996, 96, 1, 1),
+          (1003, 1001, 512, 1, 0), (777, 1999, 96, 1, 1)]
+
+
+@pytest.mark.parametrize("case", STAGED, ids=["NN", "TN", "TT", "TN_odd_N", "TT_odd_N"])
+def test_staged_epilogue_guard_bands(orc, case):
+    """Tiles staged in shared memory and written by TMA stores: every output
+    equals the oracle's within tolerance and nothing outside M x N (inside
+    ldc, or past the last row) is written -- the stores clip the ragged
+    tiles."""
+    M, N, K, ta, tb = case
+    g = torch.Generator().manual_seed(M + N)
+    A = torch.rand((K, M) if ta else (M, K), generator=g).mul_(2).sub_(1)
+    B = torch.rand((N, K) if tb else (K, N), generator=g).mul_(2).sub_(1)
+    dA, dB = padded(A.cuda(), (-A.shape[1]) % 4, 0.0), padded(B.cuda(), (-B.shape[1]) % 4, 0.0)
+    ldc = N + (-N) % 4 + 4
+    big = torch.full((M + 2, ldc), 12345.0, device="cuda")
+    C = big[:M, :N]
+    sg.gemm(dA, dB, C, 1.5, 0.0, ta, tb)
+    torch.cuda.synchronize()
+    assert torch.all(big[:M, N:] == 12345.0)
+    assert torch.all(big[M:, :] == 12345.0)
+    assert_close(C.cpu().numpy(), orc.sgemm_f64(ta, tb, 1.5, A.numpy(), B.numpy()), K, f"staged {case}")
+
+
 @pytest.mark.parametrize("op", OPS, ids=["NN", "NT", "TN", "TT"])
 def test_misaligned_pointers_use_cpasync(orc, op):
     ta, tb = op

@@ -128,6 +128,15 @@ def test_leading_dimensions_and_offsets(_cuda, orc, pads):
 
 
 @gpu
+@pytest.mark.parametrize("rows", [201, 202, 203])
+def test_ragged_output_rows_keep_padding(_cuda, orc, rows):
+    """Aligned buffers whose output rows (`rows` floats) do not end on a
+    16-byte boundary: the padding after each output row stays untouched (a
+    TMA store would write the rest of the row's last 16-byte granule)."""
+    run_transpose(orc, rows, 136, seed=rows, pad_out=(-rows) % 4 + 4)
+
+
+@gpu
 def test_torch_wrapper_and_stream(_cuda, orc):
     s = torch.cuda.Stream()
     X = torch.randn(513, 257, device="cuda")
