@@ -560,6 +560,11 @@ struct Pretranspose {
 #ifndef SG_TC_PDL
 #define SG_TC_PDL 0
 #endif
+// Tile-rows per raster group of the tensor-core kernel (L2 reuse of the
+// operand panels that concurrently running tiles share).
+#ifndef SG_TC_GROUP_M
+#define SG_TC_GROUP_M 8
+#endif
 
 sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream, bool pdl = false);
 
@@ -735,7 +740,7 @@ sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream, bool 
   const int64_t num_tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
   if (num_tiles > kMaxDim) return SGEMM_ERR_UNSUPPORTED;
   p.num_tiles = static_cast<int>(num_tiles);
-  p.group_m = 8;
+  p.group_m = SG_TC_GROUP_M;
   p.c_vec4 = (a.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   p.status = d.status;
@@ -816,7 +821,7 @@ sgemm_status_t run_tc3_presplit(const Args &a, DeviceState &d, cudaStream_t s) {
   const int64_t num_tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
   if (num_tiles > kMaxDim) return SGEMM_ERR_LAUNCH;
   p.num_tiles = static_cast<int>(num_tiles);
-  p.group_m = 8;
+  p.group_m = SG_TC_GROUP_M;
   p.c_vec4 = (a.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   p.status = d.status;
