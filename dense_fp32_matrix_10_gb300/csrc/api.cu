@@ -455,21 +455,31 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
 
   // C through staged TMA stores (the 128 x 128 TMA kernels, beta == 0, C
   // addressable by a tensor map)
+  // A tensor map of C (32-column x 128-row boxes, 128-byte swizzle), when C
+  // is TMA-addressable: for the staged stores (beta == 0) or the producer's
+  // L2 prefetch of C (beta != 0).
   CUtensorMap tmC;
   std::memset(&tmC, 0, sizeof(tmC));
   p.c_tma = 0;
-  // N % 4 == 0: a TMA store writes whole 16-byte granules at the inner edge
-  // of the tensor, so a ragged row end would get up to three floats past N
-  const bool nt_transposing = a.ta == 0 && a.tb == 1 && SG_SIMT_TRANSPOSE_A;   // no staging there
-  if (SG_EPI_TMA && producer == kTma && tile == kTile128x128 && !nt_transposing && a.beta == 0.0f &&
-      a.N % 4 == 0 && reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0) {
+  p.c_pref = 0;
+  int c_map = 0;   // 1: 2-D, 2: 3-D (strided batch)
+  if (producer == kTma && reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.ldc % 4 == 0 &&
+      (SG_EPI_TMA || a.beta != 0.0f)) {
     if (bt.count == 1) {
-      if (encode_tmap(&tmC, a.C, a.M, a.N, a.ldc, 32, 128, true)) p.c_tma = 1;
+      if (encode_tmap(&tmC, a.C, a.M, a.N, a.ldc, 32, 128, true)) c_map = 1;
     } else if (bt.sc % 4 == 0 &&
                encode_tmap_batched(&tmC, a.C, a.M, a.N, a.ldc, bt.count, bt.sc, 32, 128, true)) {
-      p.c_tma = 2;
+      c_map = 2;
     }
   }
+  // Staged stores: the 128 x 128 tiles, not the NT kernel that transposes A
+  // in shared memory, and N % 4 == 0 -- a TMA store writes whole 16-byte
+  // granules at the inner edge of the tensor, so a ragged row end would get
+  // up to three floats past N.
+  const bool nt_transposing = a.ta == 0 && a.tb == 1 && SG_SIMT_TRANSPOSE_A;
+  if (SG_EPI_TMA && c_map && tile == kTile128x128 && !nt_transposing && a.beta == 0.0f && a.N % 4 == 0)
+    p.c_tma = c_map;
+  if (a.beta != 0.0f) p.c_pref = c_map;
 
   const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
   const bool capturing = stream_capturing(stream);

@@ -95,6 +95,9 @@ struct SimtParams {
   // C written by TMA stores (EPI_TMA kernels; beta == 0 and C addressable by
   // the tmC tensor map: 2-D, or 3-D with the batch stride)
   int c_tma = 0;
+  // beta != 0 and C addressable by tmC (1: 2-D, 2: 3-D): the TMA producer
+  // prefetches each C tile into L2 before the epilogue reads it
+  int c_pref = 0;
 };
 
 // Batch index and (tile_m, tile_n) of linear tile t.
@@ -153,6 +156,13 @@ __device__ __forceinline__ int sk_for_each_segment(const SimtParams &p, int64_t 
   }
   return n;
 }
+
+// SG_SIMT_PREFETCH_C    the TMA producer asks L2 for a unit's C tile (beta != 0)
+//                        when it issues the loads of the unit's k-slice this
+//                        many before the last (0: never).
+#ifndef SG_SIMT_PREFETCH_C
+#define SG_SIMT_PREFETCH_C 2
+#endif
 
 // SG_SIMT_TRANSPOSERS  producer warps (1..3) that share the A transpose;
 // SG_SIMT_TRANSPOSER_REGS their registers per thread (the math warps get the
@@ -262,21 +272,49 @@ __device__ __forceinline__ uint32_t kmajor_offset(int row, int k) {
 }
 
 // ------------------------------------------------------------------ producer
+// TMA prefetch of one box of C into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int32_t c0, int32_t c1,
+                                                   int32_t c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 template <class Cfg>
 __device__ __forceinline__ void produce_tma(const SimtParams &p, const CUtensorMap *tmA,
-                                            const CUtensorMap *tmB, uint32_t smem_base,
-                                            uint32_t full0, uint32_t empty0, uint32_t raw_full0,
-                                            uint32_t raw_empty0, bool &ok) {
+                                            const CUtensorMap *tmB, const CUtensorMap *tmC,
+                                            uint32_t smem_base, uint32_t full0, uint32_t empty0,
+                                            uint32_t raw_full0, uint32_t raw_empty0, bool &ok) {
   uint32_t it = 0;        // k-slices whose stage copies are issued
   uint32_t raw_it = 0;    // k-slices whose raw A copies are issued
   for_each_unit(p, [&](const WorkUnit &u) {
     int bi, tm, tn;
     unit_coords(p, u.tile, bi, tm, tn);
     const int m0 = tm * Cfg::BM, n0 = tn * Cfg::BN;
+    // beta != 0: the epilogue will read this tile of C (the unit writes C, or
+    // may finish its split tile in-kernel); ask L2 for it a little ahead
+    const int pf_kt = (SG_SIMT_PREFETCH_C > 0 && p.c_pref && (u.slot < 0 || p.sk_count != nullptr))
+                          ? (u.k1 - SG_SIMT_PREFETCH_C > u.k0 ? u.k1 - SG_SIMT_PREFETCH_C : u.k0)
+                          : -1;
     for (int kt = u.k0; kt < u.k1; ++kt) {
       const uint32_t s = it % Cfg::STAGES;
       const uint32_t round = it / Cfg::STAGES;
       const int k0 = kt * Cfg::BK;
+      if (kt == pf_kt) {
+        for (int j = 0; j < Cfg::BN / 32 && n0 + 32 * j < p.N; ++j) {
+          if (p.c_pref == 2)
+            tma_prefetch_l2_3d(tmC, n0 + 32 * j, m0, bi);
+          else
+            tma_prefetch_l2_2d(tmC, n0 + 32 * j, m0);
+        }
+      }
       if (Cfg::A_TRANS) {  // A: raw k-contiguous tile into the raw ring
         const uint32_t r = raw_it % 2, rr = raw_it / 2;
         if (rr > 0 &&
@@ -842,7 +880,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::PRODUCER_REGS));
     if (Cfg::PRODUCER == kTma) {
       if (threadIdx.x == Cfg::MATH_THREADS)
-        produce_tma<Cfg>(p, &tmA, &tmB, smem_base, full0, empty0, raw_full0, raw_empty0, ok);
+        produce_tma<Cfg>(p, &tmA, &tmB, &tmC, smem_base, full0, empty0, raw_full0, raw_empty0, ok);
       else if (Cfg::A_TRANS && warp > Cfg::MATH_WARPS && warp <= Cfg::MATH_WARPS + Cfg::TRANSPOSER_WARPS)
         transpose_a<Cfg>(p, smem, full0, empty0, raw_full0, raw_empty0, warp - Cfg::MATH_WARPS - 1,
                          lane, ok);
