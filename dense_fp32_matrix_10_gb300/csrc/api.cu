@@ -74,9 +74,16 @@ const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb) {
   return &d.tcinfo[ta][tb];
 }
 
-const TcKernelInfo *tc_kernel_info_presplit(DeviceState &d) {
+const TcKernelInfo *tc_kernel_info_presplit(DeviceState &d, int bn) {
+  if (bn == 256) {
+    std::call_once(d.tcpre_wide_once, [&]() {
+      d.tcpre_wide_err = tc3_presplit_entry(256).info(&d.tcpre_wide);
+      if (d.tcpre_wide_err != cudaSuccess) cudaGetLastError();
+    });
+    return d.tcpre_wide_err == cudaSuccess ? &d.tcpre_wide : nullptr;
+  }
   std::call_once(d.tcpre_once, [&]() {
-    d.tcpre_err = tc3_presplit_entry().info(&d.tcpre);
+    d.tcpre_err = tc3_presplit_entry(128).info(&d.tcpre);
     if (d.tcpre_err != cudaSuccess) cudaGetLastError();
   });
   return d.tcpre_err == cudaSuccess ? &d.tcpre : nullptr;
@@ -781,8 +788,25 @@ sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream, bool 
 #ifndef SG_TC_PRESPLIT
 #define SG_TC_PRESPLIT 1
 #endif
+// SG_TC_WIDE  1: the pre-split kernel may run 128 x 256 tiles (0: never).
+#ifndef SG_TC_WIDE
+#define SG_TC_WIDE 1
+#endif
+// Tile width of the pre-split kernel.  A 128 x 256 tile costs about 1.9
+// times a 128 x 128 one on GB300 (8192^3 NN: 14 rounds of wide tiles in
+// 4.09 ms against 27 rounds of narrow ones in 4.13 ms, split passes
+// included); the wide tile is taken when its rounds of one tile per SM,
+// times 1.9, come to fewer than the narrow tile's (2048^3: 1 round against 2;
+// not 4096^3: 4 against 7).
+int presplit_tile_n(const Args &a, int sm_count) {
+  if (!SG_TC_WIDE) return 128;
+  const int64_t tm = cdiv(a.M, 128);
+  const int64_t narrow = cdiv(tm * cdiv(a.N, 128), sm_count), wide = cdiv(tm * cdiv(a.N, 256), sm_count);
+  return 19 * wide < 10 * narrow ? 256 : 128;
+}
+
 sgemm_status_t run_tc3_presplit(const Args &a, DeviceState &d, cudaStream_t s) {
-  const TcKernelInfo *ki = tc_kernel_info_presplit(d);
+  const TcKernelInfo *ki = tc_kernel_info_presplit(d, presplit_tile_n(a, d.sm_count));
   if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_UNSUPPORTED;
   const int64_t ldk = a.K;   // K % 4 == 0 on this path
   const size_t mat_a = (static_cast<size_t>(a.M) * ldk * sizeof(float) + 255) & ~size_t(255);
@@ -843,7 +867,7 @@ sgemm_status_t run_tc3_presplit(const Args &a, DeviceState &d, cudaStream_t s) {
     return SGEMM_ERR_LAUNCH;
   const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
   const int grid = static_cast<int>(num_tiles < slots ? num_tiles : slots);
-  if (tc3_presplit_entry().launch(p, &tmA, &tmB, &tmAs, &tmBs, grid, s, false) != cudaSuccess)
+  if (tc3_presplit_entry(ki->bn).launch(p, &tmA, &tmB, &tmAs, &tmBs, grid, s, false) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
   t_last_launches = 3;
   if (order_after_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;

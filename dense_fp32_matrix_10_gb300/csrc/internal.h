@@ -77,7 +77,8 @@ struct TcEntry {
 TcEntry tc3_entry(int transA, int transB);
 // The form that reads pre-split operands: A and B k-contiguous big parts plus
 // their small parts, all through TMA (no conversion in the kernel).
-TcEntry tc3_presplit_entry();
+// bn = 128 or 256: the output tile width.
+TcEntry tc3_presplit_entry(int bn);
 
 // Second pass of a stream-K launch (sk_fixup.cu).
 cudaError_t launch_sk_fixup(const SimtParams &p, int bm, int bn, int grid_main, int sk_tiles,

@@ -24,7 +24,7 @@ static cudaError_t tc3_info(TcKernelInfo *info) {
   cudaFuncAttributes attr;
   e = cudaFuncGetAttributes(&attr, tc3_gemm_kernel<Cfg>);
   if (e != cudaSuccess) return e;
-  if (attr.numRegs * Cfg::THREADS < 128 * (Cfg::REGS_WG0 + Cfg::REGS_EPI + 2 * Cfg::REGS_CONV))
+  if (attr.numRegs * Cfg::THREADS < Cfg::REGS_SPLIT)
     return cudaErrorInvalidConfiguration;
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, tc3_gemm_kernel<Cfg>, Cfg::THREADS,
@@ -36,13 +36,15 @@ static cudaError_t tc3_info(TcKernelInfo *info) {
   return cudaSuccess;
 }
 
-template <bool AK, bool BK, bool PRESPLIT = false>
+template <bool AK, bool BK, bool PRESPLIT = false, int BN = 128>
 static TcEntry tc3_make() {
-  using Cfg = TcConfig<AK, BK, PRESPLIT>;
+  using Cfg = TcConfig<AK, BK, PRESPLIT, BN>;
   return TcEntry{&tc3_launch<Cfg>, &tc3_info<Cfg>};
 }
 
-TcEntry tc3_presplit_entry() { return tc3_make<true, true, true>(); }
+TcEntry tc3_presplit_entry(int bn) {
+  return bn == 256 ? tc3_make<true, true, true, 256>() : tc3_make<true, true, true>();
+}
 
 TcEntry tc3_entry(int transA, int transB) {
   // A stored M x K (transA = N) and B stored N x K (transB = T) are k-contiguous.

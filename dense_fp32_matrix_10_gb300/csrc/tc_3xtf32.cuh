@@ -74,7 +74,7 @@ struct TcParams {
   int *status;
 };
 
-template <bool A_KMAJOR_, bool B_KMAJOR_, bool PRESPLIT_ = false>
+template <bool A_KMAJOR_, bool B_KMAJOR_, bool PRESPLIT_ = false, int BN_ = 128>
 struct TcConfig {
   static constexpr bool A_KMAJOR = A_KMAJOR_;
   static constexpr bool B_KMAJOR = B_KMAJOR_;
@@ -83,28 +83,37 @@ struct TcConfig {
   // the converter warps have nothing to do.
   static constexpr bool PRESPLIT = PRESPLIT_;
   static_assert(!PRESPLIT || (A_KMAJOR && B_KMAJOR), "pre-split operands are K-major");
-  static constexpr int BM = 128, BN = 128, BK = 32;
+  // BN = 256 (pre-split form only): 128 x 256 tiles, one 128 x 256 x 8 MMA
+  // per product term.  The MMAs read both operands from shared memory, and
+  // at 128 x 128 that read (8 KiB per MMA) bounds them: a run without any
+  // TMA refill was no more than 5 % faster.  The wide MMA reads 12 KiB for
+  // twice the work.
+  static constexpr int BM = 128, BN = BN_, BK = 32;
+  static_assert(BN == 128 || (BN == 256 && PRESPLIT_), "256-wide tiles: pre-split form only");
   static constexpr int TILE_BYTES = 128 * 32 * 4;  // one 128 x 32 FP32 tile
+  static constexpr int B_TILE_BYTES = BN * 32 * 4;
   // A_TMEM: an m-contiguous A (through the raw ring) is converted straight
   // into tensor memory and the MMAs read it from there, so shared memory
   // carries only B for them (its bandwidth bounds this kernel).
   static constexpr bool A_TMEM = !A_KMAJOR && SG_TC_A_TMEM;
   // MMA ring stage: A big, A small (unless A_TMEM), B big, B small (K-major,
   // 128 B swizzle).  A k-contiguous operand's big tile is its raw TMA tile.
-  static constexpr int STAGE_BYTES = (A_TMEM ? 2 : 4) * TILE_BYTES;
+  static constexpr int STAGE_BYTES = (A_TMEM ? 0 : 2 * TILE_BYTES) + 2 * B_TILE_BYTES;
   static constexpr int A_BIG = 0, A_SMALL = TILE_BYTES, B_BIG = A_TMEM ? 0 : 2 * TILE_BYTES,
-                       B_SMALL = B_BIG + TILE_BYTES;
+                       B_SMALL = B_BIG + B_TILE_BYTES;
   // Raw ring: the m/n-contiguous operands' FP32 slices, dense [32 k][128 mn].
   static constexpr int RAW_OPERANDS = (A_KMAJOR ? 0 : 1) + (B_KMAJOR ? 0 : 1);
   // Raw-ring depth: a TMA load must land within RAW_STAGES k-slices of MMA
   // work; with A in TMEM the smaller MMA stages leave room for a deeper ring.
   static constexpr int RAW_STAGES = RAW_OPERANDS ? (A_TMEM ? SG_TC_ATMEM_RAW_STAGES : SG_TC_RAW_STAGES) : 0;
   static constexpr int RAW_STAGE_BYTES = RAW_OPERANDS * TILE_BYTES;
-  static constexpr int STAGES = A_TMEM ? SG_TC_ATMEM_STAGES : ((RAW_OPERANDS == 2) ? 2 : 3);
-  // TMEM columns: two 128-column accumulators, then (A_TMEM) per stage A big
+  // (BN = 256: two stages of 96 KiB)
+  static constexpr int STAGES =
+      A_TMEM ? SG_TC_ATMEM_STAGES : ((RAW_OPERANDS == 2 || BN == 256) ? 2 : 3);
+  // TMEM columns: two BN-column accumulators, then (A_TMEM) per stage A big
   // (32 columns = 32 k) and A small (32 more).
   static constexpr int A_TMEM_COL = 256;
-  static constexpr int TMEM_COLS = A_TMEM ? 512 : 256;
+  static constexpr int TMEM_COLS = (A_TMEM || BN == 256) ? 512 : 256;
   static_assert(!A_TMEM || A_TMEM_COL + 64 * STAGES <= TMEM_COLS, "A stages exceed TMEM");
   static constexpr int RAW_OFFSET = STAGES * STAGE_BYTES;
   static constexpr int RAW_A = 0, RAW_B = A_KMAJOR ? 0 : TILE_BYTES;  // within a raw stage
@@ -115,19 +124,25 @@ struct TcConfig {
   static constexpr int NUM_BARS = 3 * STAGES + 2 * RAW_BARS + 4 + 1;
   static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
-  static constexpr int THREADS = 512;
-  static constexpr uint32_t IDESC = idesc_tf32(128, 128);
+  // BN = 256: three warpgroups (no converters; the tile's two 128-column
+  // halves go to two epilogue warpgroups)
+  static constexpr int THREADS = BN == 256 ? 384 : 512;
+  static constexpr uint32_t IDESC = idesc_tf32(128, BN);
   // Two converter warpgroups: the conversion is ~250 dependent instructions
   // per thread and k-slice with one warpgroup, more than the 768 tensor-core
   // cycles of the slice's 12 MMAs.
   static constexpr int CONVERTER_WARPS = 8;
   static constexpr int CONVERTER_THREADS = 32 * CONVERTER_WARPS;
-  static constexpr int EPILOGUE_WARPS = 4;
+  static constexpr int EPILOGUE_WARPS = BN / 32;
   static constexpr int CHUNK_KTILES = 8;  // k-slices accumulated in TMEM per promotion
   // setmaxnreg split by warpgroup: {producer, MMA, idle}, epilogue (holds a
-  // 128-float row of the tile), two converter warpgroups.
-  static constexpr int REGS_WG0 = 56, REGS_EPI = 240, REGS_CONV = 104;
-  static_assert(128 * (REGS_WG0 + REGS_EPI + 2 * REGS_CONV) <= THREADS * ((65536 / THREADS) & ~7),
+  // 128-float half row of the tile), then two converter warpgroups or (BN =
+  // 256) the second epilogue warpgroup.
+  static constexpr int REGS_WG0 = BN == 256 ? 40 : 56, REGS_EPI = BN == 256 ? 232 : 240,
+                       REGS_CONV = 104;
+  static constexpr int REGS_SPLIT =
+      128 * (REGS_WG0 + (BN == 256 ? 2 * REGS_EPI : REGS_EPI + 2 * REGS_CONV));
+  static_assert(REGS_SPLIT <= THREADS * ((65536 / THREADS) & ~7),
                 "register split exceeds the launch budget");
 };
 
@@ -158,7 +173,8 @@ __device__ __forceinline__ void tc_produce(const TcParams &p, const CUtensorMap 
                                            const TcBars<Cfg> &bar) {
   constexpr bool ANY_K = Cfg::A_KMAJOR || Cfg::B_KMAJOR;
   constexpr uint32_t K_BYTES =
-      ((Cfg::A_KMAJOR ? 1 : 0) + (Cfg::B_KMAJOR ? 1 : 0)) * Cfg::TILE_BYTES * (Cfg::PRESPLIT ? 2 : 1);
+      Cfg::PRESPLIT ? Cfg::STAGE_BYTES
+                    : ((Cfg::A_KMAJOR ? 1 : 0) + (Cfg::B_KMAJOR ? 1 : 0)) * Cfg::TILE_BYTES;
   uint32_t it = 0;        // k-slices whose copies are all issued
   bool k_issued = false;  // the k-contiguous part of slice `it` is issued
   bool ok = true;
@@ -178,14 +194,20 @@ __device__ __forceinline__ void tc_produce(const TcParams &p, const CUtensorMap 
         const uint32_t st = sbase + s * Cfg::STAGE_BYTES;
         mbar_arrive_expect_tx(bar.full(s), K_BYTES);
         if (Cfg::A_KMAJOR) tma_load_2d(st + Cfg::A_BIG, tmA, bar.full(s), k0, m0);
-        if (Cfg::B_KMAJOR) tma_load_2d(st + Cfg::B_BIG, tmB, bar.full(s), k0, n0);
+        // op(B) in boxes of 128 n rows (two for a 256-wide tile, stacked)
+#pragma unroll
+        for (int h = 0; h < Cfg::BN / 128; ++h)
+          if (Cfg::B_KMAJOR)
+            tma_load_2d(st + Cfg::B_BIG + h * Cfg::TILE_BYTES, tmB, bar.full(s), k0, n0 + 128 * h);
         if (Cfg::PRESPLIT) {
           tma_load_2d(st + Cfg::A_SMALL, tmAs, bar.full(s), k0, m0);
-          tma_load_2d(st + Cfg::B_SMALL, tmBs, bar.full(s), k0, n0);
+#pragma unroll
+          for (int h = 0; h < Cfg::BN / 128; ++h)
+            tma_load_2d(st + Cfg::B_SMALL + h * Cfg::TILE_BYTES, tmBs, bar.full(s), k0, n0 + 128 * h);
         }
         k_issued = true;
       }
-      if (Cfg::RAW_OPERANDS) {  // m/n-contiguous operands into the raw ring
+      if constexpr (Cfg::RAW_OPERANDS > 0) {  // m/n-contiguous operands into the raw ring
         const uint32_t r = it % Cfg::RAW_STAGES, rround = it / Cfg::RAW_STAGES;
         if (rround > 0 &&
             !wait_parity_bounded(bar.raw_empty(r), (rround - 1) & 1, p.wait_budget_ns, p.status)) {
@@ -206,7 +228,7 @@ __device__ __forceinline__ void tc_produce(const TcParams &p, const CUtensorMap 
       if (ANY_K)
         wait_parity_bounded(bar.full(j % Cfg::STAGES), (j / Cfg::STAGES) & 1, p.wait_budget_ns,
                             nullptr);
-      if (Cfg::RAW_OPERANDS)
+      if constexpr (Cfg::RAW_OPERANDS > 0)
         wait_parity_bounded(bar.raw_full(j % Cfg::RAW_STAGES), (j / Cfg::RAW_STAGES) & 1,
                             p.wait_budget_ns, nullptr);
     }
@@ -371,7 +393,7 @@ __device__ __forceinline__ void tc_issue(const TcParams &p, uint32_t sbase, uint
         break;
       }
       tc_fence_after_sync();
-      const uint32_t d = tmem_base + b * 128;
+      const uint32_t d = tmem_base + b * Cfg::BN;
       const int kc1 = min(kc0 + Cfg::CHUNK_KTILES, p.k_tiles);
       for (int kt = kc0; kt < kc1; ++kt, ++it) {
         const uint32_t s = it % Cfg::STAGES, round = it / Cfg::STAGES;
@@ -413,24 +435,27 @@ __device__ __forceinline__ void tc_issue(const TcParams &p, uint32_t sbase, uint
 }
 
 // ------------------------------------------------------------------ epilogue
+// Warp q of epilogue warpgroup `half` owns tile rows 32q .. 32q+31 (TMEM
+// lanes) and columns 128 * half .. +127.
 template <class Cfg>
 __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_base,
-                                            const TcBars<Cfg> &bar, int q, int lane) {
+                                            const TcBars<Cfg> &bar, int q, int half, int lane) {
+  constexpr int W = 128;   // columns per thread
   uint32_t chunk_iter = 0;
   const bool read_c = p.beta != 0.0f;
   const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
   for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-    float acc[Cfg::BN];  // this thread's row of the tile, FP32 round-to-nearest sums
+    float acc[W];  // this thread's half row of the tile, FP32 round-to-nearest sums
 #pragma unroll
-    for (int j = 0; j < Cfg::BN; ++j) acc[j] = 0.0f;
+    for (int j = 0; j < W; ++j) acc[j] = 0.0f;
     for (int kc0 = 0; kc0 < p.k_tiles; kc0 += Cfg::CHUNK_KTILES, ++chunk_iter) {
       const uint32_t b = chunk_iter & 1, use = chunk_iter >> 1;
       if (!wait_parity_bounded(bar.acc_full(b), use & 1, p.wait_budget_ns, p.status)) return;
       tc_fence_after_sync();
 #pragma unroll
-      for (int cc = 0; cc < Cfg::BN / 32; ++cc) {
+      for (int cc = 0; cc < W / 32; ++cc) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + lane_addr + b * 128 + cc * 32, v);
+        tmem_ld_32x32b_x32(tmem_base + lane_addr + b * Cfg::BN + half * W + cc * 32, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc[cc * 32 + j] += __uint_as_float(v[j]);
@@ -442,11 +467,11 @@ __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_bas
     int tm, tn;
     tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     const int row = tm * Cfg::BM + 32 * q + lane;
-    const int n0 = tn * Cfg::BN;
+    const int n0 = tn * Cfg::BN + half * W;
     if (row < p.M) {
       float *crow = p.C + static_cast<int64_t>(row) * p.ldc;
 #pragma unroll
-      for (int j = 0; j < Cfg::BN; j += 4) {
+      for (int j = 0; j < W; j += 4) {
         const int n = n0 + j;
         if (p.c_vec4 && n + 3 < p.N) {
           float4 o;
@@ -531,9 +556,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if (lane == 0) tc_issue<Cfg>(p, sbase, tmem_base, bar);
       __syncwarp();
     }
-  } else if (warp < 8) {
+  } else if (warp < 8 || Cfg::BN == 256) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::REGS_EPI));
-    tc_epilogue<Cfg>(p, tmem_base, bar, warp & 3, lane);
+    tc_epilogue<Cfg>(p, tmem_base, bar, warp & 3, (warp >> 2) - 1, lane);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::REGS_CONV));
     tc_convert<Cfg>(p, smem, bar, tmem_base, threadIdx.x - 256, warp, lane);

@@ -510,6 +510,36 @@ def test_tensor_core_split_ahead_ragged(orc, op):
         assert_close(G, R, K, f"tc split ahead {M}x{N}x{K} {op}")
 
 
+@pytest.mark.parametrize("N", [2500, 2400])
+def test_tensor_core_wide_tiles_ragged(orc, N):
+    """Split-ahead 3xTF32 products run 128 x 256 tiles whose two 128-column
+    halves are loaded as separate op(B) boxes and written by separate
+    epilogue warpgroups.  N = 2500 ends in a partly filled second half, N =
+    2400 in a second half wholly past N (its op(B) box reads only fill
+    values).  Rows depend only on their own tile row: the rows that an M =
+    1792 and an M = 1664 product of the same operands share agree bit for
+    bit.  Sampled outputs are checked against the oracle, with alpha and beta
+    (C read)."""
+    K = 512
+    g = torch.Generator().manual_seed(N)
+    A = torch.randn(1792, K, generator=g)
+    B = torch.randn(K, N, generator=g)
+    C0 = torch.rand(1792, N, generator=g).mul_(2).sub_(1)
+    dA, dB = A.cuda(), B.cuda()
+    C_full, C_part = C0.cuda(), C0[:1664].cuda()
+    sg.gemm(dA, dB, C_full, 0.75, 0.5, 0, 0, algo="tc_3xtf32")
+    n_full = sg.sgemm_last_launch_count()
+    sg.gemm(dA[:1664], dB, C_part, 0.75, 0.5, 0, 0, algo="tc_3xtf32")
+    n_part = sg.sgemm_last_launch_count()
+    torch.cuda.synchronize()
+    assert n_full == 3 and n_part == 3
+    assert torch.equal(C_full[:1664], C_part)
+    I, J = sample_indices(1792, N, 3000, seed=N)
+    J[:200] = np.arange(N - 200, N)   # the ragged last tile's columns
+    R = orc.sgemm_entries_f64(0, 0, 0.75, A.numpy(), B.numpy(), 0.5, C0.numpy(), I, J)
+    assert_close(C_full.cpu().numpy()[I, J], R, K, f"tc wide tiles N={N}")
+
+
 def test_pretransposed_on_two_streams(orc):
     """Calls on different streams share the transposed-operand scratch; the
     library orders them, so every result is right."""
