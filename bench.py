@@ -61,7 +61,7 @@ FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = {
     "simt": ["ptx.cuh", "internal.h", "simt_gemm.cuh", "simt_instances.cuh", "simt_tma_an.cu",
              "simt_tma_at.cu", "simt_cpasync_an.cu", "simt_cpasync_at.cu", "sk_fixup.cu"],
-    "tc_3xtf32": ["ptx.cuh", "tc_3xtf32.cuh", "tc_3xtf32.cu"],
+    "tc_3xtf32": ["ptx.cuh", "tc_3xtf32.cuh", "tc_3xtf32_pair.cuh", "tc_3xtf32.cu"],
     "transpose": ["transpose.cu"],
 }
 

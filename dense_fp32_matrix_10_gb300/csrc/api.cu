@@ -74,6 +74,15 @@ const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb) {
   return &d.tcinfo[ta][tb];
 }
 
+const TcKernelInfo *tc_kernel_info_pair(DeviceState &d, int bn) {
+  const int i = bn == 256 ? 1 : 0;
+  std::call_once(d.tcpair_once[i], [&]() {
+    d.tcpair_err[i] = tc3_pair_entry(bn).info(&d.tcpair[i]);
+    if (d.tcpair_err[i] != cudaSuccess) cudaGetLastError();
+  });
+  return d.tcpair_err[i] == cudaSuccess ? &d.tcpair[i] : nullptr;
+}
+
 const TcKernelInfo *tc_kernel_info_presplit(DeviceState &d, int bn) {
   if (bn == 256) {
     std::call_once(d.tcpre_wide_once, [&]() {
@@ -757,6 +766,7 @@ sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream, bool 
   const int64_t num_tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
   if (num_tiles > kMaxDim) return SGEMM_ERR_UNSUPPORTED;
   p.num_tiles = static_cast<int>(num_tiles);
+  p.wide_tiles = p.num_tiles;
   p.group_m = SG_TC_GROUP_M;
   p.c_vec4 = (a.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
@@ -788,7 +798,8 @@ sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream, bool 
 #ifndef SG_TC_PRESPLIT
 #define SG_TC_PRESPLIT 1
 #endif
-// SG_TC_WIDE  1: the pre-split kernel may run 128 x 256 tiles (0: never).
+// SG_TC_WIDE  1: the pre-split kernel may run 256-wide tiles (0: never,
+//             2: always).
 #ifndef SG_TC_WIDE
 #define SG_TC_WIDE 1
 #endif
@@ -799,14 +810,55 @@ sgemm_status_t run_tc3(const Args &a, DeviceState &d, cudaStream_t stream, bool 
 // times 1.9, come to fewer than the narrow tile's (2048^3: 1 round against 2;
 // not 4096^3: 4 against 7).
 int presplit_tile_n(const Args &a, int sm_count) {
-  if (!SG_TC_WIDE) return 128;
+  if (SG_TC_WIDE != 1) return SG_TC_WIDE ? 256 : 128;
   const int64_t tm = cdiv(a.M, 128);
   const int64_t narrow = cdiv(tm * cdiv(a.N, 128), sm_count), wide = cdiv(tm * cdiv(a.N, 256), sm_count);
   return 19 * wide < 10 * narrow ? 256 : 128;
 }
 
+// SG_TC_PAIR  1: run the pre-split product on CTA pairs (0: never).
+#ifndef SG_TC_PAIR
+#define SG_TC_PAIR 1
+#endif
+
+// Work plan on CTA pairs.  A 256 x 256 pair tile costs about 1.6 times a
+// 256 x 128 one on GB300 (4096^3 NN: 4 rounds of wide tiles in 0.46 ms
+// against 7 rounds of narrow ones in 0.50 ms, kernel alone).  Of three plans
+// -- all narrow, all wide, or whole rounds of wide tiles with the rest of the
+// tiles cut into column halves (so the last, partial round is spread over
+// twice the units) -- the one of least cost in rounds is taken.
+struct PairPlan {
+  int bn;              // tile width of the kernel: 128 or 256
+  int64_t wide_tiles;  // units [0, wide_tiles) are whole tiles
+  int64_t units;       // whole tiles, then column halves of the rest
+};
+PairPlan plan_pair(const Args &a, int64_t clusters) {
+  const int64_t tm = cdiv(a.M, 256);
+  const int64_t narrow = tm * cdiv(a.N, 128), wide = tm * cdiv(a.N, 256);
+  const int64_t full = wide / clusters, rest = wide - full * clusters;
+  const int64_t cost_narrow = 10 * cdiv(narrow, clusters);
+  const int64_t cost_wide = 16 * cdiv(wide, clusters);
+  const int64_t cost_mixed = full > 0 && rest > 0 ? 16 * full + 10 * cdiv(2 * rest, clusters)
+                                                  : cost_wide;
+  if (SG_TC_WIDE == 0 || (SG_TC_WIDE == 1 && cost_narrow < cost_wide && cost_narrow < cost_mixed))
+    return PairPlan{128, narrow, narrow};
+  if (SG_TC_WIDE == 2 || cost_wide <= cost_mixed) return PairPlan{256, wide, wide};
+  return PairPlan{256, full * clusters, full * clusters + 2 * rest};
+}
+
 sgemm_status_t run_tc3_presplit(const Args &a, DeviceState &d, cudaStream_t s) {
-  const TcKernelInfo *ki = tc_kernel_info_presplit(d, presplit_tile_n(a, d.sm_count));
+  // CTA pairs if the device runs them, else one CTA per tile
+  PairPlan plan{0, 0, 0};
+  const TcKernelInfo *ki = nullptr;
+  if (SG_TC_PAIR) {
+    const TcKernelInfo *k128 = tc_kernel_info_pair(d, 128), *k256 = tc_kernel_info_pair(d, 256);
+    if (k128 && k256) {
+      plan = plan_pair(a, k256->max_ctas / 2);
+      ki = plan.bn == 256 ? k256 : k128;
+    }
+  }
+  const bool pair = ki != nullptr;
+  if (!pair) ki = tc_kernel_info_presplit(d, presplit_tile_n(a, d.sm_count));
   if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_UNSUPPORTED;
   const int64_t ldk = a.K;   // K % 4 == 0 on this path
   const size_t mat_a = (static_cast<size_t>(a.M) * ldk * sizeof(float) + 255) & ~size_t(255);
@@ -852,22 +904,30 @@ sgemm_status_t run_tc3_presplit(const Args &a, DeviceState &d, cudaStream_t s) {
   p.tiles_m = static_cast<int>(cdiv(a.M, ki->bm));
   p.tiles_n = static_cast<int>(cdiv(a.N, ki->bn));
   p.k_tiles = static_cast<int>(cdiv(a.K, 32));
-  const int64_t num_tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  const int64_t num_tiles = pair ? plan.units : static_cast<int64_t>(p.tiles_m) * p.tiles_n;
   if (num_tiles > kMaxDim) return SGEMM_ERR_LAUNCH;
-  p.num_tiles = static_cast<int>(num_tiles);
+  p.num_tiles = static_cast<int>(num_tiles);   // work units
+  p.wide_tiles = pair ? static_cast<int>(plan.wide_tiles) : p.num_tiles;
   p.group_m = SG_TC_GROUP_M;
   p.c_vec4 = (a.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
   p.wait_budget_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   p.status = d.status;
-  CUtensorMap tmA, tmB, tmAs, tmBs;   // all K-major [128 rows][32 k] boxes, 128-byte swizzle
+  // all K-major [rows][32 k] boxes, 128-byte swizzle: 128 rows, except
+  // op(B) on CTA pairs, where each CTA loads half of a tile's n-rows
+  const int b_rows = pair ? ki->bn / 2 : 128;
+  CUtensorMap tmA, tmB, tmAs, tmBs;
   if (!encode_tmap(&tmA, A_big, a.M, a.K, lda_big, 32, 128, true) ||
       !encode_tmap(&tmAs, a_small, a.M, a.K, ldk, 32, 128, true) ||
-      !encode_tmap(&tmB, B_big, a.N, a.K, ldb_big, 32, 128, true) ||
-      !encode_tmap(&tmBs, b_small, a.N, a.K, ldk, 32, 128, true))
+      !encode_tmap(&tmB, B_big, a.N, a.K, ldb_big, 32, b_rows, true) ||
+      !encode_tmap(&tmBs, b_small, a.N, a.K, ldk, 32, b_rows, true))
     return SGEMM_ERR_LAUNCH;
-  const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
-  const int grid = static_cast<int>(num_tiles < slots ? num_tiles : slots);
-  if (tc3_presplit_entry(ki->bn).launch(p, &tmA, &tmB, &tmAs, &tmBs, grid, s, false) != cudaSuccess)
+  // persistent grid: one CTA (pair: two) per tile, at most what fits at once
+  const int per_tile = pair ? 2 : 1;
+  const int64_t slots = pair ? ki->max_ctas : static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
+  const int64_t want = num_tiles * per_tile;
+  const int grid = static_cast<int>(want < slots ? want : slots - slots % per_tile);
+  const TcEntry entry = pair ? tc3_pair_entry(ki->bn) : tc3_presplit_entry(ki->bn);
+  if (entry.launch(p, &tmA, &tmB, &tmAs, &tmBs, grid, s, false) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
   t_last_launches = 3;
   if (order_after_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;

@@ -63,6 +63,7 @@ SimtEntry simt_entry(int producer, int transA, int transB, int tile);
 // 3xTF32 tensor-core kernel (tc_3xtf32.cu), 128 x 128 tiles, one CTA per SM.
 struct TcKernelInfo {
   int bm, bn, ctas_per_sm;
+  int max_ctas;   // CTAs of this kernel resident at once on the device
 };
 // Maps: op(A), op(B), and -- for the pre-split form only -- A's and B's small
 // parts (K-major); the other forms ignore the last two.
@@ -79,6 +80,10 @@ TcEntry tc3_entry(int transA, int transB);
 // their small parts, all through TMA (no conversion in the kernel).
 // bn = 128 or 256: the output tile width.
 TcEntry tc3_presplit_entry(int bn);
+// The same product on CTA pairs (256 x bn tiles, bn = 128 or 256, launched
+// in clusters of two; grid = 2 x the pair count, p.tiles_m counting 256-row
+// tile rows).
+TcEntry tc3_pair_entry(int bn);
 
 // Second pass of a stream-K launch (sk_fixup.cu).
 cudaError_t launch_sk_fixup(const SimtParams &p, int bm, int bn, int grid_main, int sk_tiles,

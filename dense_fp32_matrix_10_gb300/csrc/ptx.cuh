@@ -126,6 +126,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *desc, uint
       : "memory");
 }
 
+// 2-D tiled load into this CTA's shared memory whose completion is counted
+// on an mbarrier of either CTA of the pair (`cbar`: shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *desc, uint32_t cbar,
+                                                 int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(desc)), "r"(cbar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 // 2-D tiled bulk tensor store shared -> global (this thread's bulk group).
 // Box elements outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const void *desc, uint32_t src, int32_t c0, int32_t c1) {
@@ -165,6 +176,41 @@ __device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
       : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
       : "memory");
   return out != 0;
+}
+
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster: shared-memory writes before it
+// (barrier initialisation included) are visible cluster-wide after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// shared::cluster address of the location at shared::cta address `saddr` in
+// the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or a
+// peer's), with release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 
 // ---------------------------------------------------------------- dependent launch
@@ -253,6 +299,43 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+
+// ------------------------------------------------- tcgen05, CTA pairs
+// A kernel uses one .cta_group throughout; these are the pair (cta_group::2)
+// forms.  Allocation and release: one warp of each CTA of the pair, the same
+// column count; both CTAs get the same tensor-memory address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Issued by one thread of the even CTA: D (M = 256: rows 0..127 in the even
+// CTA's tensor memory, 128..255 in the odd one's) (+)= A * B, A's rows and
+// B's n-columns split in halves between the two CTAs' shared memory at the
+// same descriptor addresses.
+__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the mbarrier at offset `bar` in each CTA of `mask` when
+// every pair MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
 }
 
 // Warp: 32 lanes x 32 consecutive 32-bit columns; thread t gets lane

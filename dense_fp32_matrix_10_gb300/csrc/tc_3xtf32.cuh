@@ -68,6 +68,10 @@ struct TcParams {
   int M, N, K;
   float alpha, beta;
   int tiles_m, tiles_n, k_tiles, num_tiles;
+  // CTA-pair kernel: work units [0, wide_tiles) are whole tiles; each unit
+  // beyond is one column half of a later tile (two units per tile), so the
+  // last, partial round of tiles is spread over twice the units
+  int wide_tiles;
   int group_m;
   int c_vec4;
   uint64_t wait_budget_ns;
@@ -435,6 +439,40 @@ __device__ __forceinline__ void tc_issue(const TcParams &p, uint32_t sbase, uint
 }
 
 // ------------------------------------------------------------------ epilogue
+// C[row][n0 .. n0+127] = alpha * acc + beta * C (C not read when beta = 0);
+// float4 where C allows it, elementwise at the ragged right edge.
+__device__ __forceinline__ void tc_store_row(const TcParams &p, int row, int n0,
+                                             const float (&acc)[128]) {
+  if (row >= p.M) return;
+  const bool read_c = p.beta != 0.0f;
+  float *crow = p.C + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+  for (int j = 0; j < 128; j += 4) {
+    const int n = n0 + j;
+    if (p.c_vec4 && n + 3 < p.N) {
+      float4 o;
+      if (read_c) {
+        const float4 c = *reinterpret_cast<const float4 *>(crow + n);
+        o.x = fmaf(p.alpha, acc[j + 0], p.beta * c.x);
+        o.y = fmaf(p.alpha, acc[j + 1], p.beta * c.y);
+        o.z = fmaf(p.alpha, acc[j + 2], p.beta * c.z);
+        o.w = fmaf(p.alpha, acc[j + 3], p.beta * c.w);
+      } else {
+        o.x = p.alpha * acc[j + 0];
+        o.y = p.alpha * acc[j + 1];
+        o.z = p.alpha * acc[j + 2];
+        o.w = p.alpha * acc[j + 3];
+      }
+      *reinterpret_cast<float4 *>(crow + n) = o;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (n + e < p.N)
+          crow[n + e] = read_c ? fmaf(p.alpha, acc[j + e], p.beta * crow[n + e]) : p.alpha * acc[j + e];
+    }
+  }
+}
+
 // Warp q of epilogue warpgroup `half` owns tile rows 32q .. 32q+31 (TMEM
 // lanes) and columns 128 * half .. +127.
 template <class Cfg>
@@ -442,7 +480,6 @@ __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_bas
                                             const TcBars<Cfg> &bar, int q, int half, int lane) {
   constexpr int W = 128;   // columns per thread
   uint32_t chunk_iter = 0;
-  const bool read_c = p.beta != 0.0f;
   const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
   for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
     float acc[W];  // this thread's half row of the tile, FP32 round-to-nearest sums
@@ -466,37 +503,7 @@ __device__ __forceinline__ void tc_epilogue(const TcParams &p, uint32_t tmem_bas
     }
     int tm, tn;
     tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-    const int row = tm * Cfg::BM + 32 * q + lane;
-    const int n0 = tn * Cfg::BN + half * W;
-    if (row < p.M) {
-      float *crow = p.C + static_cast<int64_t>(row) * p.ldc;
-#pragma unroll
-      for (int j = 0; j < W; j += 4) {
-        const int n = n0 + j;
-        if (p.c_vec4 && n + 3 < p.N) {
-          float4 o;
-          if (read_c) {
-            const float4 c = *reinterpret_cast<const float4 *>(crow + n);
-            o.x = fmaf(p.alpha, acc[j + 0], p.beta * c.x);
-            o.y = fmaf(p.alpha, acc[j + 1], p.beta * c.y);
-            o.z = fmaf(p.alpha, acc[j + 2], p.beta * c.z);
-            o.w = fmaf(p.alpha, acc[j + 3], p.beta * c.w);
-          } else {
-            o.x = p.alpha * acc[j + 0];
-            o.y = p.alpha * acc[j + 1];
-            o.z = p.alpha * acc[j + 2];
-            o.w = p.alpha * acc[j + 3];
-          }
-          *reinterpret_cast<float4 *>(crow + n) = o;
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (n + e < p.N)
-              crow[n + e] = read_c ? fmaf(p.alpha, acc[j + e], p.beta * crow[n + e])
-                                   : p.alpha * acc[j + e];
-        }
-      }
-    }
+    tc_store_row(p, tm * Cfg::BM + 32 * q + lane, tn * Cfg::BN + half * W, acc);
   }
 }
 

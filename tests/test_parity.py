@@ -512,9 +512,9 @@ def test_tensor_core_split_ahead_ragged(orc, op):
 
 @pytest.mark.parametrize("N", [2500, 2400])
 def test_tensor_core_wide_tiles_ragged(orc, N):
-    """Split-ahead 3xTF32 products run 128 x 256 tiles whose two 128-column
-    halves are loaded as separate op(B) boxes and written by separate
-    epilogue warpgroups.  N = 2500 ends in a partly filled second half, N =
+    """Split-ahead 3xTF32 products of this shape run whole 256-wide tiles
+    whose two 128-column halves are written by separate epilogue
+    warpgroups.  N = 2500 ends in a partly filled second half, N =
     2400 in a second half wholly past N (its op(B) box reads only fill
     values).  Rows depend only on their own tile row: the rows that an M =
     1792 and an M = 1664 product of the same operands share agree bit for
@@ -538,6 +538,38 @@ def test_tensor_core_wide_tiles_ragged(orc, N):
     J[:200] = np.arange(N - 200, N)   # the ragged last tile's columns
     R = orc.sgemm_entries_f64(0, 0, 0.75, A.numpy(), B.numpy(), 0.5, C0.numpy(), I, J)
     assert_close(C_full.cpu().numpy()[I, J], R, K, f"tc wide tiles N={N}")
+
+
+PAIR_CASES = [(1792, 1664, 4000), (1792, 1600, 4000), (2048, 1920, 2432)]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_tensor_core_cta_pairs(orc, case):
+    """Split-ahead products run on CTA pairs (tcgen05 cta_group::2): 256-row
+    tiles, each CTA holding its 128 rows of A and half of op(B)'s columns.
+    N = 4000 takes whole 256 x 256 tiles for a full round of pairs and column
+    halves for the rest; N = 2432 (19 column tiles of 128) takes 256 x 128
+    tiles.  M = 1664 (13 row tiles) leaves the last pair's second CTA wholly
+    below the matrix (its A boxes read only fill values), M = 1600 and 1920
+    partly.  Rows agree bit for bit with the same rows of a product with more
+    rows (every pair full) of the same operands, and sampled outputs match the
+    oracle, with alpha and beta (C read) and a ragged N."""
+    M_full, M, N = case
+    K = 512
+    g = torch.Generator().manual_seed(M + N)
+    A = torch.randn(M_full, K, generator=g)
+    B = torch.randn(K, N, generator=g)
+    C0 = torch.rand(M_full, N, generator=g).mul_(2).sub_(1)
+    dA, dB = A.cuda(), B.cuda()
+    C_full, C_part = C0.cuda(), C0[:M].cuda()
+    sg.gemm(dA, dB, C_full, 1.5, -0.5, 0, 0, algo="tc_3xtf32")
+    sg.gemm(dA[:M], dB, C_part, 1.5, -0.5, 0, 0, algo="tc_3xtf32")
+    assert sg.sgemm_last_launch_count() == 3
+    torch.cuda.synchronize()
+    assert torch.equal(C_full[:M], C_part)
+    I, J = sample_indices(M, N, 3000, seed=M)
+    R = orc.sgemm_entries_f64(0, 0, 1.5, A[:M].numpy(), B.numpy(), -0.5, C0[:M].numpy(), I, J)
+    assert_close(C_part.cpu().numpy()[I, J], R, K, f"tc CTA pairs {case}")
 
 
 def test_pretransposed_on_two_streams(orc):
