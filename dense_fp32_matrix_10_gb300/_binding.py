@@ -12,9 +12,11 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.environ.get("SGEMM_GB300_LIBRARY") or os.path.join(HERE, "libsgemm_gb300.so")
 
 OP_N, OP_T = 0, 1
-ALGO_AUTO, ALGO_SIMT_TMA, ALGO_SIMT_CPASYNC, ALGO_TC_3XTF32, ALGO_NAIVE, ALGO_SMEM_TILED = range(6)
+(ALGO_AUTO, ALGO_SIMT_TMA, ALGO_SIMT_CPASYNC, ALGO_TC_3XTF32, ALGO_NAIVE, ALGO_SMEM_TILED,
+ ALGO_SMALL) = range(7)
 ALGOS = {"auto": ALGO_AUTO, "simt_tma": ALGO_SIMT_TMA, "simt_cpasync": ALGO_SIMT_CPASYNC,
-         "tc_3xtf32": ALGO_TC_3XTF32, "naive": ALGO_NAIVE, "smem_tiled": ALGO_SMEM_TILED}
+         "tc_3xtf32": ALGO_TC_3XTF32, "naive": ALGO_NAIVE, "smem_tiled": ALGO_SMEM_TILED,
+         "small": ALGO_SMALL}
 STATUS = {0: "SGEMM_SUCCESS", 1: "SGEMM_ERR_INVALID_VALUE", 2: "SGEMM_ERR_ALIASING",
           3: "SGEMM_ERR_UNSUPPORTED", 4: "SGEMM_ERR_LAUNCH", 5: "SGEMM_ERR_DEVICE_TIMEOUT",
           6: "SGEMM_ERR_SCRATCH_LIMIT"}

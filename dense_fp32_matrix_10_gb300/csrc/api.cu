@@ -390,7 +390,21 @@ float *stream_k_workspace(DeviceState &d, size_t need, bool capturing) {
   return need <= d.ws_bytes ? d.ws : nullptr;
 }
 
+// Products of at most 2^26 multiply-adds with K <= 1024 run the small-product
+// kernel: one launch, no stream-K pass (GB300, CUDA-graph replays: 256^3 12.0
+// -> 5.6 us, 384^3 15.3 -> 8.9 us, 65 x 4097 x 129 20.8 -> 10.4 us,
+// 4096 x 128 x 128 16.4 -> 13.0 us; at 512^3 the two are within 15 % and
+// from 768^3, or with K = 4096, the persistent kernels are faster).
+#ifndef SG_SMALL_MAX_WORK
+#define SG_SMALL_MAX_WORK (int64_t(1) << 26)
+#endif
+bool small_wanted(const Args &a) {
+  const double work = static_cast<double>(a.M) * static_cast<double>(a.N) * static_cast<double>(a.K);
+  return work <= static_cast<double>(SG_SMALL_MAX_WORK) && a.K <= 1024 && cdiv(a.M, 32) <= 65535;
+}
+
 sgemm_algo_t auto_algo(const Args &a) {
+  if (small_wanted(a)) return SGEMM_ALGO_SMALL;
   return tma_eligible(a) ? SGEMM_ALGO_SIMT_TMA : SGEMM_ALGO_SIMT_CPASYNC;
 }
 
@@ -954,7 +968,7 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
                         const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
                         float *C, int64_t ldc, void *stream, sgemm_algo_t algo) {
   Args a{norm_op(transA), norm_op(transB), M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
-  if (static_cast<int>(algo) < SGEMM_ALGO_AUTO || static_cast<int>(algo) > SGEMM_ALGO_SMEM_TILED)
+  if (static_cast<int>(algo) < SGEMM_ALGO_AUTO || static_cast<int>(algo) > SGEMM_ALGO_SMALL)
     return SGEMM_ERR_INVALID_VALUE;
   sgemm_status_t st = validate(a, true);
   if (st != SGEMM_SUCCESS) return st;
@@ -973,7 +987,7 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
     return SGEMM_SUCCESS;
   }
 
-  if (algo == SGEMM_ALGO_AUTO && repack_wanted(a)) {
+  if (algo == SGEMM_ALGO_AUTO && !small_wanted(a) && repack_wanted(a)) {
     const sgemm_status_t st = run_pretransposed(a, *d, s, repack_plan(a, d->sm_count), false);
     if (st != SGEMM_ERR_UNSUPPORTED) return st;
     algo = SGEMM_ALGO_SIMT_CPASYNC;   // no scratch: run in place
@@ -992,10 +1006,13 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
     case SGEMM_ALGO_SIMT_CPASYNC:
       return run_simt(a, *d, kCpAsync, s);
     case SGEMM_ALGO_NAIVE:
-    case SGEMM_ALGO_SMEM_TILED: {
+    case SGEMM_ALGO_SMEM_TILED:
+    case SGEMM_ALGO_SMALL: {
       PlainParams p{A, B, C, lda, ldb, ldc, static_cast<int>(M), static_cast<int>(N),
                     static_cast<int>(K), a.ta, a.tb, alpha, beta};
-      cudaError_t e = algo == SGEMM_ALGO_NAIVE ? launch_naive(p, s) : launch_smem_tiled(p, s);
+      cudaError_t e = algo == SGEMM_ALGO_NAIVE       ? launch_naive(p, s)
+                      : algo == SGEMM_ALGO_SMEM_TILED ? launch_smem_tiled(p, s)
+                                                      : launch_small(p, s);
       if (e == cudaErrorInvalidValue) return SGEMM_ERR_UNSUPPORTED;
       if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
       t_last_launches = 1;
@@ -1088,7 +1105,7 @@ int sgemm_select_algo(int transA, int transB, int64_t M, int64_t N, int64_t K, c
   Args a{norm_op(transA), norm_op(transB), M, N, K, alpha, beta, A, lda, B, ldb,
          const_cast<float *>(C), ldc};
   if (validate(a, false) != SGEMM_SUCCESS) return -1;
-  if (repack_wanted(a)) return SGEMM_ALGO_SIMT_TMA;
+  if (!small_wanted(a) && repack_wanted(a)) return SGEMM_ALGO_SIMT_TMA;
   return static_cast<int>(auto_algo(a));
 }
 
@@ -1157,6 +1174,7 @@ const char *sgemm_algo_name(sgemm_algo_t algo) {
     case SGEMM_ALGO_TC_3XTF32: return "tc_3xtf32";
     case SGEMM_ALGO_NAIVE: return "naive";
     case SGEMM_ALGO_SMEM_TILED: return "smem_tiled";
+    case SGEMM_ALGO_SMALL: return "small";
     default: return "unknown";
   }
 }

@@ -101,6 +101,9 @@ struct PlainParams {
 };
 cudaError_t launch_naive(const PlainParams &p, cudaStream_t s);
 cudaError_t launch_smem_tiled(const PlainParams &p, cudaStream_t s);
+// SGEMM_ALGO_SMALL (small.cu); cudaErrorInvalidValue if M needs more than
+// 65535 row tiles.
+cudaError_t launch_small(const PlainParams &p, cudaStream_t s);
 cudaError_t launch_scale_c(float *C, int64_t ldc, int M, int N, float beta, cudaStream_t s);
 // out (cols x rows, ld_out) = in (rows x cols, ld_in) transposed (transpose.cu);
 // `status` is the device status word the bounded waits report to.  Unless

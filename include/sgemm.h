@@ -121,8 +121,12 @@ typedef enum sgemm_algo {
   SGEMM_ALGO_NAIVE = 4,        /* one thread per output, operands read straight
                                   from global memory (the pages' first kernel;
                                   for comparison only) */
-  SGEMM_ALGO_SMEM_TILED = 5    /* 16x16 shared-memory tiles, one output per
+  SGEMM_ALGO_SMEM_TILED = 5,   /* 16x16 shared-memory tiles, one output per
                                   thread (the pages' second kernel; comparison) */
+  SGEMM_ALGO_SMALL = 6         /* small and skinny products: one launch, no
+                                  workspace; one CTA per 32x32 tile of C, K split
+                                  across its eight warps and their partial tiles
+                                  added in a fixed order.  Any alignment/ld. */
 } sgemm_algo_t;
 
 /*

@@ -54,8 +54,8 @@ def test_strings(lib):
     assert g.sgemm_status_string(0) == "success"
     assert "overlap" in g.sgemm_status_string(2)
     assert g.sgemm_status_string(99) == "unknown status"
-    assert [g.sgemm_algo_name(i) for i in range(6)] == \
-        ["auto", "simt_tma", "simt_cpasync", "tc_3xtf32", "naive", "smem_tiled"]
+    assert [g.sgemm_algo_name(i) for i in range(7)] == \
+        ["auto", "simt_tma", "simt_cpasync", "tc_3xtf32", "naive", "smem_tiled", "small"]
     assert g.sgemm_algo_name(42) == "unknown"
     assert re.match(r"^\d+\.\d+\.\d+$", g.sgemm_version())
 
@@ -132,12 +132,18 @@ def test_select_algo_is_host_only(lib):
                                       ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
                                       ctypes.c_void_p, ctypes.c_int64, ctypes.c_float,
                                       ctypes.c_float, ctypes.c_void_p, ctypes.c_int64]
-    sel = lambda A, lda, B, ldb: lib.sgemm_select_algo(0, 0, 64, 64, 64, A, lda, B, ldb, 1.0, 0.0,
-                                                       FAKE_C, 64)
-    assert sel(FAKE_A, 64, FAKE_B, 64) == 1          # aligned, ld % 4 == 0 -> TMA
-    assert sel(FAKE_A + 4, 64, FAKE_B, 64) == 2      # A not 16-byte aligned -> cp.async
-    assert sel(FAKE_A, 65, FAKE_B, 64) == 2          # lda % 4 != 0 -> cp.async
-    assert sel(FAKE_A, 60, FAKE_B, 64) == -1         # invalid lda
+    # 512 x 512 x 384: above the small-product kernel's 2^26 multiply-adds,
+    # below the 2^27 from which TMA-ineligible operands are copied aligned
+    sel = lambda A, lda, B, ldb, K=384: lib.sgemm_select_algo(0, 0, 512, 512, K, A, lda, B, ldb,
+                                                              1.0, 0.0, FAKE_C, 512)
+    fa, fb, fc = FAKE_A, FAKE_A + 4 * 512 * 600, FAKE_A + 8 * 512 * 600   # disjoint
+    assert sel(fa, 384, fb, 512) == 1                # aligned, ld % 4 == 0 -> TMA
+    assert sel(fa + 4, 384, fb, 512) == 2            # A not 16-byte aligned -> cp.async
+    assert sel(fa, 385, fb, 512) == 2                # lda % 4 != 0 -> cp.async
+    assert sel(fa, 380, fb, 512) == -1               # invalid lda
+    # at most 2^26 multiply-adds and K <= 1024: the small-product kernel
+    assert sel(fa, 384, fb, 512, K=64) == 6
+    assert lib.sgemm_select_algo(0, 0, 64, 64, 64, fa, 64, fb, 64, 1.0, 0.0, fc, 64) == 6
 
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="needs a machine without a GPU")

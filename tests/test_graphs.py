@@ -182,3 +182,42 @@ def test_capture_before_any_workspace_exists():
                        text=True, timeout=300)
     assert p.returncode == 0, p.stderr[-3000:]
     assert p.stdout.strip().endswith("ok")
+
+
+def test_tensor_core_pairs_in_graph():
+    """A split-ahead 3xTF32 product runs as three launches, the last a
+    cluster launch of CTA pairs.  Captured in a graph (after one eager call
+    has sized the scratch), its replays, interleaved with eager tensor-core
+    calls of another shape on another stream that share the scratch, equal
+    the product run alone bit for bit."""
+    M, N, K = 2048, 2560, 512
+    A1, B1 = _operands(M, N, K, 7)
+    A2, B2 = _operands(2048, 4096, 512, 8)
+
+    def alone(A, B, m, n):
+        C = torch.empty(m, n, device="cuda")
+        sg.gemm(A, B, C, algo="tc_3xtf32")
+        assert sg.sgemm_last_launch_count() == 3
+        torch.cuda.synchronize()
+        return C.clone()
+
+    ref1, ref2 = alone(A1, B1, M, N), alone(A2, B2, 2048, 4096)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    C1 = torch.empty(M, N, device="cuda")
+    C2 = torch.empty(2048, 4096, device="cuda")
+    with torch.cuda.stream(s1):
+        sg.gemm(A1, B1, C1, algo="tc_3xtf32", stream=s1)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s1):
+        sg.gemm(A1, B1, C1, algo="tc_3xtf32", stream=s1)
+        assert sg.sgemm_last_launch_count() == 3
+    for _ in range(4):
+        C1.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        with torch.cuda.stream(s2):
+            sg.gemm(A2, B2, C2, algo="tc_3xtf32", stream=s2)
+        torch.cuda.synchronize()
+        assert torch.equal(C1, ref1)
+        assert torch.equal(C2, ref2)

@@ -19,8 +19,8 @@ from tests.parity import (assert_bit_exact, assert_close, offset_view, padded, s
 pytestmark = pytest.mark.gpu
 
 OPS = [(0, 0), (0, 1), (1, 0), (1, 1)]
-GEMM_ALGOS = ["simt_tma", "simt_cpasync", "tc_3xtf32"]
-ALL_ALGOS = ["auto", "simt_tma", "simt_cpasync", "tc_3xtf32", "naive", "smem_tiled"]
+GEMM_ALGOS = ["simt_tma", "simt_cpasync", "tc_3xtf32", "small"]
+ALL_ALGOS = ["auto", "simt_tma", "simt_cpasync", "tc_3xtf32", "naive", "smem_tiled", "small"]
 TMA_ALGOS = ("simt_tma", "tc_3xtf32")   # need 16-byte aligned rows
 
 
@@ -59,7 +59,7 @@ SMALL_CASES = [W.SMALL_256, W.SQUARE_1024, W.SWEEP[0], W.SWEEP[1], W.RAGGED[0], 
 LARGE_CASES = [W.SWEEP[2], W.SWEEP[3], W.NT_4096, W.RAGGED[1]]
 
 
-@pytest.mark.parametrize("algo", ["auto", "simt_cpasync", "tc_3xtf32"])
+@pytest.mark.parametrize("algo", ["auto", "simt_cpasync", "tc_3xtf32", "small"])
 @pytest.mark.parametrize("case", SMALL_CASES, ids=[c.name for c in SMALL_CASES])
 def test_workload_full(orc, case, algo):
     G, (A, B, C) = run_case(case, algo=algo)
@@ -67,7 +67,7 @@ def test_workload_full(orc, case, algo):
     assert_close(G, R, case.K, case.name)
 
 
-@pytest.mark.parametrize("algo", ["auto", "tc_3xtf32"])
+@pytest.mark.parametrize("algo", ["auto", "tc_3xtf32", "small"])
 @pytest.mark.parametrize("case", SMALL_CASES, ids=[c.name for c in SMALL_CASES])
 def test_workload_integer_bit_exact(orc, case, algo):
     ic = case.as_int()
@@ -135,7 +135,7 @@ def test_random_ragged_sweep(orc, algo):
     """A few dozen random shapes 1..300 per dimension, random ops, scalars and
     padded leading dimensions (the pages' advice: compare many random shapes
     with a CPU reference)."""
-    rng = np.random.default_rng({"simt_tma": 42, "simt_cpasync": 43}.get(algo, 44))
+    rng = np.random.default_rng({"simt_tma": 42, "simt_cpasync": 43, "small": 45}.get(algo, 44))
     for t in range(40):
         M, N, K = (int(x) for x in rng.integers(1, 301, size=3))
         ta, tb = int(rng.integers(0, 2)), int(rng.integers(0, 2))
@@ -143,7 +143,7 @@ def test_random_ragged_sweep(orc, algo):
         beta = float(rng.choice([0.0, 1.0, -1.5]))
         case = W.Case("sweep", M, N, K, ta, tb, "uniform", 5000 + t, alpha, beta)
         A, B, C = W.make_inputs(case)
-        if algo == "simt_cpasync":   # any padding, ld usually not a multiple of 4
+        if algo in ("simt_cpasync", "small"):   # any padding, ld usually not a multiple of 4
             ea, eb = int(rng.integers(0, 5)), int(rng.integers(0, 5))
         else:                        # pad each ld up to a multiple of 4 (TMA needs 16-byte rows)
             ea = (-A.shape[1]) % 4 + 4 * int(rng.integers(0, 3))
@@ -204,7 +204,7 @@ def test_staged_epilogue_guard_bands(orc, case):
 @pytest.mark.parametrize("op", OPS, ids=["NN", "NT", "TN", "TT"])
 def test_misaligned_pointers_use_cpasync(orc, op):
     ta, tb = op
-    M, N, K = 150, 140, 90
+    M, N, K = 650, 420, 270      # above the small-product kernel's range
     case = W.Case("mis", M, N, K, ta, tb, "uniform", 77, 1.0, 1.0)
     A, B, C = W.make_inputs(case)
     Ad, Bd = offset_view(A.cuda(), 1), offset_view(B.cuda(), 3)
