@@ -19,7 +19,9 @@ CUDA-core peak 2 * 128 * SMs * f_SM, at the 2070 MHz maximum SM clock),
 ``cpu_baseline`` (the CPU oracle timed on a bounded sample of the same product
 on this host's cores), ``clocks`` (nvidia-smi samples taken during the timed
 region), ``vs_size`` (TFLOP/s of the 512..4096 square sweep), ``configs``
-(TFLOP/s of the other workload families), ``tensor_core_3xtf32`` (the
+(TFLOP/s of the other workload families; both from back-to-back eager calls),
+``configs_graph`` (the same families' device time per call from CUDA-graph
+replays, without the host's per-call cost), ``tensor_core_3xtf32`` (the
 tensor-core kernel on the headline product), ``transpose`` (the transpose
 kernel's HBM bandwidth at 4096 x 4096 and 16384 x 16384) and
 ``library_context`` (cuBLAS FP32 on the headline product, for context),
@@ -201,29 +203,55 @@ class Dist:
 
 
 # ----------------------------------------------------------------- GPU timing
-def time_gemm(sg, torch, case, A, B, C, steps, warmup, algo, stream, record_launches=False):
+def time_gemm(sg, torch, case, A, B, C, steps, warmup, algo, stream, record_launches=False,
+              per_call_events=True):
     """Warm up, then time `steps` back-to-back calls with CUDA events on
     `stream`.  Returns (ms per step from the region, mean per-launch ms from
-    per-call events, launches counted)."""
+    per-call events -- None without them --, launches counted).  Small
+    products are host-bound: their region is timed without per-call events."""
     for _ in range(warmup):
         sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=algo, stream=stream)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
+          for _ in range(steps if per_call_events else 0)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
     start.record(stream)
     for i in range(steps):
-        ev[i][0].record(stream)
+        if per_call_events:
+            ev[i][0].record(stream)
         sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=algo, stream=stream)
-        ev[i][1].record(stream)
+        if per_call_events:
+            ev[i][1].record(stream)
         if record_launches:
             launches += sg.sgemm_last_launch_count()
     end.record(stream)
     torch.cuda.synchronize()
     region = start.elapsed_time(end) / steps
-    per_launch = sum(a.elapsed_time(b) for a, b in ev) / steps
+    per_launch = sum(a.elapsed_time(b) for a, b in ev) / steps if per_call_events else None
     return region, per_launch, launches
+
+
+def time_gemm_graph(sg, torch, case, A, B, C, algo, stream, calls=20, replays=5):
+    """Device time per call without host gaps: `calls` calls captured in one
+    CUDA graph (after an eager call has sized the library's buffers), the
+    graph replayed `replays` times between two CUDA events."""
+    sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=algo, stream=stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=algo,
+                    stream=stream)
+    g.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(replays):
+        g.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / (calls * replays)
 
 
 def time_transpose(sg, torch, rows, cols, reps, stream, flush=None):
@@ -510,12 +538,13 @@ def run_ours(args, dist):
         del out
 
     # ---- TFLOP/s vs size and the other workload families (rank 0 context)
-    vs_size, families = {}, {}
+    vs_size, families, families_graph = {}, {}, {}
     if not args.no_sweep:
         for sc in W.SWEEP:
             sA, sB, sC = (t.to(dev) for t in W.make_inputs(sc))
             n = max(5, min(200, int(2e11 / sc.flops)))
-            r, _, _ = time_gemm(sg, torch, sc, sA, sB, sC, n, 3, args.algo, stream)
+            r, _, _ = time_gemm(sg, torch, sc, sA, sB, sC, n, 3, args.algo, stream,
+                                per_call_events=False)
             vs_size[str(sc.M)] = round(tflops(sc.flops, r), 3)
             del sA, sB, sC
         for sc in [W.SMALL_256, W.SQUARE_1024, W.NT_4096, *W.RAGGED]:
@@ -524,8 +553,12 @@ def run_ours(args, dist):
             n = max(5, min(200, int(2e11 / sc.flops)))
             # beta != 0 updates C in place each call; the values drift but the
             # work per call is identical.
-            r, _, _ = time_gemm(sg, torch, sc, sA, sB, sC, n, 3, args.algo, stream)
+            r, _, _ = time_gemm(sg, torch, sc, sA, sB, sC, n, 3, args.algo, stream,
+                                per_call_events=False)
             families[sc.name] = round(tflops(sc.flops, r), 3)
+            us = 1000 * time_gemm_graph(sg, torch, sc, sA, sB, sC, args.algo, stream)
+            families_graph[sc.name] = {"us_per_call": round(us, 2),
+                                       "tflops": round(tflops(sc.flops, us / 1000), 3)}
             del sA, sB, sC, sC0
 
     result = {
@@ -545,6 +578,7 @@ def run_ours(args, dist):
         "strided_batched": batched, "ladder": ladder,
         "library_context": library_context,
         "vs_size": vs_size, "configs": families,
+        "configs_graph": families_graph or None,
         "device": {"name": props.name, "sms": sms, "cc": f"{props.major}.{props.minor}"},
     }
     if dist.rank == 0 and not args.no_cpu_baseline:
