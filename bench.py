@@ -232,24 +232,29 @@ def time_gemm(sg, torch, case, A, B, C, steps, warmup, algo, stream, record_laun
     return region, per_launch, launches
 
 
-def time_gemm_graph(sg, torch, case, A, B, C, algo, stream, calls=20, replays=5):
+def time_gemm_graph(sg, torch, case, A, B, C, algo, calls=20, replays=5):
     """Device time per call without host gaps: `calls` calls captured in one
-    CUDA graph (after an eager call has sized the library's buffers), the
-    graph replayed `replays` times between two CUDA events."""
-    sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=algo, stream=stream)
+    CUDA graph on a side stream (after an eager call there has sized the
+    library's buffers), the graph replayed `replays` times between two CUDA
+    events on that stream."""
+    cs = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=algo, stream=cs)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
+    with torch.cuda.graph(g, stream=cs):
         for _ in range(calls):
             sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=algo,
-                    stream=stream)
-    g.replay()
+                    stream=cs)
+    with torch.cuda.stream(cs):
+        g.replay()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(replays):
-        g.replay()
-    end.record(stream)
+    with torch.cuda.stream(cs):
+        start.record(cs)
+        for _ in range(replays):
+            g.replay()
+        end.record(cs)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / (calls * replays)
 
@@ -556,7 +561,7 @@ def run_ours(args, dist):
             r, _, _ = time_gemm(sg, torch, sc, sA, sB, sC, n, 3, args.algo, stream,
                                 per_call_events=False)
             families[sc.name] = round(tflops(sc.flops, r), 3)
-            us = 1000 * time_gemm_graph(sg, torch, sc, sA, sB, sC, args.algo, stream)
+            us = 1000 * time_gemm_graph(sg, torch, sc, sA, sB, sC, args.algo)
             families_graph[sc.name] = {"us_per_call": round(us, 2),
                                        "tflops": round(tflops(sc.flops, us / 1000), 3)}
             del sA, sB, sC, sC0
