@@ -33,6 +33,66 @@ __device__ __forceinline__ int swz(int k, int j) {
   return k * kTile + ((((j >> 2) ^ (k & 7)) << 2) | (j & 3));
 }
 
+// Stages the 32 rows r0 .. r0+31 of an operand panel (op(A)'s rows or
+// op(B)'s columns), k in [k0, k0 + 256), into S (swizzled [k][32]); zeros
+// outside [0, R) x [0, K).  KCONTIG: the stored rows run along k
+// (X[r * ld + k]), else along r (X[k * ld + r]).  A panel wholly inside the
+// matrix with 16-byte aligned rows is read as float4, every load issued
+// before any store; the rest element by element with predicated loads.
+// Either way a warp reads along the stored rows.
+template <bool KCONTIG>
+__device__ __forceinline__ void stage_panel(const float *__restrict__ X, int64_t ld, int R, int K,
+                                            int r0, int k0, float *S, int t) {
+  constexpr int kVecIters = kStageFloats / (4 * kThreads);   // 8 float4 per thread
+  const bool vec = (ld % 4 == 0) && ((reinterpret_cast<uintptr_t>(X) & 15) == 0) &&
+                   r0 + kTile <= R && k0 + kPassK <= K;
+  if (vec) {
+    float4 v[kVecIters];
+    if (KCONTIG) {
+      // a warp covers 8 rows x 16 k: 64-byte row segments, stores spread
+      // over 16 banks
+      const int lane = t & 31, w = t >> 5;
+      const int j = (w & 3) * 8 + (lane & 7);
+      const int qb = (w >> 2) * 4 + (lane >> 3);
+      const float *src = X + static_cast<int64_t>(r0 + j) * ld + k0 + 4 * qb;
+#pragma unroll
+      for (int it = 0; it < kVecIters; ++it) v[it] = *reinterpret_cast<const float4 *>(src + 32 * it);
+#pragma unroll
+      for (int it = 0; it < kVecIters; ++it) {
+        const int q = it * 8 + qb;
+        S[swz(4 * q, j)] = v[it].x;
+        S[swz(4 * q + 1, j)] = v[it].y;
+        S[swz(4 * q + 2, j)] = v[it].z;
+        S[swz(4 * q + 3, j)] = v[it].w;
+      }
+    } else {
+      // a warp covers 4 k x 32 rows: 128-byte row segments, one 16-byte
+      // chunk of S per lane
+      const int q = t & 7, kb = t >> 3;
+      const float *src = X + static_cast<int64_t>(k0 + kb) * ld + r0 + 4 * q;
+#pragma unroll
+      for (int it = 0; it < kVecIters; ++it)
+        v[it] = *reinterpret_cast<const float4 *>(src + static_cast<int64_t>(32 * it) * ld);
+#pragma unroll
+      for (int it = 0; it < kVecIters; ++it)
+        *reinterpret_cast<float4 *>(&S[swz(it * 32 + kb, 4 * q)]) = v[it];
+    }
+    return;
+  }
+  // element by element: consecutive lanes take consecutive elements of a
+  // stored row (256 k of one row, or 32 rows of eight k)
+#pragma unroll 16
+  for (int it = 0; it < kStageFloats / kThreads; ++it) {
+    const int k = KCONTIG ? t : it * (kThreads / kTile) + (t >> 5);
+    const int j = KCONTIG ? it : (t & 31);
+    const int r = r0 + j, gk = k0 + k;
+    float v = 0.0f;
+    if (r < R && gk < K)
+      v = KCONTIG ? X[static_cast<int64_t>(r) * ld + gk] : X[static_cast<int64_t>(gk) * ld + r];
+    S[swz(k, j)] = v;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
     small_gemm_kernel(const PlainParams p) {
   extern __shared__ __align__(16) float smem[];
@@ -48,33 +108,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int q = 0; q < 4; ++q) acc[r][q] = make_float2(0.0f, 0.0f);
 
   for (int k0 = 0; k0 < p.K; k0 += kPassK) {
-    // ---- stage op(A)[m0.., k0..] and op(B)[k0.., n0..]; zeros outside.
-    // Pass `it` of a thread covers, in the stored layout's contiguous
-    // direction, 256 consecutive k (k-contiguous operand: one row/column of
-    // the tile per pass) or eight k of 32 consecutive m/n; the passes' loads
-    // are independent, sixteen of them in flight at once.
-#pragma unroll 16
-    for (int it = 0; it < kStageFloats / kThreads; ++it) {
-      const int k = p.transA == 0 ? t : it * (kThreads / kTile) + (t >> 5);
-      const int j = p.transA == 0 ? it : (t & 31);
-      const int gm = m0 + j, gk = k0 + k;
-      float v = 0.0f;
-      if (gm < p.M && gk < p.K)
-        v = p.transA == 0 ? p.A[static_cast<int64_t>(gm) * p.lda + gk]
-                          : p.A[static_cast<int64_t>(gk) * p.lda + gm];
-      As[swz(k, j)] = v;
-    }
-#pragma unroll 16
-    for (int it = 0; it < kStageFloats / kThreads; ++it) {
-      const int k = p.transB == 1 ? t : it * (kThreads / kTile) + (t >> 5);
-      const int j = p.transB == 1 ? it : (t & 31);
-      const int gn = n0 + j, gk = k0 + k;
-      float v = 0.0f;
-      if (gn < p.N && gk < p.K)
-        v = p.transB == 0 ? p.B[static_cast<int64_t>(gk) * p.ldb + gn]
-                          : p.B[static_cast<int64_t>(gn) * p.ldb + gk];
-      Bs[swz(k, j)] = v;
-    }
+    // ---- stage op(A)[m0.., k0..] and op(B)[k0.., n0..]; zeros outside
+    if (p.transA == 0)
+      stage_panel<true>(p.A, p.lda, p.M, p.K, m0, k0, As, t);
+    else
+      stage_panel<false>(p.A, p.lda, p.M, p.K, m0, k0, As, t);
+    if (p.transB == 1)
+      stage_panel<true>(p.B, p.ldb, p.N, p.K, n0, k0, Bs, t);
+    else
+      stage_panel<false>(p.B, p.ldb, p.N, p.K, n0, k0, Bs, t);
     __syncthreads();
     // ---- this warp's 32 k of the pass, in ascending order
     const int kw = warp * 32;
