@@ -390,17 +390,23 @@ float *stream_k_workspace(DeviceState &d, size_t need, bool capturing) {
   return need <= d.ws_bytes ? d.ws : nullptr;
 }
 
-// Products of at most 2^26 multiply-adds with K <= 1024 run the small-product
-// kernel: one launch, no stream-K pass (GB300, CUDA-graph replays: 256^3 12.0
-// -> 5.6 us, 384^3 15.3 -> 8.9 us, 65 x 4097 x 129 20.8 -> 10.4 us,
-// 4096 x 128 x 128 16.4 -> 13.0 us; at 512^3 the two are within 15 % and
-// from 768^3, or with K = 4096, the persistent kernels are faster).
+// Products of at most 2^26 multiply-adds with K <= 1024 and at most 608
+// tiles of 32 x 32 (four per SM of a GB300) run the small-product kernel:
+// one launch, no stream-K pass (GB300, CUDA-graph replays: 256^3 12.0 ->
+// 5.3 us, 384^3 15.3 -> 8.4 us, 65 x 4097 x 129 20.8 -> 9.7 us,
+// 4096 x 128 x 128 16.4 -> 12.8 us).  The persistent kernels are faster from
+// 768^3, with K = 4096, and when many tiles have a short K (2048 x 2048 x 32:
+// 15.5 against 133 us).
 #ifndef SG_SMALL_MAX_WORK
 #define SG_SMALL_MAX_WORK (int64_t(1) << 26)
 #endif
+#ifndef SG_SMALL_MAX_TILES
+#define SG_SMALL_MAX_TILES 608
+#endif
 bool small_wanted(const Args &a) {
   const double work = static_cast<double>(a.M) * static_cast<double>(a.N) * static_cast<double>(a.K);
-  return work <= static_cast<double>(SG_SMALL_MAX_WORK) && a.K <= 1024 && cdiv(a.M, 32) <= 65535;
+  return work <= static_cast<double>(SG_SMALL_MAX_WORK) && a.K <= 1024 &&
+         cdiv(a.M, 32) * cdiv(a.N, 32) <= SG_SMALL_MAX_TILES;
 }
 
 sgemm_algo_t auto_algo(const Args &a) {

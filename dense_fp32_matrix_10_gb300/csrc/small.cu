@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace sg {
 namespace {
@@ -106,6 +107,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int r = 0; r < 4; ++r)
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[r][q] = make_float2(0.0f, 0.0f);
+  // launched as a programmatic dependent of the stream's previous kernel:
+  // A, B and C are touched only once that kernel has completed
+  griddep_wait();
 
   for (int k0 = 0; k0 < p.K; k0 += kPassK) {
     // ---- stage op(A)[m0.., k0..] and op(B)[k0.., n0..]; zeros outside
@@ -138,6 +142,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncthreads();   // the slices are overwritten by the next pass
   }
+
+  // the next kernel on the stream may be scheduled (it waits for this one
+  // to complete before touching memory)
+  griddep_launch_dependents();
 
   // ---- partial tiles of the eight warps, added in warp order
   float *part = smem;   // [kWarps][32][32]
@@ -180,9 +188,11 @@ cudaError_t launch_small(const PlainParams &p, cudaStream_t s) {
                                      kSmemBytes);
   });
   if (attr[dev] != cudaSuccess) return attr[dev];
-  small_gemm_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), kThreads, kSmemBytes,
-                      s>>>(p);
-  return cudaGetLastError();
+  // programmatic stream serialization: back-to-back small products overlap
+  // one kernel's launch with the previous one's tail
+  return launch_maybe_pdl(small_gemm_kernel,
+                          dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), dim3(kThreads),
+                          kSmemBytes, s, true, p);
 }
 
 }  // namespace sg

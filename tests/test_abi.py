@@ -141,8 +141,11 @@ def test_select_algo_is_host_only(lib):
     assert sel(fa + 4, 384, fb, 512) == 2            # A not 16-byte aligned -> cp.async
     assert sel(fa, 385, fb, 512) == 2                # lda % 4 != 0 -> cp.async
     assert sel(fa, 380, fb, 512) == -1               # invalid lda
-    # at most 2^26 multiply-adds and K <= 1024: the small-product kernel
+    # at most 2^26 multiply-adds, K <= 1024 and 608 tiles of 32 x 32: the
+    # small-product kernel (512 x 512 is 256 tiles)
     assert sel(fa, 384, fb, 512, K=64) == 6
+    big = lambda M, N, K: lib.sgemm_select_algo(0, 0, M, N, K, fa, K, fb, N, 1.0, 0.0, FAKE_C, N)
+    assert big(1024, 1024, 64) == 1          # 1024 tiles with a short K: the persistent kernel
     assert lib.sgemm_select_algo(0, 0, 64, 64, 64, fa, 64, fb, 64, 1.0, 0.0, fc, 64) == 6
 
 
