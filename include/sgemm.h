@@ -133,6 +133,8 @@ typedef enum sgemm_algo {
  * C = alpha * op(A) * op(B) + beta * C, kernel chosen automatically.
  * Returns SGEMM_SUCCESS once the work is queued on `stream`, or an error code
  * (see sgemm_status_t) with nothing queued.  Thread-safe.
+ * Small products -- M * N * K <= 2^26, K <= 1024 and at most 608 tiles of
+ * 32 x 32 -- run SGEMM_ALGO_SMALL: one launch, any layout, no workspace.
  * Large products whose op(A) or op(B) is k-contiguous (A stored M x K, or B
  * stored N x K) and that fill the GPU with 128 x 256 tiles first copy that
  * operand transposed into library scratch (one transpose launch each) and
