@@ -117,7 +117,9 @@ typedef enum sgemm_algo {
                                   FP32 operand split into two TF32 parts and
                                   three products accumulated.  Large products
                                   split both operands ahead into library
-                                  scratch (two extra launches). */
+                                  scratch (two extra launches) and run on CTA
+                                  pairs (clusters of two, cta_group::2 MMAs
+                                  on 256-row tiles). */
   SGEMM_ALGO_NAIVE = 4,        /* one thread per output, operands read straight
                                   from global memory (the pages' first kernel;
                                   for comparison only) */
