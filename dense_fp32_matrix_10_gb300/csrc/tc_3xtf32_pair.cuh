@@ -235,8 +235,8 @@ __device__ __forceinline__ void tcp_epilogue(const TcParams &p, uint32_t tmem_ba
 }
 
 // ------------------------------------------------------------------ kernel
-// Launched in clusters of two CTAs; p.tiles_m counts 256-row tile rows and
-// p.num_tiles the pair tiles.
+// Launched in clusters of two CTAs; p.tiles_m counts 256-row tile rows,
+// p.num_tiles the work units (whole tiles, then column halves: pair_tile).
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
