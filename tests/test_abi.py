@@ -146,6 +146,10 @@ def test_select_algo_is_host_only(lib):
     assert sel(fa, 384, fb, 512, K=64) == 6
     big = lambda M, N, K: lib.sgemm_select_algo(0, 0, M, N, K, fa, K, fb, N, 1.0, 0.0, FAKE_C, N)
     assert big(1024, 1024, 64) == 1          # 1024 tiles with a short K: the persistent kernel
+    assert big(64, 64, 2048) == 1            # K > 1024: the persistent kernel
+    assert big(64, 64, 1024) == 6            # K = 1024, 4 tiles: still the small-product kernel
+    assert big(1024, 64, 1024) == 6          # exactly 2^26 multiply-adds, 64 tiles: small
+    assert big(1024, 64, 1028) == 1          # just over 2^26 (and K > 1024): persistent
     assert lib.sgemm_select_algo(0, 0, 64, 64, 64, fa, 64, fb, 64, 1.0, 0.0, fc, 64) == 6
 
 
