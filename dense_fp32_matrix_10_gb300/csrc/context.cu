@@ -96,6 +96,11 @@ cudaError_t launch_smem_tiled(const PlainParams &p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t load_scale_c() {
+  cudaFuncAttributes attr;
+  return cudaFuncGetAttributes(&attr, scale_c_kernel);
+}
+
 cudaError_t launch_scale_c(float *C, int64_t ldc, int M, int N, float beta, cudaStream_t s) {
   return launch_scale_c_batched(C, ldc, 0, M, N, 1, beta, s);
 }

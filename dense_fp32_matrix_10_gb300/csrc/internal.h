@@ -86,6 +86,10 @@ TcEntry tc3_presplit_entry(int bn);
 TcEntry tc3_pair_entry(int bn);
 
 // Second pass of a stream-K launch (sk_fixup.cu).
+// load_sk_fixup / load_scale_c: make the CUDA runtime load these kernels now
+// (under lazy module loading it would do so at their first launch).
+cudaError_t load_sk_fixup();
+cudaError_t load_scale_c();
 cudaError_t launch_sk_fixup(const SimtParams &p, int bm, int bn, int grid_main, int sk_tiles,
                             int sm_count, cudaStream_t s);
 

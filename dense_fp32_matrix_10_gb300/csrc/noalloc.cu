@@ -1,5 +1,5 @@
 // noalloc.cu -- sgemm_noalloc(): the CUDA-core GEMM with its stream-K scratch
-// in a fixed device array that exists as soon as the library is loaded, so a
+// in a fixed __device__ array instead of a cudaMalloc'd workspace, so that a
 // call never allocates device memory.
 //
 // Why: sgemm() gets the scratch for split tiles (the partial sums that
@@ -14,14 +14,20 @@
 //     when memory is tight;
 //   * services whose device-memory footprint is fixed and checked up front.
 // Here the scratch is g_noalloc_scratch, SGEMM_NOALLOC_SCRATCH_BYTES of
-// __device__ memory that the CUDA runtime reserves on every GPU that loads the
-// library and keeps until the process exits.
+// __device__ memory that stays reserved on every GPU where it has been loaded
+// until the process exits.
 //
-// Set-up: the first call on a device, with that device current, looks up the
-// array's device address with cudaGetSymbolAddress (host code cannot use the
-// symbol itself: on the host it names a stand-in, not device memory).  That
-// first call on each device should therefore be made before any stream
-// capture begins.
+// Set-up, once per device, by the first call made with that device current
+// (any call whose arguments are valid, an empty one with M = 0 included):
+// it looks up the array's device address with cudaGetSymbolAddress (host code
+// cannot use the symbol itself: on the host it names a stand-in, not device
+// memory) and queries every kernel this entry point launches.  Under CUDA's
+// lazy module loading (the default since CUDA 12.2) those lookups are what
+// make the runtime load this library's code and reserve the array on that
+// device, so the one-time reservation happens there and not at library load.
+// Make that first call before handing the remaining device memory to your own
+// pool, and before any stream capture begins; every later call allocates
+// nothing.
 //
 // Sharing: every call on a device uses the same array and leaves its contents
 // behind.  Nothing in it has to start at zero -- the main kernel writes every
@@ -51,17 +57,26 @@ struct NoAllocDevice {
 };
 NoAllocDevice g_noalloc[kMaxDevices];
 
-// Device address of the scratch array on the current device (looked up once
-// per device), or null.
-float *noalloc_scratch() {
+// One-time set-up on the current device (see the file comment): the array's
+// device address, and every kernel this entry point may launch loaded.
+// Returns the address, or null if the set-up failed.
+float *noalloc_setup(DeviceState &d) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return nullptr;
   }
   NoAllocDevice &n = g_noalloc[dev];
-  std::call_once(n.once, [&n]() {
+  std::call_once(n.once, [&n, &d]() {
     n.err = cudaGetSymbolAddress(reinterpret_cast<void **>(&n.scratch), g_noalloc_scratch);
+    for (int producer = 0; producer < 2 && n.err == cudaSuccess; ++producer)
+      for (int ta = 0; ta < 2; ++ta)
+        for (int tb = 0; tb < 2; ++tb)
+          for (int tile : {kTile128x128, kTile128x64})
+            if (n.err == cudaSuccess && !kernel_info(d, producer, ta, tb, tile))
+              n.err = cudaErrorInvalidDeviceFunction;
+    if (n.err == cudaSuccess) n.err = load_sk_fixup();
+    if (n.err == cudaSuccess) n.err = load_scale_c();
     if (n.err != cudaSuccess) {
       cudaGetLastError();
       n.scratch = nullptr;
@@ -80,13 +95,14 @@ extern "C" sgemm_status_t sgemm_noalloc(int transA, int transB, int64_t M, int64
   sgemm_status_t st = validate(a, true);
   if (st != SGEMM_SUCCESS) return st;
   t_last_launches = 0;
-  if (M == 0 || N == 0) return SGEMM_SUCCESS;
 
+  // the set-up comes first, so that an empty call (M = 0) can be used to do it
   sgemm_status_t why = SGEMM_SUCCESS;
   DeviceState *d = device_state(&why);
   if (!d) return why;
-  float *scratch = noalloc_scratch();
+  float *scratch = noalloc_setup(*d);
   if (!scratch) return SGEMM_ERR_LAUNCH;
+  if (M == 0 || N == 0) return SGEMM_SUCCESS;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (K == 0 || alpha == 0.0f) {
@@ -130,10 +146,12 @@ extern "C" sgemm_status_t sgemm_noalloc(int transA, int transB, int64_t M, int64
   p.status = d->status;
 
   const int64_t slots = static_cast<int64_t>(d->sm_count) * ki->ctas_per_sm;
-  const SkPlan plan = plan_stream_k(num_tiles, p.k_tiles, slots, true);
+  SkPlan plan = plan_stream_k(num_tiles, p.k_tiles, slots, true);
   const size_t need =
       plan.sk_tiles > 0 ? static_cast<size_t>(2) * plan.grid * ki->bm * ki->bn * sizeof(float) : 0;
-  if (need > SGEMM_NOALLOC_SCRATCH_BYTES) return SGEMM_ERR_SCRATCH_LIMIT;
+  // split tiles whose partials would not fit the array: whole tiles only
+  // (plain waves, no scratch), as sgemm() does without a workspace
+  if (need > SGEMM_NOALLOC_SCRATCH_BYTES) plan = plan_stream_k(num_tiles, p.k_tiles, slots, false);
   p.dp_tiles = plan.dp_tiles;
   p.sk_iters = plan.sk_iters;
   p.workspace = plan.sk_tiles > 0 ? scratch : nullptr;

@@ -101,6 +101,12 @@ __global__ void __launch_bounds__(kFixupThreads) sk_fixup_kernel(const SimtParam
   }
 }
 
+cudaError_t load_sk_fixup() {
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, sk_fixup_kernel<1>);
+  return e == cudaSuccess ? cudaFuncGetAttributes(&attr, sk_fixup_kernel<8>) : e;
+}
+
 cudaError_t launch_sk_fixup(const SimtParams &p, int bm, int bn, int grid_main, int sk_tiles,
                             int sm_count, cudaStream_t s) {
   const dim3 grid(sk_tiles * (bm * bn / kChunk));
