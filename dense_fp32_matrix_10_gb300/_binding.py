@@ -68,6 +68,11 @@ def load_library():
     lib.sgemm_last_launch_count.restype = ctypes.c_int
     lib.sgemm_last_device_status.argtypes = [_VP]
     lib.sgemm_last_device_status.restype = ctypes.c_int
+    lib.sgemm_set_scratch_limit.argtypes = [ctypes.c_uint64]
+    lib.sgemm_set_scratch_limit.restype = ctypes.c_int
+    lib.sgemm_get_scratch_limit.argtypes = [ctypes.POINTER(ctypes.c_uint64),
+                                            ctypes.POINTER(ctypes.c_uint64)]
+    lib.sgemm_get_scratch_limit.restype = ctypes.c_int
     lib.sgemm_set_wait_budget_ns.argtypes = [ctypes.c_uint64]
     lib.sgemm_set_wait_budget_ns.restype = None
     lib.sgemm_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _VP]
@@ -126,7 +131,8 @@ def sgemm_transpose(rows, cols, inp, ld_in, out, ld_out, stream=None):
 
 def sgemm_noalloc(transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
     """As sgemm, for callers that may not let the library allocate device
-    memory: the scratch is a fixed array loaded with the library."""
+    memory: the scratch is a fixed __device__ array, reserved by the first
+    call on a device (an empty call with M = 0 does only that set-up)."""
     _check(load_library().sgemm_noalloc(_op(transA), _op(transB), M, N, K, alpha, A, lda, B, ldb,
                                         beta, C, ldc, stream), "sgemm_noalloc")
 
@@ -143,6 +149,23 @@ def sgemm_last_launch_count() -> int:
 def sgemm_last_device_status(stream=None) -> int:
     """Synchronise `stream`; return (and clear) the device status code."""
     return load_library().sgemm_last_device_status(stream)
+
+
+SCRATCH_UNLIMITED = (1 << 64) - 1
+
+
+def sgemm_set_scratch_limit(nbytes: int):
+    """Cap the device memory the library may own on the current device
+    (0: none; SCRATCH_UNLIMITED: no cap)."""
+    _check(load_library().sgemm_set_scratch_limit(int(nbytes)), "sgemm_set_scratch_limit")
+
+
+def sgemm_get_scratch_limit():
+    """(limit, bytes held now) on the current device."""
+    lim, held = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check(load_library().sgemm_get_scratch_limit(ctypes.byref(lim), ctypes.byref(held)),
+           "sgemm_get_scratch_limit")
+    return lim.value, held.value
 
 
 def sgemm_set_wait_budget_ns(budget_ns: int):

@@ -6,6 +6,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <functional>
 #include <mutex>
@@ -40,6 +41,12 @@ DeviceState *device_state(sgemm_status_t *why) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_device_status);
+    // SGEMM_SCRATCH_LIMIT=<bytes>: the initial scratch limit of every device
+    if (const char *env = std::getenv("SGEMM_SCRATCH_LIMIT")) {
+      char *end = nullptr;
+      const unsigned long long v = std::strtoull(env, &end, 10);
+      if (end != env && *end == '\0') d.limit.store(v);
+    }
     d.err = e;
     if (e != cudaSuccess) cudaGetLastError();
   });
@@ -197,13 +204,16 @@ int norm_op(int t) {
   }
 }
 
-// [lo, hi) byte range of a stored rows x cols matrix with leading dim ld.
-static void byte_range(const void *p, int64_t rows, int64_t cols, int64_t ld, uintptr_t *lo, uintptr_t *hi) {
+// [lo, hi) byte range of a stored rows x cols matrix with leading dim ld, in
+// 128-bit arithmetic: rows < 2^31 and ld <= 2^40 make (rows - 1) * ld + cols
+// reach 2^71 elements, past int64, and the end may lie past the address space.
+using u128 = unsigned __int128;
+static void byte_range(const void *p, int64_t rows, int64_t cols, int64_t ld, u128 *lo, u128 *hi) {
   *lo = reinterpret_cast<uintptr_t>(p);
-  *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 4);
+  *hi = *lo + 4 * (static_cast<u128>(rows - 1) * static_cast<u128>(ld) + static_cast<u128>(cols));
 }
 
-static bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+static bool overlaps(u128 a0, u128 a1, u128 b0, u128 b1) { return a0 < b1 && b0 < a1; }
 
 // Host-side validation shared by sgemm_ex and sgemm_select_algo.
 sgemm_status_t validate_shape(const Args &a) {
@@ -225,13 +235,21 @@ sgemm_status_t validate(const Args &a, bool c_writable) {
   if (c_writable && a.C == nullptr) return SGEMM_ERR_INVALID_VALUE;
   const bool need_ab = a.K > 0 && a.alpha != 0.0f;
   if (need_ab && (a.A == nullptr || a.B == nullptr)) return SGEMM_ERR_INVALID_VALUE;
-  if (need_ab && a.C != nullptr) {
-    uintptr_t c0, c1, x0, x1;
+  // A matrix that the call touches must fit in the 64-bit address space; then
+  // every element offset the kernels form (row * ld + col) fits in int64.
+  const u128 kAddressEnd = static_cast<u128>(1) << 64;
+  u128 c0 = 0, c1 = 0, x0, x1;
+  if (a.C != nullptr) {
     byte_range(a.C, a.M, a.N, a.ldc, &c0, &c1);
+    if (c1 > kAddressEnd) return SGEMM_ERR_INVALID_VALUE;
+  }
+  if (need_ab) {
     byte_range(a.A, a.ta ? a.K : a.M, a_cols, a.lda, &x0, &x1);
-    if (overlaps(c0, c1, x0, x1)) return SGEMM_ERR_ALIASING;
+    if (x1 > kAddressEnd) return SGEMM_ERR_INVALID_VALUE;
+    if (a.C != nullptr && overlaps(c0, c1, x0, x1)) return SGEMM_ERR_ALIASING;
     byte_range(a.B, a.tb ? a.N : a.K, b_cols, a.ldb, &x0, &x1);
-    if (overlaps(c0, c1, x0, x1)) return SGEMM_ERR_ALIASING;
+    if (x1 > kAddressEnd) return SGEMM_ERR_INVALID_VALUE;
+    if (a.C != nullptr && overlaps(c0, c1, x0, x1)) return SGEMM_ERR_ALIASING;
   }
   return SGEMM_SUCCESS;
 }
@@ -349,6 +367,17 @@ cudaError_t order_before_use(BufferOrder &o, cudaStream_t s, bool capturing) {
   return cudaSuccess;
 }
 
+bool reserve_scratch(DeviceState &d, uint64_t bytes) {
+  uint64_t cur = d.held.load();
+  do {
+    const uint64_t lim = d.limit.load();
+    if (cur > lim || bytes > lim - cur) return false;
+  } while (!d.held.compare_exchange_weak(cur, cur + bytes));
+  return true;
+}
+
+void release_scratch(DeviceState &d, uint64_t bytes) { d.held.fetch_sub(bytes); }
+
 cudaError_t order_after_use(BufferOrder &o, cudaStream_t s, bool capturing) {
   const cudaError_t e = capturing ? cudaEventRecordWithFlags(o.ev, s, cudaEventRecordExternal)
                                   : cudaEventRecord(o.ev, s);
@@ -368,20 +397,33 @@ using namespace sg;
 // The device's stream-K workspace (2 partial tiles per CTA slot of the largest
 // configuration), allocated on first use; null if that failed, or if it does
 // not exist yet and `capturing` (no allocation inside a stream capture).
+// Bytes of the stream-K workspace: two 128 x 256 partial tiles per SM (the
+// largest need, one CTA per SM), then the arrival counters of the in-kernel
+// fixup (zero between launches).
+size_t stream_k_workspace_bytes(const DeviceState &d) {
+  return static_cast<size_t>(2) * d.sm_count * 128 * 256 * sizeof(float) + kSkCounters * sizeof(int);
+}
+
 float *stream_k_workspace(DeviceState &d, size_t need, bool capturing) {
   if (d.ws_failed) return nullptr;
   if (!d.ws) {
     if (capturing) return nullptr;
-    // largest need: two 128 x 256 partial tiles per SM (one CTA per SM),
-    // then the arrival counters of the in-kernel fixup (zero between launches)
-    const size_t bytes = static_cast<size_t>(2) * d.sm_count * 128 * 256 * sizeof(float);
-    if (cudaMalloc(&d.ws, bytes + kSkCounters * sizeof(int)) != cudaSuccess ||
-        cudaMemset(reinterpret_cast<char *>(d.ws) + bytes, 0, kSkCounters * sizeof(int)) != cudaSuccess ||
-        cudaEventCreateWithFlags(&d.ws_order.ev, cudaEventDisableTiming) != cudaSuccess) {
+    const size_t total = stream_k_workspace_bytes(d), bytes = total - kSkCounters * sizeof(int);
+    // over the scratch limit: no workspace (not a failure; the limit may rise)
+    if (!reserve_scratch(d, total)) return nullptr;
+    if (!d.ws_order.ev && cudaEventCreateWithFlags(&d.ws_order.ev, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      release_scratch(d, total);
+      d.ws_failed = true;
+      return nullptr;
+    }
+    if (cudaMalloc(&d.ws, total) != cudaSuccess ||
+        cudaMemset(reinterpret_cast<char *>(d.ws) + bytes, 0, kSkCounters * sizeof(int)) != cudaSuccess) {
       cudaGetLastError();
       if (d.ws) cudaFree(d.ws);
       d.ws = nullptr;
       d.ws_failed = true;
+      release_scratch(d, total);
       return nullptr;
     }
     d.ws_bytes = bytes;
@@ -683,16 +725,25 @@ float *pretranspose_scratch(DeviceState &d, size_t bytes, bool capturing) {
     const bool keep = d.tr_order.in_graph && d.tr;
     if (keep && want < 2 * d.tr_bytes) want = 2 * d.tr_bytes;
     if (want > kPretransposeMaxBytes) want = bytes;
+    // the old buffer is freed (unless kept) once the new one exists: both
+    // count against the scratch limit meanwhile; over the limit, try the
+    // exact size before giving up
+    if (!reserve_scratch(d, want)) {
+      want = bytes;
+      if (!reserve_scratch(d, want)) return nullptr;   // the product runs in place
+    }
     float *fresh = nullptr;
     if (cudaMalloc(&fresh, want) != cudaSuccess) {
       cudaGetLastError();
+      release_scratch(d, want);
       return nullptr;   // not fatal: this product runs on its operands in place
     }
     if (keep) {
-      d.tr_retired.push_back(d.tr);
+      d.tr_retired.emplace_back(d.tr, d.tr_bytes);
     } else if (d.tr) {
       // cudaFree waits for work still using the old buffer
       cudaFree(d.tr);
+      release_scratch(d, d.tr_bytes);
     }
     d.tr = fresh;
     d.tr_bytes = want;
@@ -1144,6 +1195,49 @@ sgemm_status_t sgemm_last_device_status(void *stream) {
     }
   }
   return v == 0 ? SGEMM_SUCCESS : SGEMM_ERR_DEVICE_TIMEOUT;
+}
+
+sgemm_status_t sgemm_set_scratch_limit(uint64_t bytes) {
+  sgemm_status_t why = SGEMM_SUCCESS;
+  DeviceState *d = device_state(&why);
+  if (!d) return why;
+  d->limit.store(bytes);
+  if (d->held.load() <= bytes) return SGEMM_SUCCESS;
+  // Over the new limit: free the buffers no captured graph may still use
+  // (cudaFree waits for the device's queued work, which may still read them).
+  {
+    std::lock_guard<std::mutex> lock(d->ws_mu);
+    if (d->ws && !d->ws_order.in_graph) {
+      if (cudaFree(d->ws) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+      }
+      release_scratch(*d, stream_k_workspace_bytes(*d));
+      d->ws = nullptr;
+      d->ws_bytes = 0;
+      d->sk_count = nullptr;
+    }
+  }
+  std::lock_guard<std::mutex> lock(d->tr_mu);
+  if (d->tr && !d->tr_order.in_graph) {
+    if (cudaFree(d->tr) != cudaSuccess) {
+      cudaGetLastError();
+      return SGEMM_ERR_LAUNCH;
+    }
+    release_scratch(*d, d->tr_bytes);
+    d->tr = nullptr;
+    d->tr_bytes = 0;
+  }
+  return SGEMM_SUCCESS;
+}
+
+sgemm_status_t sgemm_get_scratch_limit(uint64_t *limit, uint64_t *held) {
+  sgemm_status_t why = SGEMM_SUCCESS;
+  DeviceState *d = device_state(&why);
+  if (!d) return why;
+  if (limit) *limit = d->limit.load();
+  if (held) *held = d->held.load();
+  return SGEMM_SUCCESS;
 }
 
 void sgemm_set_wait_budget_ns(uint64_t budget_ns) {

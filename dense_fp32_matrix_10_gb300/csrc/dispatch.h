@@ -10,6 +10,7 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "internal.h"
@@ -56,6 +57,14 @@ struct DeviceState {
   cudaError_t err = cudaSuccess;
   int sm_count = 0, cc_major = 0, cc_minor = 0;
   int *status = nullptr;
+  // Device memory the library may own on this device (sgemm_set_scratch_limit;
+  // initial value from the SGEMM_SCRATCH_LIMIT environment variable, else no
+  // limit) and what it holds now: the stream-K workspace, the operand scratch
+  // and scratch buffers retired under captured graphs.  An allocation first
+  // reserves its bytes against the limit (reserve_scratch) and gives them back
+  // if cudaMalloc fails.
+  std::atomic<uint64_t> limit{UINT64_MAX};
+  std::atomic<uint64_t> held{0};
   // Stream-K workspace: allocated on first use, kept until exit.  Calls that
   // use it on different streams or in graphs are ordered by ws_order.
   std::mutex ws_mu;
@@ -72,7 +81,7 @@ struct DeviceState {
   std::mutex tr_mu;
   float *tr = nullptr;
   size_t tr_bytes = 0;
-  std::vector<float *> tr_retired;
+  std::vector<std::pair<float *, size_t>> tr_retired;
   bool tr_failed = false;
   BufferOrder tr_order;
   std::once_flag kinfo_once[2][2][2][kNumSimtTiles];
@@ -93,7 +102,10 @@ constexpr int64_t kMaxDim = 0x7fffffff - 1024;
 // stream-K tiles a launch may finish in-kernel (at most two waves' worth of
 // tiles are split, far below this)
 constexpr int kSkCounters = 4096;
-constexpr int64_t kMaxLd = int64_t(1) << 40;  // keeps every byte offset in int64
+// Leading dimensions and batch strides are bounded by kMaxLd; validate() also
+// rejects a matrix whose byte range would end past 2^64 (it cannot exist), so
+// every element offset the kernels form stays below 2^62 and fits in int64.
+constexpr int64_t kMaxLd = int64_t(1) << 40;
 
 struct Args {
   int ta, tb;
@@ -145,5 +157,10 @@ struct SkPlan {
 };
 
 SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws);
+
+// Reserves `bytes` of the device's scratch limit (false, nothing reserved, if
+// they do not fit); release_scratch gives bytes back.
+bool reserve_scratch(DeviceState &d, uint64_t bytes);
+void release_scratch(DeviceState &d, uint64_t bytes);
 
 }  // namespace sg

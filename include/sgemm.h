@@ -26,16 +26,23 @@
  * Pointers: A, B and C are DEVICE pointers (cudaMalloc'd, or any allocation the
  * device can address) on the current device.  The caller owns all of them; the
  * library never frees, keeps or reallocates them.  C must not overlap A or B.
- * Device memory of the library's own: sgemm()/sgemm_ex() allocate, once per
- * device and the first time a product is split by stream-K, a workspace of
- * two 128 x 256 FP32 tiles per SM (~40 MB on 152 SMs, plus 16 KiB of
- * per-tile arrival counters for split tiles finished inside the product
- * kernel), and, the first time a
- * product copies an operand ahead (a transpose or an aligning copy, see
- * sgemm()), a scratch buffer for it (grown in 64 MiB steps, at most 2 GiB);
- * both are kept until exit.  Calls on different streams that use them are
- * ordered by events.
- * sgemm_noalloc() never allocates (see there).
+ * Device memory of the library's own, per device, all of it under a limit the
+ * caller sets with sgemm_set_scratch_limit() (initially the value of the
+ * environment variable SGEMM_SCRATCH_LIMIT in bytes, else no limit):
+ *   - a stream-K workspace (two 128 x 256 FP32 partial tiles per SM, ~40 MB
+ *     on 152 SMs, plus 16 KiB of arrival counters), allocated the first time a
+ *     product is split by stream-K;
+ *   - an operand scratch buffer (grown in 64 MiB steps, at most 2 GiB),
+ *     allocated the first time a product copies an operand ahead (a
+ *     transpose, an aligning copy or a 3xTF32 split, see sgemm());
+ * both kept until exit or until a lower limit frees them.  Calls on different
+ * streams that use them are ordered by events.  A product whose buffer would
+ * not fit under the limit runs without it (whole tiles instead of stream-K
+ * splits, operands read in place), with the same result contract.  With a
+ * limit of 0 the library allocates no device memory at all: what it owns is
+ * then one status word per device (a __device__ variable) and host-side state
+ * (tensor-map cache, events, kernel attributes).  sgemm_noalloc() never
+ * allocates (see there).
  *
  * Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
  * default stream).  Every call returns as soon as its work is queued; results
@@ -59,8 +66,10 @@
  * 3xTF32 tensor-core kernel.  The result matches the FP64-accumulated product
  * within a relative Frobenius error of 1e-5 and an absolute elementwise error of
  * 1e-4 * sqrt(K) for inputs of unit scale, and bit for bit when every input and
- * every partial sum is an integer below 2^24 in magnitude.  Denormals are kept
- * (no flush to zero).  Degenerate cases follow BLAS: M == 0 or N == 0 does
+ * every partial sum is an integer below 2^24 in magnitude.  Denormals: every
+ * kernel family except SGEMM_ALGO_TC_3XTF32 keeps them (no flush to zero), in
+ * inputs, partial sums and results; for the tensor-core family see
+ * SGEMM_ALGO_TC_3XTF32.  Degenerate cases follow BLAS: M == 0 or N == 0 does
  * nothing; K == 0 or alpha == 0 sets C = beta * C without reading A or B;
  * beta == 0 never reads C (NaN or garbage there is overwritten).
  */
@@ -97,8 +106,9 @@ typedef enum sgemm_status {
   SGEMM_ERR_LAUNCH = 4,         /* a CUDA call failed while queuing the work */
   SGEMM_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up a bounded wait (reported
                                    by sgemm_last_device_status) */
-  SGEMM_ERR_SCRATCH_LIMIT = 6   /* sgemm_noalloc: the product's split tiles need
-                                   more scratch than its fixed array holds */
+  SGEMM_ERR_SCRATCH_LIMIT = 6   /* kept for ABI stability; no call returns it
+                                   (sgemm_noalloc runs whole tiles instead
+                                   when its array is too small) */
 } sgemm_status_t;
 
 /*
@@ -233,6 +243,32 @@ SGEMM_API int sgemm_last_launch_count(void);
 SGEMM_API sgemm_status_t sgemm_last_device_status(void *stream);
 
 /*
+ * Caps, for the current device, the device memory that sgemm(), sgemm_ex()
+ * and sgemm_strided_batched() may allocate for the library's own use (the
+ * stream-K workspace and the operand scratch described at the top of this
+ * file); `bytes` = UINT64_MAX removes the cap, 0 forbids any allocation.
+ * Products queued afterwards that would need a buffer above the cap run
+ * without it, with the same result contract.  If the library already holds
+ * more than `bytes`, this call frees those buffers -- after the device has
+ * finished the work queued on it (cudaFree waits for it) -- except buffers
+ * that a captured CUDA graph may still use, which stay until exit (and keep
+ * counting against the cap).  Returns SGEMM_SUCCESS, SGEMM_ERR_UNSUPPORTED
+ * (no usable device) or SGEMM_ERR_LAUNCH (freeing failed).
+ * Not part of the pages' interface: it exists so that callers whose own
+ * allocator owns the device memory can hold the library to the ownership
+ * contract "the caller owns all device memory" (limit 0).
+ */
+SGEMM_API sgemm_status_t sgemm_set_scratch_limit(uint64_t bytes);
+
+/*
+ * The current device's scratch limit and the bytes of device memory the
+ * library holds there now (either pointer may be NULL).  The fixed array of
+ * sgemm_noalloc() is not counted.  Returns SGEMM_SUCCESS or
+ * SGEMM_ERR_UNSUPPORTED.
+ */
+SGEMM_API sgemm_status_t sgemm_get_scratch_limit(uint64_t *limit, uint64_t *held);
+
+/*
  * Sets the limit, in nanoseconds of %globaltimer, that every wait inside the
  * library's kernels observes before it gives up and records
  * SGEMM_ERR_DEVICE_TIMEOUT (default 2e9 = 2 s; 0 restores the default).
@@ -261,22 +297,27 @@ SGEMM_API sgemm_status_t sgemm_selftest_wait_timeout(uint64_t budget_ns, void *s
  * callers that may not let a library allocate.)
  *
  * sgemm() allocates its stream-K workspace with cudaMalloc the first time a
- * product needs one.  Callers that cannot allow that -- programs whose own
- * pool or caching allocator owns the device memory, latency-sensitive loops
- * (cudaMalloc may synchronise the device and can fail under memory pressure),
- * services with a fixed, audited memory footprint -- call this instead.  Its
- * scratch is a __device__ array of SGEMM_NOALLOC_SCRATCH_BYTES that every GPU
- * loading the library holds until the process exits; the call itself makes no
- * cudaMalloc, cudaFree or other allocating call.
+ * product needs one (unless sgemm_set_scratch_limit forbids it, and then
+ * splits no tiles).  Callers that cannot allow a library to allocate but
+ * still want split tiles -- programs whose own pool or caching allocator owns
+ * the device memory, latency-sensitive loops (cudaMalloc may synchronise the
+ * device and can fail under memory pressure), services with a fixed, audited
+ * memory footprint -- call this instead.  Its scratch is a __device__ array
+ * of SGEMM_NOALLOC_SCRATCH_BYTES, reserved on a device by the set-up below and
+ * held until the process exits; the call itself makes no cudaMalloc, cudaFree
+ * or other allocating call.
  *
  * Arguments, layout, numerics and degenerate cases are those of sgemm(); it
  * runs the CUDA-core kernels (128 x 128 or 128 x 64 tiles) and updates
- * sgemm_last_launch_count() like sgemm().
- * Errors: as sgemm(), plus SGEMM_ERR_SCRATCH_LIMIT (nothing queued) when the
- * product's split tiles would need more than the array holds (more than 160
- * CTAs' worth on this device).
- * First call on a device: looks up the array's device address on that device
- * (once); make it before any stream capture starts.
+ * sgemm_last_launch_count() like sgemm().  A product whose split tiles would
+ * need more than the array holds runs whole tiles only.
+ * Set-up: the first call on a device -- any call with valid arguments, an
+ * empty one (M = 0) included -- looks up the array's device address and loads
+ * every kernel this entry point launches, with that device current.  Under
+ * CUDA's lazy module loading (the default since CUDA 12.2) that is when the
+ * runtime reserves the array and the kernels' code on the device.  Make this
+ * first call before handing the rest of the device's memory to your own pool
+ * and before any stream capture.
  * Sharing: all calls use the one array and leave its contents behind; nothing
  * in it needs clearing between calls, but calls that overlap on the GPU (on
  * streams not ordered with each other) race on it.

@@ -108,6 +108,19 @@ def test_aliasing(lib):
     assert _call(lib, 0, 0, 4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 64, 4) in (0, 3)
 
 
+def test_huge_ranges_do_not_wrap(lib):
+    """Byte ranges are computed in 128-bit arithmetic: M = 2^24 rows with
+    lda = 2^40 span 2^66 bytes, past int64 and the address space -- refused as
+    an impossible matrix instead of wrapping into a small range."""
+    big_ld = 1 << 40
+    assert _call(lib, 0, 0, 1 << 24, 4, 4, FAKE_A, big_ld, FAKE_B, 4, FAKE_C, 4) == 1
+    assert _call(lib, 0, 0, 4, 4, 1 << 24, FAKE_A, 1 << 24, FAKE_B, big_ld, 1 << 45, 4) == 1
+    assert _call(lib, 0, 0, 1 << 24, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, big_ld) == 1
+    # a large matrix that does fit: 2^20 rows of 2^36 floats (2^58 bytes); C
+    # placed 2^50 bytes into A's range overlaps it
+    assert _call(lib, 0, 0, 1 << 20, 4, 4, FAKE_A, 1 << 36, FAKE_B, 4, FAKE_A + (1 << 50), 4) == 2
+
+
 def test_unknown_algo(lib):
     assert _call(lib, 0, 0, 4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, algo=17) == 1
 
