@@ -78,18 +78,21 @@ def kernel_source_hash(family: str) -> str:
 
 
 def stored_traffic(kernel_tag: str):
-    """(bytes per launch, note) from profiles/*.md lines
-    'traffic <kernel_tag> <bytes> <source hash>' if the hash still matches."""
+    """(bytes per launch, note) from the record of `kernel_tag` in
+    profiles/traffic.json, if the hash of its family's sources still matches
+    the one the capture was taken on."""
     family = next((f for f in ("tc_3xtf32", "transpose") if kernel_tag.startswith(f)), "simt")
     want = kernel_source_hash(family)
-    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
-        for ln in open(path, encoding="utf-8"):
-            m = re.match(r"^traffic\s+(\S+)\s+(\d+)\s+(\w+)\s*$", ln.strip())
-            if m and m.group(1) == kernel_tag:
-                if m.group(3) == want:
-                    return int(m.group(2)), os.path.basename(path)
-                return None, f"stale ({os.path.basename(path)} taken on {m.group(3)}, now {want})"
-    return None, "no capture"
+    try:
+        records = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["records"]
+    except (OSError, ValueError, KeyError):
+        return None, "no traffic records"
+    rec = records.get(kernel_tag)
+    if rec is None:
+        return None, "no capture"
+    if rec.get("source_hash") != want:
+        return None, f"stale ({rec.get('summary')} taken on {rec.get('source_hash')}, now {want})"
+    return int(rec["dram_bytes_per_launch"]), rec.get("summary")
 
 
 def measured_peaks():
@@ -505,7 +508,7 @@ def run_ours(args, dist):
         La, Lb = torch.randn(n, n, device=dev), torch.randn(n, n, device=dev)
         Lc = torch.empty(n, n, device=dev)
         ladder = {"workload": f"{n}^3 NN", "unit": "TFLOP/s"}
-        for algo_name in ("naive", "smem_tiled", "auto"):
+        for algo_name in ("naive", "smem_tiled", "reg_2x2", "reg_4x4", "auto"):
             sg.gemm(La, Lb, Lc, algo=algo_name, stream=stream)
             reps = 3 if algo_name != "auto" else 20
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -517,7 +520,8 @@ def run_ours(args, dist):
             torch.cuda.synchronize()
             ladder[algo_name] = round(tflops(2.0 * n ** 3, e0.elapsed_time(e1) / reps), 3)
         ladder["speedup_auto_over_naive"] = round(ladder["auto"] / ladder["naive"], 1)
-        ladder["speedup_smem_tiled_over_naive"] = round(ladder["smem_tiled"] / ladder["naive"], 2)
+        for rung in ("smem_tiled", "reg_2x2", "reg_4x4"):
+            ladder[f"speedup_{rung}_over_naive"] = round(ladder[rung] / ladder["naive"], 2)
         del La, Lb, Lc
 
     # ---- library context: cuBLAS FP32 (TF32 off) on the headline product

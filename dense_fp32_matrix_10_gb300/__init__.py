@@ -19,8 +19,8 @@ Low level (same names and arguments as the C ABI, pointers as ints, raising
 High level (torch tensors): ``gemm``, ``gemm_strided_batched``, ``transpose``.
 """
 from ._binding import (  # noqa: F401
-    ALGO_AUTO, ALGO_NAIVE, ALGO_SIMT_CPASYNC, ALGO_SIMT_TMA, ALGO_SMALL, ALGO_SMEM_TILED,
-    ALGO_TC_3XTF32,
+    ALGO_AUTO, ALGO_NAIVE, ALGO_REG_2X2, ALGO_REG_4X4, ALGO_SIMT_CPASYNC, ALGO_SIMT_TMA,
+    ALGO_SMALL, ALGO_SMEM_TILED, ALGO_TC_3XTF32,
     ALGOS, OP_N, OP_T, SCRATCH_UNLIMITED, STATUS, SgemmError, gemm, library_path, load_library,
     sgemm, sgemm_get_scratch_limit, sgemm_set_scratch_limit,
     sgemm_algo_name, sgemm_ex, sgemm_last_device_status, sgemm_last_launch_count, sgemm_noalloc,

@@ -13,10 +13,10 @@ _LIB_PATH = os.environ.get("SGEMM_GB300_LIBRARY") or os.path.join(HERE, "libsgem
 
 OP_N, OP_T = 0, 1
 (ALGO_AUTO, ALGO_SIMT_TMA, ALGO_SIMT_CPASYNC, ALGO_TC_3XTF32, ALGO_NAIVE, ALGO_SMEM_TILED,
- ALGO_SMALL) = range(7)
+ ALGO_SMALL, ALGO_REG_2X2, ALGO_REG_4X4) = range(9)
 ALGOS = {"auto": ALGO_AUTO, "simt_tma": ALGO_SIMT_TMA, "simt_cpasync": ALGO_SIMT_CPASYNC,
          "tc_3xtf32": ALGO_TC_3XTF32, "naive": ALGO_NAIVE, "smem_tiled": ALGO_SMEM_TILED,
-         "small": ALGO_SMALL}
+         "small": ALGO_SMALL, "reg_2x2": ALGO_REG_2X2, "reg_4x4": ALGO_REG_4X4}
 STATUS = {0: "SGEMM_SUCCESS", 1: "SGEMM_ERR_INVALID_VALUE", 2: "SGEMM_ERR_ALIASING",
           3: "SGEMM_ERR_UNSUPPORTED", 4: "SGEMM_ERR_LAUNCH", 5: "SGEMM_ERR_DEVICE_TIMEOUT",
           6: "SGEMM_ERR_SCRATCH_LIMIT"}

@@ -1025,7 +1025,7 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
                         const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
                         float *C, int64_t ldc, void *stream, sgemm_algo_t algo) {
   Args a{norm_op(transA), norm_op(transB), M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
-  if (static_cast<int>(algo) < SGEMM_ALGO_AUTO || static_cast<int>(algo) > SGEMM_ALGO_SMALL)
+  if (static_cast<int>(algo) < SGEMM_ALGO_AUTO || static_cast<int>(algo) > SGEMM_ALGO_REG_4X4)
     return SGEMM_ERR_INVALID_VALUE;
   sgemm_status_t st = validate(a, true);
   if (st != SGEMM_SUCCESS) return st;
@@ -1064,11 +1064,15 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
       return run_simt(a, *d, kCpAsync, s);
     case SGEMM_ALGO_NAIVE:
     case SGEMM_ALGO_SMEM_TILED:
-    case SGEMM_ALGO_SMALL: {
+    case SGEMM_ALGO_SMALL:
+    case SGEMM_ALGO_REG_2X2:
+    case SGEMM_ALGO_REG_4X4: {
       PlainParams p{A, B, C, lda, ldb, ldc, static_cast<int>(M), static_cast<int>(N),
                     static_cast<int>(K), a.ta, a.tb, alpha, beta};
       cudaError_t e = algo == SGEMM_ALGO_NAIVE       ? launch_naive(p, s)
                       : algo == SGEMM_ALGO_SMEM_TILED ? launch_smem_tiled(p, s)
+                      : algo == SGEMM_ALGO_REG_2X2    ? launch_reg_tiled(p, 2, s)
+                      : algo == SGEMM_ALGO_REG_4X4    ? launch_reg_tiled(p, 4, s)
                                                       : launch_small(p, s);
       if (e == cudaErrorInvalidValue) return SGEMM_ERR_UNSUPPORTED;
       if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
@@ -1275,6 +1279,8 @@ const char *sgemm_algo_name(sgemm_algo_t algo) {
     case SGEMM_ALGO_NAIVE: return "naive";
     case SGEMM_ALGO_SMEM_TILED: return "smem_tiled";
     case SGEMM_ALGO_SMALL: return "small";
+    case SGEMM_ALGO_REG_2X2: return "reg_2x2";
+    case SGEMM_ALGO_REG_4X4: return "reg_4x4";
     default: return "unknown";
   }
 }

@@ -105,6 +105,8 @@ struct PlainParams {
 };
 cudaError_t launch_naive(const PlainParams &p, cudaStream_t s);
 cudaError_t launch_smem_tiled(const PlainParams &p, cudaStream_t s);
+// Register-tiled comparison kernel, R x R outputs per thread (R = 2 or 4).
+cudaError_t launch_reg_tiled(const PlainParams &p, int R, cudaStream_t s);
 // SGEMM_ALGO_SMALL (small.cu); cudaErrorInvalidValue if M needs more than
 // 65535 row tiles.
 cudaError_t launch_small(const PlainParams &p, cudaStream_t s);

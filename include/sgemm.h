@@ -66,10 +66,11 @@
  * 3xTF32 tensor-core kernel.  The result matches the FP64-accumulated product
  * within a relative Frobenius error of 1e-5 and an absolute elementwise error of
  * 1e-4 * sqrt(K) for inputs of unit scale, and bit for bit when every input and
- * every partial sum is an integer below 2^24 in magnitude.  Denormals: every
- * kernel family except SGEMM_ALGO_TC_3XTF32 keeps them (no flush to zero), in
- * inputs, partial sums and results; for the tensor-core family see
- * SGEMM_ALGO_TC_3XTF32.  Degenerate cases follow BLAS: M == 0 or N == 0 does
+ * every partial sum is an integer below 2^24 in magnitude.  Denormals: no
+ * kernel family flushes them to zero; the CUDA-core families keep subnormal
+ * inputs, partial sums and results exactly as FP32 arithmetic does, and the
+ * tensor-core family rounds subnormal inputs to TF32's subnormal spacing (see
+ * SGEMM_ALGO_TC_3XTF32).  Degenerate cases follow BLAS: M == 0 or N == 0 does
  * nothing; K == 0 or alpha == 0 sets C = beta * C without reading A or B;
  * beta == 0 never reads C (NaN or garbage there is overwritten).
  */
@@ -129,16 +130,30 @@ typedef enum sgemm_algo {
                                   split both operands ahead into library
                                   scratch (two extra launches) and run on CTA
                                   pairs (clusters of two, cta_group::2 MMAs
-                                  on 256-row tiles). */
+                                  on 256-row tiles).  Subnormals are not
+                                  flushed (subnormal partial sums and results
+                                  are kept), but a subnormal input is kept
+                                  only to within 2^-137, half the spacing of
+                                  TF32 subnormals: its bits below that are
+                                  lost (exact when its significant bits fit
+                                  TF32's 10-bit mantissa). */
   SGEMM_ALGO_NAIVE = 4,        /* one thread per output, operands read straight
                                   from global memory (the pages' first kernel;
                                   for comparison only) */
   SGEMM_ALGO_SMEM_TILED = 5,   /* 16x16 shared-memory tiles, one output per
                                   thread (the pages' second kernel; comparison) */
-  SGEMM_ALGO_SMALL = 6         /* small and skinny products: one launch, no
+  SGEMM_ALGO_SMALL = 6,        /* small and skinny products: one launch, no
                                   workspace; one CTA per 32x32 tile of C, K split
                                   across its eight warps and their partial tiles
                                   added in a fixed order.  Any alignment/ld. */
+  SGEMM_ALGO_REG_2X2 = 7,      /* the pages' third kernel (register tiling,
+                                  "CUDA矩阵乘法性能优化实战..." sections 5.2-5.3):
+                                  16x16 threads, 2x2 outputs held in registers
+                                  per thread (32x32 tile), k-major shared tiles
+                                  read with float2, float2 global loads where
+                                  aligned; any layout (comparison only) */
+  SGEMM_ALGO_REG_4X4 = 8       /* the same with 4x4 outputs per thread (64x64
+                                  tile) and float4 loads (comparison only) */
 } sgemm_algo_t;
 
 /*

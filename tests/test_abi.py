@@ -54,8 +54,9 @@ def test_strings(lib):
     assert g.sgemm_status_string(0) == "success"
     assert "overlap" in g.sgemm_status_string(2)
     assert g.sgemm_status_string(99) == "unknown status"
-    assert [g.sgemm_algo_name(i) for i in range(7)] == \
-        ["auto", "simt_tma", "simt_cpasync", "tc_3xtf32", "naive", "smem_tiled", "small"]
+    assert [g.sgemm_algo_name(i) for i in range(9)] == \
+        ["auto", "simt_tma", "simt_cpasync", "tc_3xtf32", "naive", "smem_tiled", "small",
+         "reg_2x2", "reg_4x4"]
     assert g.sgemm_algo_name(42) == "unknown"
     assert re.match(r"^\d+\.\d+\.\d+$", g.sgemm_version())
 

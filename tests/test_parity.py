@@ -19,8 +19,10 @@ from tests.parity import (assert_bit_exact, assert_close, offset_view, padded, s
 pytestmark = pytest.mark.gpu
 
 OPS = [(0, 0), (0, 1), (1, 0), (1, 1)]
-GEMM_ALGOS = ["simt_tma", "simt_cpasync", "tc_3xtf32", "small"]
-ALL_ALGOS = ["auto", "simt_tma", "simt_cpasync", "tc_3xtf32", "naive", "smem_tiled", "small"]
+GEMM_ALGOS = ["simt_tma", "simt_cpasync", "tc_3xtf32", "small", "reg_2x2", "reg_4x4"]
+ANY_LAYOUT_ALGOS = ("simt_cpasync", "small", "reg_2x2", "reg_4x4")   # any alignment and ld
+ALL_ALGOS = ["auto", "simt_tma", "simt_cpasync", "tc_3xtf32", "naive", "smem_tiled", "small",
+             "reg_2x2", "reg_4x4"]
 TMA_ALGOS = ("simt_tma", "tc_3xtf32")   # need 16-byte aligned rows
 
 
@@ -158,7 +160,8 @@ def test_random_ragged_sweep(orc, algo):
     """A few dozen random shapes 1..300 per dimension, random ops, scalars and
     padded leading dimensions (the pages' advice: compare many random shapes
     with a CPU reference)."""
-    rng = np.random.default_rng({"simt_tma": 42, "simt_cpasync": 43, "small": 45}.get(algo, 44))
+    rng = np.random.default_rng({"simt_tma": 42, "simt_cpasync": 43, "small": 45, "reg_2x2": 46,
+                                 "reg_4x4": 47}.get(algo, 44))
     for t in range(40):
         M, N, K = (int(x) for x in rng.integers(1, 301, size=3))
         ta, tb = int(rng.integers(0, 2)), int(rng.integers(0, 2))
@@ -166,7 +169,7 @@ def test_random_ragged_sweep(orc, algo):
         beta = float(rng.choice([0.0, 1.0, -1.5]))
         case = W.Case("sweep", M, N, K, ta, tb, "uniform", 5000 + t, alpha, beta)
         A, B, C = W.make_inputs(case)
-        if algo in ("simt_cpasync", "small"):   # any padding, ld usually not a multiple of 4
+        if algo in ANY_LAYOUT_ALGOS:   # any padding, ld usually not a multiple of 4
             ea, eb = int(rng.integers(0, 5)), int(rng.integers(0, 5))
         else:                        # pad each ld up to a multiple of 4 (TMA needs 16-byte rows)
             ea = (-A.shape[1]) % 4 + 4 * int(rng.integers(0, 3))
@@ -239,8 +242,14 @@ def test_misaligned_pointers_use_cpasync(orc, op):
             sg.gemm(Ad, Bd, Cd, 1.0, 1.0, ta, tb, algo=algo)
     sg.gemm(Ad, Bd, Cd, 1.0, 1.0, ta, tb)
     torch.cuda.synchronize()
-    assert_close(Cd.cpu().numpy(), orc.sgemm_f64(ta, tb, 1.0, A.numpy(), B.numpy(), 1.0, C.numpy()),
-                 K, f"misaligned {op}")
+    R = orc.sgemm_f64(ta, tb, 1.0, A.numpy(), B.numpy(), 1.0, C.numpy())
+    assert_close(Cd.cpu().numpy(), R, K, f"misaligned {op}")
+    # the comparison kernels fall back to element loads and stores
+    for algo in ("reg_2x2", "reg_4x4"):
+        Cd = offset_view(C.cuda(), 2)
+        sg.gemm(Ad, Bd, Cd, 1.0, 1.0, ta, tb, algo=algo)
+        torch.cuda.synchronize()
+        assert_close(Cd.cpu().numpy(), R, K, f"misaligned {op} {algo}")
 
 
 def test_odd_leading_dimensions_are_repacked(orc):
@@ -348,17 +357,74 @@ def test_empty_outputs():
     assert sg.sgemm_last_launch_count() == 0
 
 
-def test_denormals_are_kept():
-    """No flush-to-zero on the CUDA-core kernels: products of normal numbers
-    that land in the subnormal range survive (2^-70 * 2^-70 = 2^-140, a
-    subnormal float).  (The tensor-core kernel is not held to this.)"""
-    for algo in ["simt_tma", "simt_cpasync", "naive"]:
-        A = torch.full((4, 4), 2.0 ** -70, device="cuda")
-        B = torch.full((4, 4), 2.0 ** -70, device="cuda")
-        C = torch.empty(4, 4, device="cuda")
-        sg.gemm(A, B, C, 1.0, 0.0, algo=algo)
+# (M, N, K): one CTA per tile for the tensor-core family at the first two;
+# at the third it splits the operands ahead and runs on CTA pairs
+SUBNORMAL_SHAPES = [(128, 128, 128), (256, 384, 160), (2048, 2560, 512)]
+SUBNORMAL_ALGOS = ["auto", "simt_tma", "simt_cpasync", "tc_3xtf32", "naive", "smem_tiled",
+                   "small", "reg_2x2", "reg_4x4"]
+
+
+def _small_ints(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(-8, 9, shape, generator=g).float()
+
+
+@pytest.mark.parametrize("shape", SUBNORMAL_SHAPES, ids=["%dx%dx%d" % s for s in SUBNORMAL_SHAPES])
+def test_subnormals_are_kept(orc, shape):
+    """No family flushes subnormals, the 3xTF32 tensor-core path included:
+    (1) normal inputs whose products and sums are subnormal (integers times
+    2^-70 on both sides: results are integers times 2^-140) and (2) subnormal
+    inputs whose significant bits fit TF32's 10-bit mantissa (integers times
+    2^-135) against normal ones (integers times 2^100) give every output
+    bit for bit equal to the oracle."""
+    M, N, K = shape
+    ai, bi = _small_ints((M, K), M + K), _small_ints((K, N), N + 1)
+    for A, B, what in ((ai * 2.0 ** -70, bi * 2.0 ** -70, "subnormal results"),
+                       (ai * 2.0 ** -135, bi * 2.0 ** 100, "subnormal inputs")):
+        R = orc.sgemm_f64(0, 0, 1.0, A.numpy(), B.numpy())
+        assert np.any((R != 0) & (np.abs(R) < 2.0 ** -126)) or what == "subnormal inputs"
+        dA, dB = A.cuda(), B.cuda()
+        for algo in SUBNORMAL_ALGOS:
+            if algo in ("naive", "smem_tiled") and M * N * K > 1 << 24:
+                continue
+            C = torch.empty(M, N, device="cuda")
+            sg.gemm(dA, dB, C, 1.0, 0.0, algo=algo)
+            torch.cuda.synchronize()
+            assert_bit_exact(C.cpu().numpy(), R, f"{what} {algo} {shape}")
+
+
+@pytest.mark.parametrize("shape", [SUBNORMAL_SHAPES[0], SUBNORMAL_SHAPES[2]], ids=["one_cta", "pairs"])
+def test_subnormal_inputs_beyond_tf32_resolution(orc, shape):
+    """Subnormal inputs with all 23 mantissa bits (random bit patterns) against
+    integers times 2^100.  The CUDA-core families meet the FP32 tolerance on
+    the (normal-range) results.  The 3xTF32 path represents each such input
+    as big + small TF32 parts, whose subnormal spacing is 2^-136: every input
+    is kept to within 2^-137, so |G - R| <= 2^-137 * sum_k |b_kj| (plus FP32
+    rounding of the sums) for every output -- up to about 2^-10 relative, a
+    documented precision loss of that family on subnormal inputs."""
+    M, N, K = shape
+    g = torch.Generator().manual_seed(11)
+    bits = torch.randint(1, 1 << 23, (M, K), generator=g, dtype=torch.int32)
+    bits |= torch.randint(0, 2, (M, K), generator=g, dtype=torch.int32) << 31
+    A = bits.view(torch.float32)
+    assert torch.all(A.abs() < 2.0 ** -126) and torch.all(A != 0)
+    B = _small_ints((K, N), 12) * 2.0 ** 100
+    R = orc.sgemm_f64(0, 0, 1.0, A.numpy(), B.numpy())
+    absB = np.abs(B.numpy().astype(np.float64))
+    absAB = np.abs(A.numpy().astype(np.float64)) @ absB
+    bound = 2.0 ** -137 * absB.sum(axis=0)[None, :] + 2.0 ** -20 * absAB
+    dA, dB = A.cuda(), B.cuda()
+    for algo in ["auto", "simt_tma", "simt_cpasync", "small", "reg_4x4", "tc_3xtf32"]:
+        C = torch.empty(M, N, device="cuda")
+        sg.gemm(dA, dB, C, 1.0, 0.0, algo=algo)
         torch.cuda.synchronize()
-        assert torch.all(C == 4 * 2.0 ** -140), algo
+        G = C.cpu().numpy().astype(np.float64)
+        if algo == "tc_3xtf32":
+            worst = float(np.max(np.abs(G - R) - bound))
+            assert worst <= 0, f"{algo} {shape}: exceeds the bound by {worst:.3e}"
+        else:
+            rel = np.linalg.norm(G - R) / np.linalg.norm(R)
+            assert rel <= 1e-5, f"{algo} {shape}: rel_fro {rel:.3e}"
 
 
 # --------------------------------------------------------------- streams / status

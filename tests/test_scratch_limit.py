@@ -43,9 +43,10 @@ LIMIT0_CASES = [(c, "auto") for c in W.ALL_CASES] + [(W.HEADLINE, "tc_3xtf32"),
 
 def test_limit_zero_allocates_nothing_and_matches_the_oracle(orc):
     """Every workload under limit 0: the device's free memory and the bytes the
-    library holds do not move, large products run as one launch (no stream-K
-    fixup pass, no operand copied ahead), and each whole output matches the
-    oracle (bit for bit on integer inputs)."""
+    library holds do not move, large products run as one launch when the
+    library holds nothing (no stream-K fixup pass, no operand copied ahead),
+    and each whole output matches the oracle (bit for bit on integer
+    inputs)."""
     host = [(case, algo, W.make_inputs(case)) for case, algo in LIMIT0_CASES]
     dev = [tuple(t.cuda() for t in inputs) for _, _, inputs in host]
     torch.cuda.synchronize()
@@ -71,9 +72,13 @@ def test_limit_zero_allocates_nothing_and_matches_the_oracle(orc):
     assert limit == 0
     assert free1 == free0
     assert held1 == held0
-    assert launches[W.HEADLINE.name + "auto"] == 1
-    assert launches[W.SQUARE_1024.name + "auto"] == 1
-    assert launches[W.HEADLINE.name + "tc_3xtf32"] == 1
+    if held0 == 0:
+        # nothing held (no graph kept a buffer): no fixup pass, nothing copied
+        # ahead; buffers a graph still holds may be used, since using them
+        # allocates nothing
+        assert launches[W.HEADLINE.name + "auto"] == 1
+        assert launches[W.SQUARE_1024.name + "auto"] == 1
+        assert launches[W.HEADLINE.name + "tc_3xtf32"] == 1
     for (case, algo, (A, B, C)), (_, _, dC) in zip(host, dev):
         R = orc.sgemm_f64(case.transA, case.transB, case.alpha, A.numpy(), B.numpy(), case.beta,
                           C.numpy() if case.beta != 0 else None)
@@ -170,7 +175,7 @@ def _fresh(tmp_path, env_limit=None):
 
 def test_lowering_the_limit_frees_what_the_library_holds(tmp_path):
     """In a fresh process (no graphs): the headline product takes scratch
-    (the operand transpose and, with it, nothing else); setting the limit to 0
+    (the operand transpose and the stream-K workspace); setting the limit to 0
     frees all of it and the next product allocates nothing."""
     got = _fresh(tmp_path)
     assert got["initial_limit"] == (1 << 64) - 1
