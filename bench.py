@@ -286,6 +286,35 @@ def time_transpose(sg, torch, rows, cols, reps, stream, flush=None):
     return ms, ok
 
 
+def measure_tf32_peak(torch, dev, n=8192, reps=10):
+    """TF32 tensor throughput of this GPU as cuBLAS delivers it: torch.matmul
+    of two n x n FP32 matrices with TF32 allowed, best of `reps` (CUDA events).
+    A library run (not inspected), used only as the roofline denominator of
+    the 3xTF32 kernel.  None if it cannot run."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    try:
+        torch.backends.cuda.matmul.allow_tf32 = True
+        X = torch.randn(n, n, device=dev)
+        Y = torch.randn(n, n, device=dev)
+        Z = torch.empty(n, n, device=dev)
+        for _ in range(3):
+            torch.mm(X, Y, out=Z)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.mm(X, Y, out=Z)
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del X, Y, Z
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except RuntimeError:
+        return None
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
 def tflops(flops, ms):
     return flops / (ms * 1e-3) / 1e12
 
@@ -439,8 +468,10 @@ def run_ours(args, dist):
         try:
             r, kms, _ = time_gemm(sg, torch, case, A, B, C, max(5, min(args.steps, 200)), 3,
                                   "tc_3xtf32", stream)
+            tf32_meas = measure_tf32_peak(torch, dev)
             bf16 = float(peaks.get("bf16_tflops") or FALLBACK_BF16_TFLOPS)
-            tf32_peak = bf16 * NOMINAL_TF32_OVER_BF16
+            tf32_nominal = bf16 * NOMINAL_TF32_OVER_BF16
+            tf32_peak = tf32_meas or tf32_nominal
             ach = tflops(flops, kms)
             tensor = {"value": round(tflops(flops, r), 3), "unit": "TFLOP/s",
                       "ms_per_step": round(r, 5), "algo": "tc_3xtf32",
@@ -448,9 +479,13 @@ def run_ours(args, dist):
                                    "peak": round(tf32_peak, 1), "unit": "TFLOP/s",
                                    "frac": round(ach / tf32_peak, 4),
                                    "traffic": stored_traffic(f"tc_3xtf32_{case.name}")[0],
-                                   "peak_basis": ("TF32 dense = measured bf16 burst "
+                                   "peak_basis": ("measured: cuBLAS TF32 (torch.matmul, allow_tf32) at "
+                                                  "8192^3, best of 10, in this run"
+                                                  if tf32_meas else
+                                                  "TF32 dense = measured bf16 burst "
                                                   f"{bf16:.1f} x nominal 1.1/2.25"
                                                   + ("" if peaks.get("bf16_tflops") else " (fallback)")),
+                                   "peak_nominal_from_bf16": round(tf32_nominal, 1),
                                    "peak_fp32_equivalent": round(tf32_peak / 3, 1),
                                    "frac_fp32_equivalent": round(3 * ach / tf32_peak, 4),
                                    "note": "3 TF32 MMAs per FP32 product; achieved counts 2MNK"}}
@@ -524,6 +559,24 @@ def run_ours(args, dist):
             ladder[f"speedup_{rung}_over_naive"] = round(ladder[rung] / ladder["naive"], 2)
         del La, Lb, Lc
 
+    # ---- the ownership contract: the same products with the library's scratch
+    # limit at 0 (no workspace, nothing copied ahead), then the limit restored
+    limit0 = None
+    if not args.no_limit0:
+        limit0 = {"what": "sgemm_set_scratch_limit(0): no library device memory; "
+                          "whole tiles, operands read in place"}
+        sq = W.SQUARE_1024
+        qA, qB, qC = (t.to(dev) for t in W.make_inputs(sq))
+        for lim_name, lim in (("unlimited", sg.SCRATCH_UNLIMITED), ("limit_0", 0)):
+            sg.sgemm_set_scratch_limit(lim)
+            r, _, _ = time_gemm(sg, torch, case, A, B, C, max(5, min(args.steps, 50)), 3, args.algo,
+                                stream, per_call_events=False)
+            us = 1000 * time_gemm_graph(sg, torch, sq, qA, qB, qC, args.algo)
+            limit0[lim_name] = {case.name + "_tflops": round(tflops(flops, r), 3),
+                                sq.name + "_graph_us": round(us, 2)}
+        sg.sgemm_set_scratch_limit(sg.SCRATCH_UNLIMITED)
+        del qA, qB, qC
+
     # ---- library context: cuBLAS FP32 (TF32 off) on the headline product
     library_context = None
     if not args.no_library_context:
@@ -585,7 +638,7 @@ def run_ours(args, dist):
         "e2e": e2e, "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
         "tensor_core_3xtf32": tensor, "transpose": transpose,
         "strided_batched": batched, "ladder": ladder,
-        "library_context": library_context,
+        "library_context": library_context, "scratch_limit_0": limit0,
         "vs_size": vs_size, "configs": families,
         "configs_graph": families_graph or None,
         "device": {"name": props.name, "sms": sms, "cc": f"{props.major}.{props.minor}"},
@@ -688,6 +741,8 @@ def main(argv=None):
                     help="skip the cuBLAS FP32 context number")
     ap.add_argument("--no-batched", action="store_true",
                     help="skip the extra timing of a strided batch")
+    ap.add_argument("--no-limit0", action="store_true",
+                    help="skip the products timed under a scratch limit of 0")
     ap.add_argument("--no-ladder", action="store_true",
                     help="skip the naive / shared-memory-tiled comparison kernels")
     args = ap.parse_args(argv)

@@ -308,6 +308,11 @@ int pick_simt_tile(const Args &a, int producer, int sm_count, int64_t batch) {
 #ifndef SG_SK_FIXUP_LAUNCH
 #define SG_SK_FIXUP_LAUNCH 0
 #endif
+// Split tiles are finished in-kernel while grid <= SG_SK_INKERNEL_RATIO x
+// the number of split tiles (at most about RATIO + 1 segments per tile).
+#ifndef SG_SK_INKERNEL_RATIO
+#define SG_SK_INKERNEL_RATIO 2
+#endif
 // SG_EPI_TMA 1: the 128 x 128 TMA kernels write C through a staged tile and
 // TMA stores when beta == 0 (0: always from registers).
 #ifndef SG_EPI_TMA
@@ -580,9 +585,11 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   // NN 125.3 -> 129.3 us and 256^3 11.0 -> 19.5 us).  SG_SK_FIXUP_LAUNCH 1:
   // always the separate pass.
   const bool in_kernel_fixup_kernel =
-      producer == kTma && !(a.ta == 0 && SG_SIMT_TRANSPOSE_A) && tile != kTile128x64;
+      producer == kTma && (!(a.ta == 0 && SG_SIMT_TRANSPOSE_A) || SG_SK_INKERNEL_ATRANS) &&
+      tile != kTile128x64;
   p.sk_count = (plan.sk_tiles > 0 && !SG_SK_FIXUP_LAUNCH && in_kernel_fixup_kernel &&
-                plan.grid <= 2 * static_cast<int64_t>(plan.sk_tiles) && plan.sk_tiles <= kSkCounters)
+                plan.grid <= SG_SK_INKERNEL_RATIO * static_cast<int64_t>(plan.sk_tiles) &&
+                plan.sk_tiles <= kSkCounters)
                    ? d.sk_count
                    : nullptr;
 

@@ -176,6 +176,14 @@ __device__ __forceinline__ int sk_for_each_segment(const SimtParams &p, int64_t 
 #ifndef SG_SIMT_TRANSPOSE_UNROLL
 #define SG_SIMT_TRANSPOSE_UNROLL 4
 #endif
+// SG_SIMT_CPASYNC_REGS: registers per thread of the cp.async producer warps;
+// SG_SIMT_CPASYNC_UNROLL: copies each of them unrolls.
+#ifndef SG_SIMT_CPASYNC_REGS
+#define SG_SIMT_CPASYNC_REGS 40
+#endif
+#ifndef SG_SIMT_CPASYNC_UNROLL
+#define SG_SIMT_CPASYNC_UNROLL 2
+#endif
 
 template <int WARPS_M_, int WARPS_N_, bool A_KMAJOR_, bool B_KMAJOR_, int STAGES_, int PRODUCER_,
           int TN_ = 8, bool A_TRANS_ = false>
@@ -215,7 +223,7 @@ struct SimtConfig {
   static constexpr bool LEAN_PRODUCER = (PRODUCER == kTma) && !A_TRANS;
   static constexpr int LAUNCH_REGS = (65536 / (THREADS * MIN_CTAS)) & ~7;
   static constexpr int PRODUCER_REGS =
-      LEAN_PRODUCER ? 24 : (A_TRANS ? SG_SIMT_TRANSPOSER_REGS : 40);
+      LEAN_PRODUCER ? 24 : (A_TRANS ? SG_SIMT_TRANSPOSER_REGS : SG_SIMT_CPASYNC_REGS);
   static constexpr int MATH_REGS_FIT =
       ((THREADS * LAUNCH_REGS - PRODUCER_THREADS * PRODUCER_REGS) / MATH_THREADS) & ~7;
   static constexpr int MATH_REGS = MATH_REGS_FIT < 240 ? MATH_REGS_FIT : 240;
@@ -417,6 +425,7 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
                                                 bool &ok) {
   constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
   constexpr int PT = Cfg::PRODUCER_THREADS;
+  constexpr int UNROLL = SG_SIMT_CPASYNC_UNROLL;
   uint32_t it = 0;
   for_each_unit(p, [&](const WorkUnit &u) {
     int bi, tm, tn;
@@ -436,7 +445,7 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
       const uint32_t b_dst = a_dst + Cfg::A_STAGE_BYTES;
       const int k0 = kt * BK;
       // op(A) tile: BM x 32 elements
-#pragma unroll 4
+#pragma unroll UNROLL
       for (int e = ptid; e < BM * BK; e += PT) {
         int m, k;
         uint32_t off;
@@ -457,7 +466,7 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
         cp_async_4(a_dst + off, src, in ? 4u : 0u);
       }
       // op(B) tile: 32 x BN elements
-#pragma unroll 4
+#pragma unroll UNROLL
       for (int e = ptid; e < BN * BK; e += PT) {
         int n, k;
         uint32_t off;
@@ -512,6 +521,13 @@ __device__ __forceinline__ int thread_col(int tn, int c) {
 #ifndef SG_SIMT_KC_UNROLL_WIDE
 #define SG_SIMT_KC_UNROLL_WIDE 1
 #endif
+// SG_SIMT_KA_PAIR_ROWS: k values of an m-contiguous op(A) held at once when
+// op(B) is k-contiguous (the row-paired FFMA2 form): each k costs the same two
+// LDS.128 whatever the grouping; fewer held values leave room for op(B)'s
+// 4 k x 8 column fragment.
+#ifndef SG_SIMT_KA_PAIR_ROWS
+#define SG_SIMT_KA_PAIR_ROWS 4
+#endif
 
 // SG_SIMT_TRANSPOSE_A  1: with the TMA producer, a k-contiguous op(A) tile is
 //                        rewritten m-contiguous in shared memory by three
@@ -523,9 +539,21 @@ __device__ __forceinline__ int thread_col(int tn, int c) {
 #define SG_SIMT_TRANSPOSE_A 1
 #endif
 
-template <int TN>
+// SG_SIMT_KC_UNROLL_CPASYNC: the unroll of the kernels fed by cp.async.
+// Fully unrolled they spilled 8-140 bytes; not unrolled (and with the
+// producer's copies unrolled by 2) none spills and all are faster (GB300,
+// graph replays, 1024^3 forced to cp.async: NN 98.0 -> 92.0 us, NT 117.3 ->
+// 112.1, TN 98.6 -> 90.2, TT 98.8 -> 92.8).  The TMA kernels stay fully
+// unrolled: for those reading a k-contiguous op(B) tile the spill-free
+// forms measured slower (unroll 1: 1024^3 TT 50.9 -> 52.7 us, NT 53.0 ->
+// 55.0; 4096^3 TT 2259 -> 2359 us), so their 32-80 spilled bytes are kept.
+#ifndef SG_SIMT_KC_UNROLL_CPASYNC
+#define SG_SIMT_KC_UNROLL_CPASYNC 1
+#endif
+template <class Cfg>
 __host__ __device__ constexpr int kc_unroll() {
-  return TN == 16 ? SG_SIMT_KC_UNROLL_WIDE : SG_SIMT_KC_UNROLL;
+  return Cfg::TN == 16 ? SG_SIMT_KC_UNROLL_WIDE
+         : Cfg::PRODUCER == kCpAsync ? SG_SIMT_KC_UNROLL_CPASYNC : SG_SIMT_KC_UNROLL;
 }
 
 // How the 64 accumulators of a thread are packed into 32 float2 and updated.
@@ -576,7 +604,7 @@ __device__ __forceinline__ void mma_stage(AccT<Cfg> &acc, const char *a_stage, c
   else
     b_base = b_stage + (wn * Cfg::WN + 4 * tn) * 4;  // + k * BN * 4, + 128 per column group
 
-  constexpr int KC_UNROLL = kc_unroll<TN>();
+  constexpr int KC_UNROLL = kc_unroll<Cfg>();
 #pragma unroll KC_UNROLL
   for (int kc = 0; kc < 8; ++kc) {  // 4 k per chunk
     float bk[4][8];  // k-contiguous op(B) (TN == 8): bk[kk][c]
@@ -592,7 +620,7 @@ __device__ __forceinline__ void mma_stage(AccT<Cfg> &acc, const char *a_stage, c
     // op(A) values are loaded KA k at a time (k-contiguous: one LDS of KA floats
     // per row; the wavefront count is the same for KA = 2 and 4, KA = 2 holds
     // half the registers, which the 8 x 16 tile needs).
-    constexpr int KA = (TN == 16) ? 2 : 4;
+    constexpr int KA = (TN == 16) ? 2 : (MODE == kPairRows ? SG_SIMT_KA_PAIR_ROWS : 4);
 #pragma unroll
     for (int kg = 0; kg < 4 / KA; ++kg) {
       float a[8][KA];  // a[r][j] = op(A)(row r, k = kc*4 + kg*KA + j)
@@ -787,9 +815,13 @@ __device__ __forceinline__ void stage_tile(unsigned char *staging, const AccT<Cf
 }
 
 // Kernels that can finish split tiles themselves (SimtParams::sk_count).
+// SG_SK_INKERNEL_ATRANS 1: also the kernels whose producer warps transpose A.
+#ifndef SG_SK_INKERNEL_ATRANS
+#define SG_SK_INKERNEL_ATRANS 0
+#endif
 template <class Cfg>
 __host__ __device__ constexpr bool kInKernelFixup() {
-  return Cfg::PRODUCER == kTma && !Cfg::A_TRANS && Cfg::MATH_WARPS == 8;
+  return Cfg::PRODUCER == kTma && (!Cfg::A_TRANS || SG_SK_INKERNEL_ATRANS) && Cfg::MATH_WARPS == 8;
 }
 
 // Barrier of the math warps only (the producer warps never take part), on an

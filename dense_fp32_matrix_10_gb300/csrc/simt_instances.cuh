@@ -52,9 +52,18 @@ template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR>
 struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x128> {
   using Cfg = SimtConfig<4, 2, A_KMAJOR, B_KMAJOR, 4, PRODUCER, 8, kTransA<PRODUCER, A_KMAJOR>>;
 };
+// 128 x 64 tiles run two CTAs per SM.  With the raw A ring of the in-smem
+// transpose (32 KiB) four stages would need ~129 KiB per CTA, and only one
+// CTA -- four math warps -- would fit on an SM; three stages (~105 KiB) let
+// two fit.
+#ifndef SG_SIMT_STAGES_64_TRANS
+#define SG_SIMT_STAGES_64_TRANS 3
+#endif
 template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR>
 struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x64> {
-  using Cfg = SimtConfig<4, 1, A_KMAJOR, B_KMAJOR, 4, PRODUCER, 8, kTransA<PRODUCER, A_KMAJOR>>;
+  static constexpr bool kT = kTransA<PRODUCER, A_KMAJOR>;
+  using Cfg = SimtConfig<4, 1, A_KMAJOR, B_KMAJOR, kT ? SG_SIMT_STAGES_64_TRANS : 4, PRODUCER, 8, kT>;
+  static_assert(2 * (Cfg::SMEM_BYTES + 1024) <= 233472, "two 128 x 64 CTAs must fit on an SM");
 };
 template <int PRODUCER, bool A_KMAJOR>
 struct SimtPick<PRODUCER, A_KMAJOR, false, kTile128x256> {
@@ -69,13 +78,15 @@ SimtEntry simt_make_entry() {
 
 // A stored M x K (transA = N) is the k-contiguous ("K-major") layout; B stored
 // N x K (transB = T) likewise.
-// The 128 x 256 tile exists only for n-contiguous op(B) (transB = N); a
-// request for it with transB = T gets the 128 x 128 tile.
+// The 128 x 256 tile exists only for n-contiguous op(B) (transB = N) and the
+// TMA producer (the only combination the dispatcher picks it for); any other
+// request for it gets the 128 x 128 tile.
 #define SG_DEFINE_SIMT_FAMILY(PROD, TA)                                                  \
   SimtEntry simt_entry_##PROD##_##TA(int transB, int tile) {                             \
     constexpr bool AK = (TA == 0);                                                       \
     if (transB == 0) {                                                                   \
-      if (tile == kTile128x256) return simt_make_entry<PROD, AK, false, kTile128x256>(); \
+      if constexpr (PROD == kTma)                                                        \
+        if (tile == kTile128x256) return simt_make_entry<PROD, AK, false, kTile128x256>(); \
       return tile == kTile128x128 ? simt_make_entry<PROD, AK, false, kTile128x128>()     \
                                   : simt_make_entry<PROD, AK, false, kTile128x64>();      \
     }                                                                                    \
