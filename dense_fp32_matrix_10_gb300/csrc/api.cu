@@ -339,6 +339,42 @@ SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws
   return pl;
 }
 
+// Cluster split-K (SimtParams::csk): a product whose tiles leave CTA slots
+// idle splits each tile's k-tiles over a cluster of S CTAs that add their
+// partials through distributed shared memory -- one launch, no workspace,
+// no fixup pass.  It pays where each CTA's share is short; with longer
+// shares stream-K, which balances the k-tiles over every CTA slot, is the
+// faster (GB300, graph replays, us per call, stream-K -> clusters of <= 4:
+// 512^3 NN 19.6 -> 13.5, NT 20.8 -> 14.8, 640^3 23.2 -> 22.0, 768^3 29.7 ->
+// 24.6; but 8192 x 64 x 4096 89.1 -> 98.4, 2048 x 64 x 2048 26.9 -> 30.8,
+// 1000 x 1013 x 997 57.9 -> 63.5, 1024^3 50.4 -> 50.8; clusters of 8 lost to
+// clusters of 4: 512^3 16.0 against 13.5).  So S is the larger of 4 and 2
+// for which every cluster is resident at once and each CTA gets between
+// SG_CSK_MIN_K and SG_CSK_MAX_K k-tiles.  SG_CSK 0 turns it off.
+#ifndef SG_CSK
+#define SG_CSK 1
+#endif
+#ifndef SG_CSK_MIN_K
+#define SG_CSK_MIN_K 2
+#endif
+#ifndef SG_CSK_MAX_K
+#define SG_CSK_MAX_K 8
+#endif
+#ifndef SG_CSK_MAX
+#define SG_CSK_MAX 4
+#endif
+int pick_csk(const SimtKernelInfo &ki, int64_t tiles, int64_t k_tiles, int64_t slots) {
+  if (!SG_CSK || tiles >= slots) return 0;
+  for (int i = 2; i >= 0; --i) {
+    const int S = 2 << i;
+    if (S > SG_CSK_MAX || ki.bm % S != 0) continue;
+    if (ki.max_clusters[i] >= tiles && k_tiles >= int64_t(S) * SG_CSK_MIN_K &&
+        k_tiles <= int64_t(S) * SG_CSK_MAX_K)
+      return S;
+  }
+  return 0;
+}
+
 bool stream_capturing(cudaStream_t s) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
@@ -565,6 +601,21 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   if (a.beta != 0.0f) p.c_pref = c_map;
 
   const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
+  // Under-filled products: cluster split-K, one launch and no workspace
+  const int csk = pick_csk(*ki, num_tiles, p.k_tiles, slots);
+  if (csk > 1) {
+    p.csk = csk;
+    p.dp_tiles = 0;
+    p.sk_iters = 0;
+    p.workspace = nullptr;
+    p.sk_count = nullptr;
+    if (pre && (*pre)() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    if (simt_entry(producer, a.ta, a.tb, tile)
+            .launch(p, &tmA, &tmB, &tmC, static_cast<int>(num_tiles * csk), stream, pdl, csk) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+    t_last_launches = 1;
+    return SGEMM_SUCCESS;
+  }
   const bool capturing = stream_capturing(stream);
   std::unique_lock<std::mutex> ws_lock(d.ws_mu);
   SkPlan plan = plan_stream_k(num_tiles, p.k_tiles, slots, !d.ws_failed);
@@ -599,7 +650,7 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
     return SGEMM_ERR_LAUNCH;
   if (pre && (*pre)() != cudaSuccess) return SGEMM_ERR_LAUNCH;
   cudaError_t e =
-      simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, &tmC, plan.grid, stream, pdl);
+      simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, &tmC, plan.grid, stream, pdl, 1);
   if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
   if (plan.sk_tiles > 0) {

@@ -39,15 +39,49 @@ cudaError_t launch_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
+// As launch_maybe_pdl, in clusters of `cluster` CTAs along x when cluster > 1.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t s, bool pdl, int cluster, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 struct SimtKernelInfo {
   int bm, bn, threads, smem_bytes, ctas_per_sm;
+  // clusters of 2, 4 and 8 CTAs resident at once on the device (0: that
+  // cluster size cannot be launched)
+  int max_clusters[3];
 };
 
-// Launches one instantiation; grid = number of persistent CTAs.
+// Launches one instantiation; grid = number of CTAs (persistent, or S per
+// tile with cluster split-K).
 // pdl: launch with programmatic stream serialization (it directly follows
-// another kernel of the same call on the stream).
+// another kernel of the same call on the stream).  cluster: CTAs per cluster
+// along x (1: no cluster).
 using SimtLaunchFn = cudaError_t (*)(const SimtParams &, const CUtensorMap *, const CUtensorMap *,
-                                     const CUtensorMap *, int grid, cudaStream_t, bool pdl);
+                                     const CUtensorMap *, int grid, cudaStream_t, bool pdl,
+                                     int cluster);
 // Sets the kernel's shared-memory attribute on the current device (once) and
 // reports its shape and occupancy.
 using SimtInfoFn = cudaError_t (*)(SimtKernelInfo *);

@@ -168,7 +168,7 @@ extern "C" sgemm_status_t sgemm_noalloc(int transA, int transB, int64_t M, int64
   }
   CUtensorMap tmC;   // C written straight from registers (p.c_tma == 0)
   std::memset(&tmC, 0, sizeof(tmC));
-  if (simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, &tmC, plan.grid, s, false) != cudaSuccess)
+  if (simt_entry(producer, a.ta, a.tb, tile).launch(p, &tmA, &tmB, &tmC, plan.grid, s, false, 1) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
   t_last_launches = 1;
   if (plan.sk_tiles > 0) {

@@ -212,6 +212,41 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
+// As mbar_try_wait, with acquire semantics at cluster scope: what the peers
+// released before arriving is visible after it.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded form (see wait_parity_bounded).
+__device__ __forceinline__ bool wait_parity_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                            uint64_t budget_ns, int *status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (globaltimer_ns() - t0 > budget_ns) {
+      if (status) atomicExch(status, kDevTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+// 16 bytes of a peer CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t caddr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(caddr)
+               : "memory");
+  return v;
+}
 
 // ---------------------------------------------------------------- dependent launch
 // A kernel launched with programmatic stream serialization may start while

@@ -92,6 +92,14 @@ struct SimtParams {
   // CTA that arrives last adds the tile's partials in k order and writes C.
   // Null: sk_fixup_kernel does that in a second launch.
   int *sk_count = nullptr;
+  // Cluster split-K (csk = S > 1): the kernel is launched in clusters of S
+  // CTAs along x, grid = S * num_tiles, and cluster c computes tile c with
+  // its k-tiles divided over the S CTAs (rank r takes [r*KT/S, (r+1)*KT/S)).
+  // Each CTA leaves its partial tile in its own shared memory; after a
+  // cluster-wide handshake CTA r adds rows [r*BM/S, (r+1)*BM/S) of the S
+  // partials, in rank order, through distributed shared memory and writes C.
+  // No workspace, no second launch.  0: off.
+  int csk = 0;
   // C written by TMA stores (EPI_TMA kernels; beta == 0 and C addressable by
   // the tmC tensor map: 2-D, or 3-D with the batch stride)
   int c_tma = 0;
@@ -108,15 +116,24 @@ __device__ __forceinline__ void unit_coords(const SimtParams &p, int t, int &b, 
   tile_coords(t - b * p.tiles_per_batch, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
 }
 
-// One unit of work: k-tiles [k0, k1) of tile `tile`; slot < 0 writes C.
+// One unit of work: k-tiles [k0, k1) of tile `tile`; slot -1 writes C,
+// kCskSlot is a cluster split-K share, slot >= 0 a stream-K partial.
 struct WorkUnit {
   int tile, k0, k1, slot;
 };
+constexpr int kCskSlot = -2;
 
 // Visits this CTA's units in order; f returns false to stop early.  Every
 // role of the CTA walks the same sequence.
 template <class F>
 __device__ __forceinline__ void for_each_unit(const SimtParams &p, F &&f) {
+  if (p.csk > 0) {   // cluster split-K: one share of one tile (cluster dims (S, 1, 1))
+    const int S = p.csk, r = static_cast<int>(blockIdx.x) % S;
+    const int k0 = static_cast<int>(static_cast<int64_t>(r) * p.k_tiles / S);
+    const int k1 = static_cast<int>(static_cast<int64_t>(r + 1) * p.k_tiles / S);
+    f(WorkUnit{static_cast<int>(blockIdx.x) / S, k0, k1, kCskSlot});
+    return;
+  }
   for (int t = blockIdx.x; t < p.dp_tiles; t += gridDim.x)
     if (!f(WorkUnit{t, 0, p.k_tiles, -1})) return;
   if (p.sk_iters > 0) {
@@ -860,6 +877,49 @@ __device__ __forceinline__ void add_partial(AccT<Cfg> &acc, const float *ws, int
   }
 }
 
+// Cluster split-K, after every CTA of the cluster has staged its partial
+// (dense BM x BN at stg_addr in each CTA's shared memory): the math threads
+// of CTA `rank` add rows [rank*BM/S, (rank+1)*BM/S) of the S partials in rank
+// order (0 + p0 + p1 + ...) through distributed shared memory, apply alpha
+// and beta and write C.  Not inlined: the accumulators are dead by now, and
+// inlined this code raised the register pressure of the k-loop.
+template <class Cfg>
+__device__ __noinline__ void csk_reduce(float *Cb, int64_t ldc, int m0, int n0, int M, int N, float alpha,
+                                        float beta, bool c_vec4, uint32_t stg_addr, int S, uint32_t rank,
+                                        int tid) {
+  const bool read_c = beta != 0.0f;
+  constexpr int BN4 = Cfg::BN / 4;
+  const int rows = Cfg::BM / S, r0 = static_cast<int>(rank) * rows;
+  for (int e = tid; e < rows * BN4; e += Cfg::MATH_THREADS) {
+    const int row = r0 + e / BN4, c4 = e % BN4;
+    const int m = m0 + row, n = n0 + 4 * c4;
+    if (m >= M || n >= N) continue;
+    const uint32_t off = static_cast<uint32_t>(row * Cfg::BN + 4 * c4) * 4u;
+    float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int q = 0; q < S; ++q) {
+      const float4 v = ld_dsmem_v4(map_to_rank(stg_addr + off, q));
+      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+    }
+    float *crow = Cb + static_cast<int64_t>(m) * ldc;
+    const float v[4] = {sum.x, sum.y, sum.z, sum.w};
+    if (c_vec4 && n + 3 < N) {
+      float4 o;
+      if (read_c) {
+        const float4 c = *reinterpret_cast<const float4 *>(crow + n);
+        o = make_float4(fmaf(alpha, v[0], beta * c.x), fmaf(alpha, v[1], beta * c.y),
+                        fmaf(alpha, v[2], beta * c.z), fmaf(alpha, v[3], beta * c.w));
+      } else {
+        o = make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
+      }
+      *reinterpret_cast<float4 *>(crow + n) = o;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (n + q < N) crow[n + q] = read_c ? fmaf(alpha, v[q], beta * crow[n + q]) : alpha * v[q];
+    }
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
@@ -869,6 +929,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ int s_last;   // in-kernel fixup: this CTA arrived last at its tile
   __shared__ __align__(8) uint64_t s_math_bar;
+  // cluster split-K: every partial of the cluster staged / every peer done reading
+  __shared__ __align__(8) uint64_t s_csk_bar[2];
   // 1024-byte alignment of the stage ring (required by the 128 B swizzle).
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -890,7 +952,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
       mbar_init(raw_full0 + 8 * r, 1);
       mbar_init(raw_empty0 + 8 * r, Cfg::TRANSPOSER_WARPS);
     }
-    if constexpr (kInKernelFixup<Cfg>() || Cfg::EPI_TMA) mbar_init(smem_u32(&s_math_bar), Cfg::MATH_WARPS);
+    mbar_init(smem_u32(&s_math_bar), Cfg::MATH_WARPS);
+    if (p.csk > 1) {
+      // one arrival per math warp of each of the cluster's CTAs
+      mbar_init(smem_u32(&s_csk_bar[0]), p.csk * Cfg::MATH_WARPS);
+      mbar_init(smem_u32(&s_csk_bar[1]), p.csk * Cfg::MATH_WARPS);
+    }
     fence_mbar_init();
   }
   if (Cfg::PRODUCER == kTma && threadIdx.x == Cfg::MATH_THREADS) {
@@ -899,6 +966,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     if (Cfg::EPI_TMA && p.c_tma) tma_prefetch_desc(&tmC);
   }
   __syncthreads();
+  // the peers' barriers exist before any CTA of the cluster arrives on them
+  if (p.csk > 1) cluster_sync();
   // Everything above overlaps the previous kernel of the same call (the
   // transpose of an operand) when this one was launched as its dependent; the
   // operands and C are touched only after it has finished.  The fixup pass
@@ -966,6 +1035,32 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
                   tile_n * Cfg::BN, wm, wn, tm, tn);
     return true;
   };
+  // Cluster split-K: stages this CTA's partial tile, adds this CTA's rows of
+  // the cluster's S partials in rank order (0 + p0 + p1 + ...), applies
+  // alpha / beta and writes them to C.  False if a bounded wait gave up.
+  const auto csk_finish = [&](const AccT<Cfg> &acc, int tile) -> bool {
+    const int S = p.csk;
+    const uint32_t rank = blockIdx.x % static_cast<uint32_t>(S);
+    // every math warp is past its last stage: the ring may be overwritten
+    if (!math_barrier(math_bar, math_phase, lane, p)) return false;
+    float *stg = reinterpret_cast<float *>(smem);   // dense BM x BN partial
+    store_partial<Cfg>(stg, acc, wm, wn, tm, tn);
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+    __syncwarp();
+    const uint32_t full = smem_u32(&s_csk_bar[0]), done = smem_u32(&s_csk_bar[1]);
+    if (lane == 0)
+      for (int q = 0; q < S; ++q) mbar_arrive_cluster(map_to_rank(full, q));
+    if (!wait_parity_bounded_cluster(full, 0, p.wait_budget_ns, p.status)) return false;
+    int bi, tile_m, tile_n;
+    unit_coords(p, tile, bi, tile_m, tile_n);
+    csk_reduce<Cfg>(p.C + static_cast<int64_t>(bi) * p.strideC, p.ldc, tile_m * Cfg::BM, tile_n * Cfg::BN,
+                    p.M, p.N, p.alpha, p.beta, p.c_vec4 != 0, smem_u32(stg), S, rank, threadIdx.x);
+    // this CTA's shared memory stays until every peer has read its partial
+    __syncwarp();
+    if (lane == 0)
+      for (int q = 0; q < S; ++q) mbar_arrive_cluster(map_to_rank(done, q));
+    return wait_parity_bounded_cluster(done, 0, p.wait_budget_ns, p.status);
+  };
   for_each_unit(p, [&](const WorkUnit &u) {
     AccT<Cfg> acc;
 #pragma unroll
@@ -980,6 +1075,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
+    if (u.slot == kCskSlot) return csk_finish(acc, u.tile);
     if constexpr (!kInKernelFixup<Cfg>()) {
       if (u.slot < 0) {
         return finish_tile(acc, u.tile);

@@ -10,9 +10,9 @@ namespace sg {
 
 template <class Cfg>
 cudaError_t simt_launch(const SimtParams &p, const CUtensorMap *tmA, const CUtensorMap *tmB,
-                        const CUtensorMap *tmC, int grid, cudaStream_t stream, bool pdl) {
-  return launch_maybe_pdl(simt_gemm_kernel<Cfg>, dim3(grid), dim3(Cfg::THREADS), Cfg::SMEM_BYTES,
-                          stream, pdl, *tmA, *tmB, *tmC, p);
+                        const CUtensorMap *tmC, int grid, cudaStream_t stream, bool pdl, int cluster) {
+  return launch_cluster_maybe_pdl(simt_gemm_kernel<Cfg>, dim3(grid), dim3(Cfg::THREADS), Cfg::SMEM_BYTES,
+                                  stream, pdl, cluster, *tmA, *tmB, *tmC, p);
 }
 
 template <class Cfg>
@@ -38,6 +38,27 @@ cudaError_t simt_info(SimtKernelInfo *info) {
   info->threads = Cfg::THREADS;
   info->smem_bytes = Cfg::SMEM_BYTES;
   info->ctas_per_sm = occ;
+  // clusters of 2, 4, 8 CTAs (cluster split-K) that fit at once: a cluster
+  // needs its CTAs on SMs of one GPC
+  for (int i = 0; i < 3; ++i) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 << i);
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2 << i;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, simt_gemm_kernel<Cfg>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      clusters = 0;
+    }
+    info->max_clusters[i] = clusters;
+  }
   return cudaSuccess;
 }
 

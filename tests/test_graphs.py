@@ -47,9 +47,13 @@ def _alone(A, B, M, N, ta=0, tb=0):
     return C.clone()
 
 
-@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (2048, 4864, 256), (1000, 1013, 997),
-                                   (2048, 2048, 2048)],
-                         ids=["stream_k_1024", "pretransposed_2048x4864x256", "repacked_1000x1013x997",
+# 1280 x 1024 x 1024: 80 tiles of 128 x 128, too many for clusters of two on
+# 152 SMs, so stream-K with its workspace; 768 x 768 x 512 (36 tiles of 16
+# k-tiles): cluster split-K
+@pytest.mark.parametrize("shape", [(1280, 1024, 1024), (768, 768, 512), (2048, 4864, 256),
+                                   (1000, 1013, 997), (2048, 2048, 2048)],
+                         ids=["stream_k_1280x1024x1024", "cluster_split_768x768x512",
+                              "pretransposed_2048x4864x256", "repacked_1000x1013x997",
                               "in_kernel_fixup_2048"])
 def test_graph_replays_interleaved_with_eager_calls(shape):
     M, N, K = shape
@@ -155,7 +159,7 @@ CHILD = r"""
 import sys, torch
 sys.path.insert(0, {root!r})
 import dense_fp32_matrix_10_gb300 as sg
-M = N = K = 1024
+M, N, K = 1280, 1024, 1024   # stream-K (more tiles than clusters of two fit)
 g0 = torch.Generator().manual_seed(3)
 A = torch.randn(M, K, generator=g0).cuda(); B = torch.randn(K, N, generator=g0).cuda()
 C = torch.empty(M, N, device="cuda")

@@ -495,19 +495,53 @@ def test_stream_k_is_deterministic(shape):
 def test_stream_k_launches():
     """Large products finish split tiles inside the product kernel (the CTA
     that arrives last at a tile adds its partials): one launch.  Tiles split
-    into many segments take the separate fixup pass: two launches."""
+    into many segments take the separate fixup pass: two launches.  Products
+    whose tiles fit in clusters of two or more CTAs split each tile inside its
+    cluster: one launch."""
     A = torch.randn(2048, 2048, device="cuda")
     B = torch.randn(2048, 2048, device="cuda")
     sg.gemm(A, B, transA=True)                  # TN: no operand transposed ahead
     assert sg.sgemm_last_launch_count() == 1
-    A = torch.randn(1024, 1024, device="cuda")
+    A = torch.randn(1280, 1024, device="cuda")
     B = torch.randn(1024, 1024, device="cuda")
-    sg.gemm(A, B, transA=True)                  # 64 tiles over every SM
+    sg.gemm(A, B)                               # 80 tiles over every SM, A transposed in smem
     assert sg.sgemm_last_launch_count() == 2
+    A = torch.randn(512, 512, device="cuda")
+    B = torch.randn(512, 1024, device="cuda")
+    sg.gemm(A, B, transA=True)                  # 32 tiles of 16 k-tiles: clusters
+    assert sg.sgemm_last_launch_count() == 1
     A = torch.randn(128 * 152, 256, device="cuda")
     B = torch.randn(256, 128, device="cuda")
     sg.gemm(A, B)                               # exactly one wave of whole tiles
     assert sg.sgemm_last_launch_count() == 1
+
+
+# (M, N, K, transA, transB): products with fewer tiles than CTA slots and
+# short k-ranges, split over the CTAs of a cluster (each tile's k-tiles in S
+# shares, S = 2 or 4) and reduced through distributed shared memory; 128 x 64
+# and 128 x 128 tiles, ragged in M, N and K, K not a multiple of S k-tiles
+CSK_SHAPES = [(512, 512, 512, 0, 0), (700, 650, 500, 0, 1), (300, 260, 1000, 1, 0),
+              (1024, 1024, 512, 1, 1), (129, 1000, 1000, 0, 0), (640, 640, 640, 0, 0)]
+
+
+@pytest.mark.parametrize("shape", CSK_SHAPES, ids=["%dx%dx%d_%s%s" % (s[0], s[1], s[2], "NT"[s[3]], "NT"[s[4]])
+                                                 for s in CSK_SHAPES])
+def test_cluster_split_k(orc, shape):
+    """One launch; every output against the oracle (random inputs, alpha and
+    beta) and bit for bit on integer inputs; the same bits on a second run;
+    through the TMA and the cp.async producers."""
+    M, N, K, ta, tb = shape
+    case = W.Case("csk", M, N, K, ta, tb, "uniform", 700 + M, 1.25, -0.75)
+    for algo in ("auto", "simt_cpasync"):
+        G, (A, B, C) = run_case(case, algo=algo)
+        assert sg.sgemm_last_launch_count() == 1, algo
+        R = oracle_full(orc, case, A, B, C)
+        assert_close(G, R, K, f"cluster split-K {shape} {algo}")
+        G2, _ = run_case(case, algo=algo, A=torch.from_numpy(A), B=torch.from_numpy(B), C=torch.from_numpy(C))
+        assert np.array_equal(G, G2), f"{shape} {algo}: not deterministic"
+        ic = case.as_int()
+        Gi, (Ai, Bi, Ci) = run_case(ic, algo=algo)
+        assert_bit_exact(Gi, oracle_full(orc, ic, Ai, Bi, Ci), f"cluster split-K int {shape} {algo}")
 
 
 # --------------------------------------------------------------- operands transposed ahead
@@ -685,9 +719,10 @@ def test_stream_k_on_two_streams(orc):
     library orders them, so both results are right."""
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     g = torch.Generator().manual_seed(5)
-    mats = [(torch.randn(1024, 1024, generator=g), torch.randn(1024, 1024, generator=g))
+    # 80 tiles of 128 x 128: stream-K with the workspace (too many for clusters)
+    mats = [(torch.randn(1280, 1024, generator=g), torch.randn(1024, 1024, generator=g))
             for _ in range(2)]
-    dev = [(a.cuda(), b.cuda(), torch.empty(1024, 1024, device="cuda")) for a, b in mats]
+    dev = [(a.cuda(), b.cuda(), torch.empty(1280, 1024, device="cuda")) for a, b in mats]
     torch.cuda.synchronize()
     for _ in range(5):
         with torch.cuda.stream(s1):
