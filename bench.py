@@ -262,10 +262,12 @@ def time_gemm_graph(sg, torch, case, A, B, C, algo, calls=20, replays=5):
     return start.elapsed_time(end) / (calls * replays)
 
 
-def time_transpose(sg, torch, rows, cols, reps, stream, flush=None):
+def time_transpose(sg, torch, rows, cols, reps, stream, flush=None, read_back=False):
     """Mean per-launch ms of sgemm_transpose on a rows x cols matrix (CUDA
     events around each launch on `stream`; `flush`, a buffer larger than L2,
-    is rewritten between launches, outside the events)."""
+    is rewritten between launches, outside the events, and with `read_back`
+    then read once more, so that the dirty lines the write left in L2 are
+    written back before the timed launch instead of during it)."""
     X = torch.randn(rows, cols, device=stream.device)
     Y = torch.empty(cols, rows, device=stream.device)
     for _ in range(3):
@@ -276,6 +278,8 @@ def time_transpose(sg, torch, rows, cols, reps, stream, flush=None):
         for a, b in ev:
             if flush is not None:
                 flush.fill_(1.0)
+                if read_back:
+                    flush.sum()
             a.record(stream)
             sg.transpose(X, Y, stream=stream)
             b.record(stream)
@@ -500,7 +504,9 @@ def run_ours(args, dist):
         flush = torch.empty(64 * 1024 * 1024, device=dev)    # 256 MiB > L2
         transpose = {}
         for rows, cols, fl in ((4096, 4096, flush), (16384, 16384, None)):
-            ms, ok = time_transpose(sg, torch, rows, cols, 20, stream, fl)
+            ms, ok = time_transpose(sg, torch, rows, cols, 20, stream, fl, read_back=fl is not None)
+            ms_dirty = (time_transpose(sg, torch, rows, cols, 20, stream, fl)[0]
+                        if fl is not None else None)
             gbs = 8.0 * rows * cols / (ms * 1e-3) / 1e9
             transpose[f"{rows}x{cols}"] = {
                 "ms": round(ms, 5), "same_as_torch_t": ok,
@@ -510,8 +516,16 @@ def run_ours(args, dist):
                              "algorithmic_bytes_per_launch": 8 * rows * cols,
                              "peak_basis": "measured copy bandwidth" if peaks.get("hbm_gbs")
                                            else "fallback",
-                             "l2": "flushed (256 MiB write) between launches" if fl is not None
+                             "l2": ("flushed between launches: 256 MiB written, then read "
+                                    "(clean L2; the write's dirty lines are written back "
+                                    "before the timed launch)") if fl is not None
                                    else "2 GiB per launch, larger than L2"}}
+            if ms_dirty is not None:
+                transpose[f"{rows}x{cols}"]["after_write_only_flush"] = {
+                    "ms": round(ms_dirty, 5),
+                    "gbs": round(8.0 * rows * cols / (ms_dirty * 1e-3) / 1e9, 1),
+                    "note": "256 MiB written between launches, not read back: the launch also "
+                            "writes back the flush's dirty L2 lines"}
         del flush
 
     # ---- strided batch (attention Q K^T shape) and the pages' kernel ladder
@@ -567,13 +581,16 @@ def run_ours(args, dist):
                           "whole tiles, operands read in place"}
         sq = W.SQUARE_1024
         qA, qB, qC = (t.to(dev) for t in W.make_inputs(sq))
-        for lim_name, lim in (("unlimited", sg.SCRATCH_UNLIMITED), ("limit_0", 0)):
+        # limit 0 first: no graph has used the library's buffers yet, so the
+        # limit frees them all (a buffer a graph holds would stay and be reused)
+        for lim_name, lim in (("limit_0", 0), ("unlimited", sg.SCRATCH_UNLIMITED)):
             sg.sgemm_set_scratch_limit(lim)
             r, _, _ = time_gemm(sg, torch, case, A, B, C, max(5, min(args.steps, 50)), 3, args.algo,
                                 stream, per_call_events=False)
             us = 1000 * time_gemm_graph(sg, torch, sq, qA, qB, qC, args.algo)
             limit0[lim_name] = {case.name + "_tflops": round(tflops(flops, r), 3),
-                                sq.name + "_graph_us": round(us, 2)}
+                                sq.name + "_graph_us": round(us, 2),
+                                "library_bytes_held": int(sg.sgemm_get_scratch_limit()[1])}
         sg.sgemm_set_scratch_limit(sg.SCRATCH_UNLIMITED)
         del qA, qB, qC
 

@@ -62,14 +62,15 @@ DeviceState *device_state(sgemm_status_t *why) {
   return &d;
 }
 
-const SimtKernelInfo *kernel_info(DeviceState &d, int producer, int ta, int tb, int tile) {
-  std::call_once(d.kinfo_once[producer][ta][tb][tile], [&]() {
-    d.kinfo_err[producer][ta][tb][tile] =
-        simt_entry(producer, ta, tb, tile).info(&d.kinfo[producer][ta][tb][tile]);
-    if (d.kinfo_err[producer][ta][tb][tile] != cudaSuccess) cudaGetLastError();
+const SimtKernelInfo *kernel_info(DeviceState &d, int producer, int ta, int tb, int tile, int csk) {
+  const int c = csk ? 1 : 0;
+  std::call_once(d.kinfo_once[producer][ta][tb][tile][c], [&]() {
+    d.kinfo_err[producer][ta][tb][tile][c] =
+        simt_entry(producer, ta, tb, tile, c).info(&d.kinfo[producer][ta][tb][tile][c]);
+    if (d.kinfo_err[producer][ta][tb][tile][c] != cudaSuccess) cudaGetLastError();
   });
-  if (d.kinfo_err[producer][ta][tb][tile] != cudaSuccess) return nullptr;
-  return &d.kinfo[producer][ta][tb][tile];
+  if (d.kinfo_err[producer][ta][tb][tile][c] != cudaSuccess) return nullptr;
+  return &d.kinfo[producer][ta][tb][tile][c];
 }
 
 const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb) {
@@ -601,8 +602,13 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
   if (a.beta != 0.0f) p.c_pref = c_map;
 
   const int64_t slots = static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
-  // Under-filled products: cluster split-K, one launch and no workspace
-  const int csk = pick_csk(*ki, num_tiles, p.k_tiles, slots);
+  // Under-filled products: cluster split-K (its own instantiation of the
+  // kernel, 128 x 128 and 128 x 64 tiles), one launch and no workspace
+  const SimtKernelInfo *kc = tile != kTile128x256 && num_tiles < slots
+                                 ? kernel_info(d, producer, a.ta, a.tb, tile, 1)
+                                 : nullptr;
+  const int csk = kc ? pick_csk(*kc, num_tiles, p.k_tiles, static_cast<int64_t>(d.sm_count) * kc->ctas_per_sm)
+                     : 0;
   if (csk > 1) {
     p.csk = csk;
     p.dp_tiles = 0;
@@ -610,7 +616,7 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
     p.workspace = nullptr;
     p.sk_count = nullptr;
     if (pre && (*pre)() != cudaSuccess) return SGEMM_ERR_LAUNCH;
-    if (simt_entry(producer, a.ta, a.tb, tile)
+    if (simt_entry(producer, a.ta, a.tb, tile, 1)
             .launch(p, &tmA, &tmB, &tmC, static_cast<int>(num_tiles * csk), stream, pdl, csk) != cudaSuccess)
       return SGEMM_ERR_LAUNCH;
     t_last_launches = 1;
@@ -1066,14 +1072,15 @@ sgemm_status_t run_tc3_presplit(const Args &a, DeviceState &d, cudaStream_t s) {
 }  // namespace
 
 namespace sg {
-SimtEntry simt_entry_kTma_0(int transB, int tile);
-SimtEntry simt_entry_kTma_1(int transB, int tile);
-SimtEntry simt_entry_kCpAsync_0(int transB, int tile);
-SimtEntry simt_entry_kCpAsync_1(int transB, int tile);
+SimtEntry simt_entry_kTma_0(int transB, int tile, int csk);
+SimtEntry simt_entry_kTma_1(int transB, int tile, int csk);
+SimtEntry simt_entry_kCpAsync_0(int transB, int tile, int csk);
+SimtEntry simt_entry_kCpAsync_1(int transB, int tile, int csk);
 
-SimtEntry simt_entry(int producer, int transA, int transB, int tile) {
-  if (producer == kTma) return transA ? simt_entry_kTma_1(transB, tile) : simt_entry_kTma_0(transB, tile);
-  return transA ? simt_entry_kCpAsync_1(transB, tile) : simt_entry_kCpAsync_0(transB, tile);
+SimtEntry simt_entry(int producer, int transA, int transB, int tile, int csk) {
+  if (producer == kTma)
+    return transA ? simt_entry_kTma_1(transB, tile, csk) : simt_entry_kTma_0(transB, tile, csk);
+  return transA ? simt_entry_kCpAsync_1(transB, tile, csk) : simt_entry_kCpAsync_0(transB, tile, csk);
 }
 }  // namespace sg
 

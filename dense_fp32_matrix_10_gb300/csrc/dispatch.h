@@ -84,9 +84,10 @@ struct DeviceState {
   std::vector<std::pair<float *, size_t>> tr_retired;
   bool tr_failed = false;
   BufferOrder tr_order;
-  std::once_flag kinfo_once[2][2][2][kNumSimtTiles];
-  cudaError_t kinfo_err[2][2][2][kNumSimtTiles] = {};
-  SimtKernelInfo kinfo[2][2][2][kNumSimtTiles] = {};
+  // [producer][transA][transB][tile][cluster split-K form]
+  std::once_flag kinfo_once[2][2][2][kNumSimtTiles][2];
+  cudaError_t kinfo_err[2][2][2][kNumSimtTiles][2] = {};
+  SimtKernelInfo kinfo[2][2][2][kNumSimtTiles][2] = {};
   std::once_flag tcinfo_once[2][2];
   cudaError_t tcinfo_err[2][2] = {};
   TcKernelInfo tcinfo[2][2] = {};
@@ -131,7 +132,7 @@ int norm_op(int t);
 // reason in *why.  Also clears a pending error left by earlier, unrelated
 // runtime calls, so that the launches that follow report only their own.
 DeviceState *device_state(sgemm_status_t *why);
-const SimtKernelInfo *kernel_info(DeviceState &d, int producer, int ta, int tb, int tile);
+const SimtKernelInfo *kernel_info(DeviceState &d, int producer, int ta, int tb, int tile, int csk = 0);
 const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb);
 const TcKernelInfo *tc_kernel_info_presplit(DeviceState &d, int bn);
 const TcKernelInfo *tc_kernel_info_pair(DeviceState &d, int bn);

@@ -91,8 +91,9 @@ struct SimtEntry {
   SimtInfoFn info;
 };
 
-// [producer][transA][transB][tile]
-SimtEntry simt_entry(int producer, int transA, int transB, int tile);
+// [producer][transA][transB][tile]; csk: the cluster split-K form (128 x 128
+// and 128 x 64 tiles)
+SimtEntry simt_entry(int producer, int transA, int transB, int tile, int csk = 0);
 
 // 3xTF32 tensor-core kernel (tc_3xtf32.cu), 128 x 128 tiles, one CTA per SM.
 struct TcKernelInfo {

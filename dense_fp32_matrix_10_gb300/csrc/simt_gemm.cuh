@@ -125,9 +125,9 @@ constexpr int kCskSlot = -2;
 
 // Visits this CTA's units in order; f returns false to stop early.  Every
 // role of the CTA walks the same sequence.
-template <class F>
+template <bool CSK, class F>
 __device__ __forceinline__ void for_each_unit(const SimtParams &p, F &&f) {
-  if (p.csk > 0) {   // cluster split-K: one share of one tile (cluster dims (S, 1, 1))
+  if constexpr (CSK) {   // cluster split-K: one share of one tile (cluster dims (S, 1, 1))
     const int S = p.csk, r = static_cast<int>(blockIdx.x) % S;
     const int k0 = static_cast<int>(static_cast<int64_t>(r) * p.k_tiles / S);
     const int k1 = static_cast<int>(static_cast<int64_t>(r + 1) * p.k_tiles / S);
@@ -203,8 +203,11 @@ __device__ __forceinline__ int sk_for_each_segment(const SimtParams &p, int64_t 
 #endif
 
 template <int WARPS_M_, int WARPS_N_, bool A_KMAJOR_, bool B_KMAJOR_, int STAGES_, int PRODUCER_,
-          int TN_ = 8, bool A_TRANS_ = false>
+          int TN_ = 8, bool A_TRANS_ = false, bool CSK_ = false>
 struct SimtConfig {
+  // CSK: the cluster split-K form (SimtParams::csk); a separate
+  // instantiation, so that the other kernels carry none of its code.
+  static constexpr bool CSK = CSK_;
   static constexpr int WARPS_M = WARPS_M_;
   static constexpr int WARPS_N = WARPS_N_;
   static constexpr bool A_KMAJOR = A_KMAJOR_;  // layout of A in global memory
@@ -319,7 +322,7 @@ __device__ __forceinline__ void produce_tma(const SimtParams &p, const CUtensorM
                                             uint32_t raw_full0, uint32_t raw_empty0, bool &ok) {
   uint32_t it = 0;        // k-slices whose stage copies are issued
   uint32_t raw_it = 0;    // k-slices whose raw A copies are issued
-  for_each_unit(p, [&](const WorkUnit &u) {
+  for_each_unit<Cfg::CSK>(p, [&](const WorkUnit &u) {
     int bi, tm, tn;
     unit_coords(p, u.tile, bi, tm, tn);
     const int m0 = tm * Cfg::BM, n0 = tn * Cfg::BN;
@@ -404,7 +407,7 @@ __device__ __forceinline__ void transpose_a(const SimtParams &p, unsigned char *
                                             uint32_t raw_empty0, int tw, int lane, bool &ok) {
   constexpr int BM = Cfg::BM, ITEMS = (BM / 32) * 8;
   uint32_t it = 0;
-  for_each_unit(p, [&](const WorkUnit &u) {
+  for_each_unit<Cfg::CSK>(p, [&](const WorkUnit &u) {
     for (int kt = u.k0; kt < u.k1; ++kt, ++it) {
       const uint32_t s = it % Cfg::STAGES, round = it / Cfg::STAGES;
       const uint32_t r = it % 2, rr = it / 2;
@@ -444,7 +447,7 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
   constexpr int PT = Cfg::PRODUCER_THREADS;
   constexpr int UNROLL = SG_SIMT_CPASYNC_UNROLL;
   uint32_t it = 0;
-  for_each_unit(p, [&](const WorkUnit &u) {
+  for_each_unit<Cfg::CSK>(p, [&](const WorkUnit &u) {
     int bi, tm, tn;
     unit_coords(p, u.tile, bi, tm, tn);
     const int m0 = tm * BM, n0 = tn * BN;
@@ -877,45 +880,47 @@ __device__ __forceinline__ void add_partial(AccT<Cfg> &acc, const float *ws, int
   }
 }
 
-// Cluster split-K, after every CTA of the cluster has staged its partial
-// (dense BM x BN at stg_addr in each CTA's shared memory): the math threads
+// Cluster split-K reduction, once every CTA of the cluster has staged its
+// partial (dense BM x BN at stg in each CTA's shared memory): the math threads
 // of CTA `rank` add rows [rank*BM/S, (rank+1)*BM/S) of the S partials in rank
 // order (0 + p0 + p1 + ...) through distributed shared memory, apply alpha
-// and beta and write C.  Not inlined: the accumulators are dead by now, and
-// inlined this code raised the register pressure of the k-loop.
+// and beta and write C.  Not inlined, and called after the unit loop: inlined
+// (in the loop or after it) it raised the k-loop's register pressure.
 template <class Cfg>
-__device__ __noinline__ void csk_reduce(float *Cb, int64_t ldc, int m0, int n0, int M, int N, float alpha,
-                                        float beta, bool c_vec4, uint32_t stg_addr, int S, uint32_t rank,
+__device__ __noinline__ void csk_reduce(const SimtParams &p, int tile, int S, uint32_t rank, uint32_t stg,
                                         int tid) {
-  const bool read_c = beta != 0.0f;
+  int bi, tile_m, tile_n;
+  unit_coords(p, tile, bi, tile_m, tile_n);
+  float *Cb = p.C + static_cast<int64_t>(bi) * p.strideC;
+  const bool read_c = p.beta != 0.0f;
   constexpr int BN4 = Cfg::BN / 4;
   const int rows = Cfg::BM / S, r0 = static_cast<int>(rank) * rows;
   for (int e = tid; e < rows * BN4; e += Cfg::MATH_THREADS) {
     const int row = r0 + e / BN4, c4 = e % BN4;
-    const int m = m0 + row, n = n0 + 4 * c4;
-    if (m >= M || n >= N) continue;
+    const int m = tile_m * Cfg::BM + row, n = tile_n * Cfg::BN + 4 * c4;
+    if (m >= p.M || n >= p.N) continue;
     const uint32_t off = static_cast<uint32_t>(row * Cfg::BN + 4 * c4) * 4u;
     float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     for (int q = 0; q < S; ++q) {
-      const float4 v = ld_dsmem_v4(map_to_rank(stg_addr + off, q));
+      const float4 v = ld_dsmem_v4(map_to_rank(stg + off, q));
       sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
     }
-    float *crow = Cb + static_cast<int64_t>(m) * ldc;
+    float *crow = Cb + static_cast<int64_t>(m) * p.ldc;
     const float v[4] = {sum.x, sum.y, sum.z, sum.w};
-    if (c_vec4 && n + 3 < N) {
+    if (p.c_vec4 && n + 3 < p.N) {
       float4 o;
       if (read_c) {
         const float4 c = *reinterpret_cast<const float4 *>(crow + n);
-        o = make_float4(fmaf(alpha, v[0], beta * c.x), fmaf(alpha, v[1], beta * c.y),
-                        fmaf(alpha, v[2], beta * c.z), fmaf(alpha, v[3], beta * c.w));
+        o = make_float4(fmaf(p.alpha, v[0], p.beta * c.x), fmaf(p.alpha, v[1], p.beta * c.y),
+                        fmaf(p.alpha, v[2], p.beta * c.z), fmaf(p.alpha, v[3], p.beta * c.w));
       } else {
-        o = make_float4(alpha * v[0], alpha * v[1], alpha * v[2], alpha * v[3]);
+        o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
       }
       *reinterpret_cast<float4 *>(crow + n) = o;
     } else {
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (n + q < N) crow[n + q] = read_c ? fmaf(alpha, v[q], beta * crow[n + q]) : alpha * v[q];
+        if (n + q < p.N) crow[n + q] = read_c ? fmaf(p.alpha, v[q], p.beta * crow[n + q]) : p.alpha * v[q];
     }
   }
 }
@@ -952,8 +957,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
       mbar_init(raw_full0 + 8 * r, 1);
       mbar_init(raw_empty0 + 8 * r, Cfg::TRANSPOSER_WARPS);
     }
-    mbar_init(smem_u32(&s_math_bar), Cfg::MATH_WARPS);
-    if (p.csk > 1) {
+    if constexpr (kInKernelFixup<Cfg>() || Cfg::EPI_TMA || Cfg::CSK)
+      mbar_init(smem_u32(&s_math_bar), Cfg::MATH_WARPS);
+    if constexpr (Cfg::CSK) {
       // one arrival per math warp of each of the cluster's CTAs
       mbar_init(smem_u32(&s_csk_bar[0]), p.csk * Cfg::MATH_WARPS);
       mbar_init(smem_u32(&s_csk_bar[1]), p.csk * Cfg::MATH_WARPS);
@@ -967,7 +973,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
   }
   __syncthreads();
   // the peers' barriers exist before any CTA of the cluster arrives on them
-  if (p.csk > 1) cluster_sync();
+  if constexpr (Cfg::CSK) cluster_sync();
   // Everything above overlaps the previous kernel of the same call (the
   // transpose of an operand) when this one was launched as its dependent; the
   // operands and C are touched only after it has finished.  The fixup pass
@@ -1035,33 +1041,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
                   tile_n * Cfg::BN, wm, wn, tm, tn);
     return true;
   };
-  // Cluster split-K: stages this CTA's partial tile, adds this CTA's rows of
-  // the cluster's S partials in rank order (0 + p0 + p1 + ...), applies
-  // alpha / beta and writes them to C.  False if a bounded wait gave up.
-  const auto csk_finish = [&](const AccT<Cfg> &acc, int tile) -> bool {
-    const int S = p.csk;
-    const uint32_t rank = blockIdx.x % static_cast<uint32_t>(S);
+  // Cluster split-K, first half: stages this CTA's partial tile in its own
+  // (now idle) stage ring and announces it to every CTA of the cluster.  The
+  // second half -- the reduction -- runs after the unit loop, where nothing
+  // of the k-loop is live.  False if a bounded wait gave up.
+  int csk_tile = -1;
+  const auto csk_stage = [&](const AccT<Cfg> &acc, int tile) -> bool {
     // every math warp is past its last stage: the ring may be overwritten
     if (!math_barrier(math_bar, math_phase, lane, p)) return false;
-    float *stg = reinterpret_cast<float *>(smem);   // dense BM x BN partial
-    store_partial<Cfg>(stg, acc, wm, wn, tm, tn);
+    store_partial<Cfg>(reinterpret_cast<float *>(smem), acc, wm, wn, tm, tn);
     asm volatile("fence.acq_rel.cluster;" ::: "memory");
     __syncwarp();
-    const uint32_t full = smem_u32(&s_csk_bar[0]), done = smem_u32(&s_csk_bar[1]);
     if (lane == 0)
-      for (int q = 0; q < S; ++q) mbar_arrive_cluster(map_to_rank(full, q));
-    if (!wait_parity_bounded_cluster(full, 0, p.wait_budget_ns, p.status)) return false;
-    int bi, tile_m, tile_n;
-    unit_coords(p, tile, bi, tile_m, tile_n);
-    csk_reduce<Cfg>(p.C + static_cast<int64_t>(bi) * p.strideC, p.ldc, tile_m * Cfg::BM, tile_n * Cfg::BN,
-                    p.M, p.N, p.alpha, p.beta, p.c_vec4 != 0, smem_u32(stg), S, rank, threadIdx.x);
-    // this CTA's shared memory stays until every peer has read its partial
-    __syncwarp();
-    if (lane == 0)
-      for (int q = 0; q < S; ++q) mbar_arrive_cluster(map_to_rank(done, q));
-    return wait_parity_bounded_cluster(done, 0, p.wait_budget_ns, p.status);
+      for (int q = 0; q < p.csk; ++q) mbar_arrive_cluster(map_to_rank(smem_u32(&s_csk_bar[0]), q));
+    csk_tile = tile;
+    return true;
   };
-  for_each_unit(p, [&](const WorkUnit &u) {
+  for_each_unit<Cfg::CSK>(p, [&](const WorkUnit &u) {
     AccT<Cfg> acc;
 #pragma unroll
     for (int q = 0; q < 4 * Cfg::TN; ++q) acc[q] = make_float2(0.0f, 0.0f);
@@ -1075,7 +1071,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
-    if (u.slot == kCskSlot) return csk_finish(acc, u.tile);
+    if constexpr (Cfg::CSK) return csk_stage(acc, u.tile);
     if constexpr (!kInKernelFixup<Cfg>()) {
       if (u.slot < 0) {
         return finish_tile(acc, u.tile);
@@ -1122,6 +1118,24 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
     }
     return finish_tile(acc, u.tile);
   });
+  // Cluster split-K, second half: once every CTA of the cluster has staged
+  // its partial, this CTA adds rows [rank*BM/S, (rank+1)*BM/S) of the S
+  // partials in rank order (0 + p0 + p1 + ...) through distributed shared
+  // memory, applies alpha / beta and writes C; then it keeps its shared
+  // memory until every peer has read it.
+  if constexpr (Cfg::CSK) {
+    if (csk_tile < 0) return;   // a bounded wait gave up before the partial was staged
+    const int S = p.csk;
+    const uint32_t rank = blockIdx.x % static_cast<uint32_t>(S);
+    const uint32_t full = smem_u32(&s_csk_bar[0]), done = smem_u32(&s_csk_bar[1]);
+    if (!wait_parity_bounded_cluster(full, 0, p.wait_budget_ns, p.status)) return;
+    csk_reduce<Cfg>(p, csk_tile, S, rank, smem_u32(smem), threadIdx.x);
+    __syncwarp();
+    if (lane == 0)
+      for (int q = 0; q < S; ++q) mbar_arrive_cluster(map_to_rank(done, q));
+    wait_parity_bounded_cluster(done, 0, p.wait_budget_ns, p.status);
+    return;
+  }
   // the last tile's TMA stores complete before the CTA (and its shared
   // memory) goes away
   if constexpr (Cfg::EPI_TMA) {

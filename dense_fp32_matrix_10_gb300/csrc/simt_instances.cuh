@@ -62,16 +62,16 @@ cudaError_t simt_info(SimtKernelInfo *info) {
   return cudaSuccess;
 }
 
-template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR, int TILE>
+template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR, int TILE, bool CSK>
 struct SimtPick;
 // With the TMA producer a k-contiguous A is transposed in shared memory
 // (SG_SIMT_TRANSPOSE_A).
 template <int PRODUCER, bool A_KMAJOR>
 constexpr bool kTransA = (PRODUCER == kTma) && A_KMAJOR && SG_SIMT_TRANSPOSE_A;
 
-template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR>
-struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x128> {
-  using Cfg = SimtConfig<4, 2, A_KMAJOR, B_KMAJOR, 4, PRODUCER, 8, kTransA<PRODUCER, A_KMAJOR>>;
+template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR, bool CSK>
+struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x128, CSK> {
+  using Cfg = SimtConfig<4, 2, A_KMAJOR, B_KMAJOR, 4, PRODUCER, 8, kTransA<PRODUCER, A_KMAJOR>, CSK>;
 };
 // 128 x 64 tiles run two CTAs per SM.  With the raw A ring of the in-smem
 // transpose (32 KiB) four stages would need ~129 KiB per CTA, and only one
@@ -80,20 +80,20 @@ struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x128> {
 #ifndef SG_SIMT_STAGES_64_TRANS
 #define SG_SIMT_STAGES_64_TRANS 3
 #endif
-template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR>
-struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x64> {
+template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR, bool CSK>
+struct SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, kTile128x64, CSK> {
   static constexpr bool kT = kTransA<PRODUCER, A_KMAJOR>;
-  using Cfg = SimtConfig<4, 1, A_KMAJOR, B_KMAJOR, kT ? SG_SIMT_STAGES_64_TRANS : 4, PRODUCER, 8, kT>;
+  using Cfg = SimtConfig<4, 1, A_KMAJOR, B_KMAJOR, kT ? SG_SIMT_STAGES_64_TRANS : 4, PRODUCER, 8, kT, CSK>;
   static_assert(2 * (Cfg::SMEM_BYTES + 1024) <= 233472, "two 128 x 64 CTAs must fit on an SM");
 };
-template <int PRODUCER, bool A_KMAJOR>
-struct SimtPick<PRODUCER, A_KMAJOR, false, kTile128x256> {
-  using Cfg = SimtConfig<4, 2, A_KMAJOR, false, 4, PRODUCER, 16, kTransA<PRODUCER, A_KMAJOR>>;
+template <int PRODUCER, bool A_KMAJOR, bool CSK>
+struct SimtPick<PRODUCER, A_KMAJOR, false, kTile128x256, CSK> {
+  using Cfg = SimtConfig<4, 2, A_KMAJOR, false, 4, PRODUCER, 16, kTransA<PRODUCER, A_KMAJOR>, CSK>;
 };
 
-template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR, int TILE>
+template <int PRODUCER, bool A_KMAJOR, bool B_KMAJOR, int TILE, bool CSK = false>
 SimtEntry simt_make_entry() {
-  using Cfg = typename SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, TILE>::Cfg;
+  using Cfg = typename SimtPick<PRODUCER, A_KMAJOR, B_KMAJOR, TILE, CSK>::Cfg;
   return SimtEntry{&simt_launch<Cfg>, &simt_info<Cfg>};
 }
 
@@ -101,10 +101,18 @@ SimtEntry simt_make_entry() {
 // N x K (transB = T) likewise.
 // The 128 x 256 tile exists only for n-contiguous op(B) (transB = N) and the
 // TMA producer (the only combination the dispatcher picks it for); any other
-// request for it gets the 128 x 128 tile.
+// request for it gets the 128 x 128 tile.  The cluster split-K form (csk)
+// exists for the 128 x 128 and 128 x 64 tiles.
 #define SG_DEFINE_SIMT_FAMILY(PROD, TA)                                                  \
-  SimtEntry simt_entry_##PROD##_##TA(int transB, int tile) {                             \
+  SimtEntry simt_entry_##PROD##_##TA(int transB, int tile, int csk) {                    \
     constexpr bool AK = (TA == 0);                                                       \
+    if (csk) {                                                                           \
+      if (transB == 0)                                                                   \
+        return tile == kTile128x64 ? simt_make_entry<PROD, AK, false, kTile128x64, true>() \
+                                   : simt_make_entry<PROD, AK, false, kTile128x128, true>(); \
+      return tile == kTile128x64 ? simt_make_entry<PROD, AK, true, kTile128x64, true>()  \
+                                 : simt_make_entry<PROD, AK, true, kTile128x128, true>(); \
+    }                                                                                    \
     if (transB == 0) {                                                                   \
       if constexpr (PROD == kTma)                                                        \
         if (tile == kTile128x256) return simt_make_entry<PROD, AK, false, kTile128x256>(); \
