@@ -158,8 +158,9 @@ struct SkPlan {
 };
 
 SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws);
-// CTAs per cluster of cluster split-K for this product (0: not used).
-int pick_csk(const SimtKernelInfo &ki, int64_t tiles, int64_t k_tiles, int64_t slots);
+// CTAs per cluster of cluster split-K for this product (0: not used);
+// have_ws: a stream-K workspace is available as the alternative.
+int pick_csk(const SimtKernelInfo &ki, int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws);
 
 // Reserves `bytes` of the device's scratch limit (false, nothing reserved, if
 // they do not fit); release_scratch gives bytes back.

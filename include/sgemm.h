@@ -44,6 +44,11 @@
  * (tensor-map cache, events, kernel attributes).  sgemm_noalloc() never
  * allocates (see there).
  *
+ * Environment: SGEMM_SCRATCH_LIMIT=<bytes> sets every device's initial scratch
+ * limit (see sgemm_set_scratch_limit); SGEMM_VERBOSE=1 makes each CUDA-core
+ * product print the plan it queued (kernel form, tile, grid, how split tiles
+ * are finished) to stderr.  Both are read once.
+ *
  * Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
  * default stream).  Every call returns as soon as its work is queued; results
  * are ready once the stream reaches that point.  Argument errors are detected
