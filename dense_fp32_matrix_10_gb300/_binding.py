@@ -19,7 +19,7 @@ ALGOS = {"auto": ALGO_AUTO, "simt_tma": ALGO_SIMT_TMA, "simt_cpasync": ALGO_SIMT
          "small": ALGO_SMALL, "reg_2x2": ALGO_REG_2X2, "reg_4x4": ALGO_REG_4X4}
 STATUS = {0: "SGEMM_SUCCESS", 1: "SGEMM_ERR_INVALID_VALUE", 2: "SGEMM_ERR_ALIASING",
           3: "SGEMM_ERR_UNSUPPORTED", 4: "SGEMM_ERR_LAUNCH", 5: "SGEMM_ERR_DEVICE_TIMEOUT",
-          6: "SGEMM_ERR_SCRATCH_LIMIT"}
+          6: "SGEMM_ERR_SCRATCH_LIMIT", 7: "SGEMM_ERR_DEVICE_BOUNDS"}
 
 _lib = None
 _I64 = ctypes.c_int64

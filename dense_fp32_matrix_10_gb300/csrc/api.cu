@@ -1175,7 +1175,7 @@ sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
     case SGEMM_ALGO_REG_2X2:
     case SGEMM_ALGO_REG_4X4: {
       PlainParams p{A, B, C, lda, ldb, ldc, static_cast<int>(M), static_cast<int>(N),
-                    static_cast<int>(K), a.ta, a.tb, alpha, beta};
+                    static_cast<int>(K), a.ta, a.tb, alpha, beta, d->status};
       cudaError_t e = algo == SGEMM_ALGO_NAIVE       ? launch_naive(p, s)
                       : algo == SGEMM_ALGO_SMEM_TILED ? launch_smem_tiled(p, s)
                       : algo == SGEMM_ALGO_REG_2X2    ? launch_reg_tiled(p, 2, s)
@@ -1305,7 +1305,8 @@ sgemm_status_t sgemm_last_device_status(void *stream) {
       return SGEMM_ERR_LAUNCH;
     }
   }
-  return v == 0 ? SGEMM_SUCCESS : SGEMM_ERR_DEVICE_TIMEOUT;
+  if (v == 0) return SGEMM_SUCCESS;
+  return v == kDevBounds ? SGEMM_ERR_DEVICE_BOUNDS : SGEMM_ERR_DEVICE_TIMEOUT;
 }
 
 sgemm_status_t sgemm_set_scratch_limit(uint64_t bytes) {
@@ -1373,6 +1374,7 @@ const char *sgemm_status_string(sgemm_status_t status) {
     case SGEMM_ERR_LAUNCH: return "CUDA launch failure";
     case SGEMM_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
     case SGEMM_ERR_SCRATCH_LIMIT: return "needs more scratch than the fixed no-allocation array holds";
+    case SGEMM_ERR_DEVICE_BOUNDS: return "a kernel caught an out-of-range index (debug-bounds build)";
     default: return "unknown status";
   }
 }

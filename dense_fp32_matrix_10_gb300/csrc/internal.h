@@ -137,6 +137,7 @@ struct PlainParams {
   int M, N, K;
   int transA, transB;
   float alpha, beta;
+  int *status = nullptr;   // device status word (debug-bounds builds report here)
 };
 cudaError_t launch_naive(const PlainParams &p, cudaStream_t s);
 cudaError_t launch_smem_tiled(const PlainParams &p, cudaStream_t s);

@@ -79,7 +79,20 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
 #endif
 
 // Error codes a kernel records in the device status word.
-enum : int { kDevOk = 0, kDevTimeout = 5 };
+enum : int { kDevOk = 0, kDevTimeout = 5, kDevBounds = 7 };
+
+// SGEMM_DEBUG_BOUNDS=1 builds check the shared- and global-memory indices the
+// kernels form: an index outside its tile, stage or matrix is recorded as
+// kDevBounds in the status word and the access is skipped.  In ordinary
+// builds SG_CHECK is the constant true and the checks compile away.
+#ifndef SGEMM_DEBUG_BOUNDS
+#define SGEMM_DEBUG_BOUNDS 0
+#endif
+__device__ __forceinline__ bool sg_bounds_ok(bool ok, int *status) {
+  if (!ok && status) atomicExch(status, kDevBounds);
+  return ok;
+}
+#define SG_CHECK(cond, status) (!SGEMM_DEBUG_BOUNDS || ::sg::sg_bounds_ok((cond), (status)))
 
 // Wait for phase `parity` of `bar`, giving up after `budget_ns` nanoseconds of
 // %globaltimer.  On give-up records kDevTimeout in *status and returns false;

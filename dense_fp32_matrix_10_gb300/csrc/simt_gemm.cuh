@@ -206,7 +206,8 @@ template <int WARPS_M_, int WARPS_N_, bool A_KMAJOR_, bool B_KMAJOR_, int STAGES
           int TN_ = 8, bool A_TRANS_ = false, bool CSK_ = false>
 struct SimtConfig {
   // CSK: the cluster split-K form (SimtParams::csk); a separate
-  // instantiation, so that the other kernels carry none of its code.
+  // instantiation, so that the other kernels carry none of its code.  Its
+  // partial tile is staged in the stage ring.
   static constexpr bool CSK = CSK_;
   static constexpr int WARPS_M = WARPS_M_;
   static constexpr int WARPS_N = WARPS_N_;
@@ -277,6 +278,7 @@ struct SimtConfig {
   static constexpr int FULL_COUNT =
       (PRODUCER == kTma) ? (A_TRANS ? 1 + TRANSPOSER_WARPS : 1) : PRODUCER_THREADS;
   static_assert(BM <= 256 && BN <= 256, "TMA box extent is at most 256");
+  static_assert(!CSK || BM * BN * 4 <= STAGES * STAGE_BYTES, "the cluster split-K partial fits the ring");
   static_assert(A_STAGE_BYTES % 1024 == 0 && B_STAGE_BYTES % 1024 == 0, "swizzle atom alignment");
 };
 
@@ -423,6 +425,7 @@ __device__ __forceinline__ void transpose_a(const SimtParams &p, unsigned char *
 #pragma unroll UNROLL
       for (int item = tw; item < ITEMS; item += Cfg::TRANSPOSER_WARPS) {
         const int c = item & 7, m = (item >> 3) * 32 + lane;
+        if (!SG_CHECK(m < BM && (4 * c + 3) * BM + m < Cfg::BK * BM, p.status)) continue;
         const float4 v = *reinterpret_cast<const float4 *>(raw + m * 128 + ((c ^ (m & 7)) << 4));
         dst[(4 * c + 0) * BM + m] = v.x;
         dst[(4 * c + 1) * BM + m] = v.y;
@@ -483,7 +486,8 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
         const float *src = p.A;
         if (in) src = Cfg::A_KMAJOR ? Ab + static_cast<int64_t>(gm) * p.lda + gk
                                     : Ab + static_cast<int64_t>(gk) * p.lda + gm;
-        cp_async_4(a_dst + off, src, in ? 4u : 0u);
+        if (SG_CHECK(off + 4 <= static_cast<uint32_t>(Cfg::A_STAGE_BYTES) && m < BM && k < BK, p.status))
+          cp_async_4(a_dst + off, src, in ? 4u : 0u);
       }
       // op(B) tile: 32 x BN elements
 #pragma unroll UNROLL
@@ -504,7 +508,8 @@ __device__ __forceinline__ void produce_cpasync(const SimtParams &p, uint32_t sm
         const float *src = p.B;
         if (in) src = Cfg::B_KMAJOR ? Bb + static_cast<int64_t>(gn) * p.ldb + gk
                                     : Bb + static_cast<int64_t>(gk) * p.ldb + gn;
-        cp_async_4(b_dst + off, src, in ? 4u : 0u);
+        if (SG_CHECK(off + 4 <= static_cast<uint32_t>(Cfg::B_STAGE_BYTES) && n < BN && k < BK, p.status))
+          cp_async_4(b_dst + off, src, in ? 4u : 0u);
       }
       cp_async_mbar_arrive_noinc(full0 + 8 * s);
     }
@@ -609,7 +614,7 @@ __device__ __forceinline__ float acc_get(const A &acc, int r, int c) {
 
 template <class Cfg>
 __device__ __forceinline__ void mma_stage(AccT<Cfg> &acc, const char *a_stage, const char *b_stage,
-                                          int wm, int wn, int tm, int tn) {
+                                          int wm, int wn, int tm, int tn, int *status) {
   constexpr int BM = Cfg::BM, BN = Cfg::BN, TN = Cfg::TN;
   constexpr int MODE = acc_mode<Cfg>();
   // Per-thread base pointers inside the stage.
@@ -624,6 +629,14 @@ __device__ __forceinline__ void mma_stage(AccT<Cfg> &acc, const char *a_stage, c
   else
     b_base = b_stage + (wn * Cfg::WN + 4 * tn) * 4;  // + k * BN * 4, + 128 per column group
 
+  if constexpr (SGEMM_DEBUG_BOUNDS) {
+    // the farthest byte each operand's reads reach in this stage
+    const int a_last = Cfg::A_SMEM_KMAJOR ? (wm * 32 + tm + 28) * 128 + 128
+                                          : ((31 * BM + wm * 32 + 4 * tm + 16) + 4) * 4;
+    const int b_last = Cfg::B_KMAJOR ? (wn * Cfg::WN + tn + 8 * (TN - 1)) * 128 + 128
+                                     : ((31 * BN + wn * Cfg::WN + 4 * tn + 32 * (TN / 4 - 1)) + 4) * 4;
+    if (!SG_CHECK(a_last <= Cfg::A_STAGE_BYTES && b_last <= Cfg::B_STAGE_BYTES, status)) return;
+  }
   constexpr int KC_UNROLL = kc_unroll<Cfg>();
 #pragma unroll KC_UNROLL
   for (int kc = 0; kc < 8; ++kc) {  // 4 k per chunk
@@ -719,13 +732,14 @@ __device__ __forceinline__ void epilogue(const SimtParams &p, float *Cb, const A
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const int m = m0 + wm * 32 + thread_row<Cfg>(tm, r);
-    if (m >= p.M) continue;
+    if (m >= p.M || !SG_CHECK(m - m0 < Cfg::BM, p.status)) continue;
     float *crow = Cb + static_cast<int64_t>(m) * p.ldc;
     if (!Cfg::B_KMAJOR) {
       // columns 32h + 4tn .. +3: TN/4 float4 groups
 #pragma unroll
       for (int h = 0; h < TN / 4; ++h) {
         const int n = n0 + wn * Cfg::WN + h * 32 + 4 * tn;
+        if (!SG_CHECK(n - n0 + 3 < Cfg::BN, p.status)) continue;
         float v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) v[q] = acc_get<MODE, TN>(acc, r, 4 * h + q);
@@ -755,7 +769,7 @@ __device__ __forceinline__ void epilogue(const SimtParams &p, float *Cb, const A
 #pragma unroll
       for (int c = 0; c < TN; ++c) {
         const int n = n0 + wn * Cfg::WN + thread_col<Cfg>(tn, c);
-        if (n < p.N) {
+        if (n < p.N && SG_CHECK(n - n0 < Cfg::BN, p.status)) {
           const float a = acc_get<MODE, TN>(acc, r, c);
           crow[n] = read_c ? fmaf(p.alpha, a, p.beta * crow[n]) : p.alpha * a;
         }
@@ -804,7 +818,7 @@ __device__ __forceinline__ void tma_store_3d(const void *desc, uint32_t src, int
 // of a 128-byte-swizzled TMA box, 1024-byte aligned).
 template <class Cfg>
 __device__ __forceinline__ void stage_tile(unsigned char *staging, const AccT<Cfg> &acc, float alpha,
-                                           int wm, int wn, int tm, int tn) {
+                                           int wm, int wn, int tm, int tn, int *status) {
   constexpr int MODE = acc_mode<Cfg>(), TN = Cfg::TN;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
@@ -820,6 +834,7 @@ __device__ __forceinline__ void stage_tile(unsigned char *staging, const AccT<Cf
         o.w = alpha * acc_get<MODE, TN>(acc, r, 4 * h + 3);
         unsigned char *dst = staging + (col >> 5) * (Cfg::BM * 128) + R * 128 +
                              ((((col & 31) >> 2) ^ (R & 7)) << 4);
+        if (!SG_CHECK(R < Cfg::BM && col + 3 < Cfg::BN, status)) continue;
         *reinterpret_cast<float4 *>(dst) = o;
       }
     } else {
@@ -900,6 +915,9 @@ __device__ __noinline__ void csk_reduce(const SimtParams &p, int tile, int S, ui
     const int m = tile_m * Cfg::BM + row, n = tile_n * Cfg::BN + 4 * c4;
     if (m >= p.M || n >= p.N) continue;
     const uint32_t off = static_cast<uint32_t>(row * Cfg::BN + 4 * c4) * 4u;
+    if (!SG_CHECK(row < Cfg::BM && rank < static_cast<uint32_t>(S) &&
+                      off + 16 <= static_cast<uint32_t>(Cfg::BM * Cfg::BN * 4), p.status))
+      continue;
     float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     for (int q = 0; q < S; ++q) {
       const float4 v = ld_dsmem_v4(map_to_rank(stg + off, q));
@@ -1018,7 +1036,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
         // the previous tile's stores have read the staging tile
         if (threadIdx.x == 0) bulk_wait_group_read<0>();
         if (!math_barrier(math_bar, math_phase, lane, p)) return false;
-        stage_tile<Cfg>(smem + Cfg::STAGING_OFFSET, acc, p.alpha, wm, wn, tm, tn);
+        stage_tile<Cfg>(smem + Cfg::STAGING_OFFSET, acc, p.alpha, wm, wn, tm, tn, p.status);
         fence_proxy_async_smem();
         if (!math_barrier(math_bar, math_phase, lane, p)) return false;
         if (threadIdx.x == 0) {
@@ -1067,7 +1085,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
       const uint32_t round = it / Cfg::STAGES;
       if (!wait_parity_bounded(full0 + 8 * s, round & 1, p.wait_budget_ns, p.status)) return false;
       const char *a_stage = reinterpret_cast<const char *>(smem) + s * Cfg::STAGE_BYTES;
-      mma_stage<Cfg>(acc, a_stage, a_stage + Cfg::A_STAGE_BYTES, wm, wn, tm, tn);
+      mma_stage<Cfg>(acc, a_stage, a_stage + Cfg::A_STAGE_BYTES, wm, wn, tm, tn, p.status);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
@@ -1078,14 +1096,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
       } else {
         // sk_fixup_kernel adds the partials (these kernels run the mid-size
         // products, for which the separate pass is the faster)
-        store_partial<Cfg>(p.workspace + static_cast<int64_t>(u.slot) * Cfg::BM * Cfg::BN, acc, wm, wn,
-                           tm, tn);
+        if (SG_CHECK(u.slot < 2 * static_cast<int>(gridDim.x), p.status))
+          store_partial<Cfg>(p.workspace + static_cast<int64_t>(u.slot) * Cfg::BM * Cfg::BN, acc, wm, wn,
+                             tm, tn);
       }
       return true;
     }
     if (u.slot >= 0) {
-      store_partial<Cfg>(p.workspace + static_cast<int64_t>(u.slot) * Cfg::BM * Cfg::BN, acc, wm, wn,
-                         tm, tn);
+      if (SG_CHECK(u.slot < 2 * static_cast<int>(gridDim.x), p.status))
+        store_partial<Cfg>(p.workspace + static_cast<int64_t>(u.slot) * Cfg::BM * Cfg::BN, acc, wm, wn,
+                           tm, tn);
       if (p.sk_count == nullptr) return true;   // sk_fixup_kernel adds the partials
       // count this segment in; the last to arrive adds the tile's partials
       const int ts = u.tile - p.dp_tiles;
@@ -1113,6 +1133,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_CTAS)
           acc_ref<MODE, TN>(acc, r, c) = own == 0 ? 0.0f + acc_get<MODE, TN>(acc, r, c) : 0.0f;
       sk_for_each_segment(p, gridDim.x, ts, [&](int i, int slot) {
         if (i == 0 && own == 0) return;
+        if (!SG_CHECK(slot >= 0 && slot < 2 * static_cast<int>(gridDim.x), p.status)) return;
         add_partial<Cfg>(acc, p.workspace + static_cast<int64_t>(slot) * Cfg::BM * Cfg::BN, wm, wn, tm, tn);
       });
     }

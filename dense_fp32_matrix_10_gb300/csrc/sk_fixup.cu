@@ -64,13 +64,17 @@ __global__ void __launch_bounds__(kFixupThreads) sk_fixup_kernel(const SimtParam
     const int e = chunk * kChunk + 4 * threadIdx.x;
     const int row = tm * bm + e / bn, col = tn * bn + e % bn;
     if (row >= p.M) return;
+    if (!SG_CHECK(e + 4 <= tile_elems && tile < p.num_tiles - p.dp_tiles, p.status)) return;
     float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     // partials in groups of BATCH loads in flight, added in slot order
     for (int i0 = 0; i0 < n; i0 += BATCH) {
       float4 v[BATCH];
 #pragma unroll
       for (int j = 0; j < BATCH; ++j)
-        if (i0 + j < n) v[j] = __ldcg(reinterpret_cast<const float4 *>(p.workspace + s_slot[i0 + j] * tile_elems + e));
+        if (i0 + j < n && SG_CHECK(s_slot[i0 + j] >= 0 && s_slot[i0 + j] < 2 * grid_main, p.status))
+          v[j] = __ldcg(reinterpret_cast<const float4 *>(p.workspace + s_slot[i0 + j] * tile_elems + e));
+        else if (i0 + j < n)
+          v[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
       for (int j = 0; j < BATCH; ++j) {
         if (i0 + j < n) {

@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll 4
     for (int kk = 0; kk < kend; ++kk) {
       const int k = kw + kk;
+      if (!SG_CHECK(k < kPassK && swz(k, 8 * tc + 4) + 4 <= kStageFloats, p.status)) break;
       const float4 a = *reinterpret_cast<const float4 *>(&As[swz(k, 4 * tr)]);
       const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[swz(k, 8 * tc)]);
       const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[swz(k, 8 * tc + 4)]);
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   for (int o = t; o < kTile * kTile; o += kThreads) {
     const int row = m0 + o / kTile, col = n0 + o % kTile;
+    if (!SG_CHECK(o + (kWarps - 1) * kTile * kTile < 2 * kStageFloats, p.status)) break;
     float s = part[o];
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) s += part[w * kTile * kTile + o];

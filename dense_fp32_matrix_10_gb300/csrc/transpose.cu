@@ -222,6 +222,9 @@ __global__ void __launch_bounds__(kTmThreads) transpose_tma_kernel(const __grid_
       int r0, c0;
       tma_tile_origin(p, t, r0, c0);
       mbar_arrive_expect_tx(full0 + 8 * s, kTmTileBytes);
+      // (a debug-bounds build still issues the load, so that the barrier
+      // completes; it records a tile origin outside the matrix)
+      SG_CHECK(r0 >= 0 && c0 >= 0 && r0 < p.rows && c0 < p.cols, p.status);
       tma_load_2d(in0 + s * kTmTileBytes, &in_map, full0 + 8 * s, c0, r0);
     }
     // do not let the CTA end with a load of ours still landing: wait (bounded)
@@ -270,8 +273,10 @@ __global__ void __launch_bounds__(kTmThreads) transpose_tma_kernel(const __grid_
       int r0, c0;
       tma_tile_origin(p, t, r0, c0);
       const uint32_t ob = out0 + o * OUT_TILES * kTmTileBytes;
-      tma_store_2d(&out_map, ob, r0, c0);   // out: x = input row, y = input col
-      if (SPLIT) tma_store_2d(&small_map, ob + kTmTileBytes, r0, c0);
+      if (SG_CHECK(r0 >= 0 && c0 >= 0 && r0 < p.rows && c0 < p.cols, p.status)) {
+        tma_store_2d(&out_map, ob, r0, c0);   // out: x = input row, y = input col
+        if (SPLIT) tma_store_2d(&small_map, ob + kTmTileBytes, r0, c0);
+      }
       bulk_commit_group();
     }
   }

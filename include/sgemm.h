@@ -112,9 +112,14 @@ typedef enum sgemm_status {
   SGEMM_ERR_LAUNCH = 4,         /* a CUDA call failed while queuing the work */
   SGEMM_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up a bounded wait (reported
                                    by sgemm_last_device_status) */
-  SGEMM_ERR_SCRATCH_LIMIT = 6   /* kept for ABI stability; no call returns it
+  SGEMM_ERR_SCRATCH_LIMIT = 6,  /* kept for ABI stability; no call returns it
                                    (sgemm_noalloc runs whole tiles instead
                                    when its array is too small) */
+  SGEMM_ERR_DEVICE_BOUNDS = 7   /* only in a library built with
+                                   SGEMM_DEBUG_BOUNDS=1: a kernel formed a
+                                   shared- or global-memory index outside its
+                                   tile, stage or matrix and skipped the access
+                                   (reported by sgemm_last_device_status) */
 } sgemm_status_t;
 
 /*
@@ -255,10 +260,12 @@ SGEMM_API int sgemm_last_launch_count(void);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
- * word, in which a kernel records that it gave up a bounded wait.  Returns
- * SGEMM_SUCCESS, SGEMM_ERR_DEVICE_TIMEOUT, or SGEMM_ERR_LAUNCH if the
- * synchronisation itself failed.  On a timeout it also zeroes the stream-K
- * arrival counters, which a kernel that gave up may have left mid-count.
+ * word, in which a kernel records that it gave up a bounded wait (or, in a
+ * SGEMM_DEBUG_BOUNDS=1 build, that it caught an out-of-range index).  Returns
+ * SGEMM_SUCCESS, SGEMM_ERR_DEVICE_TIMEOUT, SGEMM_ERR_DEVICE_BOUNDS, or
+ * SGEMM_ERR_LAUNCH if the synchronisation itself failed.  On an error it also
+ * zeroes the stream-K arrival counters, which a kernel that gave up may have
+ * left mid-count.
  */
 SGEMM_API sgemm_status_t sgemm_last_device_status(void *stream);
 
