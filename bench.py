@@ -577,8 +577,8 @@ def run_ours(args, dist):
     # limit at 0 (no workspace, nothing copied ahead), then the limit restored
     limit0 = None
     if not args.no_limit0:
-        limit0 = {"what": "sgemm_set_scratch_limit(0): no library device memory; "
-                          "whole tiles, operands read in place"}
+        limit0 = {"what": "sgemm_set_scratch_limit(0): no library device memory; split tiles only "
+                          "within clusters (else whole tiles), operands read in place"}
         sq = W.SQUARE_1024
         qA, qB, qC = (t.to(dev) for t in W.make_inputs(sq))
         # limit 0 first: no graph has used the library's buffers yet, so the

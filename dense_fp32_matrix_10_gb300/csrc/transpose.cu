@@ -154,9 +154,14 @@ constexpr int kTmThreads = 32 + kTmConsumers;
 // SPLIT: the split pass of the 3xTF32 product -- besides the transposed
 // values (which serve as the TF32 big parts) each output tile gets a twin
 // holding the small parts; one input stage fewer keeps two CTAs per SM.
+// Input stages of the plain form (16 KiB each): 4 fit two CTAs per SM, 2
+// fit three.
+#ifndef SG_TRANSPOSE_IN_STAGES
+#define SG_TRANSPOSE_IN_STAGES 4
+#endif
 template <bool SPLIT>
 struct TmShape {
-  static constexpr int IN_STAGES = SPLIT ? 3 : 4;
+  static constexpr int IN_STAGES = SPLIT ? 3 : SG_TRANSPOSE_IN_STAGES;
   static constexpr int OUT_TILES = SPLIT ? 2 : 1;   // per output stage
   static constexpr int SMEM = (IN_STAGES + kTmOutStages * OUT_TILES) * kTmTileBytes + 1024 /*align*/ +
                               64 /*barriers*/;
