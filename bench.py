@@ -263,31 +263,34 @@ def time_gemm_graph(sg, torch, case, A, B, C, algo, calls=20, replays=5):
 
 
 def time_transpose(sg, torch, rows, cols, reps, stream, flush=None, read_back=False):
-    """Mean per-launch ms of sgemm_transpose on a rows x cols matrix (CUDA
-    events around each launch on `stream`; `flush`, a buffer larger than L2,
-    is rewritten between launches, outside the events, and with `read_back`
+    """(mean, median) per-launch ms of sgemm_transpose on a rows x cols matrix:
+    CUDA events around each launch on `stream`, the device synchronised
+    before and after each timed launch.  `flush`, a buffer larger than L2, is
+    rewritten before each launch, outside the events, and with `read_back`
     then read once more, so that the dirty lines the write left in L2 are
-    written back before the timed launch instead of during it)."""
+    written back before the timed launch instead of during it."""
     X = torch.randn(rows, cols, device=stream.device)
     Y = torch.empty(cols, rows, device=stream.device)
     for _ in range(3):
         sg.transpose(X, Y, stream=stream)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(reps)]
+    times = []
     with torch.cuda.stream(stream):
-        for a, b in ev:
+        for _ in range(reps):
             if flush is not None:
                 flush.fill_(1.0)
                 if read_back:
                     flush.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
             a.record(stream)
             sg.transpose(X, Y, stream=stream)
             b.record(stream)
-    torch.cuda.synchronize()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
     ok = bool(torch.equal(Y, X.t()))
-    ms = sum(a.elapsed_time(b) for a, b in ev) / reps
     del X, Y
-    return ms, ok
+    times.sort()
+    return sum(times) / reps, times[reps // 2], ok
 
 
 def measure_tf32_peak(torch, dev, n=8192, reps=10):
@@ -504,12 +507,13 @@ def run_ours(args, dist):
         flush = torch.empty(64 * 1024 * 1024, device=dev)    # 256 MiB > L2
         transpose = {}
         for rows, cols, fl in ((4096, 4096, flush), (16384, 16384, None)):
-            ms, ok = time_transpose(sg, torch, rows, cols, 20, stream, fl, read_back=fl is not None)
-            ms_dirty = (time_transpose(sg, torch, rows, cols, 20, stream, fl)[0]
+            ms, ms_median, ok = time_transpose(sg, torch, rows, cols, 40, stream, fl,
+                                               read_back=fl is not None)
+            ms_dirty = (time_transpose(sg, torch, rows, cols, 40, stream, fl)[0]
                         if fl is not None else None)
             gbs = 8.0 * rows * cols / (ms * 1e-3) / 1e9
             transpose[f"{rows}x{cols}"] = {
-                "ms": round(ms, 5), "same_as_torch_t": ok,
+                "ms": round(ms, 5), "ms_median": round(ms_median, 5), "same_as_torch_t": ok,
                 "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
                              "unit": "GB/s", "frac": round(gbs / hbm, 4),
                              "traffic": stored_traffic(f"transpose_{rows}x{cols}")[0],
