@@ -93,13 +93,13 @@ const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb) {
   return &d.tcinfo[ta][tb];
 }
 
-const TcKernelInfo *tc_kernel_info_pair(DeviceState &d, int bn) {
-  const int i = bn == 256 ? 1 : 0;
-  std::call_once(d.tcpair_once[i], [&]() {
-    d.tcpair_err[i] = tc3_pair_entry(bn).info(&d.tcpair[i]);
-    if (d.tcpair_err[i] != cudaSuccess) cudaGetLastError();
+const TcKernelInfo *tc_kernel_info_pair(DeviceState &d, int bn, bool fold_a, bool fold_b) {
+  const int i = bn == 256 ? 1 : 0, fa = fold_a ? 1 : 0, fb = fold_b ? 1 : 0;
+  std::call_once(d.tcpair_once[i][fa][fb], [&]() {
+    d.tcpair_err[i][fa][fb] = tc3_pair_entry(bn, fold_a, fold_b).info(&d.tcpair[i][fa][fb]);
+    if (d.tcpair_err[i][fa][fb] != cudaSuccess) cudaGetLastError();
   });
-  return d.tcpair_err[i] == cudaSuccess ? &d.tcpair[i] : nullptr;
+  return d.tcpair_err[i][fa][fb] == cudaSuccess ? &d.tcpair[i][fa][fb] : nullptr;
 }
 
 const TcKernelInfo *tc_kernel_info_presplit(DeviceState &d, int bn) {
@@ -997,6 +997,16 @@ int presplit_tile_n(const Args &a, int sm_count) {
 #ifndef SG_TC_PAIR
 #define SG_TC_PAIR 1
 #endif
+// SG_TC_FOLD  1: on CTA pairs, compute a k-contiguous operand's small parts
+// in the kernel instead of in a split pass; 0 (default): split ahead.  The
+// folded form gives the same bits but is slower on GB300 (4096^3 NT: 0.64 ms
+// against 0.48 ms for the three launches split ahead): with three 64 KiB
+// stages the tensor cores' two stages of lead must cover the copy, the
+// conversion, the odd CTA's cluster-scope release and the accumulator
+// hand-overs that share the converter warps.
+#ifndef SG_TC_FOLD
+#define SG_TC_FOLD 0
+#endif
 
 // Work plan on CTA pairs.  A 256 x 256 pair tile costs about 1.6 times a
 // 256 x 128 one on GB300 (4096^3 NN: 4 rounds of wide tiles in 0.46 ms
@@ -1024,49 +1034,72 @@ PairPlan plan_pair(const Args &a, int64_t clusters) {
 }
 
 sgemm_status_t run_tc3_presplit(const Args &a, DeviceState &d, cudaStream_t s) {
-  // CTA pairs if the device runs them, else one CTA per tile
+  const bool tA = a.ta == 1, tB = a.tb == 0;   // operands to transpose to K-major
+  // CTA pairs if the device runs them, else one CTA per tile; on pairs a
+  // k-contiguous operand's small parts are computed in the kernel (fold)
   PairPlan plan{0, 0, 0};
   const TcKernelInfo *ki = nullptr;
+  bool fold_a = false, fold_b = false;
   if (SG_TC_PAIR) {
-    const TcKernelInfo *k128 = tc_kernel_info_pair(d, 128), *k256 = tc_kernel_info_pair(d, 256);
+    fold_a = SG_TC_FOLD && !tA;
+    fold_b = SG_TC_FOLD && !tB;
+    const TcKernelInfo *k128 = tc_kernel_info_pair(d, 128, fold_a, fold_b),
+                       *k256 = tc_kernel_info_pair(d, 256, fold_a, fold_b);
     if (k128 && k256) {
       plan = plan_pair(a, k256->max_ctas / 2);
       ki = plan.bn == 256 ? k256 : k128;
     }
   }
   const bool pair = ki != nullptr;
-  if (!pair) ki = tc_kernel_info_presplit(d, presplit_tile_n(a, d.sm_count));
+  if (!pair) {
+    fold_a = fold_b = false;
+    ki = tc_kernel_info_presplit(d, presplit_tile_n(a, d.sm_count));
+  }
   if (!ki || ki->ctas_per_sm < 1) return SGEMM_ERR_UNSUPPORTED;
   const int64_t ldk = a.K;   // K % 4 == 0 on this path
   const size_t mat_a = (static_cast<size_t>(a.M) * ldk * sizeof(float) + 255) & ~size_t(255);
   const size_t mat_b = (static_cast<size_t>(a.N) * ldk * sizeof(float) + 255) & ~size_t(255);
-  const bool tA = a.ta == 1, tB = a.tb == 0;   // operands to transpose to K-major
-  const size_t bytes = mat_a * (tA ? 2 : 1) + mat_b * (tB ? 2 : 1);
+  const size_t bytes_a = fold_a ? 0 : mat_a * (tA ? 2 : 1);
+  const size_t bytes_b = fold_b ? 0 : mat_b * (tB ? 2 : 1);
+  const bool scratch_used = bytes_a + bytes_b > 0;
   const bool capturing = stream_capturing(s);
   std::lock_guard<std::mutex> lock(d.tr_mu);
-  float *scratch = pretranspose_scratch(d, bytes, capturing);
-  if (!scratch) return SGEMM_ERR_UNSUPPORTED;
+  float *scratch = nullptr;
+  if (scratch_used) {
+    scratch = pretranspose_scratch(d, bytes_a + bytes_b, capturing);
+    if (!scratch) return SGEMM_ERR_UNSUPPORTED;
+  }
   char *cur = reinterpret_cast<char *>(scratch);
   auto take = [&cur](size_t n) {
     float *q = reinterpret_cast<float *>(cur);
     cur += n;
     return q;
   };
-  float *a_small = take(mat_a), *a_big = tA ? take(mat_a) : nullptr;
-  float *b_small = take(mat_b), *b_big = tB ? take(mat_b) : nullptr;
-  if (order_before_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  float *a_small = fold_a ? nullptr : take(mat_a), *a_big = (!fold_a && tA) ? take(mat_a) : nullptr;
+  float *b_small = fold_b ? nullptr : take(mat_b), *b_big = (!fold_b && tB) ? take(mat_b) : nullptr;
+  if (scratch_used && order_before_use(d.tr_order, s, capturing) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
+  int passes = 0;
   bool done = false;
   // A: stored M x K (k along rows) or K x M
-  if (launch_tf32_split(a.A, a.lda, tA ? static_cast<int>(a.K) : static_cast<int>(a.M),
-                        tA ? static_cast<int>(a.M) : static_cast<int>(a.K), tA, a_big, a_small, ldk,
-                        d.sm_count, d.status, s, &done) != cudaSuccess)
-    return SGEMM_ERR_LAUNCH;
-  if (!done) return SGEMM_ERR_UNSUPPORTED;   // nothing queued yet
+  if (!fold_a) {
+    if (launch_tf32_split(a.A, a.lda, tA ? static_cast<int>(a.K) : static_cast<int>(a.M),
+                          tA ? static_cast<int>(a.M) : static_cast<int>(a.K), tA, a_big, a_small,
+                          ldk, d.sm_count, d.status, s, &done) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+    if (!done) return SGEMM_ERR_UNSUPPORTED;   // nothing queued yet
+    ++passes;
+  }
   // B: stored N x K or K x N
-  if (launch_tf32_split(a.B, a.ldb, tB ? static_cast<int>(a.K) : static_cast<int>(a.N),
-                        tB ? static_cast<int>(a.N) : static_cast<int>(a.K), tB, b_big, b_small, ldk,
-                        d.sm_count, d.status, s, &done) != cudaSuccess || !done)
-    return SGEMM_ERR_LAUNCH;   // the A pass is queued: failing here is an error
+  if (!fold_b) {
+    if (launch_tf32_split(a.B, a.ldb, tB ? static_cast<int>(a.K) : static_cast<int>(a.N),
+                          tB ? static_cast<int>(a.N) : static_cast<int>(a.K), tB, b_big, b_small,
+                          ldk, d.sm_count, d.status, s, &done) != cudaSuccess)
+      return SGEMM_ERR_LAUNCH;
+    // with the A pass queued, failing here is an error
+    if (!done) return passes ? SGEMM_ERR_LAUNCH : SGEMM_ERR_UNSUPPORTED;
+    ++passes;
+  }
   const float *A_big = tA ? a_big : a.A, *B_big = tB ? b_big : a.B;
   const int64_t lda_big = tA ? ldk : a.lda, ldb_big = tB ? ldk : a.ldb;
 
@@ -1092,22 +1125,28 @@ sgemm_status_t run_tc3_presplit(const Args &a, DeviceState &d, cudaStream_t s) {
   // all K-major [rows][32 k] boxes, 128-byte swizzle: 128 rows, except
   // op(B) on CTA pairs, where each CTA loads half of a tile's n-rows
   const int b_rows = pair ? ki->bn / 2 : 128;
+  // a folded operand's small-part map is not read: its big-part map stands in
   CUtensorMap tmA, tmB, tmAs, tmBs;
   if (!encode_tmap(&tmA, A_big, a.M, a.K, lda_big, 32, 128, true) ||
-      !encode_tmap(&tmAs, a_small, a.M, a.K, ldk, 32, 128, true) ||
-      !encode_tmap(&tmB, B_big, a.N, a.K, ldb_big, 32, b_rows, true) ||
-      !encode_tmap(&tmBs, b_small, a.N, a.K, ldk, 32, b_rows, true))
+      !encode_tmap(&tmB, B_big, a.N, a.K, ldb_big, 32, b_rows, true))
+    return SGEMM_ERR_LAUNCH;
+  tmAs = tmA;
+  tmBs = tmB;
+  if ((!fold_a && !encode_tmap(&tmAs, a_small, a.M, a.K, ldk, 32, 128, true)) ||
+      (!fold_b && !encode_tmap(&tmBs, b_small, a.N, a.K, ldk, 32, b_rows, true)))
     return SGEMM_ERR_LAUNCH;
   // persistent grid: one CTA (pair: two) per tile, at most what fits at once
   const int per_tile = pair ? 2 : 1;
   const int64_t slots = pair ? ki->max_ctas : static_cast<int64_t>(d.sm_count) * ki->ctas_per_sm;
   const int64_t want = num_tiles * per_tile;
   const int grid = static_cast<int>(want < slots ? want : slots - slots % per_tile);
-  const TcEntry entry = pair ? tc3_pair_entry(ki->bn) : tc3_presplit_entry(ki->bn);
+  const TcEntry entry =
+      pair ? tc3_pair_entry(ki->bn, fold_a, fold_b) : tc3_presplit_entry(ki->bn);
   if (entry.launch(p, &tmA, &tmB, &tmAs, &tmBs, grid, s, false) != cudaSuccess)
     return SGEMM_ERR_LAUNCH;
-  t_last_launches = 3;
-  if (order_after_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  t_last_launches = 1 + passes;
+  if (scratch_used && order_after_use(d.tr_order, s, capturing) != cudaSuccess)
+    return SGEMM_ERR_LAUNCH;
   return SGEMM_SUCCESS;
 }
 

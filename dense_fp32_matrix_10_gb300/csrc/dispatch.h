@@ -91,11 +91,11 @@ struct DeviceState {
   std::once_flag tcinfo_once[2][2];
   cudaError_t tcinfo_err[2][2] = {};
   TcKernelInfo tcinfo[2][2] = {};
-  std::once_flag tcpre_once, tcpre_wide_once, tcpair_once[2];
-  cudaError_t tcpre_err = cudaSuccess, tcpre_wide_err = cudaSuccess, tcpair_err[2] = {};
+  std::once_flag tcpre_once, tcpre_wide_once, tcpair_once[2][2][2];
+  cudaError_t tcpre_err = cudaSuccess, tcpre_wide_err = cudaSuccess, tcpair_err[2][2][2] = {};
   // 128 x 128 / 128 x 256 tiles on one CTA, 256 x 128 / 256 x 256 tiles on
-  // CTA pairs
-  TcKernelInfo tcpre = {}, tcpre_wide = {}, tcpair[2] = {};
+  // CTA pairs [wide][fold_a][fold_b]
+  TcKernelInfo tcpre = {}, tcpre_wide = {}, tcpair[2][2][2] = {};
 };
 // Indices are 32-bit inside the kernels; tile origins may run up to one tile
 // past the end of a dimension.
@@ -135,7 +135,7 @@ DeviceState *device_state(sgemm_status_t *why);
 const SimtKernelInfo *kernel_info(DeviceState &d, int producer, int ta, int tb, int tile, int csk = 0);
 const TcKernelInfo *tc_kernel_info(DeviceState &d, int ta, int tb);
 const TcKernelInfo *tc_kernel_info_presplit(DeviceState &d, int bn);
-const TcKernelInfo *tc_kernel_info_pair(DeviceState &d, int bn);
+const TcKernelInfo *tc_kernel_info_pair(DeviceState &d, int bn, bool fold_a = false, bool fold_b = false);
 
 // 2-D FP32 tensor map over a row-major rows x cols matrix (row stride ld
 // elements), box box_cols x box_rows, zero fill outside; false on failure.

@@ -117,8 +117,10 @@ TcEntry tc3_entry(int transA, int transB);
 TcEntry tc3_presplit_entry(int bn);
 // The same product on CTA pairs (256 x bn tiles, bn = 128 or 256, launched
 // in clusters of two; grid = 2 x the pair count, p.tiles_m counting 256-row
-// tile rows).
-TcEntry tc3_pair_entry(int bn);
+// tile rows).  fold_a / fold_b: that operand is k-contiguous and its small
+// parts are computed in the kernel (its big-part map is the operand itself;
+// its small-part map is not read).
+TcEntry tc3_pair_entry(int bn, bool fold_a = false, bool fold_b = false);
 
 // Second pass of a stream-K launch (sk_fixup.cu).
 // load_sk_fixup / load_scale_c: make the CUDA runtime load these kernels now

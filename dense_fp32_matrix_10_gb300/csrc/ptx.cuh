@@ -296,6 +296,12 @@ __device__ __forceinline__ float4 lds128(uint32_t addr) {
   return v;
 }
 
+// 16 bytes to shared memory (shared::cta address).
+__device__ __forceinline__ void sts128(uint32_t addr, float4 v) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
 }  // namespace sg
 
 // ---------------------------------------------------------------- tcgen05

@@ -112,10 +112,18 @@ static cudaError_t tc3_pair_info(TcKernelInfo *info) {
   return cudaSuccess;
 }
 
-TcEntry tc3_pair_entry(int bn) {
-  if (bn == 256)
-    return TcEntry{&tc3_pair_launch<TcPairConfig<256>>, &tc3_pair_info<TcPairConfig<256>>};
-  return TcEntry{&tc3_pair_launch<TcPairConfig<128>>, &tc3_pair_info<TcPairConfig<128>>};
+template <int BN, bool FA, bool FB>
+static TcEntry tc3_pair_make() {
+  return TcEntry{&tc3_pair_launch<TcPairConfig<BN, FA, FB>>, &tc3_pair_info<TcPairConfig<BN, FA, FB>>};
+}
+
+TcEntry tc3_pair_entry(int bn, bool fold_a, bool fold_b) {
+  if (bn == 256) {
+    if (fold_a) return fold_b ? tc3_pair_make<256, true, true>() : tc3_pair_make<256, true, false>();
+    return fold_b ? tc3_pair_make<256, false, true>() : tc3_pair_make<256, false, false>();
+  }
+  if (fold_a) return fold_b ? tc3_pair_make<128, true, true>() : tc3_pair_make<128, true, false>();
+  return fold_b ? tc3_pair_make<128, false, true>() : tc3_pair_make<128, false, false>();
 }
 
 TcEntry tc3_entry(int transA, int transB) {

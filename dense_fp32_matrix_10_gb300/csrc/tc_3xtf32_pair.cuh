@@ -26,7 +26,9 @@
 //                both CTAs' `acc_full`;
 //   warps 4..    epilogue of this CTA's 128 rows, one warpgroup per 128
 //                columns; they release an accumulator on the even CTA's
-//                `acc_empty` (one arrival per epilogue warp of the pair).
+//                `acc_empty` (one arrival per epilogue warp of the pair);
+//                with a folded operand they also compute its small parts;
+//   warps 2, 3   idle, or converters with a folded operand at BN = 128.
 // Every wait is bounded; a CTA leaves only after its peer has also finished
 // (cluster barrier), so no copy or arrival lands in a CTA that has ended.
 #pragma once
@@ -44,8 +46,18 @@ namespace sg {
 // reading 8 KiB of operands per 128 x 256 x 8 of work), 64 KiB stages,
 // three of them; the two 128-column halves of a CTA's rows go to two
 // epilogue warpgroups.
-template <int BN_>
+// FOLD_A / FOLD_B: that operand is k-contiguous in memory, so its TMA tile
+// is its own big part; instead of loading small parts written by a split pass,
+// the CTA computes them in place (split_pair, the pass's arithmetic) once the
+// big part has landed on the CTA's raw_full barrier, and then arrives on the
+// pair's `full` barrier.  No split pass, no scratch for that operand, the
+// same values.  The converters are the epilogue warps (idle between
+// accumulator hand-overs; tcp_epilogue_fold interleaves both jobs) and, at
+// BN = 128, warps 2 and 3 as well; every converter thread keeps its whole
+// share of a stage in flight at once.
+template <int BN_, bool FOLD_A_ = false, bool FOLD_B_ = false>
 struct TcPairConfig {
+  static constexpr bool FOLD_A = FOLD_A_, FOLD_B = FOLD_B_, FOLD = FOLD_A_ || FOLD_B_;
   static constexpr int BM = 256, BN = BN_, BK = 32;   // the pair's tile
   static_assert(BN == 128 || BN == 256, "pair tiles are 128 or 256 wide");
   static constexpr int B_ROWS = BN / 2;               // this CTA's n-rows of op(B)
@@ -56,8 +68,8 @@ struct TcPairConfig {
   static constexpr int STAGES = BN == 128 ? 4 : 3;
   static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
   // full[s] (used in the even CTA), empty[s], acc_full[2], acc_empty[2] (used
-  // in the even CTA), drain
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+  // in the even CTA), drain, then raw_full[s] when a part is folded
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + (FOLD ? STAGES : 0);
   static constexpr int SMEM_BYTES = BAR_OFFSET + NUM_BARS * 8 + 16 + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
   // warpgroup 0: producer, MMA, two idle warps; then one epilogue warpgroup
@@ -69,7 +81,23 @@ struct TcPairConfig {
   static constexpr uint32_t IDESC_HALF = idesc_tf32(256, BN / 2);   // half-width units
   static constexpr int EPILOGUE_WARPS = 4 * EPILOGUE_GROUPS;
   static constexpr int CHUNK_KTILES = 8;   // k-slices (256 k) per promotion
-  static constexpr uint32_t PAIR_STAGE_TX = 2 * STAGE_BYTES;   // both CTAs' copies
+  // converters: the epilogue warps, then (BN = 128, where warpgroup 0 keeps
+  // its registers) warps 2 and 3
+  static constexpr int CONV_SIDE_WARPS = (FOLD && BN_ == 128) ? 2 : 0;
+  static constexpr int CONV_WARPS = FOLD ? EPILOGUE_WARPS + CONV_SIDE_WARPS : 0;
+  static constexpr int CONV_THREADS = 32 * CONV_WARPS;
+  // float4s per stage to convert, and per converter thread
+  static constexpr int CONV_A_VEC = FOLD_A ? A_BYTES / 16 : 0;
+  static constexpr int CONV_VEC = CONV_A_VEC + (FOLD_B ? B_BYTES / 16 : 0);
+  static constexpr int CONV_PER_THREAD = FOLD ? (CONV_VEC + CONV_THREADS - 1) / CONV_THREADS : 0;
+  // bytes landing per stage on the even CTA's `full` (both CTAs' copies of
+  // the parts not folded) and on each CTA's raw_full (its folded big parts)
+  static constexpr uint32_t PAIR_STAGE_TX =
+      2 * ((FOLD_A ? 0 : 2 * A_BYTES) + (FOLD_B ? 0 : 2 * B_BYTES));
+  static constexpr uint32_t RAW_TX = (FOLD_A ? A_BYTES : 0) + (FOLD_B ? B_BYTES : 0);
+  // arrivals completing `full`: the even producer's, and with a folded part
+  // each converter warp of both CTAs
+  static constexpr int FULL_COUNT = 1 + 2 * CONV_WARPS;
   static constexpr int REGS_WG0 = 40, REGS_EPI = 232;
   static_assert(BN == 128 || 128 * (REGS_WG0 + 2 * REGS_EPI) <= THREADS * ((65536 / THREADS) & ~7),
                 "register split exceeds the launch budget");
@@ -83,6 +111,7 @@ struct TcPairBars {
   __device__ uint32_t acc_full(uint32_t b) const { return base + 8 * (2 * Cfg::STAGES + b); }
   __device__ uint32_t acc_empty(uint32_t b) const { return base + 8 * (2 * Cfg::STAGES + 2 + b); }
   __device__ uint32_t drain() const { return base + 8 * (2 * Cfg::STAGES + 4); }
+  __device__ uint32_t raw_full(uint32_t s) const { return base + 8 * (2 * Cfg::STAGES + 5 + s); }
 };
 
 // Work unit t (p.tiles_m counts 256-row tile rows) -> first row of this
@@ -123,24 +152,106 @@ __device__ __forceinline__ void tcp_produce(const TcParams &p, const CUtensorMap
         ok = false;
         break;
       }
-      if (rank == 0) mbar_arrive_expect_tx(bar.full(s), Cfg::PAIR_STAGE_TX);
+      if (rank == 0) {
+        if (Cfg::PAIR_STAGE_TX > 0)
+          mbar_arrive_expect_tx(bar.full(s), Cfg::PAIR_STAGE_TX);
+        else
+          mbar_arrive(bar.full(s));
+      }
+      if constexpr (Cfg::FOLD) mbar_arrive_expect_tx(bar.raw_full(s), Cfg::RAW_TX);
       const uint32_t cfull = map_to_rank(bar.full(s), 0);
       const uint32_t st = sbase + s * Cfg::STAGE_BYTES;
       const int k0 = kt * Cfg::BK;
-      tma_load_2d_pair(st + Cfg::A_BIG, tmA, cfull, k0, m0);
-      tma_load_2d_pair(st + Cfg::A_SMALL, tmAs, cfull, k0, m0);
-      tma_load_2d_pair(st + Cfg::B_BIG, tmB, cfull, k0, nb);
-      tma_load_2d_pair(st + Cfg::B_SMALL, tmBs, cfull, k0, nb);
+      if constexpr (Cfg::FOLD_A) {   // the big part only, onto this CTA's raw_full
+        tma_load_2d(st + Cfg::A_BIG, tmA, bar.raw_full(s), k0, m0);
+      } else {
+        tma_load_2d_pair(st + Cfg::A_BIG, tmA, cfull, k0, m0);
+        tma_load_2d_pair(st + Cfg::A_SMALL, tmAs, cfull, k0, m0);
+      }
+      if constexpr (Cfg::FOLD_B) {
+        tma_load_2d(st + Cfg::B_BIG, tmB, bar.raw_full(s), k0, nb);
+      } else {
+        tma_load_2d_pair(st + Cfg::B_BIG, tmB, cfull, k0, nb);
+        tma_load_2d_pair(st + Cfg::B_SMALL, tmBs, cfull, k0, nb);
+      }
     }
   }
   // On give-up the even CTA lets the copies it counts land (bounded); the
-  // cluster barrier at the end keeps the odd CTA alive until then.
-  if (!ok && rank == 0) {
+  // cluster barrier at the end keeps the odd CTA alive until then.  Each CTA
+  // does the same for the copies onto its own raw_full.
+  if (!ok) {
     const uint32_t first = it > Cfg::STAGES ? it - Cfg::STAGES : 0;
-    for (uint32_t j = first; j < it; ++j)
-      wait_parity_bounded(bar.full(j % Cfg::STAGES), (j / Cfg::STAGES) & 1, p.wait_budget_ns,
-                          nullptr);
+    for (uint32_t j = first; j < it; ++j) {
+      if (rank == 0)
+        wait_parity_bounded(bar.full(j % Cfg::STAGES), (j / Cfg::STAGES) & 1, p.wait_budget_ns,
+                            nullptr);
+      if constexpr (Cfg::FOLD)
+        wait_parity_bounded(bar.raw_full(j % Cfg::STAGES), (j / Cfg::STAGES) & 1, p.wait_budget_ns,
+                            nullptr);
+    }
   }
+}
+
+// ------------------------------------------------------------------ converters
+// Converter thread ct's share of stage st: the small parts of this CTA's
+// folded big parts, written at the same byte offsets of the small-part tiles
+// (an elementwise map keeps the swizzled layout).  All loads are issued
+// before the first store.  The stores, made through the generic proxy, are
+// fenced for the tensor cores (async proxy), which read them once `full`
+// completes.
+template <class Cfg>
+__device__ __forceinline__ void tcp_convert_stage(uint32_t st, int ct) {
+  constexpr int T = Cfg::CONV_THREADS, AV = Cfg::CONV_A_VEC, V = Cfg::CONV_VEC;
+  float4 x[Cfg::CONV_PER_THREAD];
+#pragma unroll
+  for (int j = 0; j < Cfg::CONV_PER_THREAD; ++j) {
+    const int i = ct + j * T;
+    if (i < V) x[j] = lds128(st + (i < AV ? Cfg::A_BIG + 16 * i : Cfg::B_BIG + 16 * (i - AV)));
+  }
+#pragma unroll
+  for (int j = 0; j < Cfg::CONV_PER_THREAD; ++j) {
+    const int i = ct + j * T;
+    if (i < V) {
+      float4 sm;
+      float b0, b1, b2, b3;
+      split_pair(x[j].x, x[j].y, b0, b1, sm.x, sm.y);
+      split_pair(x[j].z, x[j].w, b2, b3, sm.z, sm.w);
+      sts128(st + (i < AV ? Cfg::A_SMALL + 16 * i : Cfg::B_SMALL + 16 * (i - AV)), sm);
+    }
+  }
+  fence_proxy_async_smem();
+}
+
+// Wait for stage `it`'s folded big parts, convert this thread's share, and
+// count the warp's arrival on the even CTA's `full` (in the even CTA a local
+// arrival, whose CTA-scope release covers the MMA thread of the same CTA; in
+// the odd one a release at cluster scope).
+template <class Cfg>
+__device__ __forceinline__ bool tcp_convert_one(const TcParams &p, uint32_t sbase,
+                                                const TcPairBars<Cfg> &bar, uint32_t rank,
+                                                uint32_t it, int ct, int lane) {
+  const uint32_t s = it % Cfg::STAGES, round = it / Cfg::STAGES;
+  if (!wait_parity_bounded(bar.raw_full(s), round & 1, p.wait_budget_ns, p.status)) return false;
+  tcp_convert_stage<Cfg>(sbase + s * Cfg::STAGE_BYTES, ct);
+  __syncwarp();
+  if (lane == 0) {
+    if (rank == 0)
+      mbar_arrive(bar.full(s));
+    else
+      mbar_arrive_cluster(map_to_rank(bar.full(s), 0));
+  }
+  return true;
+}
+
+// Warps 2 and 3 at BN = 128: converters only, over every stage.
+template <class Cfg>
+__device__ __forceinline__ void tcp_convert(const TcParams &p, uint32_t sbase,
+                                            const TcPairBars<Cfg> &bar, uint32_t rank, int ct,
+                                            int lane) {
+  uint32_t it = 0;
+  for (int t = cluster_id_x(); t < p.num_tiles; t += cluster_count_x())
+    for (int kt = 0; kt < p.k_tiles; ++kt, ++it)
+      if (!tcp_convert_one<Cfg>(p, sbase, bar, rank, it, ct, lane)) return;
 }
 
 // ------------------------------------------------------------------ MMA issue
@@ -165,7 +276,13 @@ __device__ __forceinline__ void tcp_issue(const TcParams &p, uint32_t sbase, uin
       const int kc1 = min(kc0 + Cfg::CHUNK_KTILES, p.k_tiles);
       for (int kt = kc0; kt < kc1; ++kt, ++it) {
         const uint32_t s = it % Cfg::STAGES, round = it / Cfg::STAGES;
-        if (!wait_parity_bounded(bar.full(s), round & 1, p.wait_budget_ns, p.status)) {
+        // with folded parts the peer's converter stores are among what
+        // `full` publishes: acquire at cluster scope
+        const bool got = Cfg::FOLD ? wait_parity_bounded_cluster(bar.full(s), round & 1,
+                                                                 p.wait_budget_ns, p.status)
+                                   : wait_parity_bounded(bar.full(s), round & 1, p.wait_budget_ns,
+                                                         p.status);
+        if (!got) {
           ok = false;
           break;
         }
@@ -234,6 +351,86 @@ __device__ __forceinline__ void tcp_epilogue(const TcParams &p, uint32_t tmem_ba
   }
 }
 
+// SG_TC_FOLD_LAG: stages converted past the end of an accumulator chunk
+// before the epilogue warps hand that chunk over (1 or 2).
+#ifndef SG_TC_FOLD_LAG
+#define SG_TC_FOLD_LAG 1
+#endif
+
+// The epilogue warps with folded parts: converters of every stage, and,
+// SG_TC_FOLD_LAG stages after the last stage of each accumulator chunk has
+// been converted, the hand-over of that chunk (so the tensor cores have work
+// queued while it runs).  The hand-overs follow the same order as in
+// tcp_epilogue; the chunk handed over is always one whose stages were all
+// converted, so neither job waits on the other's future.
+template <class Cfg>
+__device__ __forceinline__ void tcp_epilogue_fold(const TcParams &p, uint32_t sbase,
+                                                  uint32_t tmem_base, const TcPairBars<Cfg> &bar,
+                                                  uint32_t rank, int q, int half, int lane, int ct) {
+  const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+  // hand-over cursor: unit td, chunk starting at k-slice kd, chunk count cd
+  int td = cluster_id_x(), kd = 0;
+  uint32_t cd = 0;
+  int m0 = 0, n0 = 0;
+  bool whole = true;
+  if (td < p.num_tiles) pair_tile<Cfg>(p, td, rank, m0, n0, whole);
+  float acc[128];
+#pragma unroll
+  for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+  auto hand_over = [&]() -> bool {
+    const bool idle = !whole && half > 0;   // no second 128 columns
+    const uint32_t b = cd & 1, use = cd >> 1;
+    if (!wait_parity_bounded(bar.acc_full(b), use & 1, p.wait_budget_ns, p.status)) return false;
+    tc_fence_after_sync();
+    if (!idle) {
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + lane_addr + b * Cfg::BN + half * 128 + cc * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[cc * 32 + j] += __uint_as_float(v[j]);
+      }
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(map_to_rank(bar.acc_empty(b), 0));
+    ++cd;
+    kd += Cfg::CHUNK_KTILES;
+    if (kd >= p.k_tiles) {   // the unit's last chunk: write it, start the next
+      if (!idle) tc_store_row(p, m0 + 32 * q + lane, n0 + half * 128, acc);
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      kd = 0;
+      td += cluster_count_x();
+      if (td < p.num_tiles) pair_tile<Cfg>(p, td, rank, m0, n0, whole);
+    }
+    return true;
+  };
+  // last stages of the chunks awaiting hand-over, oldest first (at most
+  // SG_TC_FOLD_LAG of them)
+  constexpr uint32_t LAG = SG_TC_FOLD_LAG;
+  static_assert(LAG >= 1 && LAG <= 2 && LAG < Cfg::STAGES, "hand-over lag of 1 or 2 stages");
+  uint32_t it = 0, end0 = 0, end1 = 0;
+  int waiting = 0;
+  for (int t = cluster_id_x(); t < p.num_tiles; t += cluster_count_x()) {
+    for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+      if (!tcp_convert_one<Cfg>(p, sbase, bar, rank, it, ct, lane)) return;
+      while (waiting > 0 && end0 + LAG <= it) {
+        if (!hand_over()) return;
+        end0 = end1;
+        --waiting;
+      }
+      if ((kt + 1) % Cfg::CHUNK_KTILES == 0 || kt + 1 == p.k_tiles) {
+        if (waiting == 0) end0 = it; else end1 = it;
+        ++waiting;
+      }
+    }
+  }
+  while (waiting-- > 0)
+    if (!hand_over()) return;
+}
+
 // ------------------------------------------------------------------ kernel
 // Launched in clusters of two CTAs; p.tiles_m counts 256-row tile rows,
 // p.num_tiles the work units (whole tiles, then column halves: pair_tile).
@@ -253,8 +450,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) {
-      mbar_init(bar.full(s), 1);
+      mbar_init(bar.full(s), Cfg::FULL_COUNT);
       mbar_init(bar.empty(s), 1);
+      if constexpr (Cfg::FOLD) mbar_init(bar.raw_full(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar.acc_full(b), 1);
@@ -284,10 +482,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else if (warp == 1) {
       if (lane == 0 && rank == 0) tcp_issue<Cfg>(p, sbase, tmem_base, bar);
       __syncwarp();
+    } else if constexpr (Cfg::CONV_SIDE_WARPS > 0) {
+      tcp_convert<Cfg>(p, sbase, bar, rank, 32 * Cfg::EPILOGUE_WARPS + threadIdx.x - 64, lane);
     }
   } else {
     if (Cfg::EPILOGUE_GROUPS > 1) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::REGS_EPI));
-    tcp_epilogue<Cfg>(p, tmem_base, bar, rank, warp & 3, (warp >> 2) - 1, lane);
+    if constexpr (Cfg::FOLD)
+      tcp_epilogue_fold<Cfg>(p, sbase, tmem_base, bar, rank, warp & 3, (warp >> 2) - 1, lane,
+                             threadIdx.x - 128);
+    else
+      tcp_epilogue<Cfg>(p, tmem_base, bar, rank, warp & 3, (warp >> 2) - 1, lane);
   }
 
   tc_fence_before_sync();

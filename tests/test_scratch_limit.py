@@ -35,9 +35,11 @@ def _cuda():
 
 
 # (case, kernel family): every workload family, the tensor-core family on the
-# headline shape (whose split-ahead form needs scratch) and the integer variant
-# of the NT workload
+# headline and NT shapes (whose split-ahead forms need scratch: under limit 0
+# they run the one-launch form that splits in the kernel), and the integer
+# variant of the NT workload
 LIMIT0_CASES = [(c, "auto") for c in W.ALL_CASES] + [(W.HEADLINE, "tc_3xtf32"),
+                                                     (W.NT_4096, "tc_3xtf32"),
                                                      (W.NT_4096.as_int(), "auto")]
 
 
@@ -79,6 +81,7 @@ def test_limit_zero_allocates_nothing_and_matches_the_oracle(orc):
         assert launches[W.HEADLINE.name + "auto"] == 1
         assert launches[W.SQUARE_1024.name + "auto"] == 1
         assert launches[W.HEADLINE.name + "tc_3xtf32"] == 1
+        assert launches[W.NT_4096.name + "tc_3xtf32"] == 1
     for (case, algo, (A, B, C)), (_, _, dC) in zip(host, dev):
         R = orc.sgemm_f64(case.transA, case.transB, case.alpha, A.numpy(), B.numpy(), case.beta,
                           C.numpy() if case.beta != 0 else None)
