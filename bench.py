@@ -103,6 +103,95 @@ def measured_peaks():
         return {}
 
 
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, read-only queries) every 10 ms in a background thread, so
+    that a timed region of a few tens of milliseconds still holds several
+    samples; timestamps keep only the samples inside it.  Raises OSError where
+    NVML cannot be loaded or the device not found (ClockSampler is then
+    used)."""
+
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_uuid, period_s=0.01):
+        import ctypes
+        self.ct = ctypes
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError as e:
+            raise OSError(f"NVML not loadable: {e}")
+        if self.nvml.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        if not gpu_uuid or self.nvml.nvmlDeviceGetHandleByUUID(
+                gpu_uuid.encode(), ctypes.byref(self.handle)) != 0:
+            raise OSError("device not found through NVML")
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn or self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.period = period_s
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+
+    def _sample(self):
+        ct = self.ct
+        sm, mx, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        ok = (self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(sm)) == 0 and
+              self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ct.byref(mx)) == 0)
+        if not ok:
+            return None
+        power = pw.value / 1000.0 if self.nvml.nvmlDeviceGetPowerUsage(self.handle, ct.byref(pw)) == 0 \
+            else None
+        bits = rs.value if self.reasons_fn(self.handle, ct.byref(rs)) == 0 else 0
+        return (float(sm.value), float(mx.value), power, bits)
+
+    def _run(self):
+        while not self.stop_flag.is_set():
+            smp = self._sample()
+            if smp is not None:
+                self.samples.append((time.time(), smp))
+            self.stop_flag.wait(self.period)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+        return self
+
+    def stop(self):
+        self.stop_flag.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        self.nvml.nvmlShutdown()
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not inside:
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            inside = [p for (_, p) in near]
+            window = "nearest samples (timed region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["NVML gave no samples"],
+                    "samples": 0, "source": "nvml"}
+        pw = [p[2] for p in inside if p[2] is not None]
+        reasons = sorted({name for p in inside for bit, name in self.REASONS.items() if p[3] & bit})
+        return {"sm_mhz": statistics.median(p[0] for p in inside),
+                "sm_max_mhz": max(p[1] for p in inside),
+                "power_w_median": statistics.median(pw) if pw else None,
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "source": "nvml, 10 ms"}
+
+
+def clock_sampler(uuid):
+    """NVML sampler where NVML is available, else nvidia-smi's."""
+    try:
+        return NvmlClockSampler(uuid)
+    except (OSError, AttributeError):
+        return ClockSampler(uuid)
+
+
 class ClockSampler:
     """nvidia-smi samples every 100 ms in a background process; timestamps let
     us keep only the samples inside the timed region."""
@@ -170,7 +259,8 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "power_w_median": statistics.median(pw) if pw else None,
-                "reasons": reasons, "samples": len(inside), "window": window}
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "source": "nvidia-smi, 100 ms"}
 
 
 # ----------------------------------------------------------------- distributed
@@ -352,7 +442,7 @@ def run_ours(args, dist):
 
     # ---- device-resident timed region
     uuid = str(getattr(props, "uuid", "") or "")
-    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or None))
+    sampler = clock_sampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else (uuid or None))
     sampler.start()
     for _ in range(args.warmup):
         sg.gemm(A, B, C, case.alpha, case.beta, case.transA, case.transB, algo=args.algo, stream=stream)

@@ -308,9 +308,18 @@ int pick_simt_tile(const Args &a, int producer, int sm_count, int64_t batch) {
   // TMA producer transposes a k-contiguous A in shared memory
   const bool a_mn_in_smem = a.ta == 1 || (producer == kTma && SG_SIMT_TRANSPOSE_A);
   // the wide tile only once enough SMs get a whole tile: far below that,
-  // stream-K would cut its k-loop into short, fixup-heavy segments
-  const bool fills = cdiv(a.M, 128) * cdiv(a.N, 256) * 100 >= SG_WIDE_MIN_FILL_PCT * sm_count;
-  if (SG_SIMT_WIDE_TILE && producer == kTma && a_mn_in_smem && a.tb == 0 && fills) return kTile128x256;
+  // stream-K would cut its k-loop into short, fixup-heavy segments.  A batch
+  // (every product counted) takes it once it fills a whole wave, and only
+  // where it pads each product's N no further than the 128-wide tile does
+  // (GB300, 128 x 128 -> 128 x 256, TFLOP/s: 96 x 512x512x64 NN 41.1 -> 42.7,
+  // TN 41.5 -> 43.0, 8 x 2048^3 NN 61.7 -> 64.5; 12 x 512x512x1024 NN, 96
+  // wide tiles, 53.1 -> 51.5, so below a wave it stays narrow).
+  const bool fills = batch == 1 ? cdiv(a.M, 128) * cdiv(a.N, 256) * 100 >=
+                                      SG_WIDE_MIN_FILL_PCT * sm_count
+                                : cdiv(a.M, 128) * cdiv(a.N, 256) * batch >= sm_count;
+  const bool pad_ok = batch == 1 || cdiv(a.N, 256) * 2 == cdiv(a.N, 128);
+  if (SG_SIMT_WIDE_TILE && producer == kTma && a_mn_in_smem && a.tb == 0 && fills && pad_ok)
+    return kTile128x256;
   return kTile128x128;
 }
 
@@ -336,10 +345,22 @@ int pick_simt_tile(const Args &a, int producer, int sm_count, int64_t batch) {
 #ifndef SG_EPI_TMA
 #define SG_EPI_TMA 1
 #endif
+// SG_SK_MIN_GAIN: with at least a wave of tiles, stream-K only where
+// balancing the k-tiles over every slot shortens the busiest slot's work by
+// this many k-tiles (0: wherever the last wave is partial).  Short k-loops
+// gain less than the split segments and the fixup cost (GB300, graph-free
+// calls, 0 -> 4: 96 x 512x512x64 NT 36.6 -> 38.9 TFLOP/s, NN 39.1 -> 40.4,
+// 512 x 128x128x64 NT 27.6 -> 31.9; single products unchanged).
+#ifndef SG_SK_MIN_GAIN
+#define SG_SK_MIN_GAIN 4
+#endif
 SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws) {
   SkPlan pl{static_cast<int>(tiles), 0, 0, static_cast<int>(tiles < slots ? tiles : slots)};
   if (!have_ws || k_tiles < 2 * kMinSkSegment) return pl;
   if (tiles >= slots && tiles % slots == 0) return pl;
+  if (SG_SK_MIN_GAIN > 0 && tiles >= slots &&
+      cdiv(tiles, slots) * k_tiles * slots - tiles * k_tiles < SG_SK_MIN_GAIN * slots)
+    return pl;
   // SG_SK_REMAINDER 1: split only the tiles beyond whole waves; 0: the last
   // one to two waves' worth
   const int64_t sk = tiles < slots ? tiles
@@ -705,10 +726,11 @@ sgemm_status_t run_simt(const Args &a, DeviceState &d, int producer, cudaStream_
     if (order_after_use(d.ws_order, stream, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
   }
   if (verbose())
-    std::fprintf(stderr, "sgemm: %lldx%lldx%lld %c%c batch %lld: %s %dx%d tiles %lld (%d whole), stream-K tiles %d, grid %d, fixup %s\n",
+    std::fprintf(stderr, "sgemm: %lldx%lldx%lld %c%c batch %lld: %s %dx%d tiles %lld (%d whole), stream-K tiles %d, grid %d, fixup %s, C %s\n",
                  (long long)a.M, (long long)a.N, (long long)a.K, "NT"[a.ta], "NT"[a.tb], (long long)bt.count,
                  producer == kTma ? "tma" : "cp.async", ki->bm, ki->bn, (long long)num_tiles, plan.dp_tiles,
-                 plan.sk_tiles, plan.grid, plan.sk_tiles == 0 ? "none" : p.sk_count ? "in-kernel" : "launch");
+                 plan.sk_tiles, plan.grid, plan.sk_tiles == 0 ? "none" : p.sk_count ? "in-kernel" : "launch",
+                 p.c_tma ? "staged TMA stores" : "from registers");
   return SGEMM_SUCCESS;
 }
 

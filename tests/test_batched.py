@@ -254,6 +254,16 @@ def test_stream_k_batch(_cuda, orc):
 
 
 @gpu
+def test_wide_tile_batch(_cuda, orc):
+    """Batches whose 128 x 256 tiles fill a wave run them: NN (A transposed in
+    shared memory by the producer warps) and TN, ragged M, alpha and beta
+    (staged TMA stores and the register epilogue), integer data exact."""
+    run_batched(orc, 0, 0, 200, 512, 80, 40, seed=31)
+    run_batched(orc, 1, 0, 200, 512, 80, 40, alpha=0.5, beta=-1.5, seed=32)
+    run_batched(orc, 0, 0, 130, 256, 64, 80, kind="int", seed=33, check="exact")
+
+
+@gpu
 def test_single_product_matches_sgemm(_cuda):
     M, N, K = 300, 200, 152   # 16-byte rows: both calls take the TMA kernel
     A = torch.randn(M, K, device="cuda")
