@@ -354,24 +354,30 @@ def time_gemm_graph(sg, torch, case, A, B, C, algo, calls=20, replays=5):
 
 def time_transpose(sg, torch, rows, cols, reps, stream, flush=None, read_back=False):
     """(mean, median) per-launch ms of sgemm_transpose on a rows x cols matrix:
-    CUDA events around each launch on `stream`, the device synchronised
-    before and after each timed launch.  `flush`, a buffer larger than L2, is
-    rewritten before each launch, outside the events, and with `read_back`
-    then read once more, so that the dirty lines the write left in L2 are
-    written back before the timed launch instead of during it."""
+    CUDA events around each launch on `stream`, the device synchronised after
+    each timed launch.  `flush`, a buffer larger than L2, is rewritten before
+    each launch, outside the events, and with `read_back` then read once more,
+    so that the dirty lines the write left in L2 are written back before the
+    timed launch instead of during it.  A short device-side spin is queued
+    ahead of the first event, so that the host has enqueued the launch before
+    the GPU reaches that event: the interval is the kernel's, not the host's
+    launch latency."""
     X = torch.randn(rows, cols, device=stream.device)
     Y = torch.empty(cols, rows, device=stream.device)
     for _ in range(3):
         sg.transpose(X, Y, stream=stream)
+    spin = getattr(torch.cuda, "_sleep", None)
     times = []
     with torch.cuda.stream(stream):
         for _ in range(reps):
+            torch.cuda.synchronize()
             if flush is not None:
                 flush.fill_(1.0)
                 if read_back:
                     flush.sum()
+            if spin is not None:
+                spin(200_000)   # ~0.1 ms of GPU clock cycles
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
             a.record(stream)
             sg.transpose(X, Y, stream=stream)
             b.record(stream)

@@ -575,10 +575,17 @@ __device__ __forceinline__ int thread_col(int tn, int c) {
 #ifndef SG_SIMT_KC_UNROLL_CPASYNC
 #define SG_SIMT_KC_UNROLL_CPASYNC 1
 #endif
+// SG_SIMT_KC_UNROLL_BK: the unroll of the TMA kernels whose op(B) tile is
+// k-contiguous (op(B)'s 4 k x 8 column fragment is held per chunk).
+#ifndef SG_SIMT_KC_UNROLL_BK
+#define SG_SIMT_KC_UNROLL_BK 8
+#endif
 template <class Cfg>
 __host__ __device__ constexpr int kc_unroll() {
   return Cfg::TN == 16 ? SG_SIMT_KC_UNROLL_WIDE
-         : Cfg::PRODUCER == kCpAsync ? SG_SIMT_KC_UNROLL_CPASYNC : SG_SIMT_KC_UNROLL;
+         : Cfg::PRODUCER == kCpAsync ? SG_SIMT_KC_UNROLL_CPASYNC
+         : Cfg::B_KMAJOR             ? SG_SIMT_KC_UNROLL_BK
+                                     : SG_SIMT_KC_UNROLL;
 }
 
 // How the 64 accumulators of a thread are packed into 32 float2 and updated.
