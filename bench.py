@@ -321,7 +321,9 @@ def time_gemm(sg, torch, case, A, B, C, steps, warmup, algo, stream, record_laun
     end.record(stream)
     torch.cuda.synchronize()
     region = start.elapsed_time(end) / steps
-    per_launch = sum(a.elapsed_time(b) for a, b in ev) / steps if per_call_events else None
+    calls = [a.elapsed_time(b) for a, b in ev]
+    per_launch = sum(calls) / steps if per_call_events else None
+    time_gemm.last_calls = calls   # per-call ms of the last timed region
     return region, per_launch, launches
 
 
@@ -458,6 +460,7 @@ def run_ours(args, dist):
     t_wall0 = time.time()
     ms_region, ms_launch, launches = time_gemm(sg, torch, case, A, B, C, args.steps, 0, args.algo,
                                                stream, record_launches=True)
+    calls = sorted(time_gemm.last_calls)
     t_wall1 = time.time()
     dist.barrier()
     sampler.stop()
@@ -752,6 +755,8 @@ def run_ours(args, dist):
                    "l2": "inputs (192 MiB) larger than L2 (129 MB); no flush between steps",
                    "parallelism": "replicas" if dist.world > 1 else "single GPU"},
         "pct_of_fp32_peak": round(100 * achieved / peak, 2),
+        "per_call_ms": {"min": round(calls[0], 5), "median": round(calls[len(calls) // 2], 5),
+                        "max": round(calls[-1], 5), "calls": len(calls)} if calls else None,
         "e2e": e2e, "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
         "tensor_core_3xtf32": tensor, "transpose": transpose,
         "strided_batched": batched, "ladder": ladder,
