@@ -441,6 +441,41 @@ def test_runs_on_the_given_stream(orc):
     assert_close(C.cpu().numpy(), R, K, "side stream")
 
 
+@pytest.mark.parametrize("shape", [(512, 512, 512), (1024, 1024, 1024), (2048, 2048, 256),
+                                   (8192, 64, 1024)], ids=lambda s: "x".join(map(str, s)))
+def test_products_see_the_previous_kernels_writes(shape):
+    """Product kernels are launched as programmatic dependents of whatever
+    kernel precedes them on the stream, and touch memory only once that kernel
+    has finished.  Each call here directly follows kernels (torch's) that
+    rewrite A and B and scale C, and the next rewrite directly follows the
+    product: every result equals the same product run in isolation, bit for
+    bit (integer-valued data: exact in any order)."""
+    M, N, K = shape
+    g = torch.Generator().manual_seed(M + N + K)
+    As = [torch.randint(-4, 5, (M, K), generator=g).float().cuda() for _ in range(3)]
+    Bs = [torch.randint(-4, 5, (K, N), generator=g).float().cuda() for _ in range(3)]
+    ref = []
+    for a, b in zip(As, Bs):
+        c = torch.full((M, N), 3.0, device="cuda")
+        sg.gemm(a, b, c, 1.0, 0.5)
+        torch.cuda.synchronize()
+        ref.append(c.clone())
+    A = torch.empty(M, K, device="cuda")
+    B = torch.empty(K, N, device="cuda")
+    C = torch.empty(M, N, device="cuda")
+    outs = []
+    for it in range(6):
+        i = it % 3
+        A.copy_(As[i])
+        B.copy_(Bs[i])
+        C.fill_(3.0)
+        sg.gemm(A, B, C, 1.0, 0.5)
+        outs.append(C.clone())
+    torch.cuda.synchronize()
+    for it, c in enumerate(outs):
+        assert torch.equal(c, ref[it % 3]), f"call {it}"
+
+
 def test_launch_count_single_k_slice_is_one():
     """K = 32 is one k-slice: nothing to split, one launch for every family."""
     A = torch.rand(300, 32, device="cuda")
