@@ -907,9 +907,12 @@ __device__ __forceinline__ void add_partial(AccT<Cfg> &acc, const float *ws, int
 // of CTA `rank` add rows [rank*BM/S, (rank+1)*BM/S) of the S partials in rank
 // order (0 + p0 + p1 + ...) through distributed shared memory, apply alpha
 // and beta and write C.  Not inlined, and called after the unit loop: inlined
-// (in the loop or after it) it raised the k-loop's register pressure.
+// (in the loop or after it) it raised the k-loop's register pressure.  The
+// parameters are passed by value: through a reference to the kernel's
+// parameters its loop ran about a third slower (1024^3 under a scratch limit
+// of 0, clusters of two: 3.9 -> 3.1 us for a CTA's half tile).
 template <class Cfg>
-__device__ __noinline__ void csk_reduce(const SimtParams &p, int tile, int S, uint32_t rank, uint32_t stg,
+__device__ __noinline__ void csk_reduce(const SimtParams p, int tile, int S, uint32_t rank, uint32_t stg,
                                         int tid) {
   int bi, tile_m, tile_n;
   unit_coords(p, tile, bi, tile_m, tile_n);
