@@ -652,7 +652,9 @@ def run_ours(args, dist):
         batched = {"workload": f"{bt} x ({bm_}x{bk_}) . ({bk_}x{bn_})^T, NT (per-head Q K^T)",
                    "value": round(bach, 3), "unit": "TFLOP/s", "ms": round(bms, 5),
                    "roofline": {"bound": "alu", "achieved": round(bach, 3), "peak": round(peak, 3),
-                                "unit": "TFLOP/s", "frac": round(bach / peak, 4)}}
+                                "unit": "TFLOP/s", "frac": round(bach / peak, 4),
+                                "traffic": stored_traffic(f"simt_tma_nt_batch{bt}_{bm_}x{bn_}x{bk_}")[0],
+                                "algorithmic_bytes_per_launch": 4 * bt * (bm_ * bk_ + bn_ * bk_ + bm_ * bn_)}}
         del Q, Kt, S
     ladder = None
     if not args.no_ladder:
