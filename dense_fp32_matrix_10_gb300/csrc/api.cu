@@ -367,7 +367,9 @@ SkPlan plan_stream_k(int64_t tiles, int64_t k_tiles, int64_t slots, bool have_ws
                      : SG_SK_REMAINDER ? tiles % slots
                      : (tiles >= 2 * slots ? slots + tiles % slots : tiles);
   int64_t grid = slots;
-  if (sk * k_tiles < grid * kMinSkSegment) grid = (sk * k_tiles) / kMinSkSegment;
+  // fewer CTAs than slots only when every tile is split (whole tiles are
+  // spread over the whole grid)
+  if (sk == tiles && sk * k_tiles < grid * kMinSkSegment) grid = (sk * k_tiles) / kMinSkSegment;
   // the fixup pass handles at most 126 segments per tile (ranges >= k_tiles/120)
   if (grid > sk * 120) grid = sk * 120;
   if (grid < 2 || sk % grid == 0) return pl;  // whole tiles per CTA: plain waves
