@@ -54,7 +54,12 @@
  * are ready once the stream reaches that point.  Argument errors are detected
  * on the host before anything is queued, and then nothing is launched.  A
  * pending error left by earlier, unrelated CUDA runtime calls is cleared
- * before the call's launches, so it does not fail this call.
+ * before the call's launches, so it does not fail this call.  The product
+ * kernels are launched as programmatic dependents of whatever kernel precedes
+ * them on the stream (cudaLaunchAttributeProgrammaticStreamSerialization): one
+ * may be scheduled while that kernel finishes, but it reads and writes memory
+ * only after griddepcontrol.wait, i.e. once that kernel has completed and its
+ * writes are visible -- the stream's order is kept for every caller.
  *
  * CUDA graphs: sgemm(), sgemm_ex(), sgemm_strided_batched() and
  * sgemm_transpose() may be captured.  Inside a capture the library allocates
