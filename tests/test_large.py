@@ -123,3 +123,25 @@ def test_transpose_with_more_than_2_31_elements():
     want = ((np.arange(n)[None, :] * 3 + rows[:, None] * 7) % 1021).astype(np.float32)
     np.testing.assert_array_equal(G, want)
     del Y
+
+
+def test_strided_batch_beyond_2_31_elements():
+    """2000 products of 1100 x 1100 by a shared 1100 x 64 (stride 0): the
+    batch of A holds 2.4 G elements, so the later products' offsets pass 2^31;
+    sampled rows of the first, middle and last products, bit for bit."""
+    bt, M, K, N = 2000, 1100, 1100, 64
+    assert bt * M * K > (1 << 31)
+    A = torch.empty(bt, M, K, device="cuda")
+    c = torch.arange(K, device="cuda", dtype=torch.int64)[None, :]
+    r = torch.arange(M, device="cuda", dtype=torch.int64)[:, None]
+    for b in range(bt):   # product b: rows offset by b
+        A[b] = a_val(r + b, c).to(torch.float32)
+    B = fill(K, N, b_val).expand(bt, K, N)
+    C = sg.gemm_strided_batched(A, B)
+    torch.cuda.synchronize()
+    assert sg.sgemm_last_device_status() == 0
+    rows = np.array([0, 1, 517, M - 1])
+    for b in (0, 1, bt // 2, (1 << 31) // (M * K), bt - 2, bt - 1):
+        G = C[b][torch.as_tensor(rows, device="cuda")].cpu().numpy()
+        np.testing.assert_array_equal(G, expected_rows(rows + b, K, N), err_msg=f"product {b}")
+    del A, B, C
