@@ -465,6 +465,9 @@ def run_ours(args, dist):
     dist.barrier()
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
+    # the timed steps' output (every step writes the same C), kept for the
+    # parity check against the oracle's rows below
+    C_timed = C.cpu().numpy() if dist.rank == 0 and not args.no_cpu_baseline else None
     ms_step, value = job_rate(dist, flops, ms_region, dev)
 
     # ---- end to end through the C ABI: pinned host operands in, result out.
@@ -768,15 +771,35 @@ def run_ours(args, dist):
         "device": {"name": props.name, "sms": sms, "cc": f"{props.major}.{props.minor}"},
     }
     if dist.rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(case, A, B, seconds=args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(case, A, B, seconds=args.cpu_seconds,
+                                              keep_result=True)
+        R = result["cpu_baseline"].pop("_result")
+        if case.beta == 0.0:   # the sampled oracle rows are alpha * op(A) * op(B)
+            result["parity"] = parity_stats(C_timed[:R.shape[0]], R, case.K)
     dist.close()
     return result
 
 
+def parity_stats(G, R, K):
+    """The timed output against the oracle's rows: relative Frobenius error
+    and largest elementwise error, beside the tolerance the tests apply
+    (1e-5 relative, 1e-4 * sqrt(K) absolute)."""
+    import numpy as np
+    G = G.astype(np.float64)
+    diff = G - R
+    rel = float(np.linalg.norm(diff) / max(np.linalg.norm(R), 1e-300))
+    mx = float(np.max(np.abs(diff))) if diff.size else 0.0
+    tol_abs = 1e-4 * float(np.sqrt(K))
+    return {"rows": int(R.shape[0]), "rel_fro": rel, "max_abs": mx, "tol_rel_fro": 1e-5,
+            "tol_max_abs": tol_abs, "within_tolerance": bool(rel <= 1e-5 and mx <= tol_abs),
+            "what": "the timed steps' C against the FP64 oracle on the same rows"}
+
+
 # ----------------------------------------------------------------- CPU oracle
-def cpu_baseline(case, A=None, B=None, seconds=12.0, rows=None):
+def cpu_baseline(case, A=None, B=None, seconds=12.0, rows=None, keep_result=False):
     """The CPU oracle (as it stands) on the first `rows` output rows of the
-    product, all columns, on every core this process may use."""
+    product, all columns, on every core this process may use (with
+    keep_result, its output rides along under "_result")."""
     import numpy as np
     import oracle
     from dense_fp32_matrix_10_gb300 import workloads as W
@@ -795,13 +818,16 @@ def cpu_baseline(case, A=None, B=None, seconds=12.0, rows=None):
         rows = int(min(case.M, max(threads, probe * seconds / dt)))
     sub = np.ascontiguousarray(An[:rows])
     t0 = time.perf_counter()
-    orc.sgemm_f64(case.transA, case.transB, case.alpha, sub, Bn, threads=threads)
+    R = orc.sgemm_f64(case.transA, case.transB, case.alpha, sub, Bn, threads=threads)
     dt = time.perf_counter() - t0
     f = 2.0 * rows * case.N * case.K
-    return {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"rows 0..{rows - 1} of the {case.M}x{case.N}x{case.K} NN product, all "
-                      f"{case.N} columns ({f / 1e9:.1f} GFLOP in {dt:.1f} s, FP64 accumulation)",
-            "seconds": round(dt, 2), "rows": rows}
+    out = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "sample": f"rows 0..{rows - 1} of the {case.M}x{case.N}x{case.K} NN product, all "
+                     f"{case.N} columns ({f / 1e9:.1f} GFLOP in {dt:.1f} s, FP64 accumulation)",
+           "seconds": round(dt, 2), "rows": rows}
+    if keep_result:
+        out["_result"] = R
+    return out
 
 
 def run_reference(args, dist):
