@@ -1292,6 +1292,56 @@ sgemm_status_t sgemm(int transA, int transB, int64_t M, int64_t N, int64_t K, fl
                   SGEMM_ALGO_AUTO);
 }
 
+// SG_BATCH_TRANSPOSE_B 1: a strided batch of k-contiguous op(B) stored as
+// dense consecutive N x K blocks is transposed once, as one (batch * N) x K
+// matrix, into library scratch: product b's op(B) becomes columns
+// [b * N, (b + 1) * N) of the K x (batch * N) copy (ldb = batch * N rounded
+// to 4, batch stride N), n-contiguous, so the batch runs the 128 x 256 tile
+// that a k-contiguous op(B) cannot use.  Taken only where that tile is the
+// one the transposed batch gets and each product has at least
+// SG_BATCH_TRANSPOSE_B_MIN_M rows: the copy costs a launch and 8 bytes per
+// element of B, the wider tile saves about a tenth of the product (GB300,
+// 64 x 1024x1024x64 NT 195.0 -> 174.7 us; 96 x 512x512x64 NT 81.5 -> 82.4,
+// so not taken there).  0: never.
+#ifndef SG_BATCH_TRANSPOSE_B
+#define SG_BATCH_TRANSPOSE_B 1
+#endif
+#ifndef SG_BATCH_TRANSPOSE_B_MIN_M
+#define SG_BATCH_TRANSPOSE_B_MIN_M 1024
+#endif
+
+namespace {
+sgemm_status_t run_batched_transposed_b(const Args &a, DeviceState &d, cudaStream_t s, int64_t batch,
+                                        int64_t strideA, int64_t strideC) {
+  const int64_t rows = batch * a.N, ld2 = round4(rows);
+  if (!SG_BATCH_TRANSPOSE_B || a.tb != 1 || a.N % 4 != 0 || a.M < SG_BATCH_TRANSPOSE_B_MIN_M ||
+      rows > kMaxDim)
+    return SGEMM_ERR_UNSUPPORTED;
+  Args b = a;
+  b.tb = 0;
+  b.ldb = ld2;
+  if (pick_simt_tile(b, kTma, d.sm_count, batch) != kTile128x256) return SGEMM_ERR_UNSUPPORTED;
+  const size_t bytes = static_cast<size_t>(a.K) * ld2 * sizeof(float);
+  const bool capturing = stream_capturing(s);
+  std::lock_guard<std::mutex> lock(d.tr_mu);
+  float *scratch = pretranspose_scratch(d, bytes, capturing);
+  if (!scratch) return SGEMM_ERR_UNSUPPORTED;
+  // a call on another stream (or a graph) may still be reading the scratch
+  if (order_before_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  b.B = scratch;
+  const PreLaunch copy = [&]() -> cudaError_t {
+    return launch_transpose(a.B, a.ldb, scratch, ld2, static_cast<int>(rows), static_cast<int>(a.K),
+                            d.sm_count, d.status, s);
+  };
+  const sgemm_status_t st =
+      run_simt(b, d, kTma, s, Batch{batch, strideA, a.N, strideC}, /*pdl=*/true, &copy);
+  if (st != SGEMM_SUCCESS) return st;
+  t_last_launches += 1;
+  if (order_after_use(d.tr_order, s, capturing) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+  return SGEMM_SUCCESS;
+}
+}  // namespace
+
 sgemm_status_t sgemm_strided_batched(int transA, int transB, int64_t M, int64_t N, int64_t K,
                                      float alpha, const float *A, int64_t lda, int64_t strideA,
                                      const float *B, int64_t ldb, int64_t strideB, float beta,
@@ -1341,6 +1391,11 @@ sgemm_status_t sgemm_strided_batched(int transA, int transB, int64_t M, int64_t 
   }
   // TMA: 16-byte aligned bases, rows and batch strides
   const bool tma = tma_eligible(a) && (batch == 1 || (strideA % 4 == 0 && strideB % 4 == 0));
+  // k-contiguous op(B) in dense consecutive blocks: transposed once, ahead
+  if (tma && batch > 1 && a.tb == 1 && strideB == N * ldb) {
+    const sgemm_status_t tst = run_batched_transposed_b(a, *d, s, batch, strideA, strideC);
+    if (tst != SGEMM_ERR_UNSUPPORTED) return tst;
+  }
   return run_simt(a, *d, tma ? kTma : kCpAsync, s, Batch{batch, strideA, strideB, strideC});
 }
 

@@ -264,6 +264,21 @@ def test_wide_tile_batch(_cuda, orc):
 
 
 @gpu
+def test_nt_batch_with_op_b_transposed_ahead(_cuda, orc):
+    """A batch of k-contiguous op(B) in dense consecutive blocks, products of
+    1024 rows: op(B) is transposed once for the whole batch (two launches)
+    and the batch runs the 128 x 256 tile; every product against the oracle,
+    with alpha and beta, and integer data bit-exact.  Padded leading
+    dimensions (not dense blocks) keep the one-launch path."""
+    run_batched(orc, 0, 1, 1024, 512, 64, 10, alpha=1.5, beta=-0.5, seed=41)
+    assert sg.sgemm_last_launch_count() == 2
+    run_batched(orc, 0, 1, 1030, 512, 96, 10, kind="int", seed=42, check="exact")
+    assert sg.sgemm_last_launch_count() == 2
+    run_batched(orc, 0, 1, 1024, 512, 64, 10, ldb=68, seed=43)
+    assert sg.sgemm_last_launch_count() == 1
+
+
+@gpu
 def test_single_product_matches_sgemm(_cuda):
     M, N, K = 300, 200, 152   # 16-byte rows: both calls take the TMA kernel
     A = torch.randn(M, K, device="cuda")
