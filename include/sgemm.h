@@ -223,7 +223,12 @@ SGEMM_API sgemm_status_t sgemm_ex(int transA, int transB, int64_t M, int64_t N, 
  * C_b by beta.  Runs the CUDA-core kernels -- TMA loads (a 3-D tensor map per
  * strided operand) when bases, leading dimensions and strides are multiples of
  * 16 bytes and the map encodes, cp.async otherwise -- with the k-iterations of
- * the batch's tiles spread by stream-K like a single product's.  batch * tiles per product must stay below 2^31
+ * the batch's tiles spread by stream-K like a single product's.  A
+ * k-contiguous op(B) (transB = T) stored as dense consecutive blocks
+ * (strideB == N * ldb) of products with at least 1024 rows is first copied
+ * transposed, for the whole batch at once, into the library's operand
+ * scratch (one more launch; skipped when the scratch limit does not admit
+ * it).  batch * tiles per product must stay below 2^31
  * (SGEMM_ERR_UNSUPPORTED).
  */
 SGEMM_API sgemm_status_t sgemm_strided_batched(int transA, int transB, int64_t M, int64_t N,
