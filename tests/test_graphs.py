@@ -108,6 +108,43 @@ def test_batched_and_transpose_capture():
     assert torch.equal(C, refC) and torch.equal(T, refT)
 
 
+def test_batch_with_op_b_copied_ahead_in_graph():
+    """A dense NT batch of 1024-row products copies op(B) transposed into the
+    library scratch before the product (two launches).  Captured after an
+    eager call has sized the scratch, its replays, interleaved with eager
+    batches of another shape on another stream that share the scratch, equal
+    the batch run alone bit for bit."""
+    g0 = torch.Generator().manual_seed(21)
+    A1 = torch.randn(10, 1024, 64, generator=g0).cuda()
+    B1 = torch.randn(10, 512, 64, generator=g0).cuda()
+    A2 = torch.randn(12, 1152, 96, generator=g0).cuda()
+    B2 = torch.randn(12, 512, 96, generator=g0).cuda()
+    ref1 = sg.gemm_strided_batched(A1, B1, transB=True)
+    assert sg.sgemm_last_launch_count() == 2
+    ref2 = sg.gemm_strided_batched(A2, B2, transB=True)
+    assert sg.sgemm_last_launch_count() == 2
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    C1 = torch.empty_like(ref1)
+    C2 = torch.empty_like(ref2)
+    with torch.cuda.stream(s1):
+        sg.gemm_strided_batched(A1, B1, C1, transB=True, stream=s1)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s1):
+        sg.gemm_strided_batched(A1, B1, C1, transB=True, stream=s1)
+        assert sg.sgemm_last_launch_count() == 2
+    for _ in range(4):
+        C1.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        with torch.cuda.stream(s2):
+            sg.gemm_strided_batched(A2, B2, C2, transB=True, stream=s2)
+        torch.cuda.synchronize()
+        assert torch.equal(C1, ref1)
+        assert torch.equal(C2, ref2)
+
+
 GROW_CHILD = r"""
 import sys, torch
 sys.path.insert(0, {root!r})
